@@ -1,0 +1,172 @@
+"""fp64 CPU oracle for the row-wise log-softmax / cross-entropy path.
+
+TEST INFRASTRUCTURE ONLY: the test suite, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg are the only callers.  The product library never
+imports, links or runs anything here, and nothing here imports the product.
+
+The arithmetic lives in ``ce_oracle.c`` (plain C, fp64, one row at a time);
+this module only compiles it with gcc on first use and marshals numpy arrays.
+Inputs are taken as exact fp64 copies of the bf16/fp32 logits, and the
+temperature as the exact value of its fp32 rounding, so both sides of a parity
+check see the same numbers.
+
+Functions and the passages they follow:
+
+* :func:`selective_logsoftmax` -- "perf(rlhf): chunk selective_log_softmax
+  instead of looping per token" (ms-swift PR #10337), "PR information":
+  gather(log_softmax(logits / T)) at K indices per row with a row mask,
+  computed in the collapse-safe form of "Fix softmax collapse in CE, GRPO,
+  KL/JSD and softmax" (Liger-Kernel PR #1555), "Details".
+* :func:`cross_entropy` -- the same page's "Summary" (loss from the sum that
+  excludes the target) with ms-swift PR #10353's "PR information" (analytic
+  backward g*softmax - g*onehot, zero weight on ignored labels) and the
+  unsloth-zoo #2080 "Fix" section's -expm1(log p_t) target gradient.
+
+Pins: closed forms, 120-digit brute force, invariants and the pages' collapse
+thresholds, in ``tests/test_oracle_pins.py``.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "ce_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+
+REDUCTIONS = {"none": 0, "sum": 1, "mean": 2}
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ce_oracle.c into a shared library with gcc (IEEE fp64, OpenMP)."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    fresh = os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)
+    if fresh and not force:
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".{os.getpid()}.tmp"
+    cmd = ["gcc", "-std=c11", "-O2", "-fno-fast-math", "-ffp-contract=off", "-fopenmp",
+           "-shared", "-fPIC", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        # a test may point this at a deliberately broken copy of the oracle
+        # to check that the pins catch planted mistakes
+        lib = ctypes.CDLL(os.environ.get("GBCE_ORACLE_LIB") or build())
+        dp = ctypes.POINTER(ctypes.c_double)
+        ip = ctypes.POINTER(ctypes.c_int64)
+        i64 = ctypes.c_int64
+        lib.oracle_selective_logsoftmax.restype = i64
+        lib.oracle_selective_logsoftmax.argtypes = [
+            dp, i64, i64, i64, ip, i64, ctypes.c_double, ctypes.c_void_p, dp]
+        lib.oracle_cross_entropy.restype = i64
+        lib.oracle_cross_entropy.argtypes = [
+            dp, i64, i64, i64, ip, i64, ctypes.c_double, ctypes.c_int, ctypes.c_void_p,
+            dp, dp, dp, ip, ctypes.c_void_p, i64]
+        lib.oracle_num_threads.restype = ctypes.c_int
+        lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
+        _lib = lib
+        return lib
+
+
+def num_threads() -> int:
+    return _load().oracle_num_threads()
+
+
+def set_num_threads(n: int) -> None:
+    _load().oracle_set_num_threads(int(n))
+
+
+def _as_rows(x) -> np.ndarray:
+    x = np.asarray(x)
+    if x.ndim != 2:
+        raise ValueError("logits must be 2-D [rows, V]")
+    if x.dtype != np.float64:
+        x = x.astype(np.float64)  # exact for bf16/fp32 inputs
+    if x.strides[1] != 8:
+        x = np.ascontiguousarray(x)
+    return x
+
+
+def _ptr(a, ctype):
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def exact_temperature(temperature: float) -> float:
+    """The fp64 value of the fp32 temperature both sides use."""
+    return float(np.float32(temperature))
+
+
+def selective_logsoftmax(x, index, temperature: float = 1.0, row_mask=None):
+    """log p at K gathered indices per row; masked-out rows give 0.
+
+    Returns ``(out[rows, K] float64, n_bad_indices)``.
+    """
+    lib = _load()
+    x = _as_rows(x)
+    rows, V = x.shape
+    idx = np.ascontiguousarray(np.asarray(index, dtype=np.int64).reshape(rows, -1))
+    K = idx.shape[1]
+    mask_arr = None
+    mask_ptr = None
+    if row_mask is not None:
+        mask_arr = np.ascontiguousarray(np.asarray(row_mask).reshape(rows).astype(np.uint8))
+        mask_ptr = mask_arr.ctypes.data
+    out = np.empty((rows, K), dtype=np.float64)
+    bad = lib.oracle_selective_logsoftmax(
+        _ptr(x, ctypes.c_double), rows, V, x.strides[0] // 8, _ptr(idx, ctypes.c_int64), K,
+        exact_temperature(temperature), mask_ptr, _ptr(out, ctypes.c_double))
+    return out, int(bad)
+
+
+def cross_entropy(x, labels, ignore_index: int = -100, temperature: float = 1.0,
+                  reduction: str = "mean", grad_out=None, want_grad: bool = True):
+    """Token CE forward (and backward when ``want_grad``).
+
+    ``grad_out`` is the upstream gradient: [rows] for reduction 'none', a
+    scalar otherwise (default 1).  Returns a dict with ``logp`` [rows],
+    ``loss_rows`` [rows], ``loss`` (float), ``n_items`` (int), ``dlogits``
+    [rows, V] or None, and ``n_bad`` (out-of-range labels).
+    """
+    lib = _load()
+    x = _as_rows(x)
+    rows, V = x.shape
+    lab = np.ascontiguousarray(np.asarray(labels, dtype=np.int64).reshape(rows))
+    red = REDUCTIONS[reduction]
+    g_arr = None
+    g_ptr = None
+    if want_grad:
+        if grad_out is None:
+            grad_out = np.ones(rows) if red == 0 else np.ones(1)
+        g_arr = np.ascontiguousarray(np.asarray(grad_out, dtype=np.float64).reshape(-1))
+        if g_arr.size != (rows if red == 0 else 1):
+            raise ValueError("grad_out must have rows entries for 'none', one otherwise")
+        g_ptr = g_arr.ctypes.data
+    logp = np.empty(rows, dtype=np.float64)
+    loss_rows = np.empty(rows, dtype=np.float64)
+    loss = np.empty(1, dtype=np.float64)
+    n_items = np.empty(1, dtype=np.int64)
+    dx = np.empty((rows, V), dtype=np.float64) if want_grad else None
+    bad = lib.oracle_cross_entropy(
+        _ptr(x, ctypes.c_double), rows, V, x.strides[0] // 8, _ptr(lab, ctypes.c_int64),
+        int(ignore_index), exact_temperature(temperature), red, g_ptr,
+        _ptr(logp, ctypes.c_double), _ptr(loss_rows, ctypes.c_double),
+        _ptr(loss, ctypes.c_double), _ptr(n_items, ctypes.c_int64),
+        dx.ctypes.data if dx is not None else None, V)
+    return {"logp": logp, "loss_rows": loss_rows, "loss": float(loss[0]),
+            "n_items": int(n_items[0]), "dlogits": dx, "n_bad": int(bad)}

@@ -1,0 +1,251 @@
+/*
+ * fp64 CPU oracle for the row-wise log-softmax / token cross-entropy path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg may load this code; the product path never
+ * does, and it shares no code, header or constant with the CUDA library.
+ *
+ * It is deliberately plain: one row at a time, every sum in fp64 with
+ * Neumaier compensation, no blocking, no fusion, no reordering beyond what
+ * the definitions below state.  Rows are spread over OpenMP threads only so
+ * that the full-size workloads finish; each row's arithmetic is serial.
+ *
+ * Definitions (z_j = x_j / T, T the exact value of the fp32 temperature):
+ *
+ *   others(t)      = { j in [0,V) : j != t }
+ *   lse_others(t)  = max_{j in others(t)} z_j
+ *                    + log sum_{j in others(t)} exp(z_j - max)
+ *   log p_t        = -softplus(lse_others(t) - z_t)
+ *   softplus(a)    = max(a, 0) + log1p(exp(-|a|))
+ *
+ * This is the fp64 reference written as softplus(lse_others - x_y) that
+ * "Fix softmax collapse in CE, GRPO, KL/JSD and softmax" (Liger-Kernel PR
+ * #1555, section "Details") compares against, because a plain fp64
+ * x_y - logsumexp(x) itself collapses once the target leads the rest by
+ * more than about 36.7.  Mathematically it equals z_t - logsumexp_j z_j.
+ *
+ * Cross-entropy (same page, "Summary", first bullet; ms-swift PR #10353
+ * "PR information", second bullet):
+ *   loss_r  = -log p_{y_r}  for rows whose label is not ignore_index, else 0
+ *   sum     = sum_r loss_r;  mean = sum / n_items, n_items = #non-ignored
+ *             rows, and mean = 0 when n_items = 0 (all rows ignored)
+ *   dlogits = g_r * d(loss)/dx = (g_r/T) * (softmax(z) - onehot(y)):
+ *     j != y : (g_r/T) * exp(z_j - z_y + log p_y)
+ *     j == y : (g_r/T) * expm1(log p_y)
+ *   where the target term is the "-expm1(log p_t)" form of the unsloth-zoo
+ *   fix quoted on the same page (commit #2080, section "Fix", backward
+ *   bullet), so it never rounds to zero; ignored rows get a zero row
+ *   (ms-swift PR #10353: zero upstream weight for ignored labels).
+ *   g_r = grad_out[r] (reduction none), grad_out[0] (sum),
+ *         grad_out[0] / n_items (mean).
+ *
+ * Selective log-softmax ("perf(rlhf): chunk selective_log_softmax instead
+ * of looping per token", ms-swift PR #10337, "PR information": the naive
+ * gather(logits.log_softmax(-1)) with top-K indices, temperature and a row
+ * mask): out[r,k] = log p_{idx[r,k]} for rows with row_mask[r] != 0, and 0
+ * for masked-out rows, which are not read.
+ *
+ * An index or label outside [0,V) (and, for labels, not ignore_index)
+ * makes that row's outputs NaN and is counted in the return value.
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Neumaier (Kahan-Babuska) compensated running sum. */
+typedef struct {
+    double sum;
+    double comp;
+} oracle_sum;
+
+static void sum_add(oracle_sum *acc, double v)
+{
+    double t = acc->sum + v;
+    if (fabs(acc->sum) >= fabs(v))
+        acc->comp += (acc->sum - t) + v;
+    else
+        acc->comp += (v - t) + acc->sum;
+    acc->sum = t;
+}
+
+static double sum_value(const oracle_sum *acc) { return acc->sum + acc->comp; }
+
+/* log sum_{j != skip} exp(x_j / T); -inf when the set is empty. */
+static double lse_excluding(const double *x, int64_t V, int64_t skip, double T)
+{
+    double m = -INFINITY;
+    for (int64_t j = 0; j < V; ++j) {
+        if (j == skip)
+            continue;
+        double z = x[j] / T;
+        if (z > m)
+            m = z;
+    }
+    if (m == -INFINITY)
+        return -INFINITY;
+    oracle_sum s = {0.0, 0.0};
+    for (int64_t j = 0; j < V; ++j) {
+        if (j == skip)
+            continue;
+        sum_add(&s, exp(x[j] / T - m));
+    }
+    return m + log(sum_value(&s));
+}
+
+static double softplus(double a)
+{
+    if (a == -INFINITY)
+        return 0.0;
+    return fmax(a, 0.0) + log1p(exp(-fabs(a)));
+}
+
+/* log p_t of one row: -softplus(lse_others(t) - z_t). */
+static double row_logp(const double *x, int64_t V, int64_t t, double T)
+{
+    return -softplus(lse_excluding(x, V, t, T) - x[t] / T);
+}
+
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+void oracle_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0)
+        omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
+/*
+ * Selective log-softmax.
+ *   x        [rows, ld] fp64, row r at x + r*ld, first V entries used
+ *   idx      [rows, K] int64
+ *   row_mask [rows] uint8 or NULL (all rows live)
+ *   out      [rows, K] fp64
+ * Returns the number of out-of-range indices met in live rows.
+ */
+int64_t oracle_selective_logsoftmax(const double *x, int64_t rows, int64_t V, int64_t ld,
+                                    const int64_t *idx, int64_t K, double T,
+                                    const uint8_t *row_mask, double *out)
+{
+    int64_t bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(+ : bad)
+    for (int64_t r = 0; r < rows; ++r) {
+        const double *xr = x + r * ld;
+        for (int64_t k = 0; k < K; ++k) {
+            double *o = out + r * K + k;
+            if (row_mask && row_mask[r] == 0) {
+                *o = 0.0;
+                continue;
+            }
+            int64_t t = idx[r * K + k];
+            if (t < 0 || t >= V) {
+                *o = NAN;
+                ++bad;
+                continue;
+            }
+            *o = row_logp(xr, V, t, T);
+        }
+    }
+    return bad;
+}
+
+/*
+ * Token cross-entropy, forward and (when dx != NULL) backward.
+ *   x          [rows, ld] fp64
+ *   labels     [rows] int64, ignore_index marks rows to skip
+ *   reduction  0 = none, 1 = sum, 2 = mean
+ *   grad_out   [rows] for none, [1] otherwise; may be NULL when dx == NULL
+ *   logp_y     [rows] out: log p of the label (0 for ignored rows)
+ *   loss_rows  [rows] out: -log p of the label (0 for ignored rows)
+ *   loss       [1] out: the reduced loss (sum for none, for reference)
+ *   n_items    [1] out: number of rows whose label is not ignore_index
+ *   dx         [rows, ldx] out or NULL
+ * Returns the number of rows whose label is out of range.
+ */
+int64_t oracle_cross_entropy(const double *x, int64_t rows, int64_t V, int64_t ld,
+                             const int64_t *labels, int64_t ignore_index, double T,
+                             int reduction, const double *grad_out, double *logp_y,
+                             double *loss_rows, double *loss, int64_t *n_items,
+                             double *dx, int64_t ldx)
+{
+    int64_t count = 0;
+    for (int64_t r = 0; r < rows; ++r)
+        if (labels[r] != ignore_index)
+            ++count;
+    *n_items = count;
+
+    int64_t bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(+ : bad)
+    for (int64_t r = 0; r < rows; ++r) {
+        const double *xr = x + r * ld;
+        int64_t y = labels[r];
+        if (y == ignore_index) {
+            logp_y[r] = 0.0;
+            loss_rows[r] = 0.0;
+        } else if (y < 0 || y >= V) {
+            logp_y[r] = NAN;
+            loss_rows[r] = NAN;
+            ++bad;
+        } else {
+            logp_y[r] = row_logp(xr, V, y, T);
+            loss_rows[r] = -logp_y[r];
+        }
+    }
+
+    oracle_sum total = {0.0, 0.0};
+    for (int64_t r = 0; r < rows; ++r)
+        sum_add(&total, loss_rows[r]);
+    if (reduction == 2)
+        *loss = count > 0 ? sum_value(&total) / (double)count : 0.0;
+    else
+        *loss = sum_value(&total);
+
+    if (dx == NULL)
+        return bad;
+
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < rows; ++r) {
+        const double *xr = x + r * ld;
+        double *dr = dx + r * ldx;
+        int64_t y = labels[r];
+        if (y == ignore_index) {
+            for (int64_t j = 0; j < V; ++j)
+                dr[j] = 0.0;
+            continue;
+        }
+        if (y < 0 || y >= V) {
+            for (int64_t j = 0; j < V; ++j)
+                dr[j] = NAN;
+            continue;
+        }
+        double g;
+        if (reduction == 0)
+            g = grad_out[r];
+        else if (reduction == 1)
+            g = grad_out[0];
+        else
+            g = count > 0 ? grad_out[0] / (double)count : 0.0;
+        double scale = g / T;
+        double lp = logp_y[r];
+        double zy = xr[y] / T;
+        for (int64_t j = 0; j < V; ++j) {
+            if (j == y)
+                dr[j] = scale * expm1(lp);
+            else
+                dr[j] = scale * exp(xr[j] / T - zy + lp);
+        }
+    }
+    return bad;
+}

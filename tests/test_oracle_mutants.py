@@ -1,0 +1,53 @@
+"""Planted mistakes: each broken copy of the oracle must fail the pins.
+
+Every mutant is a one-line edit of ``oracle/ce_oracle.c`` compiled into a
+temporary library; the pin suite then runs against it in a subprocess and
+must fail.  This checks that the pins constrain every term of the oracle,
+not that the oracle is right (the pins themselves do that).
+"""
+
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "ce_oracle.c")
+
+MUTANTS = {
+    "target_not_divided_by_T": ("- x[t] / T);", "- x[t]);"),
+    "softplus_sign": ("fmax(a, 0.0) + log1p(", "fmax(a, 0.0) - log1p("),
+    "target_left_in_others": ("        if (j == skip)\n            continue;\n        sum_add",
+                              "        sum_add"),
+    "target_grad_exp_minus_one": ("scale * expm1(lp)", "scale * (exp(lp) - 1.0)"),
+    "grad_missing_inverse_T": ("double scale = g / T;", "double scale = g;"),
+    "mean_grad_not_divided": ("g = count > 0 ? grad_out[0] / (double)count : 0.0;",
+                              "g = grad_out[0];"),
+    "mean_loss_not_divided": ("*loss = count > 0 ? sum_value(&total) / (double)count : 0.0;",
+                              "*loss = sum_value(&total);"),
+    "ignored_rows_counted": ("if (labels[r] != ignore_index)\n            ++count;",
+                             "++count;"),
+    "grad_sign_flipped": ("dr[j] = scale * exp(xr[j] / T - zy + lp);",
+                          "dr[j] = -scale * exp(xr[j] / T - zy + lp);"),
+    "other_logit_target_swap": ("scale * exp(xr[j] / T - zy + lp)",
+                                "scale * exp(zy - xr[j] / T + lp)"),
+    "masked_rows_computed": ("if (row_mask && row_mask[r] == 0) {", "if (0) {"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_reject_mutant(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation site for {name} not found exactly once"
+    mutated = tmp_path / "mutant.c"
+    mutated.write_text(src.replace(old, new))
+    lib = tmp_path / "libmutant.so"
+    subprocess.run(["gcc", "-std=c11", "-O2", "-fno-fast-math", "-ffp-contract=off", "-fopenmp",
+                    "-shared", "-fPIC", str(mutated), "-o", str(lib), "-lm"], check=True)
+    env = dict(os.environ, GBCE_ORACLE_LIB=str(lib))
+    res = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                          os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                         cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert res.returncode != 0, f"pins passed with mutant {name}:\n{res.stdout[-2000:]}"

@@ -1,0 +1,356 @@
+"""Pins for the fp64 oracle, against things other than itself.
+
+Each test ties the oracle to a fact the pages or the mathematics fix:
+closed forms, a 120-digit brute force of the plain definition
+log p_t = z_t - log sum_j exp(z_j), a library routine a special case
+reduces to, invariants, the pages' printed collapse thresholds and the pages' printed
+sparse-supervision workload.  A dropped term, a wrong sign, a missing 1/T, a
+wrong index or a wrong reduction scale each fails at least one of them.
+"""
+
+import math
+from decimal import Context, Decimal
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+import oracle
+import workloads
+from conftest import read_golden
+
+CTX = Context(prec=120)
+
+
+def brute_row(row, t, T):
+    """Plain definition at 120 digits: (log p_j for all j, log p_t)."""
+    Td = Decimal(T)
+    z = [CTX.divide(Decimal(float(v)), Td) for v in row]
+    s = Decimal(0)
+    for zj in z:
+        s = CTX.add(s, CTX.exp(zj))
+    lse = CTX.ln(s)
+    return [CTX.subtract(zj, lse) for zj in z], CTX.subtract(z[t], lse)
+
+
+def brute_grad_row(row, y, T, g):
+    """(g/T) * (softmax(z) - onehot(y)) at 120 digits."""
+    logps, _ = brute_row(row, y, T)
+    scale = CTX.divide(Decimal(g), Decimal(T))
+    out = []
+    for j, lp in enumerate(logps):
+        p = CTX.exp(lp)
+        if j == y:
+            p = CTX.subtract(p, Decimal(1))
+        out.append(float(CTX.multiply(scale, p)))
+    return np.array(out)
+
+
+def rel_err(a, b):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    return np.max(np.abs(a - b) / np.maximum(np.abs(b), 1e-300))
+
+
+# --------------------------------------------------------------- closed forms
+
+@pytest.mark.parametrize("V", [1, 2, 7, 4096, 152064])
+@pytest.mark.parametrize("T", [1.0, 0.9, 0.7])
+def test_uniform_logits_give_minus_log_v(V, T):
+    rng = np.random.default_rng(V)
+    c = rng.normal()
+    x = np.full((3, V), c)
+    labels = np.array([0, V - 1, V // 2])
+    lp, bad = oracle.selective_logsoftmax(x, labels[:, None], T)
+    assert bad == 0
+    np.testing.assert_allclose(lp[:, 0], -math.log(V), rtol=1e-14, atol=1e-300)
+    g = 0.37
+    out = oracle.cross_entropy(x, labels, temperature=T, reduction="sum", grad_out=[g])
+    Te = oracle.exact_temperature(T)
+    dx = out["dlogits"]
+    for r, y in enumerate(labels):
+        want = np.full(V, g / (Te * V))
+        want[y] = g * (1.0 / V - 1.0) / Te
+        np.testing.assert_allclose(dx[r], want, rtol=1e-13, atol=1e-300)
+    np.testing.assert_allclose(out["loss"], 3 * math.log(V), rtol=1e-14)
+
+
+@pytest.mark.parametrize("V", [2, 5, 1003, 40001])
+@pytest.mark.parametrize("gap", [-3.0, 0.5, 17.0, 20.0, 30.0, 50.0])
+@pytest.mark.parametrize("T", [1.0, 0.7])
+def test_two_level_rows(V, gap, T):
+    """Target a, V-1 others b: log p = -log1p((V-1) exp((b-a)/T))."""
+    a, b = 1.25 + gap, 1.25
+    x = np.full((1, V), b)
+    y = V // 3
+    x[0, y] = a
+    lp, _ = oracle.selective_logsoftmax(x, [[y]], T)
+    Te = oracle.exact_temperature(T)
+    want = -math.log1p((V - 1) * math.exp((b - a) / Te))
+    assert lp[0, 0] == pytest.approx(want, rel=1e-13)
+    assert lp[0, 0] < 0.0
+
+
+def test_v2_reduces_to_log_sigmoid():
+    rng = np.random.default_rng(7)
+    x = rng.normal(scale=6.0, size=(200, 2))
+    y = rng.integers(0, 2, size=200)
+    for T in (1.0, 0.9, 0.7):
+        lp, _ = oracle.selective_logsoftmax(x, y[:, None], T)
+        Te = oracle.exact_temperature(T)
+        other = x[np.arange(200), 1 - y]
+        want = scipy.special.log_expit((x[np.arange(200), y] - other) / Te)
+        np.testing.assert_allclose(lp[:, 0], want, rtol=1e-13)
+
+
+def test_v1_rows_are_certain():
+    x = np.array([[3.5], [-2.0]])
+    lp, _ = oracle.selective_logsoftmax(x, [[0], [0]], 0.9)
+    assert np.all(lp == 0.0)
+    out = oracle.cross_entropy(x, [0, 0], reduction="mean")
+    assert out["loss"] == 0.0
+    assert np.all(out["dlogits"] == 0.0)
+
+
+# ------------------------------------------------------ brute force, 120 digits
+
+@pytest.mark.parametrize("V", [2, 3, 17, 64])
+@pytest.mark.parametrize("T", [1.0, 0.9, 0.7])
+def test_brute_force_logp(V, T):
+    margins = [0.0, 5.0, 17.0, 20.0, 30.0, 50.0, 80.0]
+    w = workloads.peaked_rows_tiny(V, margins, seed=V)
+    x = w.logits.numpy()
+    y = w.labels.numpy()
+    x[0] = np.random.default_rng(V).normal(scale=3.0, size=V)   # an ordinary row
+    lp, _ = oracle.selective_logsoftmax(x, y[:, None], T)
+    Te = oracle.exact_temperature(T)
+    for r in range(len(margins)):
+        _, want = brute_row(x[r], y[r], Te)
+        assert lp[r, 0] == pytest.approx(float(want), rel=1e-12), (r, margins[r])
+
+
+@pytest.mark.parametrize("V", [2, 9, 64])
+@pytest.mark.parametrize("T", [1.0, 0.7])
+def test_brute_force_gradient(V, T):
+    margins = [0.0, 17.0, 30.0, 50.0, 80.0]
+    w = workloads.peaked_rows_tiny(V, margins, seed=100 + V)
+    x = w.logits.numpy()
+    y = w.labels.numpy()
+    g = 1.3
+    out = oracle.cross_entropy(x, y, temperature=T, reduction="sum", grad_out=[g])
+    Te = oracle.exact_temperature(T)
+    for r in range(len(margins)):
+        want = brute_grad_row(x[r], y[r], Te, g)
+        assert rel_err(out["dlogits"][r], want) < 1e-11, (r, margins[r])
+
+
+def test_brute_force_k_indices_with_duplicates():
+    rng = np.random.default_rng(3)
+    V = 33
+    x = rng.normal(scale=4.0, size=(4, V))
+    x[1, 5] = x[1].max() + 30.0
+    idx = np.array([[0, 5, 5, 32], [5, 5, 1, 2], [7, 7, 7, 7], [31, 0, 16, 3]])
+    lp, _ = oracle.selective_logsoftmax(x, idx, 0.9)
+    Te = oracle.exact_temperature(0.9)
+    for r in range(4):
+        for k in range(4):
+            _, want = brute_row(x[r], idx[r, k], Te)
+            assert lp[r, k] == pytest.approx(float(want), rel=1e-12)
+    assert lp[0, 1] == lp[0, 2] and lp[2, 0] == lp[2, 3]
+
+
+# ----------------------------------------------------------------- invariants
+
+def test_invariants_on_collapse_stress_rows():
+    """logp <= 0, zero-sum gradient rows, nonzero target gradient (margins 17-50)."""
+    for dtype in (torch.float32, torch.bfloat16):
+        w = workloads.collapse_stress(dtype=dtype, rows=48, V=40001, seed=1)
+        x = workloads.to_numpy_f64(w.logits)
+        lab = w.labels.numpy()
+        out = oracle.cross_entropy(x, lab, reduction="mean")
+        live = lab != workloads.IGNORE_INDEX
+        assert out["n_items"] == int(live.sum())
+        assert np.all(out["logp"] <= 0.0)
+        dx = out["dlogits"]
+        for r in np.nonzero(live)[0]:
+            row = dx[r]
+            assert abs(math.fsum(row)) <= 1e-12 * math.fsum(np.abs(row))
+            assert row[lab[r]] < 0.0
+        assert np.all(dx[~live] == 0.0)
+        peaked = w.peaked_rows.numpy()
+        peaked = peaked[live[peaked]]
+        assert np.all(out["logp"][peaked] < 0.0)
+
+
+def test_probabilities_sum_to_one():
+    rng = np.random.default_rng(11)
+    V = 50
+    x = rng.normal(scale=5.0, size=(6, V))
+    x[2, 7] += 40.0
+    idx = np.tile(np.arange(V), (6, 1))
+    for T in (1.0, 0.7):
+        lp, _ = oracle.selective_logsoftmax(x, idx, T)
+        s = np.array([math.fsum(np.exp(r)) for r in lp])
+        np.testing.assert_allclose(s, 1.0, rtol=1e-14)
+
+
+def test_permuting_columns_permutes_outputs():
+    rng = np.random.default_rng(5)
+    V = 257
+    x = rng.normal(scale=2.0, size=(5, V))
+    y = rng.integers(0, V, size=5)
+    perm = rng.permutation(V)
+    inv = np.argsort(perm)
+    a = oracle.cross_entropy(x, y, temperature=0.9, reduction="sum", grad_out=[1.0])
+    b = oracle.cross_entropy(x[:, perm], inv[y], temperature=0.9, reduction="sum",
+                             grad_out=[1.0])
+    np.testing.assert_allclose(b["logp"], a["logp"], rtol=1e-14)
+    np.testing.assert_allclose(b["dlogits"], a["dlogits"][:, perm], rtol=1e-13, atol=1e-300)
+
+
+def test_finite_difference_gradient():
+    """The oracle's dlogits is the derivative of its own reduced loss."""
+    rng = np.random.default_rng(21)
+    V, rows = 6, 4
+    x = rng.normal(scale=2.0, size=(rows, V))
+    y = np.array([1, -100, 5, 0])
+    x[3, 0] += 8.0
+    for red, g in (("mean", [0.7]), ("sum", [1.9]), ("none", [0.3, 5.0, -1.1, 2.0])):
+        T = 0.7
+        out = oracle.cross_entropy(x, y, temperature=T, reduction=red, grad_out=g)
+        h = 1e-6
+        num = np.zeros_like(x)
+        w = np.asarray(g, dtype=np.float64)
+        for r in range(rows):
+            for j in range(V):
+                xp, xm = x.copy(), x.copy()
+                xp[r, j] += h
+                xm[r, j] -= h
+                fp = oracle.cross_entropy(xp, y, temperature=T, reduction=red, want_grad=False)
+                fm = oracle.cross_entropy(xm, y, temperature=T, reduction=red, want_grad=False)
+                if red == "none":
+                    d = (fp["loss_rows"] - fm["loss_rows"]) @ w / (2 * h)
+                else:
+                    d = w[0] * (fp["loss"] - fm["loss"]) / (2 * h)
+                num[r, j] = d
+        np.testing.assert_allclose(out["dlogits"], num, rtol=2e-6, atol=1e-9)
+
+
+# ------------------------------------------------ library reduction (control)
+
+def test_agrees_with_torch_fp64_on_ordinary_rows():
+    """Below the fp64 collapse threshold torch's fp64 log_softmax is exact enough."""
+    g = torch.Generator().manual_seed(9)
+    rows, V = 24, 3001
+    x = torch.randn((rows, V), generator=g, dtype=torch.float64) * 3
+    y = torch.randint(0, V, (rows,), generator=g)
+    x[torch.arange(8), y[:8]] = x[:8].max(dim=1).values + torch.linspace(1, 8, 8,
+                                                                         dtype=torch.float64)
+    y[20:] = -100
+    for T in (1.0, 0.9):
+        Te = oracle.exact_temperature(T)
+        out = oracle.cross_entropy(x.numpy(), y.numpy(), temperature=T, reduction="mean")
+        xt = x.clone().requires_grad_(True)
+        loss = torch.nn.functional.cross_entropy(xt / Te, y, ignore_index=-100)
+        loss.backward()
+        ref_lp = torch.log_softmax(x / Te, dim=1)
+        live = y != -100
+        want = ref_lp[torch.arange(rows)[live], y[live]].numpy()
+        np.testing.assert_allclose(out["logp"][live.numpy()], want, rtol=1e-11)
+        assert out["loss"] == pytest.approx(loss.item(), rel=1e-13)
+        np.testing.assert_allclose(out["dlogits"], xt.grad.numpy(), rtol=1e-10, atol=1e-18)
+
+
+# ---------------------------------------------------- the pages' printed values
+
+def test_collapse_thresholds_from_the_pages():
+    """The naive forms collapse exactly past the printed thresholds; the oracle does not."""
+    gold = read_golden("collapse_thresholds.txt")
+    assert round(math.log(2.0 ** 24), 1) == gold["fp32"]
+    assert round(math.log(2.0 ** 53), 1) == gold["fp64"]
+    for key, dtype in (("fp32", torch.float32), ("fp64", torch.float64)):
+        thr = gold[key]
+        for margin, collapses in ((thr - 0.3, False), (thr + 0.3, True)):
+            # two-column row: the rest's log-sum-exp is exactly the other
+            # logit, so the margin over it is `margin`; the naive form's
+            # lse - x_y is log(sum exp(x - x_max)) and softmax(x_y) its exp
+            row = torch.tensor([[0.0, margin]], dtype=dtype)
+            lse_minus_xy = torch.log(torch.exp(row - row.max()).sum()).item()
+            p_y = torch.softmax(row, dim=1)[0, 1].item()
+            assert (lse_minus_xy == 0.0) == collapses, (key, margin, lse_minus_xy)
+            assert (p_y == 1.0) == collapses, (key, margin, p_y)
+            lp, _ = oracle.selective_logsoftmax(row.double().numpy(), [[1]], 1.0)
+            assert lp[0, 0] < 0.0
+            assert lp[0, 0] == pytest.approx(-math.log1p(math.exp(-margin)), rel=1e-14)
+
+
+def test_sparse_supervision_workload_matches_page():
+    gold = read_golden("sparse_supervision.txt")
+    w = workloads.ce_sparse_bf16()
+    assert w.rows == gold["rows"] and w.vocab == gold["vocab"]
+    out = oracle.cross_entropy(workloads.to_numpy_f64(w.logits), w.labels.numpy(),
+                               reduction="none", grad_out=w.grad_out.numpy())
+    assert out["n_items"] == gold["supervised"]
+    mib = 4 * w.vocab / 2 ** 20
+    assert w.rows * mib == gold["fp32_mib_all_rows"]
+    assert out["n_items"] * mib == gold["fp32_mib_supervised_rows"]
+    live = w.labels.numpy() != workloads.IGNORE_INDEX
+    assert np.all(out["dlogits"][~live] == 0.0) and np.all(out["loss_rows"][~live] == 0.0)
+    # four contiguous spans per sample
+    for s in range(2):
+        seg = live[s * 961:(s + 1) * 961].astype(int)
+        starts = np.sum(np.diff(np.concatenate([[0], seg])) == 1)
+        assert starts == gold["spans_per_sample"]
+
+
+# ---------------------------------------------------------- selection & errors
+
+def test_reductions_and_item_count():
+    rng = np.random.default_rng(2)
+    x = rng.normal(size=(10, 40))
+    y = np.array([3, -100, 0, 39, -100, 7, 7, 1, -100, 2])
+    none = oracle.cross_entropy(x, y, reduction="none", grad_out=np.ones(10))
+    s = oracle.cross_entropy(x, y, reduction="sum")
+    m = oracle.cross_entropy(x, y, reduction="mean")
+    assert s["n_items"] == m["n_items"] == 7
+    assert s["loss"] == pytest.approx(math.fsum(none["loss_rows"]), rel=1e-15)
+    assert m["loss"] == pytest.approx(s["loss"] / 7, rel=1e-15)
+    np.testing.assert_allclose(m["dlogits"], s["dlogits"] / 7, rtol=1e-15)
+    np.testing.assert_allclose(none["dlogits"], s["dlogits"], rtol=1e-15)
+
+
+def test_all_ignored_mean_is_zero():
+    x = np.random.default_rng(0).normal(size=(5, 9))
+    out = oracle.cross_entropy(x, np.full(5, -100), reduction="mean")
+    assert out["n_items"] == 0 and out["loss"] == 0.0
+    assert np.all(out["dlogits"] == 0.0)
+
+
+def test_masked_rows_are_zero_and_unread():
+    x = np.random.default_rng(1).normal(size=(4, 12))
+    x[1] = np.nan                     # a masked row is never read
+    lp, bad = oracle.selective_logsoftmax(x, [[0], [99], [3], [4]], 1.0,
+                                          row_mask=[1, 0, 1, 0])
+    assert bad == 0 and lp[1, 0] == 0.0 and lp[3, 0] == 0.0 and np.all(np.isfinite(lp))
+    assert lp[0, 0] < 0.0 and lp[2, 0] < 0.0
+
+
+def test_out_of_range_labels_are_flagged():
+    x = np.random.default_rng(1).normal(size=(3, 8))
+    out = oracle.cross_entropy(x, [2, 8, -5], reduction="sum")
+    assert out["n_bad"] == 2
+    assert np.isnan(out["loss_rows"][1]) and np.isnan(out["loss_rows"][2])
+    assert np.all(np.isnan(out["dlogits"][1]))
+    lp, bad = oracle.selective_logsoftmax(x, [[0], [8], [-1]], 1.0)
+    assert bad == 2 and np.isnan(lp[1, 0]) and np.isnan(lp[2, 0])
+
+
+def test_strided_rows_equal_contiguous():
+    x = np.random.default_rng(4).normal(size=(6, 30))
+    view = x[:, 3:20]
+    lab = np.array([0, 1, 16, 5, 9, 2])
+    a = oracle.cross_entropy(view, lab, reduction="sum")
+    b = oracle.cross_entropy(np.ascontiguousarray(view), lab, reduction="sum")
+    np.testing.assert_array_equal(a["logp"], b["logp"])
+    np.testing.assert_array_equal(a["dlogits"], b["dlogits"])
