@@ -1,0 +1,434 @@
+"""Benchmark: HBM GB/s of CE fwd+bwd and selective log-softmax, 8192 x 152064 bf16.
+
+One step = the whole hot path over one batch of the packed RL workload
+(8 sequences x 1024 tokens = 8192 rows, vocab 152064, bf16 logits ~N(0, 2.5^2),
+5% confident rows, temperature 0.9):
+
+  * selective_logsoftmax at K = 4 gathered indices per row, and
+  * ce_fwd_bwd_fused (mean reduction, upstream gradient 1) writing dlogits.
+
+``value`` is algorithmic bytes per step (logits read once per op, dlogits
+written once, plus indices, labels and log-prob outputs) over the device time
+of the step, in GB/s, with inputs resident in HBM.  The logits (2.49 GB) are
+larger than L2, so no flush is needed between steps.  ``e2e`` is the same
+metric through the public Python API with the inputs copied from pinned host
+memory and the results (loss, log-probs) read back every step.
+
+``--impl reference`` times the fp64 CPU oracle on a bounded sample of the
+same rows instead (the only other place this file runs the oracle is the
+``cpu_baseline`` leg of the default arm).
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gbce|reference]
+Multi-GPU (one process per GPU, torchrun): every rank runs its own replica of
+the workload (independent batches, no collective on the data path); rank 0
+prints the aggregate over the max-over-ranks time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "HBM GB/s (% of GB300 peak) for CE fwd+bwd & selective logp, 8192x152064 bf16"
+UNIT = "GB/s"
+ROWS, VOCAB, K, TEMPERATURE = 8192, 152064, 4, 0.9
+FALLBACK_HBM_GBS = 6800.0
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "fused_ce_bf16_8192x152064.txt")
+
+
+def algorithmic_bytes(rows=ROWS, vocab=VOCAB, k=K, esize=2):
+    """Bytes each op must move at least once (SURVEY's per-unit figures x rows)."""
+    logits = rows * vocab * esize
+    logp = logits + rows * k * 8 + rows * k * 4          # logits + index + fp32 out
+    ce = 2 * logits + rows * 8                           # logits in, dlogits out, labels
+    return {"selective_logsoftmax": logp, "ce_fwd_bwd_fused": ce, "step": logp + ce}
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    import hashlib
+
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "cross_entropy_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per fused launch from the committed ncu summary, if still current."""
+    try:
+        fields = {}
+        with open(PROFILE_TRAFFIC) as f:
+            for line in f:
+                if ":" in line and not line.startswith((" ", "#", "|")):
+                    k, v = line.split(":", 1)
+                    fields[k.strip()] = v.strip()
+        if fields.get("kernel_source_sha256") != kernel_source_hash():
+            return None
+        return int(fields["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.device_index = device_index
+
+    def start(self):
+        try:
+            uuid = str(torch.cuda.get_device_properties(self.device_index).uuid)
+            sel = ["-i", uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"]
+        except Exception:
+            sel = []
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", *sel, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sms, maxes, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sms.append(float(parts[1]))
+                maxes.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sms:
+            return None
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxes),
+                "reasons": sorted(reasons), "samples": len(sms)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def time_oracle_sample(w_rows: dict, n_threads=None):
+    """Run the oracle on host rows; returns (seconds, rows)."""
+    import oracle
+
+    if n_threads:
+        oracle.set_num_threads(n_threads)
+    x, idx, lab = w_rows["x"], w_rows["index"], w_rows["labels"]
+    t0 = time.perf_counter()
+    oracle.selective_logsoftmax(x, idx, TEMPERATURE)
+    oracle.cross_entropy(x, lab, temperature=TEMPERATURE, reduction="none",
+                         grad_out=w_rows["grad"])
+    return time.perf_counter() - t0
+
+
+def host_sample(w, n_rows: int, seed: int = 1234):
+    import numpy as np
+
+    rng = np.random.default_rng(seed)
+    sel = np.sort(rng.choice(w.rows, size=n_rows, replace=False))
+    sel_t = torch.as_tensor(sel, device=w.logits.device)
+    return {"x": workloads.to_numpy_f64(w.logits[sel_t]),
+            "index": w.index[sel_t].cpu().numpy(), "labels": w.labels[sel_t].cpu().numpy(),
+            "grad": np.full(n_rows, 1.0 / w.rows), "rows": n_rows}
+
+
+def oracle_rows_for(seconds_target: float, w) -> int:
+    """Calibrate how many rows the oracle handles in about `seconds_target`."""
+    probe = host_sample(w, 8, seed=99)
+    t = time_oracle_sample(probe)
+    per_row = max(t / 8, 1e-4)
+    return int(max(8, min(w.rows, seconds_target / per_row)))
+
+
+def run_reference(args):
+    """The fp64 CPU oracle as it stands, on a bounded sample per step."""
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return
+    import oracle
+
+    oracle.build()
+    dev = "cuda:0" if torch.cuda.is_available() else "cpu"
+    w = workloads.grpo_bf16(device=dev, seed=0)
+    total_steps = args.steps + args.warmup
+    budget = 150.0 / max(total_steps, 1)          # whole run within a few minutes
+    n_rows = oracle_rows_for(min(budget, 10.0), w)
+    sample = host_sample(w, n_rows)
+    del w
+    for _ in range(args.warmup):
+        time_oracle_sample(sample)
+    times = [time_oracle_sample(sample) for _ in range(args.steps)]
+    step_s = statistics.median(times)
+    bytes_rows = algorithmic_bytes(rows=n_rows)["step"]
+    value = bytes_rows / step_s / 1e9
+    cores = oracle.num_threads()
+    desc = (f"{n_rows} of {ROWS} rows per step (selective logp K=4 + CE fwd+bwd), "
+            f"fp64 oracle, OpenMP over rows")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(1),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(world):
+    return {"workload": f"grpo_bf16_{ROWS}x{VOCAB}_k{K}", "rows": ROWS, "vocab": VOCAB,
+            "k": K, "temperature": TEMPERATURE, "logits_dtype": "bf16",
+            "ops": ["selective_logsoftmax", "ce_fwd_bwd_fused"], "reduction": "mean",
+            "peaked_rows": "5% with target +8..12", "l2": "inputs larger than L2 (2.49 GB "
+            "logits per op), no flush", "parallelism": f"replicas x{world}"}
+
+
+def run_gbce(args):
+    world, rank, local = dist_setup()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: the gbce arm needs a CUDA GPU")
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import cross_entropy_gb300 as gbce
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = workloads.grpo_bf16(device=dev, seed=rank)
+    x, idx, lab = w.logits, w.index, w.labels
+    grad = torch.ones(1, device=dev)
+    logp_out = torch.empty((ROWS, K), dtype=torch.float32, device=dev)
+    dlogits = torch.empty_like(x)
+    ws = gbce.new_workspace(ROWS, VOCAB, K, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(evs=None):
+        if evs is not None:
+            evs[0].record(stream)
+        gbce.selective_logsoftmax(x, idx, TEMPERATURE, out=logp_out, workspace=ws,
+                                  dev_status=status)
+        if evs is not None:
+            evs[1].record(stream)
+        out = gbce.ce_fwd_bwd_fused(x, lab, grad, temperature=TEMPERATURE, reduction="mean",
+                                    dlogits=dlogits, workspace=ws, dev_status=status)
+        if evs is not None:
+            evs[2].record(stream)
+        return out
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize(dev)
+    assert int(status.item()) == 0, "device status set during warm-up"
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    launches0 = gbce.kernel_launches()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    launches = gbce.kernel_launches() - launches0
+    barrier(world)
+    clocks = sampler.stop() if sampler else None
+    total_ms = t_start.elapsed_time(t_end)
+    logp_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    ce_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    total_ms = max_over_ranks(total_ms, world, dev)
+
+    nbytes = algorithmic_bytes()
+    ms_per_step = total_ms / args.steps
+    value = world * nbytes["step"] * args.steps / (total_ms * 1e-3) / 1e9
+    peak, peak_kind = measured_peak()
+    ce_avg = statistics.mean(ce_ms)
+    lp_avg = statistics.mean(logp_ms)
+    achieved = nbytes["ce_fwd_bwd_fused"] / (ce_avg * 1e-3) / 1e9
+    traffic = profiled_traffic()
+
+    # ---- end to end through the public API: host inputs in, results out
+    e2e = run_e2e(gbce, w, dev, stream, args, world)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w)
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": workload_config(world),
+        "frac_of_peak": value / world / peak,
+        "ops": {
+            "selective_logsoftmax": {"ms": lp_avg,
+                                     "GB/s": nbytes["selective_logsoftmax"] / lp_avg / 1e6,
+                                     "frac": nbytes["selective_logsoftmax"] / lp_avg / 1e6 / peak},
+            "ce_fwd_bwd_fused": {"ms": ce_avg, "GB/s": achieved, "frac": achieved / peak},
+        },
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "ce_fwd_bwd_fused (row_kernel fused mode + count + reduce)",
+                     "algorithmic_bytes": nbytes["ce_fwd_bwd_fused"], "peak_kind": peak_kind},
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_e2e(gbce, w, dev, stream, args, world):
+    """Same metric through the Python API with pinned host buffers copied per step."""
+    steps = max(3, min(args.steps, 20))
+    h_x = w.logits.cpu().pin_memory()
+    h_idx = w.index.cpu().pin_memory()
+    h_lab = w.labels.cpu().pin_memory()
+    d_x = torch.empty_like(w.logits)
+    d_idx = torch.empty_like(w.index)
+    d_lab = torch.empty_like(w.labels)
+    h_logp = torch.empty((ROWS, K), dtype=torch.float32).pin_memory()
+    h_loss = torch.empty((1,), dtype=torch.float32).pin_memory()
+    dlogits = torch.empty_like(w.logits)
+    grad = torch.ones(1, device=dev)
+    ws = gbce.new_workspace(ROWS, VOCAB, K, device=dev)
+
+    def one():
+        d_x.copy_(h_x, non_blocking=True)
+        d_idx.copy_(h_idx, non_blocking=True)
+        d_lab.copy_(h_lab, non_blocking=True)
+        lp = gbce.selective_logsoftmax(d_x, d_idx, TEMPERATURE, workspace=ws)
+        out = gbce.ce_fwd_bwd_fused(d_x, d_lab, grad, temperature=TEMPERATURE,
+                                    reduction="mean", dlogits=dlogits, workspace=ws)
+        h_logp.copy_(lp, non_blocking=True)
+        h_loss.copy_(out.loss.reshape(1), non_blocking=True)
+
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(steps):
+        one()
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
+    h2d = h_x.numel() * h_x.element_size() + h_idx.numel() * 8 + h_lab.numel() * 8
+    d2h = h_logp.numel() * 4 + 4
+    value = world * algorithmic_bytes()["step"] * steps / (ms * 1e-3) / 1e9
+    del h_x, d_x, dlogits
+    return {"value": value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": steps, "ms_per_step": ms / steps}
+
+
+def cpu_baseline(w):
+    import oracle
+
+    oracle.build()
+    n_rows = oracle_rows_for(10.0, w)
+    sample = host_sample(w, n_rows)
+    secs = time_oracle_sample(sample)
+    value = algorithmic_bytes(rows=n_rows)["step"] / secs / 1e9
+    return {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{n_rows} of {ROWS} rows (selective logp K=4 + CE fwd+bwd), "
+                      f"{secs:.1f} s, fp64 oracle, OpenMP over rows"}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["gbce", "reference"], default="gbce")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gbce(args)
+
+
+if __name__ == "__main__":
+    main()

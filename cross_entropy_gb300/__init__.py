@@ -1,0 +1,271 @@
+"""Row-wise log-softmax and token cross-entropy on one GB300 (sm_103a).
+
+Thin Python binding of ``libgbce.so`` (see ``include/gbce.h``).  The functions
+here only check and marshal arguments -- data pointers, strides, the current
+CUDA stream -- and allocate outputs with PyTorch; every step of the
+computation runs in the library's CUDA kernels.  There is no CPU or PyTorch
+fallback: if the library is missing or a tensor is not on a CUDA device,
+the call raises.
+
+Functions (same names as the C ABI):
+
+* :func:`selective_logsoftmax` -- log p at K gathered indices per row, with
+  temperature and row mask ("perf(rlhf): chunk selective_log_softmax instead
+  of looping per token", "PR information").
+* :func:`ce_fwd`, :func:`ce_bwd`, :func:`ce_fwd_bwd_fused` -- token
+  cross-entropy in the collapse-safe form of "Fix softmax collapse in CE,
+  GRPO, KL/JSD and softmax" ("Summary"), with the analytic backward
+  g*softmax - g*onehot of ms-swift PR #10353 ("PR information").
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import NamedTuple, Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libgbce.so")
+
+GBCE_F32, GBCE_BF16 = 0, 1
+REDUCTIONS = {"none": 0, "sum": 1, "mean": 2}
+MAX_K = 16
+DEV_BAD_LABEL, DEV_BAD_INDEX, DEV_TIMEOUT = 1, 2, 4
+
+# The C entry points and their argument types, in header order.
+_vp, _i64, _f32, _sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+_i32 = ctypes.c_int
+_SIGNATURES = {
+    "gbce_workspace_size": (_sz, [_i64, _i64, _i64]),
+    "gbce_status_string": (ctypes.c_char_p, [_i32]),
+    "gbce_kernel_launches": (ctypes.c_uint64, []),
+    "selective_logsoftmax": (_i32, [_vp, _i32, _i64, _i64, _i64, _vp, _i64, _f32, _vp, _vp,
+                                    _vp, _sz, _vp, _vp]),
+    "ce_fwd": (_i32, [_vp, _i32, _i64, _i64, _i64, _vp, _i64, _f32, _i32, _vp, _vp, _vp, _vp,
+                      _vp, _sz, _vp, _vp]),
+    "ce_bwd": (_i32, [_vp, _i32, _i64, _i64, _i64, _vp, _i64, _f32, _i32, _vp, _vp, _vp, _vp,
+                      _i64, _vp, _vp]),
+    "ce_fwd_bwd_fused": (_i32, [_vp, _i32, _i64, _i64, _i64, _vp, _i64, _f32, _i32, _vp, _vp,
+                                _vp, _vp, _vp, _vp, _i64, _vp, _sz, _vp, _vp]),
+}
+
+_lib = None
+
+
+class GbceError(RuntimeError):
+    """A libgbce call returned a non-OK status."""
+
+
+def load_library(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load libgbce.so (built by ``cross_entropy_gb300.build``); raise if absent."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    path = path or LIB_PATH
+    if not os.path.exists(path):
+        raise RuntimeError(f"libgbce.so not found at {path}: build it with "
+                           "`python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in _SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    if path == LIB_PATH:
+        _lib = lib
+    return lib
+
+
+def _check(status: int, what: str) -> None:
+    if status != 0:
+        msg = load_library().gbce_status_string(status).decode()
+        raise GbceError(f"{what}: {msg}")
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return GBCE_F32
+    if t.dtype == torch.bfloat16:
+        return GBCE_BF16
+    raise TypeError(f"logits must be float32 or bfloat16, got {t.dtype}")
+
+
+def _rows_view(logits: torch.Tensor) -> torch.Tensor:
+    """[..., V] with unit column stride -> 2-D [rows, V] view (no copy)."""
+    if not logits.is_cuda:
+        raise ValueError("logits must be a CUDA tensor (no CPU path exists)")
+    if logits.dim() < 2:
+        raise ValueError("logits must have shape [rows, vocab] or [..., vocab]")
+    if logits.stride(-1) != 1:
+        raise ValueError("logits must have unit stride along the vocabulary")
+    if logits.dim() > 2:
+        try:
+            logits = logits.view(-1, logits.shape[-1])
+        except RuntimeError as exc:
+            raise ValueError("leading dimensions of logits must flatten without a copy") from exc
+    return logits
+
+
+def _stream_ptr(stream) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def _dev_int64(x, device) -> torch.Tensor:
+    t = torch.as_tensor(x, dtype=torch.int64, device=device)
+    return t.contiguous()
+
+
+def kernel_launches() -> int:
+    """Kernels the library has enqueued in this process so far."""
+    return int(load_library().gbce_kernel_launches())
+
+
+def workspace_size(rows: int, vocab: int, k: int = 1) -> int:
+    return int(load_library().gbce_workspace_size(int(rows), int(vocab), int(k)))
+
+
+def new_workspace(rows: int, vocab: int, k: int = 1, device=None) -> torch.Tensor:
+    """A byte tensor large enough for any call on a [rows, vocab] problem."""
+    n = max(workspace_size(rows, vocab, k), 16)
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def _workspace(ws, rows, vocab, k, device):
+    if ws is None:
+        ws = new_workspace(rows, vocab, k, device)
+    return ws, int(ws.data_ptr()), int(ws.numel() * ws.element_size())
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else int(t.data_ptr())
+
+
+def selective_logsoftmax(logits: torch.Tensor, index, temperature: float = 1.0,
+                         row_mask: Optional[torch.Tensor] = None, *,
+                         out: Optional[torch.Tensor] = None,
+                         workspace: Optional[torch.Tensor] = None,
+                         dev_status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """log p_{index[r, k]} of each row at temperature T, fp32, shape index.shape.
+
+    ``index`` is [..., K] (or [...] for K = 1) int64; masked-out rows
+    (``row_mask == 0``) are not read and give 0.
+    """
+    lib = load_library()
+    lead_shape = logits.shape[:-1]
+    x = _rows_view(logits)
+    rows, V = x.shape
+    idx = _dev_int64(index, x.device)
+    squeeze = idx.dim() == len(lead_shape)
+    K = 1 if squeeze else idx.shape[-1]
+    idx = idx.reshape(rows, K)
+    mask = None
+    if row_mask is not None:
+        mask = row_mask.to(device=x.device, dtype=torch.uint8).reshape(rows).contiguous()
+    if out is None:
+        out = torch.empty((rows, K), dtype=torch.float32, device=x.device)
+    ws, ws_ptr, ws_bytes = _workspace(workspace, rows, V, K, x.device)
+    st = lib.selective_logsoftmax(x.data_ptr(), _dtype_code(x), rows, V, x.stride(0),
+                                  idx.data_ptr(), K, float(temperature), _ptr(mask),
+                                  out.data_ptr(), ws_ptr, ws_bytes, _ptr(dev_status),
+                                  _stream_ptr(stream))
+    _check(st, "selective_logsoftmax")
+    res = out.view(*lead_shape, K)
+    return res.squeeze(-1) if squeeze else res
+
+
+class CeForward(NamedTuple):
+    loss: torch.Tensor              # [rows] for 'none', [] otherwise
+    logp: Optional[torch.Tensor]    # [rows] log p of the label (0 for ignored rows)
+    lse: Optional[torch.Tensor]     # [rows] logsumexp of logits / T
+    n_items: torch.Tensor           # [] int64
+
+
+class CeFused(NamedTuple):
+    loss: torch.Tensor
+    dlogits: torch.Tensor
+    logp: Optional[torch.Tensor]
+    lse: Optional[torch.Tensor]
+    n_items: torch.Tensor
+
+
+def ce_fwd(logits: torch.Tensor, labels, ignore_index: int = -100, temperature: float = 1.0,
+           reduction: str = "mean", *, want_lse: bool = False,
+           workspace: Optional[torch.Tensor] = None, dev_status: Optional[torch.Tensor] = None,
+           stream=None) -> CeForward:
+    """Cross-entropy forward; returns loss, saved log p (for ce_bwd), lse, n_items."""
+    lib = load_library()
+    x = _rows_view(logits)
+    rows, V = x.shape
+    lab = _dev_int64(labels, x.device).reshape(rows)
+    red = REDUCTIONS[reduction]
+    loss = torch.empty((rows,) if red == 0 else (1,), dtype=torch.float32, device=x.device)
+    logp = torch.empty(rows, dtype=torch.float32, device=x.device)
+    lse = torch.empty(rows, dtype=torch.float32, device=x.device) if want_lse else None
+    n_items = torch.empty(1, dtype=torch.int64, device=x.device)
+    ws, ws_ptr, ws_bytes = _workspace(workspace, rows, V, 1, x.device)
+    st = lib.ce_fwd(x.data_ptr(), _dtype_code(x), rows, V, x.stride(0), lab.data_ptr(),
+                    int(ignore_index), float(temperature), red, loss.data_ptr(), logp.data_ptr(),
+                    _ptr(lse), n_items.data_ptr(), ws_ptr, ws_bytes, _ptr(dev_status),
+                    _stream_ptr(stream))
+    _check(st, "ce_fwd")
+    return CeForward(loss if red == 0 else loss[0], logp, lse, n_items[0])
+
+
+def ce_bwd(logits: torch.Tensor, labels, grad_out, saved_logp: torch.Tensor, n_items=None,
+           ignore_index: int = -100, temperature: float = 1.0, reduction: str = "mean", *,
+           dlogits: Optional[torch.Tensor] = None, dev_status: Optional[torch.Tensor] = None,
+           stream=None) -> torch.Tensor:
+    """dlogits = g * (softmax - onehot) / T from ce_fwd's saved log p."""
+    lib = load_library()
+    x = _rows_view(logits)
+    rows, V = x.shape
+    lab = _dev_int64(labels, x.device).reshape(rows)
+    red = REDUCTIONS[reduction]
+    g = torch.as_tensor(grad_out, dtype=torch.float32, device=x.device).reshape(-1).contiguous()
+    if g.numel() != (rows if red == 0 else 1):
+        raise ValueError("grad_out must have one entry per row for 'none', one otherwise")
+    n = None if n_items is None else _dev_int64(n_items, x.device).reshape(1)
+    if dlogits is None:
+        dlogits = torch.empty((rows, V), dtype=x.dtype, device=x.device)
+    d = _rows_view(dlogits)
+    lp = saved_logp.reshape(rows).contiguous()
+    st = lib.ce_bwd(x.data_ptr(), _dtype_code(x), rows, V, x.stride(0), lab.data_ptr(),
+                    int(ignore_index), float(temperature), red, g.data_ptr(), lp.data_ptr(),
+                    _ptr(n), d.data_ptr(), d.stride(0), _ptr(dev_status), _stream_ptr(stream))
+    _check(st, "ce_bwd")
+    return dlogits
+
+
+def ce_fwd_bwd_fused(logits: torch.Tensor, labels, grad_out=None, ignore_index: int = -100,
+                     temperature: float = 1.0, reduction: str = "mean", *,
+                     dlogits: Optional[torch.Tensor] = None, want_logp: bool = True,
+                     want_lse: bool = False, workspace: Optional[torch.Tensor] = None,
+                     dev_status: Optional[torch.Tensor] = None, stream=None) -> CeFused:
+    """Cross-entropy loss and dlogits in one call (upstream gradient known up front)."""
+    lib = load_library()
+    x = _rows_view(logits)
+    rows, V = x.shape
+    lab = _dev_int64(labels, x.device).reshape(rows)
+    red = REDUCTIONS[reduction]
+    if grad_out is None:
+        grad_out = torch.ones(rows if red == 0 else 1)
+    g = torch.as_tensor(grad_out, dtype=torch.float32, device=x.device).reshape(-1).contiguous()
+    if g.numel() != (rows if red == 0 else 1):
+        raise ValueError("grad_out must have one entry per row for 'none', one otherwise")
+    loss = torch.empty((rows,) if red == 0 else (1,), dtype=torch.float32, device=x.device)
+    logp = torch.empty(rows, dtype=torch.float32, device=x.device) if want_logp else None
+    lse = torch.empty(rows, dtype=torch.float32, device=x.device) if want_lse else None
+    n_items = torch.empty(1, dtype=torch.int64, device=x.device)
+    if dlogits is None:
+        dlogits = torch.empty((rows, V), dtype=x.dtype, device=x.device)
+    d = _rows_view(dlogits)
+    ws, ws_ptr, ws_bytes = _workspace(workspace, rows, V, 1, x.device)
+    st = lib.ce_fwd_bwd_fused(x.data_ptr(), _dtype_code(x), rows, V, x.stride(0), lab.data_ptr(),
+                              int(ignore_index), float(temperature), red, g.data_ptr(),
+                              loss.data_ptr(), _ptr(logp), _ptr(lse), n_items.data_ptr(),
+                              d.data_ptr(), d.stride(0), ws_ptr, ws_bytes, _ptr(dev_status),
+                              _stream_ptr(stream))
+    _check(st, "ce_fwd_bwd_fused")
+    return CeFused(loss if red == 0 else loss[0], dlogits, logp, lse, n_items[0])

@@ -1,0 +1,403 @@
+// C-ABI entry points of libgbce.so (declared in include/gbce.h): host-side
+// argument checks, workspace layout and kernel dispatch.  No entry point
+// allocates memory or synchronizes the host.
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "../../include/gbce.h"
+#include "gbce_internal.h"
+
+using gbce::RowParams;
+
+namespace {
+
+std::atomic<uint64_t> g_launches{0};
+
+}  // namespace
+
+void gbce::note_launches(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+namespace {
+
+// Few-row problems are split along the vocabulary so that the grid still
+// has about kSplitTargetUnits work units; a slice keeps >= kMinSplitElems.
+constexpr int64_t kSplitTargetUnits = 512;
+constexpr int64_t kMinSplitElems = 8192;
+constexpr int64_t kMaxSplits = 64;
+constexpr int64_t kMaxVocab = INT32_MAX - 64;  // columns are int32 on the device
+
+int split_count(int64_t rows, int64_t vocab)
+{
+    if (rows <= 0 || rows >= kSplitTargetUnits)
+        return 1;
+    int64_t s = (kSplitTargetUnits + rows - 1) / rows;
+    const int64_t by_vocab = vocab / kMinSplitElems;
+    if (s > by_vocab)
+        s = by_vocab;
+    if (s > kMaxSplits)
+        s = kMaxSplits;
+    return s < 1 ? 1 : static_cast<int>(s);
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct WsLayout {
+    size_t count = 0;     // int64 n_items scratch
+    size_t loss = 0;      // float [rows] per-row losses
+    size_t logp = 0;      // float [rows] per-row log p (split path)
+    size_t partials = 0;  // float2 [rows * splits]
+    size_t total = 0;
+};
+
+WsLayout ws_layout(int64_t rows, int64_t vocab)
+{
+    WsLayout w;
+    if (rows <= 0)
+        return w;
+    const int splits = split_count(rows, vocab);
+    const size_t r = static_cast<size_t>(rows);
+    size_t off = 0;
+    w.count = off;
+    off += 256;
+    w.loss = off;
+    off += align_up(r * sizeof(float), 256);
+    w.logp = off;
+    off += align_up(r * sizeof(float), 256);
+    w.partials = off;
+    if (splits > 1)
+        off += align_up(r * static_cast<size_t>(splits) * 2 * sizeof(float), 256);
+    w.total = off;
+    return w;
+}
+
+size_t elem_size(gbce_dtype dt) { return dt == GBCE_BF16 ? 2 : 4; }
+
+gbce_status check_logits(const void *logits, gbce_dtype dtype, int64_t rows, int64_t vocab,
+                         int64_t row_stride, float temperature)
+{
+    if (dtype != GBCE_F32 && dtype != GBCE_BF16)
+        return GBCE_EDTYPE;
+    if (rows < 0 || vocab < 1 || vocab > kMaxVocab || row_stride < vocab)
+        return GBCE_EINVAL;
+    if (!(std::isfinite(temperature) && temperature > 0.0f))
+        return GBCE_EINVAL;
+    if (rows == 0)
+        return GBCE_OK;
+    if (logits == nullptr)
+        return GBCE_EINVAL;
+    if (reinterpret_cast<uintptr_t>(logits) % elem_size(dtype) != 0)
+        return GBCE_EDTYPE;
+    if (row_stride > (INT64_MAX / 8) / rows)
+        return GBCE_EINVAL;
+    if (rows * static_cast<int64_t>(split_count(rows, vocab)) > INT32_MAX)
+        return GBCE_EINVAL;
+    return GBCE_OK;
+}
+
+gbce_status check_workspace(const void *ws, size_t bytes, int64_t rows, int64_t vocab)
+{
+    const WsLayout w = ws_layout(rows, vocab);
+    if (w.total == 0)
+        return GBCE_OK;
+    if (ws == nullptr || bytes < w.total || reinterpret_cast<uintptr_t>(ws) % 16 != 0)
+        return GBCE_EWORKSPACE;
+    return GBCE_OK;
+}
+
+bool ranges_overlap(const void *a, size_t abytes, const void *b, size_t bbytes)
+{
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + bbytes && b0 < a0 + abytes;
+}
+
+size_t matrix_bytes(int64_t rows, int64_t vocab, int64_t stride, gbce_dtype dt)
+{
+    return static_cast<size_t>((rows - 1) * stride + vocab) * elem_size(dt);
+}
+
+gbce_status check_dlogits(const void *logits, gbce_dtype dtype, int64_t rows, int64_t vocab,
+                          int64_t row_stride, const void *dlogits, int64_t d_stride)
+{
+    if (rows == 0)
+        return GBCE_OK;
+    if (dlogits == nullptr || d_stride < vocab || d_stride > (INT64_MAX / 8) / rows)
+        return GBCE_EINVAL;
+    if (reinterpret_cast<uintptr_t>(dlogits) % elem_size(dtype) != 0)
+        return GBCE_EDTYPE;
+    if (ranges_overlap(logits, matrix_bytes(rows, vocab, row_stride, dtype), dlogits,
+                       matrix_bytes(rows, vocab, d_stride, dtype)))
+        return GBCE_EINVAL;
+    return GBCE_OK;
+}
+
+// dlogits row r and logits row r have the same offset modulo 16 bytes for
+// every r, so a 16-byte logits vector maps onto a 16-byte dlogits vector.
+int same_vector_phase(const void *logits, int64_t row_stride, const void *dlogits,
+                      int64_t d_stride, gbce_dtype dt)
+{
+    const uintptr_t l = reinterpret_cast<uintptr_t>(logits), d = reinterpret_cast<uintptr_t>(dlogits);
+    const uint64_t es = elem_size(dt);
+    return ((l & 15u) == (d & 15u)) &&
+           (((static_cast<uint64_t>(row_stride) * es) & 15u) ==
+            ((static_cast<uint64_t>(d_stride) * es) & 15u));
+}
+
+RowParams base_params(const void *logits, gbce_dtype, int64_t rows, int64_t vocab,
+                      int64_t row_stride, float temperature, int32_t *dev_status)
+{
+    RowParams p{};
+    p.logits = logits;
+    p.rows = rows;
+    p.vocab = vocab;
+    p.row_stride = row_stride;
+    p.T = temperature;
+    // log2(e) / T rounded once from the fp64 quotient
+    p.c = static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
+    p.splits = split_count(rows, vocab);
+    p.k = 1;
+    p.dev_status = dev_status;
+    return p;
+}
+
+cudaError_t launch_rows(const RowParams &p, gbce_dtype dt, int mode, cudaStream_t s)
+{
+    return dt == GBCE_BF16 ? gbce::launch_rows<__nv_bfloat16>(p, mode, s)
+                           : gbce::launch_rows<float>(p, mode, s);
+}
+
+cudaError_t launch_combine(const RowParams &p, gbce_dtype dt, int mode, cudaStream_t s)
+{
+    return dt == GBCE_BF16 ? gbce::launch_combine<__nv_bfloat16>(p, mode, s)
+                           : gbce::launch_combine<float>(p, mode, s);
+}
+
+template <typename P>
+P *ws_at(void *ws, size_t off)
+{
+    return reinterpret_cast<P *>(static_cast<char *>(ws) + off);
+}
+
+gbce_status cuda_status(cudaError_t e) { return e == cudaSuccess ? GBCE_OK : GBCE_ECUDA; }
+
+}  // namespace
+
+extern "C" {
+
+size_t gbce_workspace_size(int64_t rows, int64_t vocab, int64_t k)
+{
+    (void)k;  // the split partials hold one (max, sum) pair per slice for any k
+    if (rows <= 0 || vocab < 1)
+        return 0;
+    return ws_layout(rows, vocab).total;
+}
+
+uint64_t gbce_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+const char *gbce_status_string(gbce_status status)
+{
+    switch (status) {
+    case GBCE_OK:
+        return "GBCE_OK";
+    case GBCE_EINVAL:
+        return "GBCE_EINVAL: invalid argument";
+    case GBCE_EDTYPE:
+        return "GBCE_EDTYPE: unsupported dtype or misaligned element pointer";
+    case GBCE_ECUDA:
+        return "GBCE_ECUDA: CUDA launch or attribute call failed";
+    case GBCE_EWORKSPACE:
+        return "GBCE_EWORKSPACE: workspace missing, misaligned or too small";
+    }
+    return "GBCE: unknown status";
+}
+
+gbce_status selective_logsoftmax(const void *logits, gbce_dtype dtype, int64_t rows,
+                                 int64_t vocab, int64_t row_stride, const int64_t *index,
+                                 int64_t k, float temperature, const uint8_t *row_mask,
+                                 float *logp_out, void *workspace, size_t workspace_bytes,
+                                 int32_t *dev_status, void *stream)
+{
+    gbce_status st = check_logits(logits, dtype, rows, vocab, row_stride, temperature);
+    if (st != GBCE_OK)
+        return st;
+    if (k < 1 || k > GBCE_MAX_K)
+        return GBCE_EINVAL;
+    if (rows == 0)
+        return GBCE_OK;
+    if (index == nullptr || logp_out == nullptr)
+        return GBCE_EINVAL;
+    if ((st = check_workspace(workspace, workspace_bytes, rows, vocab)) != GBCE_OK)
+        return st;
+    const WsLayout w = ws_layout(rows, vocab);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    RowParams p = base_params(logits, dtype, rows, vocab, row_stride, temperature, dev_status);
+    p.targets = index;
+    p.k = k;
+    p.row_mask = row_mask;
+    p.logp_out = logp_out;
+    p.partials = ws_at<float2>(workspace, w.partials);
+    cudaError_t e = launch_rows(p, dtype, gbce::kModeLogp, s);
+    if (e == cudaSuccess && p.splits > 1)
+        e = launch_combine(p, dtype, gbce::kModeLogp, s);
+    return cuda_status(e);
+}
+
+gbce_status ce_fwd(const void *logits, gbce_dtype dtype, int64_t rows, int64_t vocab,
+                   int64_t row_stride, const int64_t *labels, int64_t ignore_index,
+                   float temperature, gbce_reduction reduction, float *loss_out,
+                   float *logp_out, float *lse_out, int64_t *n_items_out, void *workspace,
+                   size_t workspace_bytes, int32_t *dev_status, void *stream)
+{
+    gbce_status st = check_logits(logits, dtype, rows, vocab, row_stride, temperature);
+    if (st != GBCE_OK)
+        return st;
+    if (reduction != GBCE_NONE && reduction != GBCE_SUM && reduction != GBCE_MEAN)
+        return GBCE_EINVAL;
+    if ((rows > 0 && (labels == nullptr || loss_out == nullptr)) ||
+        (rows == 0 && reduction != GBCE_NONE && loss_out == nullptr))
+        return GBCE_EINVAL;
+    if ((st = check_workspace(workspace, workspace_bytes, rows, vocab)) != GBCE_OK)
+        return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const WsLayout w = ws_layout(rows, vocab);
+
+    cudaError_t e = cudaSuccess;
+    float *loss_rows = loss_out;
+    if (rows > 0) {
+        if (reduction != GBCE_NONE)
+            loss_rows = ws_at<float>(workspace, w.loss);
+        RowParams p = base_params(logits, dtype, rows, vocab, row_stride, temperature, dev_status);
+        p.targets = labels;
+        p.ignore_index = ignore_index;
+        p.loss_rows = loss_rows;
+        p.logp_out = logp_out;
+        p.lse_out = lse_out;
+        p.partials = ws_at<float2>(workspace, w.partials);
+        e = launch_rows(p, dtype, gbce::kModeCe, s);
+        if (e == cudaSuccess && p.splits > 1)
+            e = launch_combine(p, dtype, gbce::kModeCe, s);
+    }
+    int64_t *n_ptr = n_items_out;
+    if (n_ptr == nullptr && rows > 0)
+        n_ptr = ws_at<int64_t>(workspace, w.count);
+    if (e == cudaSuccess && reduction != GBCE_NONE)
+        e = gbce::launch_reduce_loss(loss_rows, labels, rows, ignore_index,
+                                     static_cast<int>(reduction), nullptr, n_ptr, loss_out, s);
+    else if (e == cudaSuccess && n_items_out != nullptr)
+        e = gbce::launch_count_items(labels, rows, ignore_index, n_items_out, s);
+    return cuda_status(e);
+}
+
+gbce_status ce_bwd(const void *logits, gbce_dtype dtype, int64_t rows, int64_t vocab,
+                   int64_t row_stride, const int64_t *labels, int64_t ignore_index,
+                   float temperature, gbce_reduction reduction, const float *grad_out,
+                   const float *saved_logp, const int64_t *n_items, void *dlogits,
+                   int64_t dlogits_row_stride, int32_t *dev_status, void *stream)
+{
+    gbce_status st = check_logits(logits, dtype, rows, vocab, row_stride, temperature);
+    if (st != GBCE_OK)
+        return st;
+    if (reduction != GBCE_NONE && reduction != GBCE_SUM && reduction != GBCE_MEAN)
+        return GBCE_EINVAL;
+    if (rows == 0)
+        return GBCE_OK;
+    if (labels == nullptr || grad_out == nullptr || saved_logp == nullptr ||
+        (reduction == GBCE_MEAN && n_items == nullptr))
+        return GBCE_EINVAL;
+    if ((st = check_dlogits(logits, dtype, rows, vocab, row_stride, dlogits,
+                            dlogits_row_stride)) != GBCE_OK)
+        return st;
+
+    RowParams p = base_params(logits, dtype, rows, vocab, row_stride, temperature, dev_status);
+    p.targets = labels;
+    p.ignore_index = ignore_index;
+    p.dlogits = dlogits;
+    p.d_stride = dlogits_row_stride;
+    p.vec_store = same_vector_phase(logits, row_stride, dlogits, dlogits_row_stride, dtype);
+    p.grad_out = grad_out;
+    p.reduction = static_cast<int>(reduction);
+    p.n_items = n_items;
+    p.saved_logp = saved_logp;
+    return cuda_status(launch_rows(p, dtype, gbce::kModeGrad, static_cast<cudaStream_t>(stream)));
+}
+
+gbce_status ce_fwd_bwd_fused(const void *logits, gbce_dtype dtype, int64_t rows,
+                             int64_t vocab, int64_t row_stride, const int64_t *labels,
+                             int64_t ignore_index, float temperature,
+                             gbce_reduction reduction, const float *grad_out, float *loss_out,
+                             float *logp_out, float *lse_out, int64_t *n_items_out,
+                             void *dlogits, int64_t dlogits_row_stride, void *workspace,
+                             size_t workspace_bytes, int32_t *dev_status, void *stream)
+{
+    gbce_status st = check_logits(logits, dtype, rows, vocab, row_stride, temperature);
+    if (st != GBCE_OK)
+        return st;
+    if (reduction != GBCE_NONE && reduction != GBCE_SUM && reduction != GBCE_MEAN)
+        return GBCE_EINVAL;
+    if (rows == 0) {
+        if (reduction != GBCE_NONE && loss_out == nullptr)
+            return GBCE_EINVAL;
+        cudaStream_t s = static_cast<cudaStream_t>(stream);
+        cudaError_t e = cudaSuccess;
+        if (reduction != GBCE_NONE)
+            e = gbce::launch_reduce_loss(nullptr, labels, 0, ignore_index,
+                                         static_cast<int>(reduction), nullptr, n_items_out,
+                                         loss_out, s);
+        else if (n_items_out != nullptr)
+            e = gbce::launch_count_items(labels, 0, ignore_index, n_items_out, s);
+        return cuda_status(e);
+    }
+    if (labels == nullptr || loss_out == nullptr || grad_out == nullptr)
+        return GBCE_EINVAL;
+    if ((st = check_dlogits(logits, dtype, rows, vocab, row_stride, dlogits,
+                            dlogits_row_stride)) != GBCE_OK)
+        return st;
+    if ((st = check_workspace(workspace, workspace_bytes, rows, vocab)) != GBCE_OK)
+        return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const WsLayout w = ws_layout(rows, vocab);
+    int64_t *n_ptr = n_items_out != nullptr ? n_items_out : ws_at<int64_t>(workspace, w.count);
+    float *loss_rows = reduction == GBCE_NONE ? loss_out : ws_at<float>(workspace, w.loss);
+
+    cudaError_t e = cudaSuccess;
+    if (reduction == GBCE_MEAN || n_items_out != nullptr)
+        e = gbce::launch_count_items(labels, rows, ignore_index, n_ptr, s);
+
+    RowParams p = base_params(logits, dtype, rows, vocab, row_stride, temperature, dev_status);
+    p.targets = labels;
+    p.ignore_index = ignore_index;
+    p.loss_rows = loss_rows;
+    p.logp_out = logp_out;
+    p.lse_out = lse_out;
+    p.partials = ws_at<float2>(workspace, w.partials);
+    p.dlogits = dlogits;
+    p.d_stride = dlogits_row_stride;
+    p.vec_store = same_vector_phase(logits, row_stride, dlogits, dlogits_row_stride, dtype);
+    p.grad_out = grad_out;
+    p.reduction = static_cast<int>(reduction);
+    p.n_items = n_ptr;
+
+    if (e == cudaSuccess && p.splits == 1) {
+        e = launch_rows(p, dtype, gbce::kModeFused, s);
+    } else if (e == cudaSuccess) {
+        // few rows: split statistics, merge, then a split gradient pass
+        float *logp_buf = logp_out != nullptr ? logp_out : ws_at<float>(workspace, w.logp);
+        p.logp_out = logp_buf;
+        e = launch_rows(p, dtype, gbce::kModeCe, s);
+        if (e == cudaSuccess)
+            e = launch_combine(p, dtype, gbce::kModeCe, s);
+        p.saved_logp = logp_buf;
+        if (e == cudaSuccess)
+            e = launch_rows(p, dtype, gbce::kModeGrad, s);
+    }
+    if (e == cudaSuccess && reduction != GBCE_NONE)
+        e = gbce::launch_reduce_loss(loss_rows, labels, rows, ignore_index,
+                                     static_cast<int>(reduction), n_ptr, nullptr, loss_out, s);
+    return cuda_status(e);
+}
+
+}  // extern "C"

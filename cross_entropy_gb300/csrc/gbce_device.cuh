@@ -1,0 +1,265 @@
+// Device helpers for the sm_103a kernels: mbarrier / bulk-copy (TMA) PTX with
+// bounded waits, cache policies, and the online (max, sum) state of a row
+// sweep.  Nothing here allocates; nothing here waits without a limit.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gbce {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kNegInf = -__builtin_huge_valf();
+
+// ---------------------------------------------------------------- PTX: smem
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+                 : "memory");
+}
+
+// Makes barrier initialisation visible to the async (bulk-copy) proxy.
+__device__ __forceinline__ void fence_barrier_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for the phase with the given parity to complete, giving up after
+// ~2 s or 2^26 polls (each try_wait itself suspends for a bounded time).
+// Returns false on timeout.  Every pipeline wait in this library goes
+// through here, so no kernel can spin forever on a copy that never lands.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1; it < (1u << 26); ++it) {
+        if (mbar_try_wait(bar, parity))
+            return true;
+        if ((it & 63u) == 0 && global_timer_ns() - t0 > 2000000000ull)
+            break;
+    }
+    return false;
+}
+
+// L2 eviction-priority policies for bulk copies.
+__device__ __forceinline__ uint64_t policy_evict_first()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_last()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// 1-D bulk copy global -> shared (TMA engine), completion signalled on `bar`
+// as transaction bytes.  src, dst and bytes must be multiples of 16.
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
+                                          uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
+// Named barrier over the first `threads` threads of the CTA (warp multiple).
+__device__ __forceinline__ void named_sync(uint32_t id, uint32_t threads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// ---------------------------------------------------------- PTX: global mem
+
+__device__ __forceinline__ uint4 ld_nc_v4(const void *p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// Streaming 16-byte store: the gradient is written once and not re-read.
+__device__ __forceinline__ void st_cs_v4(void *p, uint4 v)
+{
+    asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+// ------------------------------------------------------------- arithmetic
+
+// 2^x on the SFU (relative error ~2^-22; results below 2^-126 flush to 0).
+__device__ __forceinline__ float ex2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float softplus(float a)
+{
+    return fmaxf(a, 0.0f) + log1pf(expf(-fabsf(a)));
+}
+
+// Element access for the two logit types.
+template <typename T> struct Elem;
+
+template <> struct Elem<float> {
+    static constexpr int kVec = 4;  // elements per 16-byte vector
+    __device__ static __forceinline__ void unpack(const uint4 &v, float (&f)[4])
+    {
+        f[0] = __uint_as_float(v.x);
+        f[1] = __uint_as_float(v.y);
+        f[2] = __uint_as_float(v.z);
+        f[3] = __uint_as_float(v.w);
+    }
+    __device__ static __forceinline__ uint4 pack(const float (&f)[4])
+    {
+        return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                          __float_as_uint(f[3]));
+    }
+    __device__ static __forceinline__ float load(const float *p) { return __ldg(p); }
+    __device__ static __forceinline__ void store(float *p, float v) { *p = v; }
+};
+
+template <> struct Elem<__nv_bfloat16> {
+    static constexpr int kVec = 8;
+    __device__ static __forceinline__ void unpack(const uint4 &v, float (&f)[8])
+    {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            f[2 * i] = __uint_as_float(w[i] << 16);
+            f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+    }
+    __device__ static __forceinline__ uint4 pack(const float (&f)[8])
+    {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+            w[i] = *reinterpret_cast<uint32_t *>(&h);
+        }
+        return make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    __device__ static __forceinline__ float load(const __nv_bfloat16 *p)
+    {
+        return __bfloat162float(__ldg(p));
+    }
+    __device__ static __forceinline__ void store(__nv_bfloat16 *p, float v)
+    {
+        *p = __float2bfloat16_rn(v);
+    }
+};
+
+// Online (max, sum) over a stream of logits, in the exp2 domain:
+//   m = max x_j,   s = sum_j 2^{(x_j - m) c},   c = log2(e) / T,
+// so that s = sum_j exp((x_j - m) / T).  Excluded columns are fed as -inf.
+struct OnlineMaxSum {
+    float m = kNegInf;
+    float mc = kNegInf;  // m * c, the shift applied to every term
+    float s = 0.0f;
+
+    // Fold N values (already target-masked) whose maximum is vmax.
+    template <int N>
+    __device__ __forceinline__ void add(const float (&f)[N], float vmax, float c)
+    {
+        if (vmax > m) {
+            s *= ex2((m - vmax) * c);
+            m = vmax;
+            mc = vmax * c;
+        }
+        if (vmax != kNegInf) {
+            float a = 0.0f, b = 0.0f;
+#pragma unroll
+            for (int i = 0; i < N; i += 2) {
+                a += ex2(fmaf(f[i], c, -mc));
+                if (i + 1 < N)
+                    b += ex2(fmaf(f[i + 1], c, -mc));
+            }
+            s += a + b;
+        }
+    }
+
+    __device__ __forceinline__ void add1(float x, float c)
+    {
+        float f[1] = {x};
+        add<1>(f, x, c);
+    }
+};
+
+// Merge two (max, sum) partial states with the same scale c.
+__device__ __forceinline__ void merge_max_sum(float &m, float &s, float m2, float s2, float c)
+{
+    const float M = fmaxf(m, m2);
+    if (M == kNegInf) {
+        m = M;
+        s = 0.0f;
+        return;
+    }
+    s = s * ex2((m - M) * c) + s2 * ex2((m2 - M) * c);
+    m = M;
+}
+
+// log p_t from the others' (m, s) and the target logit, all in raw logit
+// units: a = log s + (m - x_t) / T, log p = -softplus(a).  The margin
+// (m - x_t) / T is one IEEE division of an exact (bf16) or once-rounded
+// (fp32) difference, taken from the same values the sweep read, so log p
+// is never positive.  s == 0 (no other column, V == 1) gives log p = 0.
+__device__ __forceinline__ float finalize_logp(float m, float s, float xt, float T)
+{
+    if (!(s > 0.0f))
+        return (s == 0.0f) ? 0.0f : __int_as_float(0x7fc00000);
+    const float a = logf(s) + (m - xt) / T;
+    return -softplus(a);
+}
+
+}  // namespace gbce

@@ -1,0 +1,69 @@
+// Internal interface between the C-ABI layer (gbce_api.cu) and the kernel
+// translation units (one per logit type).  Not installed, not part of the ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gbce {
+
+// Counts every kernel the library enqueues (see gbce_kernel_launches()).
+void note_launches(int n);
+
+// What a row-kernel launch does with each (row, vocab slice) work unit.
+enum Mode : int {
+    kModeLogp = 0,   // selective log-softmax statistics (K gathered indices)
+    kModeCe = 1,     // cross-entropy forward statistics (label, ignore_index)
+    kModeGrad = 2,   // cross-entropy gradient from saved log p (ce_bwd)
+    kModeFused = 3,  // statistics then gradient of the same row (one launch)
+};
+
+struct RowParams {
+    const void *logits;
+    int64_t rows, vocab, row_stride;  // row_stride in elements
+
+    const int64_t *targets;  // kModeLogp: index [rows, k]; otherwise labels [rows]
+    int64_t k;               // gathered indices per row (1 for the CE modes)
+    int64_t ignore_index;
+    const uint8_t *row_mask;  // kModeLogp, nullable
+
+    float T;  // temperature
+    float c;  // log2(e) / T
+    int splits;  // vocab slices per row (1 = the CTA finalizes the row itself)
+
+    float *logp_out;   // kModeLogp: [rows, k]; CE modes: [rows] or null
+    float *loss_rows;  // CE modes: [rows]
+    float *lse_out;    // CE modes: [rows] or null
+    float2 *partials;  // [rows * splits] (max, sum) when splits > 1
+
+    void *dlogits;  // kModeGrad / kModeFused
+    int64_t d_stride;
+    int vec_store;  // dlogits rows share the logits rows' 16-byte phase
+    const float *grad_out;
+    int reduction;  // 0 none, 1 sum, 2 mean
+    const int64_t *n_items;
+    const float *saved_logp;  // kModeGrad
+
+    int32_t *dev_status;
+};
+
+// Row kernel (one CTA per work unit) for logit type T (float / bf16).
+template <typename T>
+cudaError_t launch_rows(const RowParams &p, int mode, cudaStream_t stream);
+
+// Merge per-slice partials and finalize the row outputs (splits > 1).
+template <typename T>
+cudaError_t launch_combine(const RowParams &p, int mode, cudaStream_t stream);
+
+// n_items = #(labels != ignore_index) into *n_out (one CTA).
+cudaError_t launch_count_items(const int64_t *labels, int64_t rows, int64_t ignore_index,
+                               int64_t *n_out, cudaStream_t stream);
+
+// loss_out[0] = sum (SUM) or sum / n (MEAN, 0 when n == 0) of loss_rows in a
+// fixed order with fp64 accumulation; when count_into is non-null the item
+// count is computed first and stored there (and used for MEAN).
+cudaError_t launch_reduce_loss(const float *loss_rows, const int64_t *labels, int64_t rows,
+                               int64_t ignore_index, int reduction, const int64_t *n_in,
+                               int64_t *count_into, float *loss_out, cudaStream_t stream);
+
+}  // namespace gbce

@@ -1,0 +1,642 @@
+// Row kernels for the row-wise log-softmax / cross-entropy path (sm_103a).
+//
+// One CTA per work unit = (row, vocab slice).  Warp NCW is the producer: its
+// lane 0 streams the slice's 16-byte-aligned body through a ring of shared-
+// memory stages with 1-D bulk copies (TMA engine, mbarrier completion).  The
+// other NCW warps consume each stage: unpack 16-byte vectors, keep an online
+// (max, sum) that excludes the target column(s), and -- in the gradient modes
+// -- write dlogits with 16-byte streaming stores.  The row's misaligned head
+// and tail (when a row does not start on a 16-byte boundary) are read with
+// scalar loads.
+//
+// Sources, by title and section:
+//  * the sum that leaves out the target and loss = softplus(log s_others +
+//    m - x_y): "Fix softmax collapse in CE, GRPO, KL/JSD and softmax"
+//    (Liger-Kernel PR #1555), "Summary";
+//  * skipping the target per 16-byte vector instead of per element is the
+//    per-block target skip of the unsloth-zoo #2080 commit quoted there
+//    ("Fix", forward bullet) at vector granularity: a vector that holds a
+//    target takes a masked slow path, every other vector none;
+//  * one launch over all rows instead of a chunk loop: "perf(rlhf): chunk
+//    selective_log_softmax instead of looping per token", "PR information";
+//  * rows with an ignored label are skipped before any read of their
+//    logits, and the gradient is g*softmax - g*onehot in a separate buffer:
+//    ms-swift PR #10353, "PR information";
+//  * a slice split with a later merge of (max, sum) partials: the split
+//    partial/combine kernels of the unsloth-zoo #2080 commit ("Fix").
+#pragma once
+
+#include <atomic>
+
+#include "gbce_device.cuh"
+#include "gbce_internal.h"
+#include "../../include/gbce.h"
+
+namespace gbce {
+
+constexpr int kConsumerWarps = 8;
+constexpr int kChunkBytes = 16384;
+constexpr int kStages = 4;
+constexpr int kRowThreads = (kConsumerWarps + 1) * 32;
+constexpr int kRingBytes = kStages * kChunkBytes;
+constexpr int kRingAlign = 128;  // bulk copies need 16-byte aligned shared addresses
+constexpr int kDynSmemBytes = kRingBytes + kRingAlign;
+
+struct RowGeom {
+    int64_t head;   // scalar elements before the first 16-byte boundary
+    int64_t nvec;   // whole 16-byte vectors after them
+    int64_t tail0;  // first element after the vectors (scalar tail)
+};
+
+template <typename T>
+__device__ __forceinline__ RowGeom row_geom(const T *row, int64_t V)
+{
+    constexpr int VEC = Elem<T>::kVec;
+    const uint32_t mis = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(row) & 15u);
+    int64_t head = static_cast<int64_t>(((16u - mis) & 15u) / sizeof(T));
+    if (head > V)
+        head = V;
+    const int64_t nvec = (V - head) / VEC;
+    return {head, nvec, head + nvec * VEC};
+}
+
+template <int KMAX>
+__device__ __forceinline__ bool span_has_target(const int32_t (&tg)[KMAX], int32_t col0, int n)
+{
+    bool hit = false;
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k)
+        hit |= static_cast<uint32_t>(tg[k] - col0) < static_cast<uint32_t>(n);
+    return hit;
+}
+
+template <int KMAX>
+__device__ __forceinline__ bool is_target(const int32_t (&tg)[KMAX], int32_t col)
+{
+    bool hit = false;
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k)
+        hit |= (tg[k] == col);
+    return hit;
+}
+
+// Fold one 16-byte vector of logits into the running (max, sum).
+template <typename T, int KMAX>
+__device__ __forceinline__ void stats_vector(OnlineMaxSum &st, const uint4 &raw, int32_t col0,
+                                             const int32_t (&tg)[KMAX], float c)
+{
+    constexpr int VEC = Elem<T>::kVec;
+    float f[VEC];
+    Elem<T>::unpack(raw, f);
+    if (span_has_target<KMAX>(tg, col0, VEC)) {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e)
+            if (is_target<KMAX>(tg, col0 + e))
+                f[e] = kNegInf;
+    }
+    float vmax = f[0];
+#pragma unroll
+    for (int e = 1; e < VEC; ++e)
+        vmax = fmaxf(vmax, f[e]);
+    st.add<VEC>(f, vmax, c);
+}
+
+// dlogits of one 16-byte vector: g/T * exp((x_j - x_y)/T + log p), and
+// g/T * expm1(log p) at the label column.
+template <typename T>
+__device__ __forceinline__ uint4 grad_vector(const uint4 &raw, int32_t col0, int32_t y, float xy,
+                                             float c, float kb, float gscale, float dy,
+                                             float (&d)[Elem<T>::kVec])
+{
+    constexpr int VEC = Elem<T>::kVec;
+    float f[VEC];
+    Elem<T>::unpack(raw, f);
+#pragma unroll
+    for (int e = 0; e < VEC; ++e)
+        d[e] = gscale * ex2(fmaf(f[e] - xy, c, kb));
+    if (static_cast<uint32_t>(y - col0) < static_cast<uint32_t>(VEC)) {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e)
+            if (col0 + e == y)
+                d[e] = dy;
+    }
+    return Elem<T>::pack(d);
+}
+
+// log p of target k, whose "others" are every column outside the target set
+// S (already folded into (mS, sS)) plus the distinct members of S other
+// than target k itself.
+template <int KMAX>
+__device__ __forceinline__ float logp_with_targets(float mS, float sS, const int32_t *tg,
+                                                   const float *xt, int K, int k, float c,
+                                                   float T)
+{
+    float m = mS, s = sS;
+    const int32_t tk = tg[k];
+    for (int j = 0; j < K; ++j) {
+        const int32_t tj = tg[j];
+        if (tj < 0 || tj == tk)
+            continue;
+        bool dup = false;
+        for (int i = 0; i < j; ++i)
+            dup |= (tg[i] == tj);
+        if (!dup)
+            merge_max_sum(m, s, xt[j], 1.0f, c);
+    }
+    return finalize_logp(m, s, xt[k], T);
+}
+
+__device__ __forceinline__ float upstream_grad(const RowParams &p, int64_t r)
+{
+    if (p.reduction == 0)
+        return p.grad_out[r];
+    if (p.reduction == 1)
+        return p.grad_out[0];
+    const int64_t n = *p.n_items;
+    return n > 0 ? p.grad_out[0] / static_cast<float>(n) : 0.0f;
+}
+
+__device__ __forceinline__ void report(int32_t *dev_status, int bits)
+{
+    if (dev_status != nullptr)
+        atomicOr(dev_status, bits);
+}
+
+// Fill this unit's slice of a dlogits row with `value` (0 for an ignored
+// row, NaN for a bad label), using every thread of the CTA.
+template <typename T>
+__device__ void fill_row_slice(T *drow, int64_t V, int split, int splits, float value)
+{
+    constexpr int VEC = Elem<T>::kVec;
+    const RowGeom g = row_geom<T>(drow, V);
+    const int64_t v0 = g.nvec * split / splits, v1 = g.nvec * (split + 1) / splits;
+    float f[VEC];
+#pragma unroll
+    for (int e = 0; e < VEC; ++e)
+        f[e] = value;
+    const uint4 pat = Elem<T>::pack(f);
+    uint4 *body = reinterpret_cast<uint4 *>(drow + g.head);
+    for (int64_t v = v0 + threadIdx.x; v < v1; v += blockDim.x)
+        st_cs_v4(body + v, pat);
+    if (split == 0)
+        for (int64_t e = threadIdx.x; e < g.head; e += blockDim.x)
+            Elem<T>::store(drow + e, value);
+    if (split == splits - 1)
+        for (int64_t e = g.tail0 + threadIdx.x; e < V; e += blockDim.x)
+            Elem<T>::store(drow + e, value);
+}
+
+template <typename T, int MODE, int KMAX>
+__global__ void __launch_bounds__(kRowThreads, 2) row_kernel(const RowParams p)
+{
+    using E = Elem<T>;
+    constexpr int VEC = E::kVec;
+    constexpr int NCW = kConsumerWarps;
+    constexpr int NC = NCW * 32;
+    constexpr int CV = kChunkBytes / 16;  // vectors per full chunk
+    constexpr int PER_THREAD = CV / NC;
+    static_assert(CV % NC == 0, "chunk must split evenly over consumer threads");
+    constexpr bool kStats = (MODE != kModeGrad);
+    constexpr bool kGrad = (MODE == kModeGrad || MODE == kModeFused);
+    constexpr int kPasses = (MODE == kModeFused) ? 2 : 1;
+
+    extern __shared__ __align__(128) uint8_t dyn_smem[];
+    uint8_t *ring = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(dyn_smem) + (kRingAlign - 1)) & ~uintptr_t(kRingAlign - 1));
+    __shared__ uint64_t full_bar[kStages];
+    __shared__ uint64_t empty_bar[kStages];
+    __shared__ float red_m[NCW], red_s[NCW];
+    __shared__ float s_xt[KMAX];
+    __shared__ int32_t s_tg[KMAX];
+    __shared__ float bc_m, bc_s, bc_logp;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int64_t unit = blockIdx.x;
+    const int64_t r = unit / p.splits;
+    const int split = static_cast<int>(unit - r * p.splits);
+    const int64_t V = p.vocab;
+    const T *row = static_cast<const T *>(p.logits) + r * p.row_stride;
+    T *drow = kGrad ? static_cast<T *>(p.dlogits) + r * p.d_stride : nullptr;
+
+    // ---- row selection, before any read of this row's logits
+    int32_t tg[KMAX];
+    int32_t y = -1;
+    int state = 0;  // 0 live, 1 skipped (ignored label / masked row), 2 bad label
+    if (MODE == kModeLogp) {
+        if (p.row_mask != nullptr && p.row_mask[r] == 0)
+            state = 1;
+#pragma unroll
+        for (int k = 0; k < KMAX; ++k) {
+            int64_t t = -1;
+            if (state == 0 && k < p.k)
+                t = p.targets[r * p.k + k];
+            tg[k] = (t >= 0 && t < V) ? static_cast<int32_t>(t) : -1;
+        }
+    } else {
+        const int64_t lab = p.targets[r];
+        if (lab == p.ignore_index)
+            state = 1;
+        else if (lab < 0 || lab >= V)
+            state = 2;
+        y = state == 0 ? static_cast<int32_t>(lab) : -1;
+#pragma unroll
+        for (int k = 0; k < KMAX; ++k)
+            tg[k] = (k == 0) ? y : -1;
+    }
+
+    if (state != 0) {
+        const float fill = state == 1 ? 0.0f : __int_as_float(0x7fc00000);
+        const bool direct = (p.splits == 1);
+        if (MODE == kModeLogp) {
+            if (direct && tid < p.k)
+                p.logp_out[r * p.k + tid] = 0.0f;
+        } else {
+            if (tid == 0 && (direct || MODE == kModeGrad) && split == 0 && state == 2)
+                report(p.dev_status, GBCE_DEV_BAD_LABEL);
+            if (tid == 0 && direct && MODE != kModeGrad) {
+                p.loss_rows[r] = fill;
+                if (p.logp_out)
+                    p.logp_out[r] = fill;
+                if (p.lse_out)
+                    p.lse_out[r] = fill;
+            }
+            if (kGrad)
+                fill_row_slice<T>(drow, V, split, p.splits, fill);
+        }
+        return;
+    }
+
+    const RowGeom g = row_geom<T>(row, V);
+    const int64_t v0 = g.nvec * split / p.splits;
+    const int64_t v1 = g.nvec * (split + 1) / p.splits;
+    const int64_t nchunks = (v1 - v0 + CV - 1) / CV;
+    const int64_t total = nchunks * kPasses;
+    const char *body = reinterpret_cast<const char *>(row + g.head) + v0 * 16;
+    const int64_t body_bytes = (v1 - v0) * 16;
+
+    if (tid == 0) {
+#pragma unroll
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], NCW);
+        }
+        fence_barrier_init();
+    }
+    if (kStats) {
+        // target logits, for the finalize step (loaded while the sweep runs)
+#pragma unroll
+        for (int k = 0; k < KMAX; ++k)
+            if (tid == k) {
+                s_tg[k] = tg[k];
+                s_xt[k] = tg[k] >= 0 ? E::load(row + tg[k]) : 0.0f;
+            }
+    }
+    __syncthreads();
+
+    // ------------------------------------------------------------ producer
+    if (warp == NCW) {
+        if (lane == 0 && total > 0) {
+            const uint64_t keep = policy_evict_last();
+            const uint64_t stream = policy_evict_first();
+            int64_t i = 0;
+            bool ok = true;
+            for (; i < total; ++i) {
+                const int slot = static_cast<int>(i % kStages);
+                if (i >= kStages &&
+                    !mbar_wait(&empty_bar[slot], static_cast<uint32_t>((i / kStages - 1) & 1))) {
+                    ok = false;
+                    break;
+                }
+                const int64_t ci = i % nchunks;
+                const int64_t off = ci * kChunkBytes;
+                const int64_t left = body_bytes - off;
+                const uint32_t bytes =
+                    static_cast<uint32_t>(left < kChunkBytes ? left : kChunkBytes);
+                const bool first_of_two = (kPasses == 2 && i < nchunks);
+                mbar_arrive_expect_tx(&full_bar[slot], bytes);
+                bulk_load(ring + slot * kChunkBytes, body + off, bytes, &full_bar[slot],
+                          first_of_two ? keep : stream);
+            }
+            if (!ok)
+                report(p.dev_status, GBCE_DEV_TIMEOUT);
+            // no copy may still be in flight when the CTA exits
+            for (int64_t j = (i > kStages ? i - kStages : 0); j < i; ++j)
+                mbar_wait(&full_bar[j % kStages], static_cast<uint32_t>((j / kStages) & 1));
+        }
+        return;
+    }
+
+    // ------------------------------------------------------------ consumers
+    const float c = p.c;
+    int64_t seq = 0;  // chunk sequence number across passes (slot, parity)
+    bool alive = true;
+    float logp = 0.0f, xy = 0.0f;
+
+    if (kStats) {
+        OnlineMaxSum st;
+        if (split == 0)
+            for (int64_t e = tid; e < g.head; e += NC) {
+                const float x = E::load(row + e);
+                st.add1(is_target<KMAX>(tg, static_cast<int32_t>(e)) ? kNegInf : x, c);
+            }
+        if (split == p.splits - 1)
+            for (int64_t e = g.tail0 + tid; e < V; e += NC) {
+                const float x = E::load(row + e);
+                st.add1(is_target<KMAX>(tg, static_cast<int32_t>(e)) ? kNegInf : x, c);
+            }
+        for (int64_t i = 0; i < nchunks; ++i, ++seq) {
+            const int slot = static_cast<int>(seq % kStages);
+            if (alive && !mbar_wait(&full_bar[slot], static_cast<uint32_t>((seq / kStages) & 1))) {
+                alive = false;
+                report(p.dev_status, GBCE_DEV_TIMEOUT);
+            }
+            if (alive) {
+                const uint4 *chunk = reinterpret_cast<const uint4 *>(ring + slot * kChunkBytes);
+                const int64_t nv = (v1 - v0 - i * CV) < CV ? (v1 - v0 - i * CV) : CV;
+                const int32_t colbase = static_cast<int32_t>(g.head + (v0 + i * CV) * VEC);
+                if (nv == CV) {
+                    uint4 raw[PER_THREAD];
+#pragma unroll
+                    for (int u = 0; u < PER_THREAD; ++u)
+                        raw[u] = chunk[tid + u * NC];
+#pragma unroll
+                    for (int u = 0; u < PER_THREAD; ++u)
+                        stats_vector<T, KMAX>(st, raw[u], colbase + (tid + u * NC) * VEC, tg, c);
+                } else {
+                    for (int v = tid; v < nv; v += NC)
+                        stats_vector<T, KMAX>(st, chunk[v], colbase + v * VEC, tg, c);
+                }
+            }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&empty_bar[slot]);
+        }
+
+        // CTA-wide merge of the per-thread (max, sum) in a fixed order
+        float m = st.m, s = st.s;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
+            const float s2 = __shfl_xor_sync(0xffffffffu, s, off);
+            merge_max_sum(m, s, m2, s2, c);
+        }
+        if (lane == 0) {
+            red_m[warp] = m;
+            red_s[warp] = s;
+        }
+        named_sync(1, NC);
+        if (warp == 0) {
+            m = lane < NCW ? red_m[lane] : kNegInf;
+            s = lane < NCW ? red_s[lane] : 0.0f;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
+                const float s2 = __shfl_xor_sync(0xffffffffu, s, off);
+                merge_max_sum(m, s, m2, s2, c);
+            }
+            if (lane == 0) {
+                if (p.splits > 1) {
+                    p.partials[unit] = make_float2(m, s);
+                } else if (MODE == kModeLogp) {
+                    bc_m = m;
+                    bc_s = s;
+                } else {
+                    xy = s_xt[0];
+                    logp = finalize_logp(m, s, xy, p.T);
+                    p.loss_rows[r] = -logp;
+                    if (p.logp_out)
+                        p.logp_out[r] = logp;
+                    if (p.lse_out)
+                        p.lse_out[r] = xy / p.T - logp;
+                    bc_logp = logp;
+                }
+            }
+        }
+        if (MODE == kModeLogp && p.splits == 1) {
+            named_sync(1, NC);
+            if (tid < p.k) {
+                float out;
+                if (s_tg[tid] < 0) {
+                    out = __int_as_float(0x7fc00000);
+                    report(p.dev_status, GBCE_DEV_BAD_INDEX);
+                } else {
+                    out = logp_with_targets<KMAX>(bc_m, bc_s, s_tg, s_xt, static_cast<int>(p.k),
+                                                  tid, c, p.T);
+                }
+                p.logp_out[r * p.k + tid] = out;
+            }
+        }
+        if (MODE == kModeFused) {
+            named_sync(1, NC);
+            logp = bc_logp;
+            xy = s_xt[0];
+        }
+    }
+
+    if (kGrad) {
+        if (MODE == kModeGrad) {
+            logp = p.saved_logp[r];
+            xy = E::load(row + y);
+        }
+        const float gscale = upstream_grad(p, r) / p.T;
+        const float kb = logp * kLog2e;
+        const float dy = gscale * expm1f(logp);
+        if (split == 0)
+            for (int64_t e = tid; e < g.head; e += NC) {
+                const float x = E::load(row + e);
+                E::store(drow + e, e == y ? dy : gscale * ex2(fmaf(x - xy, c, kb)));
+            }
+        if (split == p.splits - 1)
+            for (int64_t e = g.tail0 + tid; e < V; e += NC) {
+                const float x = E::load(row + e);
+                E::store(drow + e, e == y ? dy : gscale * ex2(fmaf(x - xy, c, kb)));
+            }
+        for (int64_t i = 0; i < nchunks; ++i, ++seq) {
+            const int slot = static_cast<int>(seq % kStages);
+            if (alive && !mbar_wait(&full_bar[slot], static_cast<uint32_t>((seq / kStages) & 1))) {
+                alive = false;
+                report(p.dev_status, GBCE_DEV_TIMEOUT);
+            }
+            if (alive) {
+                const uint4 *chunk = reinterpret_cast<const uint4 *>(ring + slot * kChunkBytes);
+                const int64_t nv = (v1 - v0 - i * CV) < CV ? (v1 - v0 - i * CV) : CV;
+                const int64_t vbase = v0 + i * CV;
+                const int32_t colbase = static_cast<int32_t>(g.head + vbase * VEC);
+                T *dbase = drow + g.head + vbase * VEC;
+                if (nv == CV && p.vec_store) {
+                    uint4 raw[PER_THREAD];
+#pragma unroll
+                    for (int u = 0; u < PER_THREAD; ++u)
+                        raw[u] = chunk[tid + u * NC];
+#pragma unroll
+                    for (int u = 0; u < PER_THREAD; ++u) {
+                        const int v = tid + u * NC;
+                        float d[VEC];
+                        st_cs_v4(dbase + v * VEC, grad_vector<T>(raw[u], colbase + v * VEC, y, xy,
+                                                                 c, kb, gscale, dy, d));
+                    }
+                } else {
+                    for (int v = tid; v < nv; v += NC) {
+                        float d[VEC];
+                        const uint4 out = grad_vector<T>(chunk[v], colbase + v * VEC, y, xy, c,
+                                                         kb, gscale, dy, d);
+                        if (p.vec_store) {
+                            st_cs_v4(dbase + v * VEC, out);
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < VEC; ++e)
+                                E::store(dbase + v * VEC + e, d[e]);
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&empty_bar[slot]);
+        }
+    }
+}
+
+// Merge the slices' (max, sum) partials of each row in slice order and write
+// the row's outputs.  One thread per row.
+template <typename T, int MODE>
+__global__ void combine_kernel(const RowParams p)
+{
+    using E = Elem<T>;
+    const int64_t r = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (r >= p.rows)
+        return;
+    const T *row = static_cast<const T *>(p.logits) + r * p.row_stride;
+    const int64_t V = p.vocab;
+    const float c = p.c;
+    const float nan = __int_as_float(0x7fc00000);
+
+    if (MODE == kModeLogp) {
+        if (p.row_mask != nullptr && p.row_mask[r] == 0) {
+            for (int64_t k = 0; k < p.k; ++k)
+                p.logp_out[r * p.k + k] = 0.0f;
+            return;
+        }
+    } else {
+        const int64_t lab = p.targets[r];
+        if (lab == p.ignore_index || lab < 0 || lab >= V) {
+            const float fill = lab == p.ignore_index ? 0.0f : nan;
+            if (lab != p.ignore_index)
+                report(p.dev_status, GBCE_DEV_BAD_LABEL);
+            p.loss_rows[r] = fill;
+            if (p.logp_out)
+                p.logp_out[r] = fill;
+            if (p.lse_out)
+                p.lse_out[r] = fill;
+            return;
+        }
+    }
+
+    float m = kNegInf, s = 0.0f;
+    for (int i = 0; i < p.splits; ++i) {
+        const float2 part = p.partials[r * p.splits + i];
+        merge_max_sum(m, s, part.x, part.y, c);
+    }
+
+    if (MODE == kModeLogp) {
+        int32_t tg[GBCE_MAX_K];
+        float xt[GBCE_MAX_K];
+        const int K = static_cast<int>(p.k);
+        for (int k = 0; k < K; ++k) {
+            const int64_t t = p.targets[r * p.k + k];
+            tg[k] = (t >= 0 && t < V) ? static_cast<int32_t>(t) : -1;
+            xt[k] = tg[k] >= 0 ? E::load(row + tg[k]) : 0.0f;
+        }
+        for (int k = 0; k < K; ++k) {
+            float out;
+            if (tg[k] < 0) {
+                out = nan;
+                report(p.dev_status, GBCE_DEV_BAD_INDEX);
+            } else {
+                out = logp_with_targets<GBCE_MAX_K>(m, s, tg, xt, K, k, c, p.T);
+            }
+            p.logp_out[r * p.k + k] = out;
+        }
+    } else {
+        const float xy = E::load(row + p.targets[r]);
+        const float logp = finalize_logp(m, s, xy, p.T);
+        p.loss_rows[r] = -logp;
+        if (p.logp_out)
+            p.logp_out[r] = logp;
+        if (p.lse_out)
+            p.lse_out[r] = xy / p.T - logp;
+    }
+}
+
+// The opt-in to more than 48 KB of dynamic shared memory is an attribute of
+// the function in each device's context: set it once per device.
+template <typename Kernel>
+static cudaError_t ensure_smem_attr(Kernel kernel, int bytes, std::atomic<uint64_t> &done)
+{
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess)
+        return err;
+    const uint64_t bit = dev < 64 ? (1ull << dev) : 0ull;
+    if (bit != 0 && (done.load(std::memory_order_relaxed) & bit) != 0)
+        return cudaSuccess;
+    err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (err == cudaSuccess)
+        done.fetch_or(bit, std::memory_order_relaxed);
+    return err;
+}
+
+template <typename T, int MODE, int KMAX>
+static cudaError_t launch_row_kernel(const RowParams &p, cudaStream_t stream)
+{
+    static std::atomic<uint64_t> attr_done{0};
+    auto kernel = row_kernel<T, MODE, KMAX>;
+    cudaError_t err = ensure_smem_attr(kernel, kDynSmemBytes, attr_done);
+    if (err != cudaSuccess)
+        return err;
+    const int64_t units = p.rows * p.splits;
+    kernel<<<static_cast<unsigned>(units), kRowThreads, kDynSmemBytes, stream>>>(p);
+    note_launches(1);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_rows(const RowParams &p, int mode, cudaStream_t stream)
+{
+    if (p.rows == 0)
+        return cudaSuccess;
+    switch (mode) {
+    case kModeLogp:
+        if (p.k <= 1)
+            return launch_row_kernel<T, kModeLogp, 1>(p, stream);
+        if (p.k <= 4)
+            return launch_row_kernel<T, kModeLogp, 4>(p, stream);
+        return launch_row_kernel<T, kModeLogp, GBCE_MAX_K>(p, stream);
+    case kModeCe:
+        return launch_row_kernel<T, kModeCe, 1>(p, stream);
+    case kModeGrad:
+        return launch_row_kernel<T, kModeGrad, 1>(p, stream);
+    case kModeFused:
+        return launch_row_kernel<T, kModeFused, 1>(p, stream);
+    default:
+        return cudaErrorInvalidValue;
+    }
+}
+
+template <typename T>
+cudaError_t launch_combine(const RowParams &p, int mode, cudaStream_t stream)
+{
+    if (p.rows == 0)
+        return cudaSuccess;
+    const int threads = 128;
+    const unsigned blocks = static_cast<unsigned>((p.rows + threads - 1) / threads);
+    if (mode == kModeLogp)
+        combine_kernel<T, kModeLogp><<<blocks, threads, 0, stream>>>(p);
+    else
+        combine_kernel<T, kModeCe><<<blocks, threads, 0, stream>>>(p);
+    note_launches(1);
+    return cudaGetLastError();
+}
+
+}  // namespace gbce

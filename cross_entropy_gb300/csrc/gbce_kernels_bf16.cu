@@ -1,0 +1,7 @@
+// bf16-logit instantiations of the row kernels.
+#include "gbce_kernels.cuh"
+
+namespace gbce {
+template cudaError_t launch_rows<__nv_bfloat16>(const RowParams &, int, cudaStream_t);
+template cudaError_t launch_combine<__nv_bfloat16>(const RowParams &, int, cudaStream_t);
+}  // namespace gbce

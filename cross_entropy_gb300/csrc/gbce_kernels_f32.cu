@@ -1,0 +1,7 @@
+// fp32-logit instantiations of the row kernels.
+#include "gbce_kernels.cuh"
+
+namespace gbce {
+template cudaError_t launch_rows<float>(const RowParams &, int, cudaStream_t);
+template cudaError_t launch_combine<float>(const RowParams &, int, cudaStream_t);
+}  // namespace gbce

@@ -1,0 +1,200 @@
+/*
+ * gbce.h -- C ABI of libgbce.so: row-wise log-softmax and token cross-entropy
+ * over a [rows, vocab] logit matrix on one NVIDIA GB300 (sm_103a).
+ *
+ * What is computed (z_j = x_j / T for a row x of length V, temperature T):
+ *
+ *   log p_t = -softplus( log sum_{j != t} exp(z_j - m_t) + m_t - z_t ),
+ *   m_t     = max_{j != t} z_j,   softplus(a) = max(a,0) + log1p(exp(-|a|)),
+ *
+ * which equals z_t - logsumexp_j z_j but never rounds to exactly 0 (and is
+ * never positive) when the target leads the other logits by a wide margin.
+ * This is the collapse-safe form of "Fix softmax collapse in CE, GRPO,
+ * KL/JSD and softmax" (Liger-Kernel PR #1555), section "Summary": the first
+ * pass also accumulates the sum without the target, and the loss is
+ * softplus(log(sum_others) + m - x_y).
+ *
+ * Conventions shared by every entry point:
+ *
+ *  - Memory.  Every pointer argument is DEVICE memory owned by the caller,
+ *    except that `stream` is a cudaStream_t handle (NULL = legacy default
+ *    stream).  The library allocates nothing, frees nothing and keeps no
+ *    state between calls; scratch space is the caller's `workspace`.
+ *  - Layout.  Logits are row-major: row r starts `r * row_stride` ELEMENTS
+ *    after `logits`, and its first `vocab` elements are used.  row_stride >=
+ *    vocab.  Index, label, mask and per-row outputs are dense.  The logits
+ *    pointer must be aligned to its element size; rows need not be 16-byte
+ *    aligned (a misaligned head/tail is read with scalar loads).
+ *  - Types.  Logits are fp32 or bf16; every computation is fp32; log-probs,
+ *    losses and log-sum-exps are written as fp32; dlogits have the logits'
+ *    type (bf16 rounded to nearest even).
+ *  - Asynchrony.  Every call only enqueues work on `stream` and returns; it
+ *    never synchronizes the host.  The returned status reports HOST-side
+ *    argument checks (and launch errors) only.
+ *  - Device-side errors.  A label or index outside [0, vocab) (labels equal
+ *    to ignore_index excepted) sets a bit in `*dev_status` (atomic OR; pass
+ *    NULL to skip reporting) and makes that row's outputs NaN.  A pipeline
+ *    wait that exceeds its time limit sets GBCE_DEV_TIMEOUT and the kernel
+ *    returns instead of hanging.  Nothing traps.  The caller zeroes
+ *    *dev_status and reads it whenever it likes.
+ *  - Threading.  Calls on different streams may run concurrently provided
+ *    their output and workspace buffers do not overlap.
+ */
+#ifndef GBCE_H
+#define GBCE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GBCE_OK = 0,
+    GBCE_EINVAL = 1,     /* null pointer, bad size/stride/temperature, aliasing */
+    GBCE_EDTYPE = 2,     /* unsupported dtype or misaligned element pointer */
+    GBCE_ECUDA = 3,      /* a CUDA launch or attribute call failed */
+    GBCE_EWORKSPACE = 4  /* workspace smaller than gbce_workspace_size() */
+} gbce_status;
+
+typedef enum { GBCE_F32 = 0, GBCE_BF16 = 1 } gbce_dtype;
+
+typedef enum { GBCE_NONE = 0, GBCE_SUM = 1, GBCE_MEAN = 2 } gbce_reduction;
+
+/* Bits OR-ed into *dev_status by the kernels. */
+#define GBCE_DEV_BAD_LABEL 1   /* a label outside [0, vocab) and != ignore_index */
+#define GBCE_DEV_BAD_INDEX 2   /* a gather index outside [0, vocab) */
+#define GBCE_DEV_TIMEOUT 4     /* a pipeline wait gave up; outputs of that row are invalid */
+
+/* Largest number of gathered indices per row that selective_logsoftmax takes. */
+#define GBCE_MAX_K 16
+
+/*
+ * Bytes of workspace that any call on a [rows, vocab] problem with k indices
+ * per row needs (k = 1 for the cross-entropy calls).  A pure function of its
+ * arguments: no CUDA call, valid for any device.  Returns 0 for rows <= 0.
+ */
+size_t gbce_workspace_size(int64_t rows, int64_t vocab, int64_t k);
+
+/* Static, human-readable name of a status code. */
+const char *gbce_status_string(gbce_status status);
+
+/*
+ * Number of kernels this library has enqueued in this process so far (all
+ * devices, all streams), for accounting in benchmarks.  Thread-safe.
+ */
+uint64_t gbce_kernel_launches(void);
+
+/*
+ * Selective log-softmax: logp_out[r, k] = log p_{index[r, k]} of row r at
+ * temperature T, for rows with row_mask[r] != 0 (or all rows when row_mask
+ * is NULL); masked-out rows are not read and get 0.
+ *
+ * Source: "perf(rlhf): chunk selective_log_softmax instead of looping per
+ * token" (ms-swift PR #10337), "PR information": the naive
+ * gather(logits.log_softmax(-1)) with top-K indices, temperature and a row
+ * mask, here in one launch over all rows; accurate log-probs as in "Fix
+ * softmax collapse ..." (Liger-Kernel PR #1555), "Summary", second bullet.
+ *
+ *   logits     [rows, row_stride] fp32/bf16
+ *   index      [rows, k] int64, 1 <= k <= GBCE_MAX_K; duplicates allowed
+ *   row_mask   [rows] uint8 or NULL
+ *   logp_out   [rows, k] fp32
+ *   workspace  >= gbce_workspace_size(rows, vocab, k) bytes (may be NULL
+ *              when that size is 0), 16-byte aligned
+ * Errors: GBCE_EINVAL for NULL logits/index/logp_out with rows > 0,
+ * vocab < 1, row_stride < vocab, k outside [1, GBCE_MAX_K], temperature not
+ * finite and > 0; GBCE_EDTYPE; GBCE_EWORKSPACE.  Out-of-range indices of
+ * live rows: GBCE_DEV_BAD_INDEX and a NaN output for that (r, k).
+ */
+gbce_status selective_logsoftmax(const void *logits, gbce_dtype dtype, int64_t rows,
+                                 int64_t vocab, int64_t row_stride, const int64_t *index,
+                                 int64_t k, float temperature, const uint8_t *row_mask,
+                                 float *logp_out, void *workspace, size_t workspace_bytes,
+                                 int32_t *dev_status, void *stream);
+
+/*
+ * Token cross-entropy forward.  For rows whose label is not ignore_index:
+ * loss_r = -log p_{labels[r]} at temperature T; ignored rows are skipped
+ * before any read of their logits and get loss 0.
+ *
+ * Source: "Fix softmax collapse ..." (Liger-Kernel PR #1555), "Summary",
+ * first bullet (loss = softplus(log(sum_others) + m - x_y)); row selection
+ * before any vocabulary work from ms-swift PR #10353, "PR information".
+ *
+ *   labels      [rows] int64
+ *   reduction   GBCE_NONE: loss_out[rows] = loss_r;
+ *               GBCE_SUM:  loss_out[0] = sum_r loss_r;
+ *               GBCE_MEAN: loss_out[0] = sum_r loss_r / n_items, 0 when
+ *               n_items == 0 (all rows ignored).
+ *   logp_out    [rows] fp32 or NULL: log p of the label (0 when ignored);
+ *               ce_bwd takes it back as saved_logp.
+ *   lse_out     [rows] fp32 or NULL: logsumexp_j z_j (0 when ignored).
+ *   n_items_out [1] int64 or NULL: number of rows with label != ignore_index.
+ *   workspace   >= gbce_workspace_size(rows, vocab, 1) bytes.
+ * Sums are deterministic (fixed order) and taken in fp64.
+ * Errors: as selective_logsoftmax; bad labels set GBCE_DEV_BAD_LABEL and
+ * give NaN for that row (and hence a NaN sum/mean).
+ */
+gbce_status ce_fwd(const void *logits, gbce_dtype dtype, int64_t rows, int64_t vocab,
+                   int64_t row_stride, const int64_t *labels, int64_t ignore_index,
+                   float temperature, gbce_reduction reduction, float *loss_out,
+                   float *logp_out, float *lse_out, int64_t *n_items_out, void *workspace,
+                   size_t workspace_bytes, int32_t *dev_status, void *stream);
+
+/*
+ * Token cross-entropy backward from saved statistics:
+ *   dlogits[r, j] = (g_r / T) * exp(z_j - z_y + log p_y)   for j != y,
+ *   dlogits[r, y] = (g_r / T) * expm1(log p_y),
+ * i.e. g_r * (softmax - onehot) / T with the target term in the form that
+ * does not round to zero; ignored rows get a zero row.  g_r = grad_out[r]
+ * (NONE), grad_out[0] (SUM) or grad_out[0] / n_items (MEAN, 0 when
+ * n_items == 0).
+ *
+ * Source: ms-swift PR #10353, "PR information", second bullet (backward
+ * computed directly as g*softmax - g*onehot, zero weight for ignored
+ * labels, a separate gradient buffer); the target term -expm1(log p_t) from
+ * the unsloth-zoo #2080 commit quoted on "Fix softmax collapse ..."
+ * (section "Fix", backward bullet).
+ *
+ *   grad_out    [rows] (NONE) or [1] fp32, device
+ *   saved_logp  [rows] fp32 from ce_fwd's logp_out (same logits, labels, T)
+ *   n_items     [1] int64 from ce_fwd; required for GBCE_MEAN, else ignored
+ *   dlogits     [rows, dlogits_row_stride] of the logits' dtype; must not
+ *               overlap the logits; dlogits_row_stride >= vocab
+ * Errors: GBCE_EINVAL for NULL required pointers, overlap, bad strides or
+ * temperature; bad labels set GBCE_DEV_BAD_LABEL and give a NaN row.
+ */
+gbce_status ce_bwd(const void *logits, gbce_dtype dtype, int64_t rows, int64_t vocab,
+                   int64_t row_stride, const int64_t *labels, int64_t ignore_index,
+                   float temperature, gbce_reduction reduction, const float *grad_out,
+                   const float *saved_logp, const int64_t *n_items, void *dlogits,
+                   int64_t dlogits_row_stride, int32_t *dev_status, void *stream);
+
+/*
+ * Cross-entropy forward and backward in one call: the outputs of ce_fwd
+ * and, with the upstream gradient known in advance, those of ce_bwd.  Each
+ * row's logits are read from HBM once; the gradient pass re-reads them from
+ * on-chip memory or L2.
+ *
+ * Source: as ce_fwd and ce_bwd; taking the gradient in the forward when the
+ * upstream gradient is known follows the fused losses described in the
+ * unsloth-zoo #2079 commit on "Fix softmax collapse ..." ("Summary").
+ *
+ * Arguments as in ce_fwd and ce_bwd; loss_out, dlogits and grad_out are
+ * required, logp_out / lse_out / n_items_out are optional.
+ */
+gbce_status ce_fwd_bwd_fused(const void *logits, gbce_dtype dtype, int64_t rows,
+                             int64_t vocab, int64_t row_stride, const int64_t *labels,
+                             int64_t ignore_index, float temperature,
+                             gbce_reduction reduction, const float *grad_out, float *loss_out,
+                             float *logp_out, float *lse_out, int64_t *n_items_out,
+                             void *dlogits, int64_t dlogits_row_stride, void *workspace,
+                             size_t workspace_bytes, int32_t *dev_status, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GBCE_H */

@@ -1,0 +1,81 @@
+"""Comparison helpers for GPU-vs-oracle parity, with the stated tolerances.
+
+Tolerances (floating point, against the fp64 oracle):
+  log p, element-wise relative: 2e-5 for fp32 logits, 1e-5 for bf16 logits;
+    exactly 0 where the oracle gives exactly 0 (masked rows, V = 1); never > 0.
+  dlogits, per row ||got - ref||_2 / ||ref||_2: 2e-5 fp32, 4e-3 bf16;
+    ignored rows exactly zero.
+  reduced loss, relative: 2e-5.
+  zero-sum rows: |sum_j dx_j| <= tol * sum_j |dx_j| (fp64 host sums), tol
+    1e-5 fp32 / 4e-3 bf16.
+Integer results (item counts, skipped rows) are compared exactly.
+"""
+
+import math
+
+import numpy as np
+import torch
+
+LOGP_TOL = {torch.float32: 2e-5, torch.bfloat16: 1e-5}
+GRAD_TOL = {torch.float32: 2e-5, torch.bfloat16: 4e-3}
+LOSS_TOL = 2e-5
+ZERO_SUM_TOL = {torch.float32: 1e-5, torch.bfloat16: 4e-3}
+
+
+def to_f64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().float().cpu().double().numpy()
+
+
+def assert_logp_close(got, ref, dtype, what="logp"):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    assert np.all(np.isnan(got) == np.isnan(ref)), f"{what}: NaN pattern differs"
+    ok = ~np.isnan(ref)
+    g, r = got[ok], ref[ok]
+    assert np.all(g <= 0.0), f"{what}: positive log p {g.max()}"
+    zero = r == 0.0
+    assert np.all(g[zero] == 0.0), f"{what}: nonzero where the oracle is exactly 0"
+    rel = np.abs(g[~zero] - r[~zero]) / np.abs(r[~zero])
+    tol = LOGP_TOL[dtype]
+    worst = rel.max() if rel.size else 0.0
+    assert worst <= tol, f"{what}: worst relative error {worst:.3e} > {tol:.0e}"
+    return worst
+
+
+def assert_grad_rows_close(got, ref, dtype, what="dlogits"):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape
+    tol = GRAD_TOL[dtype]
+    worst = 0.0
+    for r in range(ref.shape[0]):
+        if np.all(np.isnan(ref[r])):
+            assert np.all(np.isnan(got[r])), f"{what}: row {r} should be NaN"
+            continue
+        nr = np.linalg.norm(ref[r])
+        if nr == 0.0:
+            assert np.all(got[r] == 0.0), f"{what}: row {r} should be exactly zero"
+            continue
+        e = np.linalg.norm(got[r] - ref[r]) / nr
+        worst = max(worst, e)
+        assert e <= tol, f"{what}: row {r} relative error {e:.3e} > {tol:.0e}"
+    return worst
+
+
+def assert_zero_sum_rows(got, dtype, rows=None):
+    got = np.asarray(got, dtype=np.float64)
+    tol = ZERO_SUM_TOL[dtype]
+    for r in (range(got.shape[0]) if rows is None else rows):
+        row = got[r]
+        s_abs = math.fsum(np.abs(row))
+        if s_abs == 0.0:
+            continue
+        assert abs(math.fsum(row)) <= tol * s_abs, f"row {r}: gradient does not sum to zero"
+
+
+def assert_loss_close(got: float, ref: float, what="loss"):
+    if ref == 0.0:
+        assert got == 0.0, f"{what}: {got} != 0"
+        return
+    assert abs(got - ref) <= LOSS_TOL * abs(ref), f"{what}: {got} vs {ref}"

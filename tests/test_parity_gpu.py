@@ -1,0 +1,376 @@
+"""GPU parity: the CUDA library through its C ABI against the fp64 oracle.
+
+Inputs are the seeded workloads; the oracle sees exact fp64 copies of the
+same bf16/fp32 logits.  Tolerances are in tests/helpers.py.
+"""
+
+import hashlib
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from helpers import (assert_grad_rows_close, assert_logp_close, assert_loss_close,
+                     assert_zero_sum_rows, to_f64)
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    import cross_entropy_gb300 as gbce
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    import __graft_entry__
+
+    __graft_entry__.build()
+    gbce.load_library()
+
+
+def new_status():
+    return torch.zeros(1, dtype=torch.int32, device=DEV)
+
+
+def run_all(w: workloads.Workload, temperature=None, reduction=None, grad_out=None,
+            rows_sel=None):
+    """Every entry point on one workload; oracle on `rows_sel` (default all rows)."""
+    T = w.temperature if temperature is None else temperature
+    red = w.reduction if reduction is None else reduction
+    g = w.grad_out if grad_out is None else grad_out
+    x = w.logits.to(DEV)
+    lab = w.labels.to(DEV)
+    status = new_status()
+    res = {}
+    res["logp_sel"] = gbce.selective_logsoftmax(
+        x, w.index.to(DEV), T, None if w.row_mask is None else w.row_mask.to(DEV),
+        dev_status=status)
+    fwd = gbce.ce_fwd(x, lab, temperature=T, reduction=red, want_lse=True, dev_status=status)
+    res["fwd"] = fwd
+    res["bwd"] = gbce.ce_bwd(x, lab, g.to(DEV), fwd.logp, fwd.n_items, temperature=T,
+                             reduction=red, dev_status=status)
+    res["fused"] = gbce.ce_fwd_bwd_fused(x, lab, g.to(DEV), temperature=T, reduction=red,
+                                         want_lse=True, dev_status=status)
+    torch.cuda.synchronize()
+    res["status"] = int(status.item())
+
+    sel = np.arange(w.rows) if rows_sel is None else np.asarray(rows_sel)
+    x64 = workloads.to_numpy_f64(w.logits[torch.as_tensor(sel)])
+    lab_np = w.labels.cpu().numpy()
+    mask_np = None if w.row_mask is None else w.row_mask.cpu().numpy()[sel]
+    ref_lp, _ = oracle.selective_logsoftmax(x64, w.index.cpu().numpy()[sel], T, mask_np)
+    n_full = int((lab_np != workloads.IGNORE_INDEX).sum())
+    g_np = g.cpu().double().numpy()
+    if red == "none":
+        g_rows = g_np[sel]
+    elif red == "sum":
+        g_rows = np.full(len(sel), g_np[0])
+    else:
+        g_rows = np.full(len(sel), g_np[0] / n_full if n_full else 0.0)
+    ref = oracle.cross_entropy(x64, lab_np[sel], temperature=T, reduction="none",
+                               grad_out=g_rows)
+    ref["n_full"] = n_full
+    return res, ref, sel
+
+
+def check_all(w, res, ref, sel, reduction=None, check_scalar_vs_oracle=True, T=None):
+    dt = w.logits.dtype
+    red = w.reduction if reduction is None else reduction
+    T = w.temperature if T is None else T
+    assert res["status"] == 0
+    assert_logp_close(to_f64(res["logp_sel"])[sel], ref_logp_sel(w, sel, T), dt, "selective")
+    fwd, fused = res["fwd"], res["fused"]
+    assert int(fwd.n_items.item()) == ref["n_full"] == int(fused.n_items.item())
+    for name, lp in (("ce_fwd logp", fwd.logp), ("fused logp", fused.logp)):
+        assert_logp_close(to_f64(lp)[sel], ref["logp"], dt, name)
+    live = w.labels.cpu().numpy()[sel] != workloads.IGNORE_INDEX
+    lse = to_f64(fwd.lse)[sel]
+    assert np.all(lse[~live] == 0.0)
+    lse_ref = workloads.to_numpy_f64(w.logits[torch.as_tensor(sel)])[
+        np.arange(len(sel)), np.where(live, w.labels.cpu().numpy()[sel], 0)] / \
+        oracle.exact_temperature(T) - ref["logp"]
+    np.testing.assert_allclose(lse[live], lse_ref[live], rtol=2e-6, atol=2e-6)
+    # per-row losses and the reduced loss
+    if red == "none":
+        assert_logp_close(-to_f64(fwd.loss)[sel], -ref["loss_rows"], dt, "loss rows")
+        assert_logp_close(-to_f64(fused.loss)[sel], -ref["loss_rows"], dt, "fused loss rows")
+    else:
+        lp_all = to_f64(fwd.logp)
+        total = -np.sum(lp_all)
+        want = total if red == "sum" else (total / ref["n_full"] if ref["n_full"] else 0.0)
+        assert_loss_close(float(fwd.loss.item()), want, "ce_fwd loss vs its rows")
+        assert_loss_close(float(fused.loss.item()), want, "fused loss vs its rows")
+        if check_scalar_vs_oracle and len(sel) == w.rows:
+            s = float(np.sum(ref["loss_rows"]))
+            want_o = s if red == "sum" else (s / ref["n_full"] if ref["n_full"] else 0.0)
+            assert_loss_close(float(fused.loss.item()), want_o, "fused loss vs oracle")
+    for name, d in (("ce_bwd", res["bwd"]), ("fused", fused.dlogits)):
+        got = to_f64(d[torch.as_tensor(sel, device=d.device)])
+        assert_grad_rows_close(got, ref["dlogits"], dt, name)
+        assert_zero_sum_rows(got, dt)
+
+
+def ref_logp_sel(w, sel, T):
+    mask = None if w.row_mask is None else w.row_mask.cpu().numpy()[sel]
+    out, _ = oracle.selective_logsoftmax(workloads.to_numpy_f64(w.logits[torch.as_tensor(sel)]),
+                                         w.index.cpu().numpy()[sel], T, mask)
+    return out
+
+
+# ------------------------------------------------------------ the workloads
+
+def test_ce_small_fp32_64x4096():
+    w = workloads.ce_small_fp32()
+    res, ref, sel = run_all(w)
+    check_all(w, res, ref, sel)
+    # the 20-margin rows keep a nonzero, negative target gradient
+    d = to_f64(res["fused"].dlogits)
+    lab = w.labels.numpy()
+    for r in w.peaked_rows.numpy():
+        assert d[r, lab[r]] < 0.0
+
+
+def test_ce_sparse_bf16_1922x4096():
+    w = workloads.ce_sparse_bf16()
+    res, ref, sel = run_all(w)
+    check_all(w, res, ref, sel, reduction="none")
+    live = w.labels.numpy() != workloads.IGNORE_INDEX
+    fused = res["fused"]
+    assert int(fused.n_items.item()) == 256
+    d = fused.dlogits
+    assert torch.all(d[torch.as_tensor(~live, device=DEV)] == 0)
+    # upstream weight 1/256 with reduction none == mean with upstream 1
+    mean = gbce.ce_fwd_bwd_fused(w.logits.to(DEV), w.labels.to(DEV), torch.ones(1),
+                                 reduction="mean")
+    assert torch.equal(mean.dlogits, d)
+    assert_loss_close(float(mean.loss.item()), float(fused.loss.sum().item()))
+
+
+@pytest.mark.parametrize("T", [1.0, 0.9])
+def test_logp_bf16_1024x32768(T):
+    w = workloads.logp_bf16()
+    x = w.logits.to(DEV)
+    status = new_status()
+    got = gbce.selective_logsoftmax(x, w.index.to(DEV), T, w.row_mask.to(DEV),
+                                    dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref, _ = oracle.selective_logsoftmax(workloads.to_numpy_f64(w.logits), w.index.numpy(), T,
+                                         w.row_mask.numpy())
+    g = to_f64(got)
+    assert_logp_close(g, ref, torch.bfloat16)
+    masked = w.row_mask.numpy() == 0
+    assert masked.sum() == 154 and np.all(g[masked] == 0.0)
+
+
+def sample_rows(w, n_plain=24, seed=0):
+    rng = np.random.default_rng(seed)
+    rows = set(rng.choice(w.rows, size=n_plain, replace=False).tolist())
+    if w.peaked_rows is not None:
+        pk = w.peaked_rows.cpu().numpy()
+        rows |= set(rng.choice(pk, size=min(24, len(pk)), replace=False).tolist())
+    rows |= {0, w.rows - 1}
+    return np.array(sorted(rows))
+
+
+def test_grpo_bf16_8192x152064_k4_full_size():
+    """Full size, launch configuration of the benchmark; oracle on sampled rows."""
+    w = workloads.grpo_bf16(device=DEV)
+    sel = sample_rows(w)
+    res, ref, sel = run_all(w, rows_sel=sel)
+    check_all(w, res, ref, sel)
+    # invariants on every row
+    lp = res["logp_sel"]
+    assert bool(torch.all(lp <= 0)) and bool(torch.all(torch.isfinite(lp)))
+    fused = res["fused"]
+    assert int(fused.n_items.item()) == w.rows
+    d = fused.dlogits
+    lab = w.labels.to(DEV)
+    tgt = d.gather(1, lab[:, None])[:, 0].float()
+    assert bool(torch.all(tgt < 0)), "every row keeps a negative target gradient"
+    rowsum = d.double().sum(dim=1)
+    rowabs = d.double().abs().sum(dim=1)
+    assert bool(torch.all(rowsum.abs() <= 4e-3 * rowabs))
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_collapse_stress_2048x151936_full_size(dtype):
+    w = workloads.collapse_stress(dtype=dtype, device=DEV)
+    sel = sample_rows(w, n_plain=32, seed=1)
+    res, ref, sel = run_all(w, rows_sel=sel)
+    check_all(w, res, ref, sel)
+    fused = res["fused"]
+    live = (w.labels != workloads.IGNORE_INDEX)
+    assert int(fused.n_items.item()) == int(live.sum().item()) == 2048 - 205
+    # logp <= 0 and nonzero on every confident row; target gradient nonzero
+    lp = fused.logp
+    assert bool(torch.all(lp <= 0))
+    pk = w.peaked_rows
+    assert bool(torch.all(lp[pk] < 0)), "a confident row collapsed to log p = 0"
+    tgt = fused.dlogits[pk, w.labels[pk]].float()
+    assert bool(torch.all(tgt < 0)), "a confident row lost its target gradient"
+    d = fused.dlogits.double()
+    tol = 1e-5 if dtype == torch.float32 else 4e-3
+    rows_live = live.nonzero()[:, 0]
+    assert bool(torch.all(d[rows_live].sum(1).abs() <= tol * d[rows_live].abs().sum(1)))
+    assert bool(torch.all(d[~live] == 0))
+
+
+# ------------------------------------------------------------ edge cases
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("V", [1, 2, 7, 1003, 4099, 40001])
+def test_odd_vocab_sizes(dtype, V):
+    rows = 37
+    w = workloads.collapse_stress(dtype=dtype, rows=rows, V=max(V, 4), seed=V)
+    if V < 4:
+        x = torch.randn((rows, V), generator=torch.Generator().manual_seed(V)).to(dtype)
+        lab = torch.randint(0, V, (rows,), generator=torch.Generator().manual_seed(V + 1))
+        lab[::5] = workloads.IGNORE_INDEX
+        w.logits, w.labels = x, lab
+        w.index = torch.where(lab < 0, 0, lab)[:, None]
+        w.row_mask = (lab >= 0).to(torch.uint8)
+    res, ref, sel = run_all(w, temperature=0.7)
+    check_all(w, res, ref, sel, T=0.7)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_strided_misaligned_rows_and_unaligned_dlogits(dtype):
+    g = torch.Generator().manual_seed(5)
+    rows, V = 29, 5000
+    big = torch.randn((rows, V + 13), generator=g).mul(3).to(dtype)
+    x_cpu = big[:, 3:3 + V]            # row starts 6 or 12 bytes past 16-byte boundaries
+    lab = torch.randint(0, V, (rows,), generator=g)
+    lab[4] = workloads.IGNORE_INDEX
+    x = big.to(DEV)[:, 3:3 + V]
+    assert x.stride(0) == V + 13
+    ref = oracle.cross_entropy(workloads.to_numpy_f64(x_cpu), lab.numpy(), temperature=0.9,
+                               reduction="sum", grad_out=[0.5])
+    # dlogits with a different 16-byte phase than the logits (scalar-store path)
+    dbig = torch.empty((rows, V + 1), dtype=dtype, device=DEV)
+    d = dbig[:, 1:]
+    out = gbce.ce_fwd_bwd_fused(x, lab.to(DEV), torch.tensor([0.5]), temperature=0.9,
+                                reduction="sum", dlogits=d)
+    d2 = gbce.ce_bwd(x, lab.to(DEV), torch.tensor([0.5]), out.logp, out.n_items,
+                     temperature=0.9, reduction="sum")
+    torch.cuda.synchronize()
+    assert_logp_close(to_f64(out.logp), ref["logp"], dtype)
+    assert_grad_rows_close(to_f64(d), ref["dlogits"], dtype, "fused, unaligned dlogits")
+    assert_grad_rows_close(to_f64(d2), ref["dlogits"], dtype, "ce_bwd")
+    assert_loss_close(float(out.loss.item()), ref["loss"])
+
+
+@pytest.mark.parametrize("rows", [1, 3, 100])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_few_rows_split_vocab(rows, dtype):
+    """Few rows with a large vocabulary take the split partial + combine path."""
+    w = workloads.collapse_stress(dtype=dtype, rows=rows, V=152064, seed=rows)
+    res, ref, sel = run_all(w, temperature=0.9)
+    check_all(w, res, ref, sel, T=0.9)
+
+
+def test_topk_duplicates_and_k16():
+    g = torch.Generator().manual_seed(8)
+    rows, V = 40, 9000
+    x_cpu = torch.randn((rows, V), generator=g).mul(2).to(torch.bfloat16)
+    idx = torch.randint(0, V, (rows, 16), generator=g)
+    idx[:, 5] = idx[:, 2]                # duplicates
+    idx[3, :] = 17                       # all the same column
+    x_cpu[7, idx[7, 0]] = 60.0           # a confident gathered column
+    mask = torch.ones(rows, dtype=torch.uint8)
+    mask[11] = 0
+    for K in (16, 4, 1):
+        got = gbce.selective_logsoftmax(x_cpu.to(DEV), idx[:, :K].to(DEV), 0.9, mask.to(DEV))
+        ref, _ = oracle.selective_logsoftmax(workloads.to_numpy_f64(x_cpu), idx[:, :K].numpy(),
+                                             0.9, mask.numpy())
+        g64 = to_f64(got)
+        assert_logp_close(g64, ref, torch.bfloat16, f"K={K}")
+        if K == 16:
+            assert np.all(g64[:, 5] == g64[:, 2])
+            assert np.all(g64[3] == g64[3, 0])
+
+
+def test_all_ignored_and_mean_is_zero():
+    x = torch.randn((9, 300), device=DEV)
+    lab = torch.full((9,), -100, device=DEV)
+    out = gbce.ce_fwd_bwd_fused(x, lab, torch.ones(1), reduction="mean")
+    fwd = gbce.ce_fwd(x, lab, reduction="mean")
+    torch.cuda.synchronize()
+    assert out.loss.item() == 0.0 and fwd.loss.item() == 0.0
+    assert int(out.n_items.item()) == 0
+    assert bool(torch.all(out.dlogits == 0))
+
+
+def test_empty_batch():
+    x = torch.empty((0, 128), device=DEV)
+    lab = torch.empty((0,), dtype=torch.int64, device=DEV)
+    out = gbce.ce_fwd_bwd_fused(x, lab, torch.ones(1), reduction="mean")
+    lp = gbce.selective_logsoftmax(x, lab[:, None], 1.0)
+    torch.cuda.synchronize()
+    assert out.loss.item() == 0.0 and int(out.n_items.item()) == 0 and lp.numel() == 0
+
+
+def test_bad_labels_and_indices_are_reported_not_trapped():
+    x = torch.randn((6, 500), device=DEV)
+    lab = torch.tensor([1, 500, -3, -100, 2, 499], device=DEV)
+    status = new_status()
+    out = gbce.ce_fwd_bwd_fused(x, lab, torch.ones(1), reduction="sum", dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & gbce.DEV_BAD_LABEL
+    lp = out.logp.cpu()
+    assert torch.isnan(lp[1]) and torch.isnan(lp[2]) and lp[3] == 0
+    assert torch.isfinite(lp[[0, 4, 5]]).all()
+    assert torch.isnan(out.dlogits[1]).all() and (out.dlogits[3] == 0).all()
+    status.zero_()
+    idx = torch.tensor([[0, 3], [600, 1], [2, -1], [4, 4], [5, 6], [7, 8]], device=DEV)
+    got = gbce.selective_logsoftmax(x, idx, 1.0, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == gbce.DEV_BAD_INDEX
+    g = got.cpu()
+    assert torch.isnan(g[1, 0]) and torch.isnan(g[2, 1]) and torch.isfinite(g[1, 1])
+    # the context is still usable
+    assert float(torch.ones(1, device=DEV).sum().item()) == 1.0
+
+
+def test_repeatable_bytes_and_inputs_untouched():
+    w = workloads.collapse_stress(dtype=torch.bfloat16, rows=600, V=32000, seed=4)
+    x = w.logits.to(DEV)
+    lab = w.labels.to(DEV)
+    h0 = hashlib.sha256(x.view(torch.int16).cpu().numpy().tobytes()).hexdigest()
+    a = gbce.ce_fwd_bwd_fused(x, lab, torch.ones(1), temperature=0.9)
+    b = gbce.ce_fwd_bwd_fused(x, lab, torch.ones(1), temperature=0.9)
+    fwd = gbce.ce_fwd(x, lab, temperature=0.9)
+    d1 = gbce.ce_bwd(x, lab, torch.ones(1), fwd.logp, fwd.n_items, temperature=0.9)
+    d2 = gbce.ce_bwd(x, lab, torch.ones(1), fwd.logp, fwd.n_items, temperature=0.9)
+    torch.cuda.synchronize()
+    assert torch.equal(a.dlogits, b.dlogits) and torch.equal(a.loss, b.loss)
+    assert torch.equal(d1, d2)
+    assert torch.equal(fwd.loss, a.loss)
+    h1 = hashlib.sha256(x.view(torch.int16).cpu().numpy().tobytes()).hexdigest()
+    assert h0 == h1, "logits were modified"
+
+
+def test_three_d_logits_flatten():
+    x = torch.randn((2, 5, 700), device=DEV, dtype=torch.bfloat16)
+    idx = torch.randint(0, 700, (2, 5), device=DEV)
+    got = gbce.selective_logsoftmax(x, idx, 1.0)
+    assert got.shape == (2, 5)
+    ref, _ = oracle.selective_logsoftmax(workloads.to_numpy_f64(x.reshape(10, 700)),
+                                         idx.reshape(10, 1).cpu().numpy(), 1.0)
+    assert_logp_close(to_f64(got).reshape(10, 1), ref, torch.bfloat16)
+
+
+def test_stream_argument_is_honoured():
+    s = torch.cuda.Stream()
+    w = workloads.ce_small_fp32(device=DEV)
+    with torch.cuda.stream(s):
+        out = gbce.ce_fwd_bwd_fused(w.logits, w.labels, torch.ones(1, device=DEV))
+    s.synchronize()
+    ref = oracle.cross_entropy(workloads.to_numpy_f64(w.logits), w.labels.cpu().numpy(),
+                               reduction="mean")
+    assert_loss_close(float(out.loss.item()), ref["loss"])
