@@ -49,8 +49,11 @@ FALLBACK_HBM_GBS = 6800.0
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "fused_ce_bf16_8192x152064.txt")
 
 
-def algorithmic_bytes(rows=ROWS, vocab=VOCAB, k=K, esize=2):
-    """Bytes each op must move at least once (SURVEY's per-unit figures x rows)."""
+def algorithmic_bytes(rows=None, vocab=VOCAB, k=K, esize=2):
+    """Bytes each op must move at least once: per row, the logits read once per
+    op, the dlogits row written once, the K indices, the label and the K fp32
+    log-probs."""
+    rows = ROWS if rows is None else rows
     logits = rows * vocab * esize
     logp = logits + rows * k * 8 + rows * k * 4          # logits + index + fp32 out
     ce = 2 * logits + rows * 8                           # logits in, dlogits out, labels
@@ -220,7 +223,7 @@ def run_reference(args):
 
     oracle.build()
     dev = "cuda:0" if torch.cuda.is_available() else "cpu"
-    w = workloads.grpo_bf16(device=dev, seed=0)
+    w = workloads.grpo_bf16(device=dev, seed=0, rows=ROWS)
     total_steps = args.steps + args.warmup
     budget = 150.0 / max(total_steps, 1)          # whole run within a few minutes
     n_rows = oracle_rows_for(min(budget, 10.0), w)
@@ -266,7 +269,7 @@ def run_gbce(args):
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    w = workloads.grpo_bf16(device=dev, seed=rank)
+    w = workloads.grpo_bf16(device=dev, seed=rank, rows=ROWS)
     x, idx, lab = w.logits, w.index, w.labels
     grad = torch.ones(1, device=dev)
     logp_out = torch.empty((ROWS, K), dtype=torch.float32, device=dev)
@@ -325,7 +328,7 @@ def run_gbce(args):
     traffic = profiled_traffic()
 
     # ---- end to end through the public API: host inputs in, results out
-    e2e = run_e2e(gbce, w, dev, stream, args, world)
+    e2e = None if args.no_e2e else run_e2e(gbce, w, dev, stream, args, world)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -415,13 +418,18 @@ def cpu_baseline(w):
 
 
 def main():
+    global ROWS
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gbce", "reference"], default="gbce")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--rows", type=int, default=ROWS,
+                    help="rows of the workload (a smaller case for profiling captures)")
     args = ap.parse_args()
+    ROWS = args.rows
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

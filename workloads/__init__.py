@@ -174,7 +174,7 @@ def collapse_stress(dtype=torch.float32, device="cpu", seed: int = 0, rows: int 
     logits = _normal(rows, V, 1.0, dtype, g, device)
     labels = torch.randint(0, V, (rows,), generator=g, device=device)
     perm = torch.randperm(rows, generator=g, device=device)
-    n_ign = (rows * 10 + 5) // 100
+    n_ign = (rows * 10 + 50) // 100          # round(10% of rows): 205 of 2048
     n_peak = rows // 2
     ignored, peaked = perm[:n_ign], perm[n_ign:n_ign + n_peak]
     levels = torch.tensor([17.0, 20.0, 30.0, 50.0], device=device)
