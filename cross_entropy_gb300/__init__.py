@@ -49,6 +49,8 @@ _SIGNATURES = {
                       _i64, _vp, _vp]),
     "ce_fwd_bwd_fused": (_i32, [_vp, _i32, _i64, _i64, _i64, _vp, _i64, _f32, _i32, _vp, _vp,
                                 _vp, _vp, _vp, _vp, _i64, _vp, _sz, _vp, _vp]),
+    "ce_fwd_bwd_fused_noalloc": (_i32, [_vp, _i32, _i64, _i64, _i64, _vp, _i64, _f32, _i32,
+                                        _vp, _vp, _vp, _vp, _vp, _vp, _i64, _vp, _vp]),
 }
 
 _lib = None
@@ -269,3 +271,39 @@ def ce_fwd_bwd_fused(logits: torch.Tensor, labels, grad_out=None, ignore_index: 
                               _stream_ptr(stream))
     _check(st, "ce_fwd_bwd_fused")
     return CeFused(loss if red == 0 else loss[0], dlogits, logp, lse, n_items[0])
+
+
+def ce_fwd_bwd_fused_noalloc(logits: torch.Tensor, labels, grad_out=None,
+                             ignore_index: int = -100, temperature: float = 1.0,
+                             reduction: str = "mean", *, dlogits: Optional[torch.Tensor] = None,
+                             dev_status: Optional[torch.Tensor] = None, stream=None) -> CeFused:
+    """ce_fwd_bwd_fused with the library's built-in scratch instead of a workspace.
+
+    For callers that cannot supply scratch memory (see include/gbce.h).  The
+    outputs allocated here are the caller's, as with every other call; the
+    library itself allocates nothing.  Calls whose GPU work overlaps share the
+    built-in scratch and race.
+    """
+    lib = load_library()
+    x = _rows_view(logits)
+    rows, V = x.shape
+    lab = _dev_int64(labels, x.device).reshape(rows)
+    red = REDUCTIONS[reduction]
+    if grad_out is None:
+        grad_out = torch.ones(rows if red == 0 else 1)
+    g = torch.as_tensor(grad_out, dtype=torch.float32, device=x.device).reshape(-1).contiguous()
+    if g.numel() != (rows if red == 0 else 1):
+        raise ValueError("grad_out must have one entry per row for 'none', one otherwise")
+    loss = torch.empty((rows,) if red == 0 else (1,), dtype=torch.float32, device=x.device)
+    logp = torch.empty(rows, dtype=torch.float32, device=x.device)
+    n_items = torch.empty(1, dtype=torch.int64, device=x.device)
+    if dlogits is None:
+        dlogits = torch.empty((rows, V), dtype=x.dtype, device=x.device)
+    d = _rows_view(dlogits)
+    st = lib.ce_fwd_bwd_fused_noalloc(x.data_ptr(), _dtype_code(x), rows, V, x.stride(0),
+                                      lab.data_ptr(), int(ignore_index), float(temperature), red,
+                                      g.data_ptr(), loss.data_ptr(), logp.data_ptr(), None,
+                                      n_items.data_ptr(), d.data_ptr(), d.stride(0),
+                                      _ptr(dev_status), _stream_ptr(stream))
+    _check(st, "ce_fwd_bwd_fused_noalloc")
+    return CeFused(loss if red == 0 else loss[0], dlogits, logp, None, n_items[0])

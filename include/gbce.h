@@ -193,6 +193,37 @@ gbce_status ce_fwd_bwd_fused(const void *logits, gbce_dtype dtype, int64_t rows,
                              void *dlogits, int64_t dlogits_row_stride, void *workspace,
                              size_t workspace_bytes, int32_t *dev_status, void *stream);
 
+/*
+ * ce_fwd_bwd_fused without a caller workspace and without any allocation.
+ *
+ * The pages have no counterpart: this exists for callers that cannot provide
+ * scratch memory -- a C program or plugin without a device allocator of its
+ * own, which must not call cudaMalloc on its hot path (cudaMalloc can
+ * synchronize the device, and next to a framework's caching allocator it can
+ * fail or fragment memory).  The scratch is a fixed array of
+ * GBCE_NOALLOC_SCRATCH_BYTES bytes inside the library's device image, held on
+ * every GPU that loads the library until the process exits.
+ *
+ * Arguments and results are those of ce_fwd_bwd_fused minus the workspace.
+ * Returns GBCE_EWORKSPACE, before any GPU work, when
+ * gbce_workspace_size(rows, vocab, 1) > GBCE_NOALLOC_SCRATCH_BYTES (about
+ * 130 000 rows at large vocabularies).  The first call on each device looks
+ * up the array's device address (cudaGetSymbolAddress) with that device
+ * current; make that first call before any stream capture.  All calls share
+ * the one array: calls whose GPU work overlaps (e.g. on two streams) race and
+ * must be serialized by the caller.  Nothing in the array needs zeroing:
+ * each call writes every scratch value before reading it.
+ */
+#define GBCE_NOALLOC_SCRATCH_BYTES (1u << 20)
+gbce_status ce_fwd_bwd_fused_noalloc(const void *logits, gbce_dtype dtype, int64_t rows,
+                                     int64_t vocab, int64_t row_stride, const int64_t *labels,
+                                     int64_t ignore_index, float temperature,
+                                     gbce_reduction reduction, const float *grad_out,
+                                     float *loss_out, float *logp_out, float *lse_out,
+                                     int64_t *n_items_out, void *dlogits,
+                                     int64_t dlogits_row_stride, int32_t *dev_status,
+                                     void *stream);
+
 #ifdef __cplusplus
 }
 #endif
