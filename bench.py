@@ -160,8 +160,16 @@ def dist_setup():
         import torch.distributed as dist
 
         os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
-        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+        backend = os.environ.get("GBCE_DIST_BACKEND") or (
+            "nccl" if torch.cuda.is_available() else "gloo")
+        dist.init_process_group(backend)
     return world, rank, local
+
+
+def aggregate_gbs(world: int, bytes_per_step: int, steps: int, max_ms: float) -> float:
+    """Whole-job GB/s: every rank moves bytes_per_step per step (weak scaling),
+    over the slowest rank's time."""
+    return world * bytes_per_step * steps / (max_ms * 1e-3) / 1e9
 
 
 def max_over_ranks(x: float, world: int, device) -> float:
@@ -320,7 +328,7 @@ def run_gbce(args):
 
     nbytes = algorithmic_bytes()
     ms_per_step = total_ms / args.steps
-    value = world * nbytes["step"] * args.steps / (total_ms * 1e-3) / 1e9
+    value = aggregate_gbs(world, nbytes["step"], args.steps, total_ms)
     peak, peak_kind = measured_peak()
     ce_avg = statistics.mean(ce_ms)
     lp_avg = statistics.mean(logp_ms)
@@ -398,7 +406,7 @@ def run_e2e(gbce, w, dev, stream, args, world):
     ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
     h2d = h_x.numel() * h_x.element_size() + h_idx.numel() * 8 + h_lab.numel() * 8
     d2h = h_logp.numel() * 4 + 4
-    value = world * algorithmic_bytes()["step"] * steps / (ms * 1e-3) / 1e9
+    value = aggregate_gbs(world, algorithmic_bytes()["step"], steps, ms)
     del h_x, d_x, dlogits
     return {"value": value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "steps": steps, "ms_per_step": ms / steps}

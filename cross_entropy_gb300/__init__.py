@@ -27,7 +27,9 @@ from typing import NamedTuple, Optional
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "_build", "libgbce.so")
+# GBCE_LIBRARY may name another build of the same library (e.g. one built
+# with a different kernel option) to load instead of the in-tree one.
+LIB_PATH = os.environ.get("GBCE_LIBRARY") or os.path.join(_HERE, "_build", "libgbce.so")
 
 GBCE_F32, GBCE_BF16 = 0, 1
 REDUCTIONS = {"none": 0, "sum": 1, "mean": 2}

@@ -56,6 +56,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return done != 0;
 }
 
+// Same, with acquire at cluster scope: for barriers whose transactions are
+// stores from other CTAs of the cluster.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
 __device__ __forceinline__ uint64_t global_timer_ns()
 {
     uint64_t t;
@@ -73,7 +88,25 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
         return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1; it < (1u << 26); ++it) {
+#ifdef GBCE_WAIT_SLEEP_NS  // build option: back off between polls
+        __nanosleep(GBCE_WAIT_SLEEP_NS);
+#endif
         if (mbar_try_wait(bar, parity))
+            return true;
+        if ((it & 63u) == 0 && global_timer_ns() - t0 > 2000000000ull)
+            break;
+    }
+    return false;
+}
+
+// Bounded wait for a barrier completed by peer CTAs' st.async stores.
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity)
+{
+    if (mbar_try_wait_cluster(bar, parity))
+        return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1; it < (1u << 26); ++it) {
+        if (mbar_try_wait_cluster(bar, parity))
             return true;
         if ((it & 63u) == 0 && global_timer_ns() - t0 > 2000000000ull)
             break;
@@ -114,6 +147,68 @@ __device__ __forceinline__ void named_sync(uint32_t id, uint32_t threads)
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
+// ------------------------------------------------------ PTX: thread-block clusters
+
+__device__ __forceinline__ uint32_t cluster_rank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_size()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_index()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_count()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+    return r;
+}
+
+// All threads of all CTAs of the cluster; used once, right after barrier
+// initialisation (whose fence.mbarrier_init makes the barriers visible to
+// the cluster), so that no CTA stores into a peer's shared memory before the
+// peer's mbarriers exist.  Every CTA of a cluster is co-scheduled and
+// reaches it without waiting on any data.  The arrive is relaxed: nothing
+// but the barrier initialisation has to be ordered, and that has its fence.
+__device__ __forceinline__ void cluster_sync_all()
+{
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\t"
+                 "barrier.cluster.wait.aligned;" ::: "memory");
+}
+
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t smem_address, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_address), "r"(rank));
+    return r;
+}
+
+// Store two floats into a peer CTA's shared memory; completion is counted
+// as 8 transaction bytes on the peer's mbarrier at `remote_bar`.
+__device__ __forceinline__ void st_async_pair(uint32_t remote_addr, float a, float b,
+                                              uint32_t remote_bar)
+{
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(
+            remote_addr),
+        "f"(a), "f"(b), "r"(remote_bar)
+        : "memory");
+}
+
 // ---------------------------------------------------------- PTX: global mem
 
 __device__ __forceinline__ uint4 ld_nc_v4(const void *p)
@@ -146,6 +241,70 @@ __device__ __forceinline__ float ex2(float x)
 __device__ __forceinline__ float softplus(float a)
 {
     return fmaxf(a, 0.0f) + log1pf(expf(-fabsf(a)));
+}
+
+// ------------------------------------------------- packed fp32 (sm_100+)
+// Two fp32 lanes per instruction: fma/add/mul.rn.f32x2 on a 64-bit register.
+
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+// Exact max of two packed bf16 pairs (a NaN operand yields the other one).
+__device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+__device__ __forceinline__ float fmax3(float a, float b, float c)
+{
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w)
+{
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+// Round a pair to bf16 (nearest even) and pack it, .x in the low half.
+__device__ __forceinline__ uint32_t float2_to_bf16x2(float2 v)
+{
+    uint32_t d;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(v.y), "f"(v.x));
+    return d;
 }
 
 // Element access for the two logit types.
@@ -203,30 +362,52 @@ template <> struct Elem<__nv_bfloat16> {
 // Online (max, sum) over a stream of logits, in the exp2 domain:
 //   m = max x_j,   s = sum_j 2^{(x_j - m) c},   c = log2(e) / T,
 // so that s = sum_j exp((x_j - m) / T).  Excluded columns are fed as -inf.
+// The sum is kept in two packed pairs (four independent accumulators).
 struct OnlineMaxSum {
     float m = kNegInf;
-    float mc = kNegInf;  // m * c, the shift applied to every term
-    float s = 0.0f;
+    float nmc = __builtin_huge_valf();  // -m * c, the shift added to every x * c
+    float2 sa = make_float2(0.0f, 0.0f);
+    float2 sb = make_float2(0.0f, 0.0f);
 
-    // Fold N values (already target-masked) whose maximum is vmax.
+    // New running maximum `vmax` for the values about to be added; returns
+    // false when there is nothing to add (all of them are -inf).
+    __device__ __forceinline__ bool raise_to(float vmax, float c)
+    {
+        if (vmax > m) {
+            const float f = ex2((m - vmax) * c);
+            const float2 ff = make_float2(f, f);
+            sa = fmul2(sa, ff);
+            sb = fmul2(sb, ff);
+            m = vmax;
+            nmc = -vmax * c;
+        }
+        return vmax != kNegInf;
+    }
+
+    // Add 2^{x c - m c} for the four values of two packed pairs.
+    __device__ __forceinline__ void add_pairs(float2 p, float2 q, float c)
+    {
+        const float2 cc = make_float2(c, c), kk = make_float2(nmc, nmc);
+        const float2 zp = ffma2(p, cc, kk), zq = ffma2(q, cc, kk);
+        sa = fadd2(sa, make_float2(ex2(zp.x), ex2(zp.y)));
+        sb = fadd2(sb, make_float2(ex2(zq.x), ex2(zq.y)));
+    }
+
+    // Fold N unpacked values (masked columns already -inf).
     template <int N>
     __device__ __forceinline__ void add(const float (&f)[N], float vmax, float c)
     {
-        if (vmax > m) {
-            s *= ex2((m - vmax) * c);
-            m = vmax;
-            mc = vmax * c;
-        }
-        if (vmax != kNegInf) {
-            float a = 0.0f, b = 0.0f;
+        if (!raise_to(vmax, c))
+            return;
+        float a = 0.0f, b = 0.0f;
 #pragma unroll
-            for (int i = 0; i < N; i += 2) {
-                a += ex2(fmaf(f[i], c, -mc));
-                if (i + 1 < N)
-                    b += ex2(fmaf(f[i + 1], c, -mc));
-            }
-            s += a + b;
+        for (int i = 0; i < N; i += 2) {
+            a += ex2(fmaf(f[i], c, nmc));
+            if (i + 1 < N)
+                b += ex2(fmaf(f[i + 1], c, nmc));
         }
+        sa.x += a;
+        sb.x += b;
     }
 
     __device__ __forceinline__ void add1(float x, float c)
@@ -234,9 +415,17 @@ struct OnlineMaxSum {
         float f[1] = {x};
         add<1>(f, x, c);
     }
+
+    // The thread's (max, sum) pair.
+    __device__ __forceinline__ float sum() const
+    {
+        return __fadd_rn(__fadd_rn(sa.x, sa.y), __fadd_rn(sb.x, sb.y));
+    }
 };
 
-// Merge two (max, sum) partial states with the same scale c.
+// Merge two (max, sum) partial states with the same scale c.  Exactly
+// commutative (no fused multiply-add), so every lane of a butterfly
+// reduction ends with the same bits.
 __device__ __forceinline__ void merge_max_sum(float &m, float &s, float m2, float s2, float c)
 {
     const float M = fmaxf(m, m2);
@@ -245,7 +434,7 @@ __device__ __forceinline__ void merge_max_sum(float &m, float &s, float m2, floa
         s = 0.0f;
         return;
     }
-    s = s * ex2((m - M) * c) + s2 * ex2((m2 - M) * c);
+    s = __fadd_rn(__fmul_rn(s, ex2((m - M) * c)), __fmul_rn(s2, ex2((m2 - M) * c)));
     m = M;
 }
 

@@ -41,6 +41,7 @@ constexpr int kRowThreads = (kConsumerWarps + 1) * 32;
 constexpr int kRingBytes = kStages * kChunkBytes;
 constexpr int kRingAlign = 128;  // bulk copies need 16-byte aligned shared addresses
 constexpr int kDynSmemBytes = kRingBytes + kRingAlign;
+constexpr int kMaxClusterCtas = 8;  // portable cluster size limit
 
 struct RowGeom {
     int64_t head;   // scalar elements before the first 16-byte boundary
@@ -61,16 +62,6 @@ __device__ __forceinline__ RowGeom row_geom(const T *row, int64_t V)
 }
 
 template <int KMAX>
-__device__ __forceinline__ bool span_has_target(const int32_t (&tg)[KMAX], int32_t col0, int n)
-{
-    bool hit = false;
-#pragma unroll
-    for (int k = 0; k < KMAX; ++k)
-        hit |= static_cast<uint32_t>(tg[k] - col0) < static_cast<uint32_t>(n);
-    return hit;
-}
-
-template <int KMAX>
 __device__ __forceinline__ bool is_target(const int32_t (&tg)[KMAX], int32_t col)
 {
     bool hit = false;
@@ -80,7 +71,30 @@ __device__ __forceinline__ bool is_target(const int32_t (&tg)[KMAX], int32_t col
     return hit;
 }
 
-// Fold one 16-byte vector of logits into the running (max, sum).
+// Index of the 16-byte body vector that holds each target column, or -1
+// when the column is in the scalar head/tail or the slot is unused.
+template <typename T, int KMAX>
+__device__ __forceinline__ void target_vectors(const int32_t (&tg)[KMAX], const RowGeom &g,
+                                               int32_t (&tv)[KMAX])
+{
+    constexpr int VEC = Elem<T>::kVec;
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k)
+        tv[k] = (tg[k] >= g.head && tg[k] < g.tail0) ? static_cast<int32_t>((tg[k] - g.head) / VEC)
+                                                    : -1;
+}
+
+template <int KMAX>
+__device__ __forceinline__ bool vector_has_target(const int32_t (&tv)[KMAX], int32_t v)
+{
+    bool hit = false;
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k)
+        hit |= (tv[k] == v);
+    return hit;
+}
+
+// Fold one 16-byte vector of logits, masking target columns (slow path).
 template <typename T, int KMAX>
 __device__ __forceinline__ void stats_vector(OnlineMaxSum &st, const uint4 &raw, int32_t col0,
                                              const int32_t (&tg)[KMAX], float c)
@@ -88,12 +102,10 @@ __device__ __forceinline__ void stats_vector(OnlineMaxSum &st, const uint4 &raw,
     constexpr int VEC = Elem<T>::kVec;
     float f[VEC];
     Elem<T>::unpack(raw, f);
-    if (span_has_target<KMAX>(tg, col0, VEC)) {
 #pragma unroll
-        for (int e = 0; e < VEC; ++e)
-            if (is_target<KMAX>(tg, col0 + e))
-                f[e] = kNegInf;
-    }
+    for (int e = 0; e < VEC; ++e)
+        if (is_target<KMAX>(tg, col0 + e))
+            f[e] = kNegInf;
     float vmax = f[0];
 #pragma unroll
     for (int e = 1; e < VEC; ++e)
@@ -101,27 +113,188 @@ __device__ __forceinline__ void stats_vector(OnlineMaxSum &st, const uint4 &raw,
     st.add<VEC>(f, vmax, c);
 }
 
-// dlogits of one 16-byte vector: g/T * exp((x_j - x_y)/T + log p), and
-// g/T * expm1(log p) at the label column.
-template <typename T>
-__device__ __forceinline__ uint4 grad_vector(const uint4 &raw, int32_t col0, int32_t y, float xy,
-                                             float c, float kb, float gscale, float dy,
-                                             float (&d)[Elem<T>::kVec])
+// Packed fast paths for vectors that hold no target column.
+template <typename T> struct FastVec;
+
+template <> struct FastVec<__nv_bfloat16> {
+    __device__ static __forceinline__ uint32_t pmax(const uint4 &a)
+    {
+        return bf16x2_max(bf16x2_max(a.x, a.y), bf16x2_max(a.z, a.w));
+    }
+    __device__ static __forceinline__ float unpack_max(uint32_t m)
+    {
+        return fmaxf(__uint_as_float(m << 16), __uint_as_float(m & 0xffff0000u));
+    }
+    __device__ static __forceinline__ float vmax(const uint4 &a) { return unpack_max(pmax(a)); }
+    __device__ static __forceinline__ float vmax(const uint4 &a, const uint4 &b)
+    {
+        return unpack_max(bf16x2_max(pmax(a), pmax(b)));
+    }
+    __device__ static __forceinline__ void add(OnlineMaxSum &st, const uint4 &a, float c)
+    {
+        st.add_pairs(bf16x2_to_float2(a.x), bf16x2_to_float2(a.y), c);
+        st.add_pairs(bf16x2_to_float2(a.z), bf16x2_to_float2(a.w), c);
+    }
+};
+
+template <> struct FastVec<float> {
+    __device__ static __forceinline__ float vmax(const uint4 &a)
+    {
+        return fmaxf(fmax3(__uint_as_float(a.x), __uint_as_float(a.y), __uint_as_float(a.z)),
+                     __uint_as_float(a.w));
+    }
+    __device__ static __forceinline__ float vmax(const uint4 &a, const uint4 &b)
+    {
+        return fmax3(fmax3(__uint_as_float(a.x), __uint_as_float(a.y), __uint_as_float(a.z)),
+                     fmax3(__uint_as_float(a.w), __uint_as_float(b.x), __uint_as_float(b.y)),
+                     fmaxf(__uint_as_float(b.z), __uint_as_float(b.w)));
+    }
+    __device__ static __forceinline__ void add(OnlineMaxSum &st, const uint4 &a, float c)
+    {
+        st.add_pairs(make_float2(__uint_as_float(a.x), __uint_as_float(a.y)),
+                     make_float2(__uint_as_float(a.z), __uint_as_float(a.w)), c);
+    }
+};
+
+// Fold body vectors va (and vb) of a row; col0 = first column of vector 0.
+template <typename T, int KMAX>
+__device__ __forceinline__ void stats_one(OnlineMaxSum &st, const uint4 &a, int32_t va,
+                                          int32_t col0, const int32_t (&tv)[KMAX],
+                                          const int32_t (&tg)[KMAX], float c)
 {
     constexpr int VEC = Elem<T>::kVec;
-    float f[VEC];
-    Elem<T>::unpack(raw, f);
-#pragma unroll
-    for (int e = 0; e < VEC; ++e)
-        d[e] = gscale * ex2(fmaf(f[e] - xy, c, kb));
-    if (static_cast<uint32_t>(y - col0) < static_cast<uint32_t>(VEC)) {
-#pragma unroll
-        for (int e = 0; e < VEC; ++e)
-            if (col0 + e == y)
-                d[e] = dy;
+    if (vector_has_target<KMAX>(tv, va)) {
+        stats_vector<T, KMAX>(st, a, col0 + va * VEC, tg, c);
+        return;
     }
-    return Elem<T>::pack(d);
+    if (st.raise_to(FastVec<T>::vmax(a), c))
+        FastVec<T>::add(st, a, c);
 }
+
+template <typename T, int KMAX>
+__device__ __forceinline__ void stats_two(OnlineMaxSum &st, const uint4 &a, const uint4 &b,
+                                          int32_t va, int32_t vb, int32_t col0,
+                                          const int32_t (&tv)[KMAX], const int32_t (&tg)[KMAX],
+                                          float c)
+{
+    constexpr int VEC = Elem<T>::kVec;
+    if (vector_has_target<KMAX>(tv, va) || vector_has_target<KMAX>(tv, vb)) {
+        stats_vector<T, KMAX>(st, a, col0 + va * VEC, tg, c);
+        stats_vector<T, KMAX>(st, b, col0 + vb * VEC, tg, c);
+        return;
+    }
+    if (st.raise_to(FastVec<T>::vmax(a, b), c)) {
+        FastVec<T>::add(st, a, c);
+        FastVec<T>::add(st, b, c);
+    }
+}
+
+// Per-row constants of the gradient pass.  The exponent carries an offset
+// of +32 that g/T takes back as 2^-32, so that entries far below 2^-126
+// (confident rows) come out as exact fp32 subnormals although ex2 itself
+// flushes subnormal results; |g/T| < 2^-90 skips the offset.
+struct GradConsts {
+    float nxy;  // -x_y
+    float c;    // log2(e) / T
+    float kb;   // log p * log2(e) + offset
+    float kbx;  // kb - x_y * c: the bf16 path's exponent is x * c + kbx
+    float gs;   // g / T * 2^-offset
+    float dy;   // g / T * expm1(log p), the label column
+};
+
+__device__ __forceinline__ GradConsts grad_consts(float xy, float c, float logp, float gscale)
+{
+    const bool offset = fabsf(gscale) >= 0x1p-90f;
+    GradConsts k;
+    k.nxy = -xy;
+    k.c = c;
+    k.kb = fmaf(logp, kLog2e, offset ? 32.0f : 0.0f);
+    k.kbx = fmaf(-xy, c, k.kb);
+    k.gs = offset ? gscale * 0x1p-32f : gscale;
+    k.dy = gscale * expm1f(logp);
+    return k;
+}
+
+// dlogits of one element j != y: g/T * exp((x_j - x_y)/T + log p).
+__device__ __forceinline__ float grad_scalar(float x, const GradConsts &k)
+{
+    return k.gs * ex2(fmaf(x + k.nxy, k.c, k.kb));
+}
+
+// dlogits of one 16-byte vector.  yoff = label column - first column of
+// the vector; only the one vector of a row that holds the label (unsigned
+// yoff < VEC) takes the patch branch.  run() returns the packed vector;
+// run_unpacked() the fp32 values, for stores that cannot be 16-byte.
+template <typename T> struct GradVec;
+
+template <> struct GradVec<__nv_bfloat16> {
+    // bf16 logits are exact in fp32 and |x c| is small, so x c + (kb - x_y c)
+    // in one fused multiply-add stays within a few fp32 ulps of the exponent.
+    __device__ static __forceinline__ uint4 run(const uint4 &raw, int32_t yoff, const GradConsts &k)
+    {
+        const float2 cc = make_float2(k.c, k.c), kk = make_float2(k.kbx, k.kbx);
+        const float2 gg = make_float2(k.gs, k.gs);
+        const auto one = [&](uint32_t w) {
+            const float2 z = ffma2(bf16x2_to_float2(w), cc, kk);
+            return float2_to_bf16x2(fmul2(make_float2(ex2(z.x), ex2(z.y)), gg));
+        };
+        uint4 o = make_uint4(one(raw.x), one(raw.y), one(raw.z), one(raw.w));
+        if (static_cast<uint32_t>(yoff) < 8u) {
+            const uint32_t dyb = __bfloat16_as_ushort(__float2bfloat16_rn(k.dy));
+            const bool hi = (yoff & 1) != 0;
+            const auto patch = [&](uint32_t v) {
+                return hi ? ((v & 0x0000ffffu) | (dyb << 16)) : ((v & 0xffff0000u) | dyb);
+            };
+            const int pair = yoff >> 1;
+            o.x = pair == 0 ? patch(o.x) : o.x;
+            o.y = pair == 1 ? patch(o.y) : o.y;
+            o.z = pair == 2 ? patch(o.z) : o.z;
+            o.w = pair == 3 ? patch(o.w) : o.w;
+        }
+        return o;
+    }
+    __device__ static __forceinline__ void run_unpacked(const uint4 &raw, int32_t yoff,
+                                                        const GradConsts &k, float (&d)[8])
+    {
+        float f[8];
+        Elem<__nv_bfloat16>::unpack(raw, f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            d[e] = (e == yoff) ? k.dy : k.gs * ex2(fmaf(f[e], k.c, k.kbx));
+    }
+};
+
+template <> struct GradVec<float> {
+    __device__ static __forceinline__ uint4 run(const uint4 &raw, int32_t yoff, const GradConsts &k)
+    {
+        const float2 nn = make_float2(k.nxy, k.nxy), cc = make_float2(k.c, k.c);
+        const float2 kk = make_float2(k.kb, k.kb), gg = make_float2(k.gs, k.gs);
+        const float2 p0 = make_float2(__uint_as_float(raw.x), __uint_as_float(raw.y));
+        const float2 p1 = make_float2(__uint_as_float(raw.z), __uint_as_float(raw.w));
+        const float2 z0 = ffma2(fadd2(p0, nn), cc, kk), z1 = ffma2(fadd2(p1, nn), cc, kk);
+        const float2 d0 = fmul2(make_float2(ex2(z0.x), ex2(z0.y)), gg);
+        const float2 d1 = fmul2(make_float2(ex2(z1.x), ex2(z1.y)), gg);
+        uint4 o = make_uint4(__float_as_uint(d0.x), __float_as_uint(d0.y), __float_as_uint(d1.x),
+                             __float_as_uint(d1.y));
+        if (static_cast<uint32_t>(yoff) < 4u) {
+            const uint32_t dyb = __float_as_uint(k.dy);
+            o.x = yoff == 0 ? dyb : o.x;
+            o.y = yoff == 1 ? dyb : o.y;
+            o.z = yoff == 2 ? dyb : o.z;
+            o.w = yoff == 3 ? dyb : o.w;
+        }
+        return o;
+    }
+    __device__ static __forceinline__ void run_unpacked(const uint4 &raw, int32_t yoff,
+                                                        const GradConsts &k, float (&d)[4])
+    {
+        float f[4];
+        Elem<float>::unpack(raw, f);
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            d[e] = (e == yoff) ? k.dy : grad_scalar(f[e], k);
+    }
+};
 
 // log p of target k, whose "others" are every column outside the target set
 // S (already folded into (mS, sS)) plus the distinct members of S other
@@ -209,6 +382,8 @@ __global__ void __launch_bounds__(kRowThreads, 2) row_kernel(const RowParams p)
     __shared__ float s_xt[KMAX];
     __shared__ int32_t s_tg[KMAX];
     __shared__ float bc_m, bc_s, bc_logp;
+    __shared__ uint64_t xbar;                   // fused, cluster of CTAs per row
+    __shared__ float2 xchg[kMaxClusterCtas];    // every CTA's (max, sum) partial
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -247,14 +422,15 @@ __global__ void __launch_bounds__(kRowThreads, 2) row_kernel(const RowParams p)
 
     if (state != 0) {
         const float fill = state == 1 ? 0.0f : __int_as_float(0x7fc00000);
-        const bool direct = (p.splits == 1);
+        // direct: this launch writes the row's outputs (no separate merge)
+        const bool direct = (p.splits == 1) || MODE == kModeFused;
         if (MODE == kModeLogp) {
             if (direct && tid < p.k)
                 p.logp_out[r * p.k + tid] = 0.0f;
         } else {
             if (tid == 0 && (direct || MODE == kModeGrad) && split == 0 && state == 2)
                 report(p.dev_status, GBCE_DEV_BAD_LABEL);
-            if (tid == 0 && direct && MODE != kModeGrad) {
+            if (tid == 0 && direct && split == 0 && MODE != kModeGrad) {
                 p.loss_rows[r] = fill;
                 if (p.logp_out)
                     p.logp_out[r] = fill;
@@ -268,6 +444,8 @@ __global__ void __launch_bounds__(kRowThreads, 2) row_kernel(const RowParams p)
     }
 
     const RowGeom g = row_geom<T>(row, V);
+    int32_t tv[KMAX];
+    target_vectors<T, KMAX>(tg, g, tv);
     const int64_t v0 = g.nvec * split / p.splits;
     const int64_t v1 = g.nvec * (split + 1) / p.splits;
     const int64_t nchunks = (v1 - v0 + CV - 1) / CV;
@@ -275,12 +453,16 @@ __global__ void __launch_bounds__(kRowThreads, 2) row_kernel(const RowParams p)
     const char *body = reinterpret_cast<const char *>(row + g.head) + v0 * 16;
     const int64_t body_bytes = (v1 - v0) * 16;
 
+    // fused with a cluster of CTAs per row: the CTAs swap (max, sum) partials
+    const bool exchange = (MODE == kModeFused && p.splits > 1);
     if (tid == 0) {
 #pragma unroll
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full_bar[s], 1);
             mbar_init(&empty_bar[s], NCW);
         }
+        if (exchange)
+            mbar_init(&xbar, 1);
         fence_barrier_init();
     }
     if (kStats) {
@@ -293,6 +475,8 @@ __global__ void __launch_bounds__(kRowThreads, 2) row_kernel(const RowParams p)
             }
     }
     __syncthreads();
+    if (exchange)
+        cluster_sync_all();  // every peer's xbar exists before any partial is sent
 
     // ------------------------------------------------------------ producer
     if (warp == NCW) {
@@ -354,18 +538,23 @@ __global__ void __launch_bounds__(kRowThreads, 2) row_kernel(const RowParams p)
             if (alive) {
                 const uint4 *chunk = reinterpret_cast<const uint4 *>(ring + slot * kChunkBytes);
                 const int64_t nv = (v1 - v0 - i * CV) < CV ? (v1 - v0 - i * CV) : CV;
-                const int32_t colbase = static_cast<int32_t>(g.head + (v0 + i * CV) * VEC);
+                const int32_t vb0 = static_cast<int32_t>(v0 + i * CV);  // body vector of chunk[0]
+                const int32_t col0 = static_cast<int32_t>(g.head);
                 if (nv == CV) {
                     uint4 raw[PER_THREAD];
 #pragma unroll
                     for (int u = 0; u < PER_THREAD; ++u)
                         raw[u] = chunk[tid + u * NC];
 #pragma unroll
-                    for (int u = 0; u < PER_THREAD; ++u)
-                        stats_vector<T, KMAX>(st, raw[u], colbase + (tid + u * NC) * VEC, tg, c);
+                    for (int u = 0; u + 1 < PER_THREAD; u += 2)
+                        stats_two<T, KMAX>(st, raw[u], raw[u + 1], vb0 + tid + u * NC,
+                                        vb0 + tid + (u + 1) * NC, col0, tv, tg, c);
+                    if (PER_THREAD & 1)
+                        stats_one<T, KMAX>(st, raw[PER_THREAD - 1], vb0 + tid + (PER_THREAD - 1) * NC,
+                                        col0, tv, tg, c);
                 } else {
                     for (int v = tid; v < nv; v += NC)
-                        stats_vector<T, KMAX>(st, chunk[v], colbase + v * VEC, tg, c);
+                        stats_one<T, KMAX>(st, chunk[v], vb0 + v, col0, tv, tg, c);
                 }
             }
             __syncwarp();
@@ -374,7 +563,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) row_kernel(const RowParams p)
         }
 
         // CTA-wide merge of the per-thread (max, sum) in a fixed order
-        float m = st.m, s = st.s;
+        float m = st.m, s = st.sum();
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
             const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
@@ -396,7 +585,14 @@ __global__ void __launch_bounds__(kRowThreads, 2) row_kernel(const RowParams p)
                 merge_max_sum(m, s, m2, s2, c);
             }
             if (lane == 0) {
-                if (p.splits > 1) {
+                if (exchange) {
+                    const uint32_t C = static_cast<uint32_t>(p.splits);
+                    mbar_arrive_expect_tx(&xbar, C * static_cast<uint32_t>(sizeof(float2)));
+                    const uint32_t slot = smem_addr(&xchg[split]);
+                    const uint32_t bar = smem_addr(&xbar);
+                    for (uint32_t t = 0; t < C; ++t)
+                        st_async_pair(map_to_rank(slot, t), m, s, map_to_rank(bar, t));
+                } else if (p.splits > 1) {
                     p.partials[unit] = make_float2(m, s);
                 } else if (MODE == kModeLogp) {
                     bc_m = m;
@@ -427,7 +623,36 @@ __global__ void __launch_bounds__(kRowThreads, 2) row_kernel(const RowParams p)
                 p.logp_out[r * p.k + tid] = out;
             }
         }
-        if (MODE == kModeFused) {
+        if (MODE == kModeFused && exchange) {
+            // warp 0 waits for the cluster's partials and finalizes; the
+            // other warps wait on the named barrier, issuing nothing
+            if (warp == 0) {
+                if (!mbar_wait_cluster(&xbar, 0)) {
+                    alive = false;
+                    report(p.dev_status, GBCE_DEV_TIMEOUT);
+                }
+                if (lane == 0) {
+                    float M = kNegInf, Ssum = 0.0f;
+                    for (int t = 0; t < p.splits; ++t) {
+                        const float2 part = xchg[t];
+                        merge_max_sum(M, Ssum, part.x, part.y, c);
+                    }
+                    const float x_y = s_xt[0];
+                    const float lp = finalize_logp(M, Ssum, x_y, p.T);
+                    bc_logp = lp;
+                    if (split == 0) {
+                        p.loss_rows[r] = -lp;
+                        if (p.logp_out)
+                            p.logp_out[r] = lp;
+                        if (p.lse_out)
+                            p.lse_out[r] = x_y / p.T - lp;
+                    }
+                }
+            }
+            named_sync(1, NC);
+            logp = bc_logp;
+            xy = s_xt[0];
+        } else if (MODE == kModeFused) {
             named_sync(1, NC);
             logp = bc_logp;
             xy = s_xt[0];
@@ -439,19 +664,13 @@ __global__ void __launch_bounds__(kRowThreads, 2) row_kernel(const RowParams p)
             logp = p.saved_logp[r];
             xy = E::load(row + y);
         }
-        const float gscale = upstream_grad(p, r) / p.T;
-        const float kb = logp * kLog2e;
-        const float dy = gscale * expm1f(logp);
+        const GradConsts gk = grad_consts(xy, c, logp, upstream_grad(p, r) / p.T);
         if (split == 0)
-            for (int64_t e = tid; e < g.head; e += NC) {
-                const float x = E::load(row + e);
-                E::store(drow + e, e == y ? dy : gscale * ex2(fmaf(x - xy, c, kb)));
-            }
+            for (int64_t e = tid; e < g.head; e += NC)
+                E::store(drow + e, e == y ? gk.dy : grad_scalar(E::load(row + e), gk));
         if (split == p.splits - 1)
-            for (int64_t e = g.tail0 + tid; e < V; e += NC) {
-                const float x = E::load(row + e);
-                E::store(drow + e, e == y ? dy : gscale * ex2(fmaf(x - xy, c, kb)));
-            }
+            for (int64_t e = g.tail0 + tid; e < V; e += NC)
+                E::store(drow + e, e == y ? gk.dy : grad_scalar(E::load(row + e), gk));
         for (int64_t i = 0; i < nchunks; ++i, ++seq) {
             const int slot = static_cast<int>(seq % kStages);
             if (alive && !mbar_wait(&full_bar[slot], static_cast<uint32_t>((seq / kStages) & 1))) {
@@ -462,7 +681,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) row_kernel(const RowParams p)
                 const uint4 *chunk = reinterpret_cast<const uint4 *>(ring + slot * kChunkBytes);
                 const int64_t nv = (v1 - v0 - i * CV) < CV ? (v1 - v0 - i * CV) : CV;
                 const int64_t vbase = v0 + i * CV;
-                const int32_t colbase = static_cast<int32_t>(g.head + vbase * VEC);
+                const int32_t ybase = y - static_cast<int32_t>(g.head + vbase * VEC);
                 T *dbase = drow + g.head + vbase * VEC;
                 if (nv == CV && p.vec_store) {
                     uint4 raw[PER_THREAD];
@@ -472,22 +691,18 @@ __global__ void __launch_bounds__(kRowThreads, 2) row_kernel(const RowParams p)
 #pragma unroll
                     for (int u = 0; u < PER_THREAD; ++u) {
                         const int v = tid + u * NC;
-                        float d[VEC];
-                        st_cs_v4(dbase + v * VEC, grad_vector<T>(raw[u], colbase + v * VEC, y, xy,
-                                                                 c, kb, gscale, dy, d));
+                        st_cs_v4(dbase + v * VEC, GradVec<T>::run(raw[u], ybase - v * VEC, gk));
                     }
+                } else if (p.vec_store) {
+                    for (int v = tid; v < nv; v += NC)
+                        st_cs_v4(dbase + v * VEC, GradVec<T>::run(chunk[v], ybase - v * VEC, gk));
                 } else {
                     for (int v = tid; v < nv; v += NC) {
                         float d[VEC];
-                        const uint4 out = grad_vector<T>(chunk[v], colbase + v * VEC, y, xy, c,
-                                                         kb, gscale, dy, d);
-                        if (p.vec_store) {
-                            st_cs_v4(dbase + v * VEC, out);
-                        } else {
+                        GradVec<T>::run_unpacked(chunk[v], ybase - v * VEC, gk, d);
 #pragma unroll
-                            for (int e = 0; e < VEC; ++e)
-                                E::store(dbase + v * VEC + e, d[e]);
-                        }
+                        for (int e = 0; e < VEC; ++e)
+                            E::store(dbase + v * VEC + e, d[e]);
                     }
                 }
             }
@@ -587,6 +802,35 @@ static cudaError_t ensure_smem_attr(Kernel kernel, int bytes, std::atomic<uint64
     return err;
 }
 
+template <typename T>
+cudaError_t launch_rows_dispatch(const RowParams &p, int mode, cudaStream_t stream);
+
+// Fused mode with a cluster of p.splits CTAs per row (one per vocab slice).
+template <typename T>
+static cudaError_t launch_fused_row_cluster(const RowParams &p, cudaStream_t stream)
+{
+    static std::atomic<uint64_t> attr_done{0};
+    auto kernel = row_kernel<T, kModeFused, 1>;
+    cudaError_t err = ensure_smem_attr(kernel, kDynSmemBytes, attr_done);
+    if (err != cudaSuccess)
+        return err;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(p.rows * p.splits), 1, 1);
+    cfg.blockDim = dim3(kRowThreads, 1, 1);
+    cfg.dynamicSmemBytes = kDynSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(p.splits);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    err = cudaLaunchKernelEx(&cfg, kernel, p);
+    note_launches(1);
+    return err;
+}
+
 template <typename T, int MODE, int KMAX>
 static cudaError_t launch_row_kernel(const RowParams &p, cudaStream_t stream)
 {
@@ -606,6 +850,14 @@ cudaError_t launch_rows(const RowParams &p, int mode, cudaStream_t stream)
 {
     if (p.rows == 0)
         return cudaSuccess;
+    return launch_rows_dispatch<T>(p, mode, stream);
+}
+
+// One CTA per work unit; the fallback for every shape the persistent kernels
+// do not take.
+template <typename T>
+cudaError_t launch_rows_per_unit(const RowParams &p, int mode, cudaStream_t stream)
+{
     switch (mode) {
     case kModeLogp:
         if (p.k <= 1)

@@ -1,5 +1,5 @@
 // fp32-logit instantiations of the row kernels.
-#include "gbce_kernels.cuh"
+#include "gbce_dispatch.cuh"
 
 namespace gbce {
 template cudaError_t launch_rows<float>(const RowParams &, int, cudaStream_t);

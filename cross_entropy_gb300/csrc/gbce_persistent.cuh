@@ -1,0 +1,307 @@
+// Persistent fused cross-entropy forward + backward (sm_103a).
+//
+// One CTA per SM walks rows r = blockIdx.x, r += gridDim.x.  Its producer
+// lane streams, without gaps, row r's statistics pass (bulk copies with L2
+// evict_last), row r's gradient pass (the same bytes again, now L2 hits),
+// then row r+1's statistics pass, ... through a ring of 32 KB stages.  The
+// consumer warps fold pass-1 chunks into the row's online (max, sum),
+// finalize log p between the passes, and write dlogits from pass-2 chunks.
+//
+// Why one CTA per SM: a row must stay in L2 from its first read to its
+// re-read, so the L2 footprint is (rows in flight) x (row bytes).  One row
+// per SM (152 x 304 KB = 46 MB at vocab 152064 bf16) fits the 126 MB L2 next
+// to the dlogits stream; two rows per SM, as one CTA per row at two CTAs per
+// SM has, does not, and the gradient pass then re-reads part of each row
+// from HBM.  Persistence keeps the ring full across row boundaries, so the
+// one CTA never idles HBM while it merges a row's statistics.
+//
+// Sources, by title and section: the sum over the columns other than the
+// target and loss = softplus(log s_others + m - x_y), "Fix softmax collapse
+// in CE, GRPO, KL/JSD and softmax" (Liger-Kernel PR #1555), "Summary"; the
+// -expm1(log p) target gradient, the unsloth-zoo #2080 commit quoted there,
+// "Fix"; ignored rows skipped before any vocabulary read and g*softmax -
+// g*onehot into a separate buffer, ms-swift PR #10353, "PR information".
+#pragma once
+
+#include "gbce_kernels.cuh"
+
+namespace gbce {
+
+constexpr int kPersistWarps = 16;     // consumer warps
+constexpr int kPersistChunk = 32768;  // bytes per ring stage
+constexpr int kPersistStages = 4;     // 128 KB ring: one CTA per SM
+constexpr int kPersistThreads = (kPersistWarps + 1) * 32;
+constexpr int kPersistDynSmem = kPersistStages * kPersistChunk + kRingAlign;
+
+template <typename T>
+__global__ void __launch_bounds__(kPersistThreads, 1) persistent_fused_kernel(const RowParams p)
+{
+    using E = Elem<T>;
+    constexpr int VEC = E::kVec;
+    constexpr int NCW = kPersistWarps;
+    constexpr int NC = NCW * 32;
+    constexpr int S = kPersistStages;
+    constexpr int CHUNK = kPersistChunk;
+    constexpr int CV = CHUNK / 16;
+    constexpr int PER_THREAD = CV / NC;
+    static_assert(CV % NC == 0 && PER_THREAD % 2 == 0, "chunk must split evenly into pairs");
+    static_assert((S & (S - 1)) == 0, "stage count must be a power of two");
+
+    extern __shared__ __align__(128) uint8_t dyn_smem[];
+    uint8_t *ring = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(dyn_smem) + (kRingAlign - 1)) & ~uintptr_t(kRingAlign - 1));
+    __shared__ uint64_t full_bar[S];
+    __shared__ uint64_t empty_bar[S];
+    __shared__ float red_m[NCW], red_s[NCW];
+    __shared__ float bc_logp;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int64_t V = p.vocab;
+    const float c = p.c;
+
+    if (tid == 0) {
+#pragma unroll
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], NCW);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    // ------------------------------------------------------------ producer
+    if (warp == NCW) {
+        if (lane == 0) {
+            const uint64_t keep = policy_evict_last();
+            const uint64_t stream = policy_evict_first();
+            uint32_t seq = 0;
+            bool ok = true;
+            for (int64_t r = blockIdx.x; r < p.rows && ok; r += gridDim.x) {
+                const int64_t lab = p.targets[r];
+                if (lab == p.ignore_index || lab < 0 || lab >= V)
+                    continue;
+                const T *row = static_cast<const T *>(p.logits) + r * p.row_stride;
+                const RowGeom g = row_geom<T>(row, V);
+                const char *body = reinterpret_cast<const char *>(row + g.head);
+                const int64_t bytes_total = g.nvec * 16;
+                for (int pass = 0; pass < 2 && ok; ++pass) {
+                    for (int64_t off = 0; off < bytes_total; off += CHUNK, ++seq) {
+                        const uint32_t slot = seq & (S - 1);
+                        if (seq >= S && !mbar_wait(&empty_bar[slot], ((seq / S) - 1) & 1)) {
+                            ok = false;
+                            break;
+                        }
+                        const int64_t left = bytes_total - off;
+                        const uint32_t bytes = static_cast<uint32_t>(left < CHUNK ? left : CHUNK);
+                        mbar_arrive_expect_tx(&full_bar[slot], bytes);
+                        bulk_load(ring + slot * CHUNK, body + off, bytes, &full_bar[slot],
+                                  pass == 0 ? keep : stream);
+                    }
+                }
+            }
+            if (!ok)
+                report(p.dev_status, GBCE_DEV_TIMEOUT);
+            for (uint32_t j = (seq > S ? seq - S : 0); j < seq; ++j)
+                mbar_wait(&full_bar[j & (S - 1)], (j / S) & 1);
+        }
+        return;
+    }
+
+    // ------------------------------------------------------------ consumers
+    uint32_t seq = 0;
+    bool alive = true;
+    for (int64_t r = blockIdx.x; r < p.rows; r += gridDim.x) {
+        const T *row = static_cast<const T *>(p.logits) + r * p.row_stride;
+        T *drow = static_cast<T *>(p.dlogits) + r * p.d_stride;
+        const int64_t lab = p.targets[r];
+        if (lab == p.ignore_index || lab < 0 || lab >= V) {
+            const bool bad = lab != p.ignore_index;
+            const float fill = bad ? __int_as_float(0x7fc00000) : 0.0f;
+            if (tid == 0) {
+                if (bad)
+                    report(p.dev_status, GBCE_DEV_BAD_LABEL);
+                p.loss_rows[r] = fill;
+                if (p.logp_out)
+                    p.logp_out[r] = fill;
+                if (p.lse_out)
+                    p.lse_out[r] = fill;
+            }
+            const RowGeom gd = row_geom<T>(drow, V);
+            float f[VEC];
+#pragma unroll
+            for (int e = 0; e < VEC; ++e)
+                f[e] = fill;
+            const uint4 pat = E::pack(f);
+            uint4 *body = reinterpret_cast<uint4 *>(drow + gd.head);
+            for (int64_t v = tid; v < gd.nvec; v += NC)
+                st_cs_v4(body + v, pat);
+            for (int64_t e = tid; e < gd.head; e += NC)
+                E::store(drow + e, fill);
+            for (int64_t e = gd.tail0 + tid; e < V; e += NC)
+                E::store(drow + e, fill);
+            continue;
+        }
+        const int32_t y = static_cast<int32_t>(lab);
+        const int32_t tg[1] = {y};
+        const RowGeom g = row_geom<T>(row, V);
+        int32_t tv[1];
+        target_vectors<T, 1>(tg, g, tv);
+        const int64_t nchunks = (g.nvec * 16 + CHUNK - 1) / CHUNK;
+        const int32_t col0 = static_cast<int32_t>(g.head);
+        // the label logit and the upstream gradient are read now (every thread,
+        // one cached address each), so their latency hides under pass 1
+        const float xy = E::load(row + y);
+        const float gscale = upstream_grad(p, r) / p.T;
+
+        // pass 1: statistics
+        OnlineMaxSum st;
+        for (int64_t e = tid; e < g.head; e += NC)
+            st.add1(e == y ? kNegInf : E::load(row + e), c);
+        for (int64_t e = g.tail0 + tid; e < V; e += NC)
+            st.add1(e == y ? kNegInf : E::load(row + e), c);
+        for (int64_t i = 0; i < nchunks; ++i, ++seq) {
+            const uint32_t slot = seq & (S - 1);
+            if (alive && !mbar_wait(&full_bar[slot], (seq / S) & 1)) {
+                alive = false;
+                report(p.dev_status, GBCE_DEV_TIMEOUT);
+            }
+            if (alive) {
+                const uint4 *chunk = reinterpret_cast<const uint4 *>(ring + slot * CHUNK);
+                const int32_t vb0 = static_cast<int32_t>(i * CV);
+                const int32_t nv = static_cast<int32_t>((g.nvec - i * CV) < CV ? (g.nvec - i * CV) : CV);
+                if (nv == CV) {
+                    uint4 raw[PER_THREAD];
+#pragma unroll
+                    for (int u = 0; u < PER_THREAD; ++u)
+                        raw[u] = chunk[tid + u * NC];
+#pragma unroll
+                    for (int u = 0; u < PER_THREAD; u += 2)
+                        stats_two<T, 1>(st, raw[u], raw[u + 1], vb0 + tid + u * NC,
+                                        vb0 + tid + (u + 1) * NC, col0, tv, tg, c);
+                } else {
+                    for (int v = tid; v < nv; v += NC)
+                        stats_one<T, 1>(st, chunk[v], vb0 + v, col0, tv, tg, c);
+                }
+            }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&empty_bar[slot]);
+        }
+
+        // merge: warp shuffles, then warp 0 over the warps, then finalize
+        float m = st.m, s = st.sum();
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
+            const float s2 = __shfl_xor_sync(0xffffffffu, s, off);
+            merge_max_sum(m, s, m2, s2, c);
+        }
+        if (lane == 0) {
+            red_m[warp] = m;
+            red_s[warp] = s;
+        }
+        named_sync(1, NC);
+        if (warp == 0) {
+            m = lane < NCW ? red_m[lane] : kNegInf;
+            s = lane < NCW ? red_s[lane] : 0.0f;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
+                const float s2 = __shfl_xor_sync(0xffffffffu, s, off);
+                merge_max_sum(m, s, m2, s2, c);
+            }
+            if (lane == 0) {
+                const float lp = finalize_logp(m, s, xy, p.T);
+                bc_logp = lp;
+                p.loss_rows[r] = -lp;
+                if (p.logp_out)
+                    p.logp_out[r] = lp;
+                if (p.lse_out)
+                    p.lse_out[r] = xy / p.T - lp;
+            }
+        }
+        named_sync(1, NC);
+        const GradConsts gk = grad_consts(xy, c, bc_logp, gscale);
+
+        // pass 2: gradient
+        for (int64_t e = tid; e < g.head; e += NC)
+            E::store(drow + e, e == y ? gk.dy : grad_scalar(E::load(row + e), gk));
+        for (int64_t e = g.tail0 + tid; e < V; e += NC)
+            E::store(drow + e, e == y ? gk.dy : grad_scalar(E::load(row + e), gk));
+        for (int64_t i = 0; i < nchunks; ++i, ++seq) {
+            const uint32_t slot = seq & (S - 1);
+            if (alive && !mbar_wait(&full_bar[slot], (seq / S) & 1)) {
+                alive = false;
+                report(p.dev_status, GBCE_DEV_TIMEOUT);
+            }
+            if (alive) {
+                const uint4 *chunk = reinterpret_cast<const uint4 *>(ring + slot * CHUNK);
+                const int64_t vbase = i * CV;
+                const int32_t nv = static_cast<int32_t>((g.nvec - vbase) < CV ? (g.nvec - vbase) : CV);
+                const int32_t ybase = y - static_cast<int32_t>(g.head + vbase * VEC);
+                T *dbase = drow + g.head + vbase * VEC;
+                if (nv == CV && p.vec_store) {
+                    uint4 raw[PER_THREAD];
+#pragma unroll
+                    for (int u = 0; u < PER_THREAD; ++u)
+                        raw[u] = chunk[tid + u * NC];
+#pragma unroll
+                    for (int u = 0; u < PER_THREAD; ++u) {
+                        const int v = tid + u * NC;
+                        st_cs_v4(dbase + v * VEC, GradVec<T>::run(raw[u], ybase - v * VEC, gk));
+                    }
+                } else if (p.vec_store) {
+                    for (int v = tid; v < nv; v += NC)
+                        st_cs_v4(dbase + v * VEC, GradVec<T>::run(chunk[v], ybase - v * VEC, gk));
+                } else {
+                    for (int v = tid; v < nv; v += NC) {
+                        float d[VEC];
+                        GradVec<T>::run_unpacked(chunk[v], ybase - v * VEC, gk, d);
+#pragma unroll
+                        for (int e = 0; e < VEC; ++e)
+                            E::store(dbase + v * VEC + e, d[e]);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&empty_bar[slot]);
+        }
+    }
+}
+
+// Streaming multiprocessors of the current device (cached per device).
+inline int device_sm_count()
+{
+    static std::atomic<int> cache[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return 0;
+    if (dev >= 0 && dev < 64) {
+        const int v = cache[dev].load(std::memory_order_relaxed);
+        if (v > 0)
+            return v;
+    }
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 0;
+    if (dev >= 0 && dev < 64)
+        cache[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
+
+template <typename T>
+cudaError_t launch_persistent_fused(const RowParams &p, int grid, cudaStream_t stream)
+{
+    static std::atomic<uint64_t> attr_done{0};
+    auto kernel = persistent_fused_kernel<T>;
+    cudaError_t err = ensure_smem_attr(kernel, kPersistDynSmem, attr_done);
+    if (err != cudaSuccess)
+        return err;
+    kernel<<<grid, kPersistThreads, kPersistDynSmem, stream>>>(p);
+    note_launches(1);
+    return cudaGetLastError();
+}
+
+}  // namespace gbce

@@ -59,7 +59,19 @@ __device__ int64_t count_items(const int64_t *labels, int64_t rows, int64_t igno
                                int64_t *scratch)
 {
     int64_t n = 0;
-    for (int64_t r = threadIdx.x; r < rows; r += kReduceThreads)
+    int64_t r0 = 0;
+    if ((reinterpret_cast<uintptr_t>(labels) & 15u) == 0) {
+        // two labels per 16-byte load, several loads in flight per thread
+        const longlong2 *v = reinterpret_cast<const longlong2 *>(labels);
+        const int64_t nv = rows / 2;
+#pragma unroll 4
+        for (int64_t i = threadIdx.x; i < nv; i += kReduceThreads) {
+            const longlong2 w = v[i];
+            n += (w.x != ignore_index) + (w.y != ignore_index);
+        }
+        r0 = nv * 2;
+    }
+    for (int64_t r = r0 + threadIdx.x; r < rows; r += kReduceThreads)
         n += (labels[r] != ignore_index);
     return block_sum_i64(n, scratch);
 }
@@ -90,8 +102,21 @@ __global__ void __launch_bounds__(kReduceThreads)
     } else if (threadIdx.x == 0) {
         s_n = n_in != nullptr ? *n_in : 0;
     }
+    // per-thread partial over a fixed set of rows, in a fixed order
     double acc = 0.0;
-    for (int64_t r = threadIdx.x; r < rows; r += kReduceThreads)
+    int64_t r0 = 0;
+    if ((reinterpret_cast<uintptr_t>(loss_rows) & 15u) == 0) {
+        const float4 *v = reinterpret_cast<const float4 *>(loss_rows);
+        const int64_t nv = rows / 4;
+#pragma unroll 4
+        for (int64_t i = threadIdx.x; i < nv; i += kReduceThreads) {
+            const float4 w = v[i];
+            acc += (static_cast<double>(w.x) + static_cast<double>(w.y)) +
+                   (static_cast<double>(w.z) + static_cast<double>(w.w));
+        }
+        r0 = nv * 4;
+    }
+    for (int64_t r = r0 + threadIdx.x; r < rows; r += kReduceThreads)
         acc += static_cast<double>(loss_rows[r]);
     const double total = block_sum_f64(acc, dscratch);  // ends with __syncthreads
     if (threadIdx.x == 0) {
