@@ -357,7 +357,8 @@ def run_gbce(args):
         },
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "ce_fwd_bwd_fused (row_kernel fused mode + count + reduce)",
+                     "kernel": "ce_fwd_bwd_fused call: persistent_fused_kernel + item count "
+                               "+ loss reduction (events around the whole call)",
                      "algorithmic_bytes": nbytes["ce_fwd_bwd_fused"], "peak_kind": peak_kind},
         "e2e": e2e,
         "gpu_launches": launches,

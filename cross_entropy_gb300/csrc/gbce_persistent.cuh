@@ -27,9 +27,21 @@
 
 namespace gbce {
 
-constexpr int kPersistWarps = 16;     // consumer warps
-constexpr int kPersistChunk = 32768;  // bytes per ring stage
-constexpr int kPersistStages = 4;     // 128 KB ring: one CTA per SM
+// Shape of the persistent CTA (build options GBCE_PERSIST_* override it;
+// 16 warps x 4 stages of 32 KB measured best on GB300 against 16 x 16 KB x 8,
+// 8 x 32 KB x 4 and 16 x 64 KB x 2).
+#ifndef GBCE_PERSIST_WARPS
+#define GBCE_PERSIST_WARPS 16
+#endif
+#ifndef GBCE_PERSIST_CHUNK
+#define GBCE_PERSIST_CHUNK 32768
+#endif
+#ifndef GBCE_PERSIST_STAGES
+#define GBCE_PERSIST_STAGES 4
+#endif
+constexpr int kPersistWarps = GBCE_PERSIST_WARPS;    // consumer warps
+constexpr int kPersistChunk = GBCE_PERSIST_CHUNK;    // bytes per ring stage
+constexpr int kPersistStages = GBCE_PERSIST_STAGES;  // 128 KB ring: one CTA per SM
 constexpr int kPersistThreads = (kPersistWarps + 1) * 32;
 constexpr int kPersistDynSmem = kPersistStages * kPersistChunk + kRingAlign;
 
