@@ -341,6 +341,12 @@ def run_gbce(args):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w)
+    per_config = None
+    if not args.no_configs:
+        del x, idx, lab, dlogits
+        w = None
+        torch.cuda.empty_cache()
+        per_config = measure_configs(gbce, dev, stream, peak)
     if rank != 0:
         return
     line = {
@@ -364,8 +370,114 @@ def run_gbce(args):
         "gpu_launches": launches,
         "clocks": clocks,
         "cpu_baseline": cpu,
+        "per_config": per_config,
     }
     print(json.dumps(line), flush=True)
+
+
+def op_bytes(w, op, k=1):
+    """Algorithmic bytes of one call: logits of live rows read once, dlogits
+    of every row written once, int64 labels / indices and fp32 outputs."""
+    es = w.logits.element_size()
+    rows, V = w.rows, w.vocab
+    if op == "logp":
+        live = rows if w.row_mask is None else int(w.row_mask.sum().item())
+        return live * V * es + rows * k * 8 + rows * k * 4 + (0 if w.row_mask is None else rows)
+    live = int((w.labels != workloads.IGNORE_INDEX).sum().item())
+    read = live * V * es + rows * 8
+    if op == "ce_fwd":
+        return read + rows * 4
+    if op == "ce_bwd":
+        return read + rows * V * es + rows * 4
+    return read + rows * V * es  # fused
+
+
+def time_op(fn, stream, reps, flush=None):
+    """Median CUDA-event time (ms) of one call, L2 flushed before each rep.
+
+    The call is captured once in a CUDA graph and replayed, so the time is
+    the GPU's and not the Python launch path's (the library's calls never
+    synchronize or allocate, so they capture); eager calls if capture fails.
+    """
+    fn()
+    torch.cuda.synchronize()
+    run = fn
+    try:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            fn()
+        run = graph.replay
+    except Exception:  # noqa: BLE001 - fall back to eager timing
+        run = fn
+    times = []
+    for _ in range(reps + 2):
+        if flush is not None:
+            flush.fill_(1.0)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        run()
+        b.record(stream)
+        b.synchronize()
+        times.append(a.elapsed_time(b))
+    return statistics.median(times[2:])
+
+
+def measure_configs(gbce, dev, stream, peak):
+    """Every seeded workload, each op timed alone: ms, rows/s, GB/s, fraction."""
+    flush = torch.empty(128 * 1024 * 1024, dtype=torch.float32, device=dev)  # 512 MB > L2
+    out = {}
+
+    def record(name, w, op, ms, k=1):
+        nb = op_bytes(w, op, k)
+        gbs = nb / (ms * 1e-3) / 1e9
+        out[name] = {"ms": round(ms, 5), "rows_per_s": round(w.rows / (ms * 1e-3)),
+                     "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4), "bytes": nb}
+
+    def ce_ops(tag, w, T, red, g):
+        x, lab = w.logits, w.labels
+        d = torch.empty_like(x)
+        ws = gbce.new_workspace(w.rows, w.vocab, 1, device=dev)
+        fwd = gbce.ce_fwd(x, lab, temperature=T, reduction=red, workspace=ws)
+        fl = flush if w.logits.numel() * w.logits.element_size() < (256 << 20) else None
+        record(f"{tag}/ce_fwd_bwd_fused", w, "fused", time_op(
+            lambda: gbce.ce_fwd_bwd_fused(x, lab, g, temperature=T, reduction=red, dlogits=d,
+                                          workspace=ws), stream, 10, fl))
+        record(f"{tag}/ce_fwd", w, "ce_fwd", time_op(
+            lambda: gbce.ce_fwd(x, lab, temperature=T, reduction=red, workspace=ws),
+            stream, 10, fl))
+        record(f"{tag}/ce_bwd", w, "ce_bwd", time_op(
+            lambda: gbce.ce_bwd(x, lab, g, fwd.logp, fwd.n_items, temperature=T, reduction=red,
+                                dlogits=d), stream, 10, fl))
+
+    def logp_op(tag, w, T):
+        x, idx = w.logits, w.index
+        mask = w.row_mask
+        o = torch.empty((w.rows, idx.shape[1]), dtype=torch.float32, device=dev)
+        ws = gbce.new_workspace(w.rows, w.vocab, idx.shape[1], device=dev)
+        fl = flush if w.logits.numel() * w.logits.element_size() < (256 << 20) else None
+        record(f"{tag}/selective_logsoftmax", w, "logp", time_op(
+            lambda: gbce.selective_logsoftmax(x, idx, T, mask, out=o, workspace=ws),
+            stream, 10, fl), k=idx.shape[1])
+
+    w = workloads.ce_small_fp32(device=dev)
+    ce_ops("ce_small_fp32_64x4096", w, 1.0, "mean", torch.ones(1, device=dev))
+    logp_op("ce_small_fp32_64x4096", w, 1.0)
+    w = workloads.ce_sparse_bf16(device=dev)
+    ce_ops("ce_sparse_bf16_1922x4096", w, 1.0, "none", w.grad_out)
+    w = workloads.logp_bf16(device=dev)
+    logp_op("logp_bf16_1024x32768_T1.0", w, 1.0)
+    logp_op("logp_bf16_1024x32768_T0.9", w, 0.9)
+    for dt, tag in ((torch.float32, "fp32"), (torch.bfloat16, "bf16")):
+        w = workloads.collapse_stress(dtype=dt, device=dev)
+        ce_ops(f"collapse_{tag}_2048x151936", w, 1.0, "mean", torch.ones(1, device=dev))
+        logp_op(f"collapse_{tag}_2048x151936", w, 1.0)
+        del w
+    w = workloads.grpo_bf16(device=dev, rows=ROWS)
+    ce_ops(f"grpo_bf16_{ROWS}x{VOCAB}", w, TEMPERATURE, "mean", torch.ones(1, device=dev))
+    del w, flush
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_e2e(gbce, w, dev, stream, args, world):
@@ -435,6 +547,8 @@ def main():
     ap.add_argument("--impl", choices=["gbce", "reference"], default="gbce")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-workload, per-op timings")
     ap.add_argument("--rows", type=int, default=ROWS,
                     help="rows of the workload (a smaller case for profiling captures)")
     args = ap.parse_args()

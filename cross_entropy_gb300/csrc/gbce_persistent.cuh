@@ -27,21 +27,24 @@
 
 namespace gbce {
 
-// Shape of the persistent CTA (build options GBCE_PERSIST_* override it;
-// 16 warps x 4 stages of 32 KB measured best on GB300 against 16 x 16 KB x 8,
-// 8 x 32 KB x 4 and 16 x 64 KB x 2).
+// Shape of the persistent CTA (build options GBCE_PERSIST_* override it).
+// Measured on GB300 at 8192 x 152064 bf16, consumer warps x chunk x stages:
+// 8 x 32K x 4: 75%, 16 x 16K x 8: 80%, 16 x 64K x 2: 78%, 16 x 32K x 4: 86%,
+// 20 x 40K x 4: 91.5%, 24 x 48K x 4: 94.8%, 28 x 28K x 4: 81% of measured
+// HBM bandwidth -- more warps hide the exp chains' latency as long as each
+// thread still gets four 16-byte vectors per chunk.
 #ifndef GBCE_PERSIST_WARPS
-#define GBCE_PERSIST_WARPS 16
+#define GBCE_PERSIST_WARPS 24
 #endif
 #ifndef GBCE_PERSIST_CHUNK
-#define GBCE_PERSIST_CHUNK 32768
+#define GBCE_PERSIST_CHUNK 49152
 #endif
 #ifndef GBCE_PERSIST_STAGES
 #define GBCE_PERSIST_STAGES 4
 #endif
 constexpr int kPersistWarps = GBCE_PERSIST_WARPS;    // consumer warps
 constexpr int kPersistChunk = GBCE_PERSIST_CHUNK;    // bytes per ring stage
-constexpr int kPersistStages = GBCE_PERSIST_STAGES;  // 128 KB ring: one CTA per SM
+constexpr int kPersistStages = GBCE_PERSIST_STAGES;  // 192 KB ring: one CTA per SM
 constexpr int kPersistThreads = (kPersistWarps + 1) * 32;
 constexpr int kPersistDynSmem = kPersistStages * kPersistChunk + kRingAlign;
 
@@ -57,7 +60,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persistent_fused_kernel(co
     constexpr int CV = CHUNK / 16;
     constexpr int PER_THREAD = CV / NC;
     static_assert(CV % NC == 0 && PER_THREAD % 2 == 0, "chunk must split evenly into pairs");
-    static_assert((S & (S - 1)) == 0, "stage count must be a power of two");
+    static_assert(kPersistThreads <= 1024, "at most 1024 threads per CTA");
 
     extern __shared__ __align__(128) uint8_t dyn_smem[];
     uint8_t *ring = reinterpret_cast<uint8_t *>(
@@ -87,7 +90,8 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persistent_fused_kernel(co
         if (lane == 0) {
             const uint64_t keep = policy_evict_last();
             const uint64_t stream = policy_evict_first();
-            uint32_t seq = 0;
+            uint32_t seq = 0;          // chunks issued
+            uint32_t slot = 0, lap = 0;  // ring position of chunk seq, and its lap
             bool ok = true;
             for (int64_t r = blockIdx.x; r < p.rows && ok; r += gridDim.x) {
                 const int64_t lab = p.targets[r];
@@ -99,8 +103,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persistent_fused_kernel(co
                 const int64_t bytes_total = g.nvec * 16;
                 for (int pass = 0; pass < 2 && ok; ++pass) {
                     for (int64_t off = 0; off < bytes_total; off += CHUNK, ++seq) {
-                        const uint32_t slot = seq & (S - 1);
-                        if (seq >= S && !mbar_wait(&empty_bar[slot], ((seq / S) - 1) & 1)) {
+                        if (lap > 0 && !mbar_wait(&empty_bar[slot], (lap - 1) & 1)) {
                             ok = false;
                             break;
                         }
@@ -109,19 +112,24 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persistent_fused_kernel(co
                         mbar_arrive_expect_tx(&full_bar[slot], bytes);
                         bulk_load(ring + slot * CHUNK, body + off, bytes, &full_bar[slot],
                                   pass == 0 ? keep : stream);
+                        if (++slot == S) {
+                            slot = 0;
+                            ++lap;
+                        }
                     }
                 }
             }
             if (!ok)
                 report(p.dev_status, GBCE_DEV_TIMEOUT);
+            // no copy may still be in flight when the CTA exits
             for (uint32_t j = (seq > S ? seq - S : 0); j < seq; ++j)
-                mbar_wait(&full_bar[j & (S - 1)], (j / S) & 1);
+                mbar_wait(&full_bar[j % S], (j / S) & 1);
         }
         return;
     }
 
     // ------------------------------------------------------------ consumers
-    uint32_t seq = 0;
+    uint32_t slot = 0, lap = 0;  // ring position of the next chunk, and its lap
     bool alive = true;
     for (int64_t r = blockIdx.x; r < p.rows; r += gridDim.x) {
         const T *row = static_cast<const T *>(p.logits) + r * p.row_stride;
@@ -172,9 +180,8 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persistent_fused_kernel(co
             st.add1(e == y ? kNegInf : E::load(row + e), c);
         for (int64_t e = g.tail0 + tid; e < V; e += NC)
             st.add1(e == y ? kNegInf : E::load(row + e), c);
-        for (int64_t i = 0; i < nchunks; ++i, ++seq) {
-            const uint32_t slot = seq & (S - 1);
-            if (alive && !mbar_wait(&full_bar[slot], (seq / S) & 1)) {
+        for (int64_t i = 0; i < nchunks; ++i) {
+            if (alive && !mbar_wait(&full_bar[slot], lap & 1)) {
                 alive = false;
                 report(p.dev_status, GBCE_DEV_TIMEOUT);
             }
@@ -199,6 +206,10 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persistent_fused_kernel(co
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&empty_bar[slot]);
+            if (++slot == S) {
+                slot = 0;
+                ++lap;
+            }
         }
 
         // merge: warp shuffles, then warp 0 over the warps, then finalize
@@ -241,9 +252,8 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persistent_fused_kernel(co
             E::store(drow + e, e == y ? gk.dy : grad_scalar(E::load(row + e), gk));
         for (int64_t e = g.tail0 + tid; e < V; e += NC)
             E::store(drow + e, e == y ? gk.dy : grad_scalar(E::load(row + e), gk));
-        for (int64_t i = 0; i < nchunks; ++i, ++seq) {
-            const uint32_t slot = seq & (S - 1);
-            if (alive && !mbar_wait(&full_bar[slot], (seq / S) & 1)) {
+        for (int64_t i = 0; i < nchunks; ++i) {
+            if (alive && !mbar_wait(&full_bar[slot], lap & 1)) {
                 alive = false;
                 report(p.dev_status, GBCE_DEV_TIMEOUT);
             }
@@ -279,6 +289,10 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persistent_fused_kernel(co
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&empty_bar[slot]);
+            if (++slot == S) {
+                slot = 0;
+                ++lap;
+            }
         }
     }
 }
