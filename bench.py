@@ -342,7 +342,7 @@ def run_gbce(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w)
     per_config = None
-    if not args.no_configs:
+    if world == 1 and not args.no_configs:
         del x, idx, lab, dlogits
         w = None
         torch.cuda.empty_cache()
@@ -473,6 +473,10 @@ def measure_configs(gbce, dev, stream, peak):
         ce_ops(f"collapse_{tag}_2048x151936", w, 1.0, "mean", torch.ones(1, device=dev))
         logp_op(f"collapse_{tag}_2048x151936", w, 1.0)
         del w
+    # few rows, large vocabulary: the split-vocab partial + combine path
+    w = workloads.grpo_bf16(device=dev, rows=64, seed=7)
+    ce_ops("split_bf16_64x152064", w, TEMPERATURE, "mean", torch.ones(1, device=dev))
+    logp_op("split_bf16_64x152064", w, TEMPERATURE)
     w = workloads.grpo_bf16(device=dev, rows=ROWS)
     ce_ops(f"grpo_bf16_{ROWS}x{VOCAB}", w, TEMPERATURE, "mean", torch.ones(1, device=dev))
     del w, flush

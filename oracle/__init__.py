@@ -17,6 +17,9 @@ Functions and the passages they follow:
   gather(log_softmax(logits / T)) at K indices per row with a row mask,
   computed in the collapse-safe form of "Fix softmax collapse in CE, GRPO,
   KL/JSD and softmax" (Liger-Kernel PR #1555), "Details".
+* :func:`selective_logsoftmax_backward` -- the gradient of sum_k g_k log p_{t_k}:
+  (1/T)(sum_{k: t_k = j} g_k - G p_j), with the gathered columns in the
+  -expm1(log p_t) form of the same page's "Summary" (second bullet).
 * :func:`cross_entropy` -- the same page's "Summary" (loss from the sum that
   excludes the target) with ms-swift PR #10353's "PR information" (analytic
   backward g*softmax - g*onehot, zero weight on ignored labels) and the
@@ -78,6 +81,9 @@ def _load():
         lib.oracle_cross_entropy.argtypes = [
             dp, i64, i64, i64, ip, i64, ctypes.c_double, ctypes.c_int, ctypes.c_void_p,
             dp, dp, dp, ip, ctypes.c_void_p, i64]
+        lib.oracle_selective_logsoftmax_backward.restype = i64
+        lib.oracle_selective_logsoftmax_backward.argtypes = [
+            dp, i64, i64, i64, ip, i64, ctypes.c_double, ctypes.c_void_p, dp, dp, i64]
         lib.oracle_num_threads.restype = ctypes.c_int
         lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
         _lib = lib
@@ -132,6 +138,30 @@ def selective_logsoftmax(x, index, temperature: float = 1.0, row_mask=None):
         _ptr(x, ctypes.c_double), rows, V, x.strides[0] // 8, _ptr(idx, ctypes.c_int64), K,
         exact_temperature(temperature), mask_ptr, _ptr(out, ctypes.c_double))
     return out, int(bad)
+
+
+def selective_logsoftmax_backward(x, index, grad, temperature: float = 1.0, row_mask=None):
+    """dL/dx for upstream grad[r, k] = dL/d log p_{index[r, k]}; masked rows 0.
+
+    Returns ``(dx[rows, V] float64, n_bad_rows)``.
+    """
+    lib = _load()
+    x = _as_rows(x)
+    rows, V = x.shape
+    idx = np.ascontiguousarray(np.asarray(index, dtype=np.int64).reshape(rows, -1))
+    K = idx.shape[1]
+    g = np.ascontiguousarray(np.asarray(grad, dtype=np.float64).reshape(rows, K))
+    mask_arr = None
+    mask_ptr = None
+    if row_mask is not None:
+        mask_arr = np.ascontiguousarray(np.asarray(row_mask).reshape(rows).astype(np.uint8))
+        mask_ptr = mask_arr.ctypes.data
+    dx = np.empty((rows, V), dtype=np.float64)
+    bad = lib.oracle_selective_logsoftmax_backward(
+        _ptr(x, ctypes.c_double), rows, V, x.strides[0] // 8, _ptr(idx, ctypes.c_int64), K,
+        exact_temperature(temperature), mask_ptr, _ptr(g, ctypes.c_double),
+        _ptr(dx, ctypes.c_double), V)
+    return dx, int(bad)
 
 
 def cross_entropy(x, labels, ignore_index: int = -100, temperature: float = 1.0,

@@ -45,6 +45,15 @@
  * mask): out[r,k] = log p_{idx[r,k]} for rows with row_mask[r] != 0, and 0
  * for masked-out rows, which are not read.
  *
+ * Selective log-softmax backward (the gradient a GRPO-style loss sends
+ * through the gathered log-probs; "Fix softmax collapse ..." page, "Summary",
+ * second bullet, and the unsloth-zoo #2080 "Fix" section's -expm1(log p_t)):
+ * with upstream g_k = dL/d out[r,k] and G = sum_k g_k,
+ *   dL/dx_j = (1/T) * ( sum_{k : idx[r,k] = j} g_k  -  G * p_j ),
+ * written at a gathered column t (g_t = sum of g_k over the k that gather t)
+ * as (1/T) * ( -g_t * expm1(log p_t) - (G - g_t) * exp(log p_t) ), which
+ * keeps 1 - p_t exact when p_t rounds to 1; masked-out rows get a zero row.
+ *
  * An index or label outside [0,V) (and, for labels, not ignore_index)
  * makes that row's outputs NaN and is counted in the return value.
  */
@@ -245,6 +254,76 @@ int64_t oracle_cross_entropy(const double *x, int64_t rows, int64_t V, int64_t l
                 dr[j] = scale * expm1(lp);
             else
                 dr[j] = scale * exp(xr[j] / T - zy + lp);
+        }
+    }
+    return bad;
+}
+
+/*
+ * Selective log-softmax backward.
+ *   x         [rows, ld] fp64
+ *   idx       [rows, K] int64
+ *   row_mask  [rows] uint8 or NULL
+ *   grad      [rows, K] fp64: dL/d out[r, k]
+ *   dx        [rows, ldx] out
+ * Returns the number of rows with an out-of-range index (their rows NaN).
+ */
+int64_t oracle_selective_logsoftmax_backward(const double *x, int64_t rows, int64_t V,
+                                             int64_t ld, const int64_t *idx, int64_t K, double T,
+                                             const uint8_t *row_mask, const double *grad,
+                                             double *dx, int64_t ldx)
+{
+    int64_t bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(+ : bad)
+    for (int64_t r = 0; r < rows; ++r) {
+        const double *xr = x + r * ld;
+        double *dr = dx + r * ldx;
+        if (row_mask && row_mask[r] == 0) {
+            for (int64_t j = 0; j < V; ++j)
+                dr[j] = 0.0;
+            continue;
+        }
+        int row_bad = 0;
+        for (int64_t k = 0; k < K; ++k)
+            if (idx[r * K + k] < 0 || idx[r * K + k] >= V)
+                row_bad = 1;
+        if (row_bad) {
+            for (int64_t j = 0; j < V; ++j)
+                dr[j] = NAN;
+            ++bad;
+            continue;
+        }
+        /* log-sum-exp of the whole row, then p_j = exp(z_j - lse) */
+        double m = -INFINITY;
+        for (int64_t j = 0; j < V; ++j)
+            if (xr[j] / T > m)
+                m = xr[j] / T;
+        oracle_sum s = {0.0, 0.0};
+        for (int64_t j = 0; j < V; ++j)
+            sum_add(&s, exp(xr[j] / T - m));
+        const double lse = m + log(sum_value(&s));
+        oracle_sum G = {0.0, 0.0};
+        for (int64_t k = 0; k < K; ++k)
+            sum_add(&G, grad[r * K + k]);
+        const double Gv = sum_value(&G);
+        for (int64_t j = 0; j < V; ++j)
+            dr[j] = -(Gv / T) * exp(xr[j] / T - lse);
+        /* gathered columns, each once, in the collapse-safe form */
+        for (int64_t k = 0; k < K; ++k) {
+            const int64_t t = idx[r * K + k];
+            int seen = 0;
+            for (int64_t i = 0; i < k; ++i)
+                if (idx[r * K + i] == t)
+                    seen = 1;
+            if (seen)
+                continue;
+            oracle_sum gt = {0.0, 0.0};
+            for (int64_t i = 0; i < K; ++i)
+                if (idx[r * K + i] == t)
+                    sum_add(&gt, grad[r * K + i]);
+            const double g_t = sum_value(&gt);
+            const double lp = row_logp(xr, V, t, T);
+            dr[t] = (-g_t * expm1(lp) - (Gv - g_t) * exp(lp)) / T;
         }
     }
     return bad;

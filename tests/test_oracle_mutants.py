@@ -32,7 +32,15 @@ MUTANTS = {
                           "dr[j] = -scale * exp(xr[j] / T - zy + lp);"),
     "other_logit_target_swap": ("scale * exp(xr[j] / T - zy + lp)",
                                 "scale * exp(zy - xr[j] / T + lp)"),
-    "masked_rows_computed": ("if (row_mask && row_mask[r] == 0) {", "if (0) {"),
+    "masked_rows_computed": ("if (row_mask && row_mask[r] == 0) {\n                *o = 0.0;",
+                             "if (0) {\n                *o = 0.0;"),
+    "sel_bwd_target_term_sign": ("dr[t] = (-g_t * expm1(lp) - (Gv - g_t) * exp(lp)) / T;",
+                                 "dr[t] = (g_t * expm1(lp) - (Gv - g_t) * exp(lp)) / T;"),
+    "sel_bwd_others_use_all_of_G": ("- (Gv - g_t) * exp(lp)) / T;", "- Gv * exp(lp)) / T;"),
+    "sel_bwd_duplicates_not_summed": ("                if (idx[r * K + i] == t)\n                    sum_add(&gt",
+                                      "                if (i == k)\n                    sum_add(&gt"),
+    "sel_bwd_missing_inverse_T": ("dr[j] = -(Gv / T) * exp(xr[j] / T - lse);",
+                                  "dr[j] = -Gv * exp(xr[j] / T - lse);"),
 }
 
 

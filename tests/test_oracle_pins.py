@@ -354,3 +354,91 @@ def test_strided_rows_equal_contiguous():
     b = oracle.cross_entropy(np.ascontiguousarray(view), lab, reduction="sum")
     np.testing.assert_array_equal(a["logp"], b["logp"])
     np.testing.assert_array_equal(a["dlogits"], b["dlogits"])
+
+
+# --------------------------------------------- selective log-softmax backward
+
+def brute_selective_grad(row, idx, g, T):
+    """(1/T) (sum_{k: t_k = j} g_k - G p_j) at 120 digits."""
+    logps, _ = brute_row(row, 0, T)
+    G = Decimal(0)
+    for gk in g:
+        G = CTX.add(G, Decimal(float(gk)))
+    out = []
+    for j, lp in enumerate(logps):
+        acc = CTX.multiply(CTX.minus(G), CTX.exp(lp))
+        for t, gk in zip(idx, g):
+            if t == j:
+                acc = CTX.add(acc, Decimal(float(gk)))
+        out.append(float(CTX.divide(acc, Decimal(T))))
+    return np.array(out)
+
+
+@pytest.mark.parametrize("V", [2, 5, 33])
+@pytest.mark.parametrize("T", [1.0, 0.7])
+def test_selective_backward_brute_force(V, T):
+    margins = [0.0, 17.0, 30.0, 50.0, 80.0]
+    w = workloads.peaked_rows_tiny(V, margins, seed=200 + V)
+    x = w.logits.numpy()
+    y = w.labels.numpy()
+    rng = np.random.default_rng(V)
+    K = 3
+    idx = np.stack([y, rng.integers(0, V, size=len(margins)), y], axis=1)  # duplicates of y
+    g = rng.normal(size=(len(margins), K))
+    dx, bad = oracle.selective_logsoftmax_backward(x, idx, g, T)
+    assert bad == 0
+    Te = oracle.exact_temperature(T)
+    for r in range(len(margins)):
+        want = brute_selective_grad(x[r], idx[r], g[r], Te)
+        scale = np.max(np.abs(want))
+        assert np.max(np.abs(dx[r] - want)) <= 1e-12 * scale, (r, margins[r])
+        # the gathered label column keeps its (tiny) exact value
+        assert dx[r, y[r]] == pytest.approx(want[y[r]], rel=1e-10, abs=1e-300)
+
+
+def test_selective_backward_finite_difference():
+    rng = np.random.default_rng(31)
+    V, rows, K = 7, 3, 2
+    x = rng.normal(scale=2.0, size=(rows, V))
+    idx = np.array([[1, 4], [2, 2], [6, 0]])
+    g = rng.normal(size=(rows, K))
+    T = 0.8
+    dx, _ = oracle.selective_logsoftmax_backward(x, idx, g, T)
+    h = 1e-6
+    num = np.zeros_like(x)
+    for r in range(rows):
+        for j in range(V):
+            xp, xm = x.copy(), x.copy()
+            xp[r, j] += h
+            xm[r, j] -= h
+            fp, _ = oracle.selective_logsoftmax(xp, idx, T)
+            fm, _ = oracle.selective_logsoftmax(xm, idx, T)
+            num[r, j] = np.sum(g * (fp - fm)) / (2 * h)
+    np.testing.assert_allclose(dx, num, rtol=2e-6, atol=1e-9)
+
+
+def test_selective_backward_k1_is_minus_ce_backward():
+    """For one gathered index, d(g log p_t)/dx is the CE gradient with upstream -g."""
+    w = workloads.collapse_stress(dtype=torch.float32, rows=16, V=3001, seed=5)
+    x = workloads.to_numpy_f64(w.logits)
+    lab = w.index.numpy()[:, 0]
+    g = np.random.default_rng(0).normal(size=16)
+    dx, _ = oracle.selective_logsoftmax_backward(x, lab[:, None], g[:, None], 0.9)
+    ce = oracle.cross_entropy(x, lab, temperature=0.9, reduction="none", grad_out=-g)
+    np.testing.assert_allclose(dx, ce["dlogits"], rtol=1e-12, atol=1e-300)
+
+
+def test_selective_backward_uniform_rows_and_invariants():
+    V, T = 40, 0.9
+    x = np.full((3, V), 0.3)
+    idx = np.array([[0, 5], [7, 7], [39, 1]])
+    g = np.array([[1.0, 2.0], [0.5, 0.25], [-1.0, 3.0]])
+    dx, _ = oracle.selective_logsoftmax_backward(x, idx, g, T, row_mask=[1, 1, 0])
+    Te = oracle.exact_temperature(T)
+    for r in range(2):
+        want = np.full(V, -g[r].sum() / (V * Te))
+        for t, gk in zip(idx[r], g[r]):
+            want[t] += gk / Te
+        np.testing.assert_allclose(dx[r], want, rtol=1e-12)
+        assert abs(math.fsum(dx[r])) <= 1e-13 * math.fsum(np.abs(dx[r]))
+    assert np.all(dx[2] == 0.0)
