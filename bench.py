@@ -380,9 +380,13 @@ def op_bytes(w, op, k=1):
     of every row written once, int64 labels / indices and fp32 outputs."""
     es = w.logits.element_size()
     rows, V = w.rows, w.vocab
-    if op == "logp":
+    if op in ("logp", "logp_bwd"):
         live = rows if w.row_mask is None else int(w.row_mask.sum().item())
-        return live * V * es + rows * k * 8 + rows * k * 4 + (0 if w.row_mask is None else rows)
+        mask = 0 if w.row_mask is None else rows
+        if op == "logp":
+            return live * V * es + rows * k * 8 + rows * k * 4 + mask
+        # logits in, dlogits out, index + upstream gradient + saved log-probs
+        return live * V * es + rows * V * es + rows * k * (8 + 4 + 4) + mask
     live = int((w.labels != workloads.IGNORE_INDEX).sum().item())
     read = live * V * es + rows * 8
     if op == "ce_fwd":
@@ -450,15 +454,22 @@ def measure_configs(gbce, dev, stream, peak):
             lambda: gbce.ce_bwd(x, lab, g, fwd.logp, fwd.n_items, temperature=T, reduction=red,
                                 dlogits=d), stream, 10, fl))
 
-    def logp_op(tag, w, T):
-        x, idx = w.logits, w.index
+    def logp_op(tag, w, T, backward=False, k=None):
+        x, idx = w.logits, (w.index if k is None else w.index[:, :k].contiguous())
         mask = w.row_mask
-        o = torch.empty((w.rows, idx.shape[1]), dtype=torch.float32, device=dev)
-        ws = gbce.new_workspace(w.rows, w.vocab, idx.shape[1], device=dev)
+        K_ = idx.shape[1]
+        o = torch.empty((w.rows, K_), dtype=torch.float32, device=dev)
+        ws = gbce.new_workspace(w.rows, w.vocab, K_, device=dev)
         fl = flush if w.logits.numel() * w.logits.element_size() < (256 << 20) else None
         record(f"{tag}/selective_logsoftmax", w, "logp", time_op(
             lambda: gbce.selective_logsoftmax(x, idx, T, mask, out=o, workspace=ws),
-            stream, 10, fl), k=idx.shape[1])
+            stream, 10, fl), k=K_)
+        if backward:
+            g = torch.ones((w.rows, K_), device=dev)
+            d = torch.empty_like(x)
+            record(f"{tag}/selective_logsoftmax_bwd", w, "logp_bwd", time_op(
+                lambda: gbce.selective_logsoftmax_bwd(x, idx, g, o, T, mask, dlogits=d),
+                stream, 10, fl), k=K_)
 
     w = workloads.ce_small_fp32(device=dev)
     ce_ops("ce_small_fp32_64x4096", w, 1.0, "mean", torch.ones(1, device=dev))
@@ -479,6 +490,8 @@ def measure_configs(gbce, dev, stream, peak):
     logp_op("split_bf16_64x152064", w, TEMPERATURE)
     w = workloads.grpo_bf16(device=dev, rows=ROWS)
     ce_ops(f"grpo_bf16_{ROWS}x{VOCAB}", w, TEMPERATURE, "mean", torch.ones(1, device=dev))
+    logp_op(f"grpo_bf16_{ROWS}x{VOCAB}_k4", w, TEMPERATURE, backward=True)
+    logp_op(f"grpo_bf16_{ROWS}x{VOCAB}_k1", w, TEMPERATURE, backward=True, k=1)
     del w, flush
     torch.cuda.empty_cache()
     return out

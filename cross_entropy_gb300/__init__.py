@@ -11,7 +11,8 @@ Functions (same names as the C ABI):
 
 * :func:`selective_logsoftmax` -- log p at K gathered indices per row, with
   temperature and row mask ("perf(rlhf): chunk selective_log_softmax instead
-  of looping per token", "PR information").
+  of looping per token", "PR information"); :func:`selective_logsoftmax_bwd`
+  its gradient, the one a GRPO-style loss sends back.
 * :func:`ce_fwd`, :func:`ce_bwd`, :func:`ce_fwd_bwd_fused` -- token
   cross-entropy in the collapse-safe form of "Fix softmax collapse in CE,
   GRPO, KL/JSD and softmax" ("Summary"), with the analytic backward
@@ -45,6 +46,8 @@ _SIGNATURES = {
     "gbce_kernel_launches": (ctypes.c_uint64, []),
     "selective_logsoftmax": (_i32, [_vp, _i32, _i64, _i64, _i64, _vp, _i64, _f32, _vp, _vp,
                                     _vp, _sz, _vp, _vp]),
+    "selective_logsoftmax_bwd": (_i32, [_vp, _i32, _i64, _i64, _i64, _vp, _i64, _f32, _vp, _vp,
+                                        _vp, _vp, _i64, _vp, _vp]),
     "ce_fwd": (_i32, [_vp, _i32, _i64, _i64, _i64, _vp, _i64, _f32, _i32, _vp, _vp, _vp, _vp,
                       _vp, _sz, _vp, _vp]),
     "ce_bwd": (_i32, [_vp, _i32, _i64, _i64, _i64, _vp, _i64, _f32, _i32, _vp, _vp, _vp, _vp,
@@ -177,6 +180,40 @@ def selective_logsoftmax(logits: torch.Tensor, index, temperature: float = 1.0,
     _check(st, "selective_logsoftmax")
     res = out.view(*lead_shape, K)
     return res.squeeze(-1) if squeeze else res
+
+
+def selective_logsoftmax_bwd(logits: torch.Tensor, index, grad_logp, saved_logp,
+                             temperature: float = 1.0, row_mask: Optional[torch.Tensor] = None,
+                             *, dlogits: Optional[torch.Tensor] = None,
+                             dev_status: Optional[torch.Tensor] = None,
+                             stream=None) -> torch.Tensor:
+    """dL/dlogits for upstream grad_logp = dL/d selective_logsoftmax(...).
+
+    ``index``, ``grad_logp`` and ``saved_logp`` have the forward's output
+    shape ([..., K], or [...] for K = 1); masked-out rows get zero.
+    """
+    lib = load_library()
+    lead_shape = logits.shape[:-1]
+    x = _rows_view(logits)
+    rows, V = x.shape
+    idx = _dev_int64(index, x.device)
+    K = 1 if idx.dim() == len(lead_shape) else idx.shape[-1]
+    idx = idx.reshape(rows, K)
+    g = torch.as_tensor(grad_logp, dtype=torch.float32, device=x.device).reshape(rows, K)
+    g = g.contiguous()
+    lp = saved_logp.to(torch.float32).reshape(rows, K).contiguous()
+    mask = None
+    if row_mask is not None:
+        mask = row_mask.to(device=x.device, dtype=torch.uint8).reshape(rows).contiguous()
+    if dlogits is None:
+        dlogits = torch.empty_like(logits)
+    d = _rows_view(dlogits)
+    st = lib.selective_logsoftmax_bwd(x.data_ptr(), _dtype_code(x), rows, V, x.stride(0),
+                                      idx.data_ptr(), K, float(temperature), _ptr(mask),
+                                      g.data_ptr(), lp.data_ptr(), d.data_ptr(), d.stride(0),
+                                      _ptr(dev_status), _stream_ptr(stream))
+    _check(st, "selective_logsoftmax_bwd")
+    return dlogits
 
 
 class CeForward(NamedTuple):

@@ -246,6 +246,39 @@ gbce_status selective_logsoftmax(const void *logits, gbce_dtype dtype, int64_t r
     return cuda_status(e);
 }
 
+gbce_status selective_logsoftmax_bwd(const void *logits, gbce_dtype dtype, int64_t rows,
+                                     int64_t vocab, int64_t row_stride, const int64_t *index,
+                                     int64_t k, float temperature, const uint8_t *row_mask,
+                                     const float *grad_logp, const float *saved_logp,
+                                     void *dlogits, int64_t dlogits_row_stride,
+                                     int32_t *dev_status, void *stream)
+{
+    gbce_status st = check_logits(logits, dtype, rows, vocab, row_stride, temperature);
+    if (st != GBCE_OK)
+        return st;
+    if (k < 1 || k > GBCE_MAX_K)
+        return GBCE_EINVAL;
+    if (rows == 0)
+        return GBCE_OK;
+    if (index == nullptr || grad_logp == nullptr || saved_logp == nullptr)
+        return GBCE_EINVAL;
+    if ((st = check_dlogits(logits, dtype, rows, vocab, row_stride, dlogits,
+                            dlogits_row_stride)) != GBCE_OK)
+        return st;
+
+    RowParams p = base_params(logits, dtype, rows, vocab, row_stride, temperature, dev_status);
+    p.targets = index;
+    p.k = k;
+    p.row_mask = row_mask;
+    p.dlogits = dlogits;
+    p.d_stride = dlogits_row_stride;
+    p.vec_store = same_vector_phase(logits, row_stride, dlogits, dlogits_row_stride, dtype);
+    p.grad_out = grad_logp;
+    p.saved_logp = saved_logp;
+    return cuda_status(
+        launch_rows(p, dtype, gbce::kModeLogpGrad, static_cast<cudaStream_t>(stream)));
+}
+
 gbce_status ce_fwd(const void *logits, gbce_dtype dtype, int64_t rows, int64_t vocab,
                    int64_t row_stride, const int64_t *labels, int64_t ignore_index,
                    float temperature, gbce_reduction reduction, float *loss_out,

@@ -16,6 +16,7 @@ enum Mode : int {
     kModeCe = 1,     // cross-entropy forward statistics (label, ignore_index)
     kModeGrad = 2,   // cross-entropy gradient from saved log p (ce_bwd)
     kModeFused = 3,  // statistics then gradient of the same row (one launch)
+    kModeLogpGrad = 4,  // selective log-softmax gradient from saved log p (K indices)
 };
 
 struct RowParams {
@@ -39,10 +40,10 @@ struct RowParams {
     void *dlogits;  // kModeGrad / kModeFused
     int64_t d_stride;
     int vec_store;  // dlogits rows share the logits rows' 16-byte phase
-    const float *grad_out;
+    const float *grad_out;    // CE: [rows] or [1]; kModeLogpGrad: [rows, k]
     int reduction;  // 0 none, 1 sum, 2 mean
     const int64_t *n_items;
-    const float *saved_logp;  // kModeGrad
+    const float *saved_logp;  // kModeGrad: [rows]; kModeLogpGrad: [rows, k]
 
     int32_t *dev_status;
 };

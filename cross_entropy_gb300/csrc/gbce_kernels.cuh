@@ -369,8 +369,9 @@ __global__ void __launch_bounds__(kRowThreads, 2) row_kernel(const RowParams p)
     constexpr int CV = kChunkBytes / 16;  // vectors per full chunk
     constexpr int PER_THREAD = CV / NC;
     static_assert(CV % NC == 0, "chunk must split evenly over consumer threads");
-    constexpr bool kStats = (MODE != kModeGrad);
-    constexpr bool kGrad = (MODE == kModeGrad || MODE == kModeFused);
+    constexpr bool kStats = (MODE != kModeGrad && MODE != kModeLogpGrad);
+    constexpr bool kGrad = (MODE == kModeGrad || MODE == kModeFused || MODE == kModeLogpGrad);
+    constexpr bool kGather = (MODE == kModeLogp || MODE == kModeLogpGrad);  // K indices
     constexpr int kPasses = (MODE == kModeFused) ? 2 : 1;
 
     extern __shared__ __align__(128) uint8_t dyn_smem[];
@@ -380,6 +381,8 @@ __global__ void __launch_bounds__(kRowThreads, 2) row_kernel(const RowParams p)
     __shared__ uint64_t empty_bar[kStages];
     __shared__ float red_m[NCW], red_s[NCW];
     __shared__ float s_xt[KMAX];
+    __shared__ float s_dt[KMAX];       // kModeLogpGrad: gradient at each gathered column
+    __shared__ float s_G, s_lp0;       // kModeLogpGrad: sum of upstream, log p of index 0
     __shared__ int32_t s_tg[KMAX];
     __shared__ float bc_m, bc_s, bc_logp;
     __shared__ uint64_t xbar;                   // fused, cluster of CTAs per row
@@ -397,17 +400,23 @@ __global__ void __launch_bounds__(kRowThreads, 2) row_kernel(const RowParams p)
     // ---- row selection, before any read of this row's logits
     int32_t tg[KMAX];
     int32_t y = -1;
-    int state = 0;  // 0 live, 1 skipped (ignored label / masked row), 2 bad label
-    if (MODE == kModeLogp) {
+    int state = 0;  // 0 live, 1 skipped (ignored label / masked row), 2 bad label / index
+    if (kGather) {
         if (p.row_mask != nullptr && p.row_mask[r] == 0)
             state = 1;
+        bool any_bad = false;
 #pragma unroll
         for (int k = 0; k < KMAX; ++k) {
             int64_t t = -1;
-            if (state == 0 && k < p.k)
+            if (state == 0 && k < p.k) {
                 t = p.targets[r * p.k + k];
+                any_bad |= (t < 0 || t >= V);
+            }
             tg[k] = (t >= 0 && t < V) ? static_cast<int32_t>(t) : -1;
         }
+        // the forward NaNs just the bad (r, k); its gradient NaNs the row
+        if (MODE == kModeLogpGrad && any_bad)
+            state = 2;
     } else {
         const int64_t lab = p.targets[r];
         if (lab == p.ignore_index)
@@ -427,6 +436,10 @@ __global__ void __launch_bounds__(kRowThreads, 2) row_kernel(const RowParams p)
         if (MODE == kModeLogp) {
             if (direct && tid < p.k)
                 p.logp_out[r * p.k + tid] = 0.0f;
+        } else if (MODE == kModeLogpGrad) {
+            if (tid == 0 && split == 0 && state == 2)
+                report(p.dev_status, GBCE_DEV_BAD_INDEX);
+            fill_row_slice<T>(drow, V, split, p.splits, fill);
         } else {
             if (tid == 0 && (direct || MODE == kModeGrad) && split == 0 && state == 2)
                 report(p.dev_status, GBCE_DEV_BAD_LABEL);
@@ -464,6 +477,35 @@ __global__ void __launch_bounds__(kRowThreads, 2) row_kernel(const RowParams p)
         if (exchange)
             mbar_init(&xbar, 1);
         fence_barrier_init();
+    }
+    if (MODE == kModeLogpGrad) {
+        // gathered column t: (1/T)(-g_t expm1(log p_t) - (G - g_t) exp(log p_t)),
+        // g_t the upstream of every k that gathers t; every other column j:
+        // -(G/T) exp((x_j - x_{t0})/T + log p_{t0})
+        if (tid < p.k) {
+            const float *gr = p.grad_out + r * p.k;
+            float G = 0.0f, gt = 0.0f;
+            int32_t mine = -1;
+#pragma unroll
+            for (int k = 0; k < KMAX; ++k)
+                if (k == tid)
+                    mine = tg[k];
+#pragma unroll
+            for (int k = 0; k < KMAX; ++k)
+                if (k < p.k) {
+                    const float gk = gr[k];
+                    G += gk;
+                    if (tg[k] == mine)
+                        gt += gk;
+                }
+            const float lp = p.saved_logp[r * p.k + tid];
+            s_dt[tid] = (-gt * expm1f(lp) - (G - gt) * expf(lp)) / p.T;
+            if (tid == 0) {
+                s_G = G;
+                s_lp0 = lp;
+                s_xt[0] = E::load(row + mine);
+            }
+        }
     }
     if (kStats) {
         // target logits, for the finalize step (loaded while the sweep runs)
@@ -659,7 +701,66 @@ __global__ void __launch_bounds__(kRowThreads, 2) row_kernel(const RowParams p)
         }
     }
 
-    if (kGrad) {
+    if (MODE == kModeLogpGrad) {
+        const GradConsts gk = grad_consts(s_xt[0], c, s_lp0, -s_G / p.T);
+        float dtv[KMAX];
+#pragma unroll
+        for (int k = 0; k < KMAX; ++k)
+            dtv[k] = s_dt[k];
+        const auto at_target = [&](int32_t col, float dflt) {
+            float v = dflt;
+#pragma unroll
+            for (int k = 0; k < KMAX; ++k)
+                v = (tg[k] == col) ? dtv[k] : v;
+            return v;
+        };
+        constexpr int32_t kNoLabel = 0x7fffffff;
+        if (split == 0)
+            for (int64_t e = tid; e < g.head; e += NC)
+                E::store(drow + e, at_target(static_cast<int32_t>(e),
+                                             grad_scalar(E::load(row + e), gk)));
+        if (split == p.splits - 1)
+            for (int64_t e = g.tail0 + tid; e < V; e += NC)
+                E::store(drow + e, at_target(static_cast<int32_t>(e),
+                                             grad_scalar(E::load(row + e), gk)));
+        for (int64_t i = 0; i < nchunks; ++i, ++seq) {
+            const int slot = static_cast<int>(seq % kStages);
+            if (alive && !mbar_wait(&full_bar[slot], static_cast<uint32_t>((seq / kStages) & 1))) {
+                alive = false;
+                report(p.dev_status, GBCE_DEV_TIMEOUT);
+            }
+            if (alive) {
+                const uint4 *chunk = reinterpret_cast<const uint4 *>(ring + slot * kChunkBytes);
+                const int64_t nv = (v1 - v0 - i * CV) < CV ? (v1 - v0 - i * CV) : CV;
+                const int64_t vbase = v0 + i * CV;
+                T *dbase = drow + g.head + vbase * VEC;
+                for (int v = tid; v < nv; v += NC) {
+                    const uint4 raw = chunk[v];
+                    const int32_t vb = static_cast<int32_t>(vbase + v);
+                    if (!vector_has_target<KMAX>(tv, vb) && p.vec_store) {
+                        st_cs_v4(dbase + v * VEC, GradVec<T>::run(raw, kNoLabel, gk));
+                        continue;
+                    }
+                    float d[VEC];
+                    GradVec<T>::run_unpacked(raw, kNoLabel, gk, d);
+                    const int32_t col0v = static_cast<int32_t>(g.head) + vb * VEC;
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e)
+                        d[e] = at_target(col0v + e, d[e]);
+                    if (p.vec_store) {
+                        st_cs_v4(dbase + v * VEC, E::pack(d));
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < VEC; ++e)
+                            E::store(dbase + v * VEC + e, d[e]);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&empty_bar[slot]);
+        }
+    } else if (kGrad) {
         if (MODE == kModeGrad) {
             logp = p.saved_logp[r];
             xy = E::load(row + y);
@@ -871,6 +972,12 @@ cudaError_t launch_rows_per_unit(const RowParams &p, int mode, cudaStream_t stre
         return launch_row_kernel<T, kModeGrad, 1>(p, stream);
     case kModeFused:
         return launch_row_kernel<T, kModeFused, 1>(p, stream);
+    case kModeLogpGrad:
+        if (p.k <= 1)
+            return launch_row_kernel<T, kModeLogpGrad, 1>(p, stream);
+        if (p.k <= 4)
+            return launch_row_kernel<T, kModeLogpGrad, 4>(p, stream);
+        return launch_row_kernel<T, kModeLogpGrad, GBCE_MAX_K>(p, stream);
     default:
         return cudaErrorInvalidValue;
     }

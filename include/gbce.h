@@ -115,6 +115,39 @@ gbce_status selective_logsoftmax(const void *logits, gbce_dtype dtype, int64_t r
                                  int32_t *dev_status, void *stream);
 
 /*
+ * Selective log-softmax backward: the gradient of sum_k g[r, k] *
+ * log p_{index[r, k]} with respect to the logits,
+ *   dlogits[r, j] = (1/T) * ( sum_{k : index[r, k] = j} g[r, k] - G_r * p_j ),
+ * G_r = sum_k g[r, k], with every gathered column t evaluated as
+ *   (1/T) * ( -g_t * expm1(log p_t) - (G_r - g_t) * exp(log p_t) )
+ * (g_t = the upstream of every k that gathers t) so that 1 - p_t keeps its
+ * value when p_t rounds to 1; masked-out rows get a zero row.
+ *
+ * Source: the gradient a GRPO-style loss sends back through the accurate
+ * log-probs of "Fix softmax collapse in CE, GRPO, KL/JSD and softmax"
+ * (Liger-Kernel PR #1555), "Summary", second bullet (-expm1(logp) for
+ * 1 - p_y); gradients are part of the checked behaviour of "perf(rlhf):
+ * chunk selective_log_softmax instead of looping per token", "PR
+ * information".
+ *
+ *   index       [rows, k] int64, as given to selective_logsoftmax
+ *   row_mask    [rows] uint8 or NULL
+ *   grad_logp   [rows, k] fp32, device: dL/d logp_out
+ *   saved_logp  [rows, k] fp32: selective_logsoftmax's output for the same
+ *               logits, index and temperature
+ *   dlogits     [rows, dlogits_row_stride], the logits' dtype; must not
+ *               overlap the logits
+ * Errors: as ce_bwd; a row with an index outside [0, vocab) sets
+ * GBCE_DEV_BAD_INDEX and gets a NaN row.
+ */
+gbce_status selective_logsoftmax_bwd(const void *logits, gbce_dtype dtype, int64_t rows,
+                                     int64_t vocab, int64_t row_stride, const int64_t *index,
+                                     int64_t k, float temperature, const uint8_t *row_mask,
+                                     const float *grad_logp, const float *saved_logp,
+                                     void *dlogits, int64_t dlogits_row_stride,
+                                     int32_t *dev_status, void *stream);
+
+/*
  * Token cross-entropy forward.  For rows whose label is not ignore_index:
  * loss_r = -log p_{labels[r]} at temperature T; ignored rows are skipped
  * before any read of their logits and get loss 0.

@@ -1,0 +1,137 @@
+"""GPU parity of selective_logsoftmax_bwd (the GRPO-style gradient through the
+gathered log-probs) against the fp64 oracle, through the C ABI."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from helpers import assert_grad_rows_close, assert_zero_sum_rows, to_f64
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    import cross_entropy_gb300 as gbce
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    import __graft_entry__
+
+    __graft_entry__.build()
+    gbce.load_library()
+
+
+def run_case(x_cpu, idx, g, T, mask=None, rows_sel=None, dlogits=None, x_dev=None):
+    """GPU forward + backward on x; oracle backward on rows_sel."""
+    x = x_cpu.to(DEV) if x_dev is None else x_dev
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    m_dev = None if mask is None else mask.to(DEV)
+    lp = gbce.selective_logsoftmax(x, idx.to(DEV), T, m_dev, dev_status=status)
+    d = gbce.selective_logsoftmax_bwd(x, idx.to(DEV), g.to(DEV), lp, T, m_dev,
+                                      dlogits=dlogits, dev_status=status)
+    torch.cuda.synchronize()
+    sel = np.arange(x_cpu.shape[0]) if rows_sel is None else np.asarray(rows_sel)
+    st = torch.as_tensor(sel)
+    ref, bad = oracle.selective_logsoftmax_backward(
+        workloads.to_numpy_f64(x_cpu[st]), idx.numpy()[sel], g.double().numpy()[sel], T,
+        None if mask is None else mask.numpy()[sel])
+    got = to_f64(d[st.to(DEV)])
+    return got, ref, int(status.item()), bad
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("K", [1, 4])
+def test_matches_oracle_with_masks_and_duplicates(dtype, K):
+    gen = torch.Generator().manual_seed(40 + K)
+    rows, V = 600, 32003
+    w = workloads.collapse_stress(dtype=dtype, rows=rows, V=V, seed=K)
+    idx = torch.randint(0, V, (rows, K), generator=gen)
+    idx[:, 0] = torch.where(w.labels >= 0, w.labels, idx[:, 0])   # confident rows' label first
+    if K > 1:
+        idx[::3, 2] = idx[::3, 0]                                  # duplicates
+    mask = (torch.rand(rows, generator=gen) > 0.1).to(torch.uint8)
+    g = torch.randn((rows, K), generator=gen)
+    sel = np.arange(0, rows, 7)
+    got, ref, status, bad = run_case(w.logits, idx, g, 0.9, mask, rows_sel=sel)
+    assert status == 0 and bad == 0
+    assert_grad_rows_close(got, ref, dtype, "selective_logsoftmax_bwd")
+    assert_zero_sum_rows(got, dtype)
+    assert np.all(got[mask.numpy()[sel] == 0] == 0.0)
+
+
+def test_confident_rows_keep_their_target_gradient():
+    w = workloads.collapse_stress(dtype=torch.float32, rows=520, V=151936, seed=9)
+    idx = torch.where(w.labels >= 0, w.labels, 0)[:, None]
+    g = torch.full((520, 1), -1.0)              # e.g. a positive advantage
+    pk = w.peaked_rows.numpy()
+    sel = pk[w.labels.numpy()[pk] >= 0][:40]
+    got, ref, status, _ = run_case(w.logits, idx, g, 1.0, rows_sel=sel)
+    assert status == 0
+    assert_grad_rows_close(got, ref, torch.float32)
+    cols = idx.numpy()[sel, 0]
+    # d(-log p_t)/dx_t = -(1 - p_t) / T: tiny but never rounded to zero
+    assert np.all(got[np.arange(len(sel)), cols] < 0.0)
+    assert_zero_sum_rows(got, torch.float32)
+
+
+@pytest.mark.parametrize("rows", [1, 3])
+def test_few_rows_split_path(rows):
+    w = workloads.collapse_stress(dtype=torch.bfloat16, rows=rows, V=152064, seed=rows)
+    idx = torch.randint(0, 152064, (rows, 4), generator=torch.Generator().manual_seed(3))
+    g = torch.randn((rows, 4), generator=torch.Generator().manual_seed(4))
+    got, ref, status, _ = run_case(w.logits, idx, g, 0.9)
+    assert status == 0
+    assert_grad_rows_close(got, ref, torch.bfloat16)
+
+
+def test_strided_rows_unaligned_dlogits():
+    gen = torch.Generator().manual_seed(12)
+    rows, V = 530, 9001
+    big = torch.randn((rows, V + 5), generator=gen).mul(3)
+    x_cpu = big[:, 2:2 + V]
+    idx = torch.randint(0, V, (rows, 4), generator=gen)
+    g = torch.randn((rows, 4), generator=gen)
+    dbig = torch.empty((rows, V + 3), device=DEV)
+    d = dbig[:, 3:]
+    got, ref, status, _ = run_case(x_cpu, idx, g, 0.7, rows_sel=np.arange(0, rows, 11),
+                                   dlogits=d, x_dev=big.to(DEV)[:, 2:2 + V])
+    assert status == 0
+    assert_grad_rows_close(got, ref, torch.float32)
+
+
+def test_full_size_grpo_k4():
+    w = workloads.grpo_bf16(device=DEV)
+    g = torch.randn((w.rows, 4), device=DEV, generator=torch.Generator(device=DEV).manual_seed(1))
+    lp = gbce.selective_logsoftmax(w.logits, w.index, 0.9)
+    d = gbce.selective_logsoftmax_bwd(w.logits, w.index, g, lp, 0.9)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(0)
+    sel = np.sort(np.concatenate([rng.choice(w.rows, 20, replace=False),
+                                  w.peaked_rows.cpu().numpy()[:12]]))
+    st = torch.as_tensor(sel, device=DEV)
+    ref, _ = oracle.selective_logsoftmax_backward(workloads.to_numpy_f64(w.logits[st]),
+                                                  w.index[st].cpu().numpy(),
+                                                  g[st].double().cpu().numpy(), 0.9)
+    assert_grad_rows_close(to_f64(d[st]), ref, torch.bfloat16)
+    rs = d.double().sum(1).abs()
+    ra = d.double().abs().sum(1)
+    assert bool(torch.all(rs <= 4e-3 * ra))
+
+
+def test_bad_index_gives_nan_row_and_status():
+    x = torch.randn((4, 300), device=DEV)
+    idx = torch.tensor([[1, 2], [300, 3], [4, -1], [5, 5]], device=DEV)
+    g = torch.ones((4, 2), device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    lp = gbce.selective_logsoftmax(x, idx.clamp(0, 299), 1.0)
+    d = gbce.selective_logsoftmax_bwd(x, idx, g, lp, 1.0, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == gbce.DEV_BAD_INDEX
+    assert torch.isnan(d[1]).all() and torch.isnan(d[2]).all()
+    assert torch.isfinite(d[0]).all() and torch.isfinite(d[3]).all()
