@@ -20,6 +20,9 @@ Functions and the passages they follow:
 * :func:`selective_logsoftmax_backward` -- the gradient of sum_k g_k log p_{t_k}:
   (1/T)(sum_{k: t_k = j} g_k - G p_j), with the gathered columns in the
   -expm1(log p_t) form of the same page's "Summary" (second bullet).
+* :func:`entropy` -- -sum_j p_j log p_j per row, the reference column's term
+  from its accurate log p (the per-token entropy of the unsloth-zoo #2080
+  commit quoted on the same page, "Fix").
 * :func:`cross_entropy` -- the same page's "Summary" (loss from the sum that
   excludes the target) with ms-swift PR #10353's "PR information" (analytic
   backward g*softmax - g*onehot, zero weight on ignored labels) and the
@@ -84,6 +87,8 @@ def _load():
         lib.oracle_selective_logsoftmax_backward.restype = i64
         lib.oracle_selective_logsoftmax_backward.argtypes = [
             dp, i64, i64, i64, ip, i64, ctypes.c_double, ctypes.c_void_p, dp, dp, i64]
+        lib.oracle_entropy.restype = i64
+        lib.oracle_entropy.argtypes = [dp, i64, i64, i64, ip, ctypes.c_double, ctypes.c_void_p, dp]
         lib.oracle_num_threads.restype = ctypes.c_int
         lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
         _lib = lib
@@ -162,6 +167,27 @@ def selective_logsoftmax_backward(x, index, grad, temperature: float = 1.0, row_
         exact_temperature(temperature), mask_ptr, _ptr(g, ctypes.c_double),
         _ptr(dx, ctypes.c_double), V)
     return dx, int(bad)
+
+
+def entropy(x, ref, temperature: float = 1.0, live=None):
+    """-sum_j p_j log p_j per row, column ref[r] entering with its accurate log p.
+
+    Rows with live[r] == 0 give 0.  Returns ``(out[rows] float64, n_bad)``.
+    """
+    lib = _load()
+    x = _as_rows(x)
+    rows, V = x.shape
+    t = np.ascontiguousarray(np.asarray(ref, dtype=np.int64).reshape(rows))
+    live_arr = None
+    live_ptr = None
+    if live is not None:
+        live_arr = np.ascontiguousarray(np.asarray(live).reshape(rows).astype(np.uint8))
+        live_ptr = live_arr.ctypes.data
+    out = np.empty(rows, dtype=np.float64)
+    bad = lib.oracle_entropy(_ptr(x, ctypes.c_double), rows, V, x.strides[0] // 8,
+                             _ptr(t, ctypes.c_int64), exact_temperature(temperature), live_ptr,
+                             _ptr(out, ctypes.c_double))
+    return out, int(bad)
 
 
 def cross_entropy(x, labels, ignore_index: int = -100, temperature: float = 1.0,

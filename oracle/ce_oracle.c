@@ -54,6 +54,13 @@
  * as (1/T) * ( -g_t * expm1(log p_t) - (G - g_t) * exp(log p_t) ), which
  * keeps 1 - p_t exact when p_t rounds to 1; masked-out rows get a zero row.
  *
+ * Entropy of a row's softmax (the per-token entropy the unsloth-zoo #2080
+ * commit computes beside the log-probs, "Fix"): H = -sum_j p_j log p_j.  The
+ * reference column t (the label, or a row's first gathered index) enters
+ * with its collapse-safe log p_t, every other column with
+ * log p_j = z_j - lse, lse = z_t - log p_t; so a row whose t holds almost all
+ * of the mass keeps its small positive entropy instead of rounding to 0.
+ *
  * An index or label outside [0,V) (and, for labels, not ignore_index)
  * makes that row's outputs NaN and is counted in the return value.
  */
@@ -115,6 +122,51 @@ static double softplus(double a)
 static double row_logp(const double *x, int64_t V, int64_t t, double T)
 {
     return -softplus(lse_excluding(x, V, t, T) - x[t] / T);
+}
+
+/* -sum_j p_j log p_j of one row, with column t's term from its accurate log p. */
+static double row_entropy(const double *x, int64_t V, int64_t t, double T)
+{
+    const double lp_t = row_logp(x, V, t, T);
+    const double lse = x[t] / T - lp_t;
+    oracle_sum h = {0.0, 0.0};
+    sum_add(&h, -exp(lp_t) * lp_t);
+    for (int64_t j = 0; j < V; ++j) {
+        if (j == t)
+            continue;
+        const double lp = x[j] / T - lse;
+        sum_add(&h, -exp(lp) * lp);
+    }
+    return sum_value(&h);
+}
+
+/*
+ * Row entropy.
+ *   x        [rows, ld] fp64
+ *   ref      [rows] int64: the reference column of each row
+ *   live     [rows] uint8 or NULL: rows with 0 are skipped (entropy 0)
+ *   out      [rows] fp64
+ * Returns the number of live rows whose reference column is out of range.
+ */
+int64_t oracle_entropy(const double *x, int64_t rows, int64_t V, int64_t ld, const int64_t *ref,
+                       double T, const uint8_t *live, double *out)
+{
+    int64_t bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(+ : bad)
+    for (int64_t r = 0; r < rows; ++r) {
+        if (live && live[r] == 0) {
+            out[r] = 0.0;
+            continue;
+        }
+        const int64_t t = ref[r];
+        if (t < 0 || t >= V) {
+            out[r] = NAN;
+            ++bad;
+            continue;
+        }
+        out[r] = row_entropy(x + r * ld, V, t, T);
+    }
+    return bad;
 }
 
 int oracle_num_threads(void)

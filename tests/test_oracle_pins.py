@@ -442,3 +442,59 @@ def test_selective_backward_uniform_rows_and_invariants():
         np.testing.assert_allclose(dx[r], want, rtol=1e-12)
         assert abs(math.fsum(dx[r])) <= 1e-13 * math.fsum(np.abs(dx[r]))
     assert np.all(dx[2] == 0.0)
+
+
+# --------------------------------------------------------------- row entropy
+
+def brute_entropy(row, T):
+    logps, _ = brute_row(row, 0, T)
+    h = Decimal(0)
+    for lp in logps:
+        h = CTX.subtract(h, CTX.multiply(CTX.exp(lp), lp))
+    return float(h)
+
+
+@pytest.mark.parametrize("V", [2, 5, 33])
+@pytest.mark.parametrize("T", [1.0, 0.7])
+def test_entropy_brute_force(V, T):
+    margins = [0.0, 5.0, 17.0, 30.0, 50.0]
+    w = workloads.peaked_rows_tiny(V, margins, seed=300 + V)
+    x = w.logits.numpy()
+    y = w.labels.numpy()
+    x[0] = np.random.default_rng(V).normal(scale=3.0, size=V)
+    h, bad = oracle.entropy(x, y, T)
+    assert bad == 0
+    Te = oracle.exact_temperature(T)
+    for r in range(len(margins)):
+        want = brute_entropy(x[r], Te)
+        assert h[r] == pytest.approx(want, rel=1e-11, abs=1e-300), (r, margins[r])
+        assert h[r] > 0.0          # never collapses to 0 for a finite margin
+
+
+def test_entropy_closed_forms_and_bounds():
+    V = 1000
+    x = np.full((2, V), 0.25)
+    h, _ = oracle.entropy(x, [3, 999], 0.8)
+    np.testing.assert_allclose(h, math.log(V), rtol=1e-14)      # uniform: log V
+    # two-level row: target a, V-1 others b
+    a, b, T = 4.0, 1.0, 1.0
+    x = np.full((1, V), b)
+    x[0, 10] = a
+    p_t = 1.0 / (1.0 + (V - 1) * math.exp(b - a))
+    p_o = (1.0 - p_t) / (V - 1)
+    want = -p_t * math.log(p_t) - (V - 1) * p_o * math.log(p_o)
+    assert oracle.entropy(x, [10], T)[0][0] == pytest.approx(want, rel=1e-13)
+    # V = 1: certain, the reference column does not change the value
+    assert oracle.entropy(np.array([[2.0]]), [0], 1.0)[0][0] == 0.0
+    rng = np.random.default_rng(8)
+    x = rng.normal(scale=4, size=(20, 77))
+    h1, _ = oracle.entropy(x, rng.integers(0, 77, 20), 0.9)
+    h2, _ = oracle.entropy(x, rng.integers(0, 77, 20), 0.9)
+    np.testing.assert_allclose(h1, h2, rtol=1e-12)              # any reference column
+    assert np.all(h1 >= 0.0) and np.all(h1 <= math.log(77))
+
+
+def test_entropy_skips_dead_rows_and_flags_bad_references():
+    x = np.random.default_rng(1).normal(size=(3, 9))
+    h, bad = oracle.entropy(x, [1, 50, 2], 1.0, live=[1, 1, 0])
+    assert bad == 1 and np.isnan(h[1]) and h[2] == 0.0 and h[0] > 0.0
