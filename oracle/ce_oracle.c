@@ -124,18 +124,25 @@ static double row_logp(const double *x, int64_t V, int64_t t, double T)
     return -softplus(lse_excluding(x, V, t, T) - x[t] / T);
 }
 
+/* -p log p for p = e^lp, with 0 log 0 = 0. */
+static double neg_plogp(double lp)
+{
+    const double p = exp(lp);
+    return p == 0.0 ? 0.0 : -p * lp;
+}
+
 /* -sum_j p_j log p_j of one row, with column t's term from its accurate log p. */
 static double row_entropy(const double *x, int64_t V, int64_t t, double T)
 {
     const double lp_t = row_logp(x, V, t, T);
-    const double lse = x[t] / T - lp_t;
+    /* logsumexp of all columns; the others' alone when p_t is exactly 0 */
+    const double lse = lp_t == -INFINITY ? lse_excluding(x, V, t, T) : x[t] / T - lp_t;
     oracle_sum h = {0.0, 0.0};
-    sum_add(&h, -exp(lp_t) * lp_t);
+    sum_add(&h, neg_plogp(lp_t));
     for (int64_t j = 0; j < V; ++j) {
         if (j == t)
             continue;
-        const double lp = x[j] / T - lse;
-        sum_add(&h, -exp(lp) * lp);
+        sum_add(&h, neg_plogp(x[j] / T - lse));
     }
     return sum_value(&h);
 }

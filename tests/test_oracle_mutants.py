@@ -39,8 +39,8 @@ MUTANTS = {
     "sel_bwd_others_use_all_of_G": ("- (Gv - g_t) * exp(lp)) / T;", "- Gv * exp(lp)) / T;"),
     "sel_bwd_duplicates_not_summed": ("                if (idx[r * K + i] == t)\n                    sum_add(&gt",
                                       "                if (i == k)\n                    sum_add(&gt"),
-    "entropy_target_term_dropped": ("    sum_add(&h, -exp(lp_t) * lp_t);\n", ""),
-    "entropy_lse_sign": ("const double lse = x[t] / T - lp_t;", "const double lse = x[t] / T + lp_t;"),
+    "entropy_target_term_dropped": ("    sum_add(&h, neg_plogp(lp_t));\n", ""),
+    "entropy_lse_sign": (": x[t] / T - lp_t;", ": x[t] / T + lp_t;"),
     "sel_bwd_missing_inverse_T": ("dr[j] = -(Gv / T) * exp(xr[j] / T - lse);",
                                   "dr[j] = -Gv * exp(xr[j] / T - lse);"),
 }

@@ -498,3 +498,15 @@ def test_entropy_skips_dead_rows_and_flags_bad_references():
     x = np.random.default_rng(1).normal(size=(3, 9))
     h, bad = oracle.entropy(x, [1, 50, 2], 1.0, live=[1, 1, 0])
     assert bad == 1 and np.isnan(h[1]) and h[2] == 0.0 and h[0] > 0.0
+
+
+def test_entropy_ignores_zero_probability_columns():
+    # a column at -inf has p = 0 and adds nothing (0 log 0 = 0), also as the
+    # reference column
+    rng = np.random.default_rng(21)
+    base = rng.normal(scale=2, size=(1, 40))
+    x = np.concatenate([base, np.full((1, 3), -np.inf)], axis=1)
+    want = oracle.entropy(base, [5], 0.9)[0][0]
+    for ref in (5, 40, 42):
+        got, bad = oracle.entropy(x, [ref], 0.9)
+        assert bad == 0 and got[0] == pytest.approx(want, rel=1e-13), ref
