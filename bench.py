@@ -380,11 +380,13 @@ def op_bytes(w, op, k=1):
     of every row written once, int64 labels / indices and fp32 outputs."""
     es = w.logits.element_size()
     rows, V = w.rows, w.vocab
-    if op in ("logp", "logp_bwd"):
+    if op in ("logp", "logp_ent", "logp_bwd"):
         live = rows if w.row_mask is None else int(w.row_mask.sum().item())
         mask = 0 if w.row_mask is None else rows
         if op == "logp":
             return live * V * es + rows * k * 8 + rows * k * 4 + mask
+        if op == "logp_ent":  # + one fp32 entropy per row
+            return live * V * es + rows * k * 8 + rows * k * 4 + rows * 4 + mask
         # logits in, dlogits out, index + upstream gradient + saved log-probs
         return live * V * es + rows * V * es + rows * k * (8 + 4 + 4) + mask
     live = int((w.labels != workloads.IGNORE_INDEX).sum().item())
@@ -454,7 +456,7 @@ def measure_configs(gbce, dev, stream, peak):
             lambda: gbce.ce_bwd(x, lab, g, fwd.logp, fwd.n_items, temperature=T, reduction=red,
                                 dlogits=d), stream, 10, fl))
 
-    def logp_op(tag, w, T, backward=False, k=None):
+    def logp_op(tag, w, T, backward=False, k=None, entropy=False):
         x, idx = w.logits, (w.index if k is None else w.index[:, :k].contiguous())
         mask = w.row_mask
         K_ = idx.shape[1]
@@ -464,6 +466,11 @@ def measure_configs(gbce, dev, stream, peak):
         record(f"{tag}/selective_logsoftmax", w, "logp", time_op(
             lambda: gbce.selective_logsoftmax(x, idx, T, mask, out=o, workspace=ws),
             stream, 10, fl), k=K_)
+        if entropy:
+            h = torch.empty(w.rows, dtype=torch.float32, device=dev)
+            record(f"{tag}/selective_logsoftmax+entropy", w, "logp_ent", time_op(
+                lambda: gbce.selective_logsoftmax(x, idx, T, mask, out=o, entropy_out=h,
+                                                  workspace=ws), stream, 10, fl), k=K_)
         if backward:
             g = torch.ones((w.rows, K_), device=dev)
             d = torch.empty_like(x)
@@ -482,16 +489,16 @@ def measure_configs(gbce, dev, stream, peak):
     for dt, tag in ((torch.float32, "fp32"), (torch.bfloat16, "bf16")):
         w = workloads.collapse_stress(dtype=dt, device=dev)
         ce_ops(f"collapse_{tag}_2048x151936", w, 1.0, "mean", torch.ones(1, device=dev))
-        logp_op(f"collapse_{tag}_2048x151936", w, 1.0)
+        logp_op(f"collapse_{tag}_2048x151936", w, 1.0, entropy=True)
         del w
     # few rows, large vocabulary: the split-vocab partial + combine path
     w = workloads.grpo_bf16(device=dev, rows=64, seed=7)
     ce_ops("split_bf16_64x152064", w, TEMPERATURE, "mean", torch.ones(1, device=dev))
-    logp_op("split_bf16_64x152064", w, TEMPERATURE)
+    logp_op("split_bf16_64x152064", w, TEMPERATURE, entropy=True)
     w = workloads.grpo_bf16(device=dev, rows=ROWS)
     ce_ops(f"grpo_bf16_{ROWS}x{VOCAB}", w, TEMPERATURE, "mean", torch.ones(1, device=dev))
-    logp_op(f"grpo_bf16_{ROWS}x{VOCAB}_k4", w, TEMPERATURE, backward=True)
-    logp_op(f"grpo_bf16_{ROWS}x{VOCAB}_k1", w, TEMPERATURE, backward=True, k=1)
+    logp_op(f"grpo_bf16_{ROWS}x{VOCAB}_k4", w, TEMPERATURE, backward=True, entropy=True)
+    logp_op(f"grpo_bf16_{ROWS}x{VOCAB}_k1", w, TEMPERATURE, backward=True, k=1, entropy=True)
     del w, flush
     torch.cuda.empty_cache()
     return out

@@ -45,7 +45,7 @@ _SIGNATURES = {
     "gbce_status_string": (ctypes.c_char_p, [_i32]),
     "gbce_kernel_launches": (ctypes.c_uint64, []),
     "selective_logsoftmax": (_i32, [_vp, _i32, _i64, _i64, _i64, _vp, _i64, _f32, _vp, _vp,
-                                    _vp, _sz, _vp, _vp]),
+                                    _vp, _vp, _sz, _vp, _vp]),
     "selective_logsoftmax_bwd": (_i32, [_vp, _i32, _i64, _i64, _i64, _vp, _i64, _f32, _vp, _vp,
                                         _vp, _vp, _i64, _vp, _vp]),
     "ce_fwd": (_i32, [_vp, _i32, _i64, _i64, _i64, _vp, _i64, _f32, _i32, _vp, _vp, _vp, _vp,
@@ -152,12 +152,16 @@ def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
 def selective_logsoftmax(logits: torch.Tensor, index, temperature: float = 1.0,
                          row_mask: Optional[torch.Tensor] = None, *,
                          out: Optional[torch.Tensor] = None,
+                         with_entropy: bool = False,
+                         entropy_out: Optional[torch.Tensor] = None,
                          workspace: Optional[torch.Tensor] = None,
-                         dev_status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+                         dev_status: Optional[torch.Tensor] = None, stream=None):
     """log p_{index[r, k]} of each row at temperature T, fp32, shape index.shape.
 
     ``index`` is [..., K] (or [...] for K = 1) int64; masked-out rows
-    (``row_mask == 0``) are not read and give 0.
+    (``row_mask == 0``) are not read and give 0.  With ``with_entropy`` (or an
+    ``entropy_out`` [...] fp32 buffer) the same sweep also gives each row's
+    softmax entropy, and the call returns ``(logp, entropy)``.
     """
     lib = load_library()
     lead_shape = logits.shape[:-1]
@@ -172,14 +176,23 @@ def selective_logsoftmax(logits: torch.Tensor, index, temperature: float = 1.0,
         mask = row_mask.to(device=x.device, dtype=torch.uint8).reshape(rows).contiguous()
     if out is None:
         out = torch.empty((rows, K), dtype=torch.float32, device=x.device)
+    ent = entropy_out
+    if ent is None and with_entropy:
+        ent = torch.empty(rows, dtype=torch.float32, device=x.device)
+    if ent is not None and (ent.dtype != torch.float32 or not ent.is_contiguous()
+                            or ent.numel() != rows):
+        raise ValueError("entropy_out must be a contiguous fp32 tensor with one value per row")
     ws, ws_ptr, ws_bytes = _workspace(workspace, rows, V, K, x.device)
     st = lib.selective_logsoftmax(x.data_ptr(), _dtype_code(x), rows, V, x.stride(0),
                                   idx.data_ptr(), K, float(temperature), _ptr(mask),
-                                  out.data_ptr(), ws_ptr, ws_bytes, _ptr(dev_status),
+                                  out.data_ptr(), _ptr(ent), ws_ptr, ws_bytes, _ptr(dev_status),
                                   _stream_ptr(stream))
     _check(st, "selective_logsoftmax")
     res = out.view(*lead_shape, K)
-    return res.squeeze(-1) if squeeze else res
+    res = res.squeeze(-1) if squeeze else res
+    if ent is None:
+        return res
+    return res, ent.view(lead_shape)
 
 
 def selective_logsoftmax_bwd(logits: torch.Tensor, index, grad_logp, saved_logp,

@@ -50,6 +50,7 @@ struct WsLayout {
     size_t loss = 0;      // float [rows] per-row losses
     size_t logp = 0;      // float [rows] per-row log p (split path)
     size_t partials = 0;  // float2 [rows * splits]
+    size_t partials_h = 0;  // float [rows * splits]: selective_logsoftmax's entropy moments
     size_t total = 0;
 };
 
@@ -70,6 +71,9 @@ WsLayout ws_layout(int64_t rows, int64_t vocab)
     w.partials = off;
     if (splits > 1)
         off += align_up(r * static_cast<size_t>(splits) * 2 * sizeof(float), 256);
+    w.partials_h = off;
+    if (splits > 1)
+        off += align_up(r * static_cast<size_t>(splits) * sizeof(float), 256);
     w.total = off;
     return w;
 }
@@ -217,8 +221,8 @@ const char *gbce_status_string(gbce_status status)
 gbce_status selective_logsoftmax(const void *logits, gbce_dtype dtype, int64_t rows,
                                  int64_t vocab, int64_t row_stride, const int64_t *index,
                                  int64_t k, float temperature, const uint8_t *row_mask,
-                                 float *logp_out, void *workspace, size_t workspace_bytes,
-                                 int32_t *dev_status, void *stream)
+                                 float *logp_out, float *entropy_out, void *workspace,
+                                 size_t workspace_bytes, int32_t *dev_status, void *stream)
 {
     gbce_status st = check_logits(logits, dtype, rows, vocab, row_stride, temperature);
     if (st != GBCE_OK)
@@ -239,10 +243,13 @@ gbce_status selective_logsoftmax(const void *logits, gbce_dtype dtype, int64_t r
     p.k = k;
     p.row_mask = row_mask;
     p.logp_out = logp_out;
+    p.entropy_out = entropy_out;
     p.partials = ws_at<float2>(workspace, w.partials);
-    cudaError_t e = launch_rows(p, dtype, gbce::kModeLogp, s);
+    p.partials_h = ws_at<float>(workspace, w.partials_h);
+    const int mode = entropy_out != nullptr ? gbce::kModeLogpEnt : gbce::kModeLogp;
+    cudaError_t e = launch_rows(p, dtype, mode, s);
     if (e == cudaSuccess && p.splits > 1)
-        e = launch_combine(p, dtype, gbce::kModeLogp, s);
+        e = launch_combine(p, dtype, mode, s);
     return cuda_status(e);
 }
 

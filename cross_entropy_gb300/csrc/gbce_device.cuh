@@ -363,19 +363,30 @@ template <> struct Elem<__nv_bfloat16> {
 //   m = max x_j,   s = sum_j 2^{(x_j - m) c},   c = log2(e) / T,
 // so that s = sum_j exp((x_j - m) / T).  Excluded columns are fed as -inf.
 // The sum is kept in two packed pairs (four independent accumulators).
-struct OnlineMaxSum {
+template <bool ENT>
+struct OnlineStats {
     float m = kNegInf;
     float nmc = __builtin_huge_valf();  // -m * c, the shift added to every x * c
     float2 sa = make_float2(0.0f, 0.0f);
     float2 sb = make_float2(0.0f, 0.0f);
+    // ENT: sums of 2^z * z, z = (x - m) c <= 0 (the entropy's first moment)
+    float2 ha = make_float2(0.0f, 0.0f);
+    float2 hb = make_float2(0.0f, 0.0f);
 
     // New running maximum `vmax` for the values about to be added; returns
     // false when there is nothing to add (all of them are -inf).
     __device__ __forceinline__ bool raise_to(float vmax, float c)
     {
         if (vmax > m) {
-            const float f = ex2((m - vmax) * c);
+            const float d = (m - vmax) * c;
+            const float f = ex2(d);
             const float2 ff = make_float2(f, f);
+            if (ENT && m != kNegInf) {
+                // every z drops by -d: sum 2^z z -> f (sum 2^z z + d sum 2^z)
+                const float2 dd = make_float2(d, d);
+                ha = fmul2(ffma2(sa, dd, ha), ff);
+                hb = fmul2(ffma2(sb, dd, hb), ff);
+            }
             sa = fmul2(sa, ff);
             sb = fmul2(sb, ff);
             m = vmax;
@@ -384,13 +395,26 @@ struct OnlineMaxSum {
         return vmax != kNegInf;
     }
 
-    // Add 2^{x c - m c} for the four values of two packed pairs.
+    // z with -inf raised to a finite value far below the ex2 range, so that a
+    // -inf logit (2^z = 0) adds 0 to h instead of 0 * -inf; a NaN stays NaN.
+    __device__ static __forceinline__ float zfin(float z) { return fmaxf(z, -0x1p100f); }
+
+    // Add 2^{x c - m c} for the four values of two packed pairs.  The h terms
+    // skip zfin (one instruction per element on the hot path): a -inf logit
+    // here turns h into NaN while the sum stays finite, and the kernel then
+    // rescans that thread's columns with zfin (rescan_entropy_moment).
     __device__ __forceinline__ void add_pairs(float2 p, float2 q, float c)
     {
         const float2 cc = make_float2(c, c), kk = make_float2(nmc, nmc);
         const float2 zp = ffma2(p, cc, kk), zq = ffma2(q, cc, kk);
-        sa = fadd2(sa, make_float2(ex2(zp.x), ex2(zp.y)));
-        sb = fadd2(sb, make_float2(ex2(zq.x), ex2(zq.y)));
+        const float2 ep = make_float2(ex2(zp.x), ex2(zp.y));
+        const float2 eq = make_float2(ex2(zq.x), ex2(zq.y));
+        sa = fadd2(sa, ep);
+        sb = fadd2(sb, eq);
+        if (ENT) {
+            ha = ffma2(ep, zp, ha);
+            hb = ffma2(eq, zq, hb);
+        }
     }
 
     // Fold N unpacked values (masked columns already -inf).
@@ -399,15 +423,28 @@ struct OnlineMaxSum {
     {
         if (!raise_to(vmax, c))
             return;
-        float a = 0.0f, b = 0.0f;
+        float a = 0.0f, b = 0.0f, ah = 0.0f, bh = 0.0f;
 #pragma unroll
         for (int i = 0; i < N; i += 2) {
-            a += ex2(fmaf(f[i], c, nmc));
-            if (i + 1 < N)
-                b += ex2(fmaf(f[i + 1], c, nmc));
+            const float za = fmaf(f[i], c, nmc);
+            const float ea = ex2(za);
+            a += ea;
+            if (ENT)
+                ah = fmaf(ea, zfin(za), ah);
+            if (i + 1 < N) {
+                const float zb = fmaf(f[i + 1], c, nmc);
+                const float eb = ex2(zb);
+                b += eb;
+                if (ENT)
+                    bh = fmaf(eb, zfin(zb), bh);
+            }
         }
         sa.x += a;
         sb.x += b;
+        if (ENT) {
+            ha.x += ah;
+            hb.x += bh;
+        }
     }
 
     __device__ __forceinline__ void add1(float x, float c)
@@ -421,7 +458,14 @@ struct OnlineMaxSum {
     {
         return __fadd_rn(__fadd_rn(sa.x, sa.y), __fadd_rn(sb.x, sb.y));
     }
+    // ENT: the thread's sum of 2^z z.
+    __device__ __forceinline__ float hsum() const
+    {
+        return __fadd_rn(__fadd_rn(ha.x, ha.y), __fadd_rn(hb.x, hb.y));
+    }
 };
+
+using OnlineMaxSum = OnlineStats<false>;
 
 // Merge two (max, sum) partial states with the same scale c.  Exactly
 // commutative (no fused multiply-add), so every lane of a butterfly
@@ -438,6 +482,38 @@ __device__ __forceinline__ void merge_max_sum(float &m, float &s, float m2, floa
     m = M;
 }
 
+// merge_max_sum for states that also carry h = sum 2^z z (z = (x - m) c):
+// moving a part from its max m_i to M shifts its z by d_i = (m_i - M) c, so
+// h_i -> 2^{d_i} (h_i + d_i s_i).  Exactly commutative like merge_max_sum.
+__device__ __forceinline__ void merge_max_sum_h(float &m, float &s, float &h, float m2, float s2,
+                                                float h2, float c)
+{
+    const float M = fmaxf(m, m2);
+    if (M == kNegInf) {
+        m = M;
+        s = 0.0f;
+        h = 0.0f;
+        return;
+    }
+    const auto part = [&](float mi, float si, float hi, float &sv, float &hv) {
+        if (mi == kNegInf) {
+            sv = 0.0f;
+            hv = 0.0f;
+            return;
+        }
+        const float d = __fmul_rn(__fsub_rn(mi, M), c);
+        const float f = ex2(d);
+        sv = __fmul_rn(si, f);
+        hv = __fmul_rn(__fadd_rn(hi, __fmul_rn(d, si)), f);
+    };
+    float sa, ha, sb, hb;
+    part(m, s, h, sa, ha);
+    part(m2, s2, h2, sb, hb);
+    s = __fadd_rn(sa, sb);
+    h = __fadd_rn(ha, hb);
+    m = M;
+}
+
 // log p_t from the others' (m, s) and the target logit, all in raw logit
 // units: a = log s + (m - x_t) / T, log p = -softplus(a).  The margin
 // (m - x_t) / T is one IEEE division of an exact (bf16) or once-rounded
@@ -449,6 +525,28 @@ __device__ __forceinline__ float finalize_logp(float m, float s, float xt, float
         return (s == 0.0f) ? 0.0f : __int_as_float(0x7fc00000);
     const float a = logf(s) + (m - xt) / T;
     return -softplus(a);
+}
+
+// Entropy -sum_j p_j log p_j of a row from the others' state (m, s, h) --
+// every column but the reference column t, h = sum 2^z z in base-2 units --
+// and x_t.  With a = log s + (m - x_t)/T (log p_t = -softplus(a)),
+//   p_t = sigmoid(-a), 1 - p_t = sigmoid(a),
+//   log sum_all e^{(x_j - m)/T} = log s + softplus(-a) =: L,
+//   H = p_t softplus(a) + (1 - p_t) (L - ln2 h / s),
+// a sum of non-negative terms: nothing cancels when t holds almost all of
+// the mass (the confident rows), and 1 - p_t never rounds to 0 there.
+__device__ __forceinline__ float finalize_entropy(float m, float s, float h, float xt, float T)
+{
+    if (!(s > 0.0f))
+        return (s == 0.0f) ? 0.0f : __int_as_float(0x7fc00000);
+    const float ls = logf(s);
+    const float a = ls + (m - xt) / T;
+    const float sp = softplus(a), spn = softplus(-a);
+    const float pt = expf(-sp);  // e^{log p_t}
+    const float q = -expm1f(-sp);
+    const float mean_u = (h / s) * 0.69314718055994531f;  // <= 0
+    const float ht = pt > 0.0f ? pt * sp : 0.0f;
+    return fmaf(q, (ls + spn) - mean_u, ht);
 }
 
 }  // namespace gbce

@@ -17,6 +17,7 @@ enum Mode : int {
     kModeGrad = 2,   // cross-entropy gradient from saved log p (ce_bwd)
     kModeFused = 3,  // statistics then gradient of the same row (one launch)
     kModeLogpGrad = 4,  // selective log-softmax gradient from saved log p (K indices)
+    kModeLogpEnt = 5,   // kModeLogp plus the entropy of each row
 };
 
 struct RowParams {
@@ -36,6 +37,8 @@ struct RowParams {
     float *loss_rows;  // CE modes: [rows]
     float *lse_out;    // CE modes: [rows] or null
     float2 *partials;  // [rows * splits] (max, sum) when splits > 1
+    float *entropy_out;  // kModeLogpEnt: [rows]
+    float *partials_h;   // kModeLogpEnt, splits > 1: [rows * splits] sum 2^z z
 
     void *dlogits;  // kModeGrad / kModeFused
     int64_t d_stride;

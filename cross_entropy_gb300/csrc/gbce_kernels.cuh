@@ -95,8 +95,8 @@ __device__ __forceinline__ bool vector_has_target(const int32_t (&tv)[KMAX], int
 }
 
 // Fold one 16-byte vector of logits, masking target columns (slow path).
-template <typename T, int KMAX>
-__device__ __forceinline__ void stats_vector(OnlineMaxSum &st, const uint4 &raw, int32_t col0,
+template <typename T, int KMAX, typename S>
+__device__ __forceinline__ void stats_vector(S &st, const uint4 &raw, int32_t col0,
                                              const int32_t (&tg)[KMAX], float c)
 {
     constexpr int VEC = Elem<T>::kVec;
@@ -130,7 +130,8 @@ template <> struct FastVec<__nv_bfloat16> {
     {
         return unpack_max(bf16x2_max(pmax(a), pmax(b)));
     }
-    __device__ static __forceinline__ void add(OnlineMaxSum &st, const uint4 &a, float c)
+    template <typename S>
+    __device__ static __forceinline__ void add(S &st, const uint4 &a, float c)
     {
         st.add_pairs(bf16x2_to_float2(a.x), bf16x2_to_float2(a.y), c);
         st.add_pairs(bf16x2_to_float2(a.z), bf16x2_to_float2(a.w), c);
@@ -149,7 +150,8 @@ template <> struct FastVec<float> {
                      fmax3(__uint_as_float(a.w), __uint_as_float(b.x), __uint_as_float(b.y)),
                      fmaxf(__uint_as_float(b.z), __uint_as_float(b.w)));
     }
-    __device__ static __forceinline__ void add(OnlineMaxSum &st, const uint4 &a, float c)
+    template <typename S>
+    __device__ static __forceinline__ void add(S &st, const uint4 &a, float c)
     {
         st.add_pairs(make_float2(__uint_as_float(a.x), __uint_as_float(a.y)),
                      make_float2(__uint_as_float(a.z), __uint_as_float(a.w)), c);
@@ -157,13 +159,13 @@ template <> struct FastVec<float> {
 };
 
 // Fold body vectors va (and vb) of a row; col0 = first column of vector 0.
-template <typename T, int KMAX>
-__device__ __forceinline__ void stats_one(OnlineMaxSum &st, const uint4 &a, int32_t va,
+template <typename T, int KMAX, typename S>
+__device__ __forceinline__ void stats_one(S &st, const uint4 &a, int32_t va,
                                           int32_t col0, const int32_t (&tv)[KMAX],
-                                          const int32_t (&tg)[KMAX], float c)
+                                          const int32_t (&tg)[KMAX], float c, bool check = true)
 {
     constexpr int VEC = Elem<T>::kVec;
-    if (vector_has_target<KMAX>(tv, va)) {
+    if (check && vector_has_target<KMAX>(tv, va)) {
         stats_vector<T, KMAX>(st, a, col0 + va * VEC, tg, c);
         return;
     }
@@ -171,14 +173,14 @@ __device__ __forceinline__ void stats_one(OnlineMaxSum &st, const uint4 &a, int3
         FastVec<T>::add(st, a, c);
 }
 
-template <typename T, int KMAX>
-__device__ __forceinline__ void stats_two(OnlineMaxSum &st, const uint4 &a, const uint4 &b,
+template <typename T, int KMAX, typename S>
+__device__ __forceinline__ void stats_two(S &st, const uint4 &a, const uint4 &b,
                                           int32_t va, int32_t vb, int32_t col0,
                                           const int32_t (&tv)[KMAX], const int32_t (&tg)[KMAX],
-                                          float c)
+                                          float c, bool check = true)
 {
     constexpr int VEC = Elem<T>::kVec;
-    if (vector_has_target<KMAX>(tv, va) || vector_has_target<KMAX>(tv, vb)) {
+    if (check && (vector_has_target<KMAX>(tv, va) || vector_has_target<KMAX>(tv, vb))) {
         stats_vector<T, KMAX>(st, a, col0 + va * VEC, tg, c);
         stats_vector<T, KMAX>(st, b, col0 + vb * VEC, tg, c);
         return;
@@ -187,6 +189,44 @@ __device__ __forceinline__ void stats_two(OnlineMaxSum &st, const uint4 &a, cons
         FastVec<T>::add(st, a, c);
         FastVec<T>::add(st, b, c);
     }
+}
+
+// h = sum 2^z z (z = x c - m c, target columns left out) over the columns
+// one consumer thread swept -- its share of the head and tail, and the body
+// vectors vb with (vb - v0) % nc == tid -- re-read from global memory with
+// -inf logits adding 0.  Taken only by a thread whose packed h went NaN on a
+// -inf logit while its sum stayed finite.
+template <typename T, int KMAX>
+__device__ __forceinline__ float rescan_entropy_moment(const T *row, const RowGeom &g, int64_t V,
+                                                   int64_t v0, int64_t v1, bool first, bool last,
+                                                   const int32_t (&tg)[KMAX], float c, float nmc,
+                                                   int tid, int nc)
+{
+    using E = Elem<T>;
+    constexpr int VEC = E::kVec;
+    using S = OnlineStats<true>;
+    float h = 0.0f;
+    const auto term = [&](float x, int64_t col) {
+        if (!is_target<KMAX>(tg, static_cast<int32_t>(col))) {
+            const float z = fmaf(x, c, nmc);
+            h = fmaf(ex2(z), S::zfin(z), h);
+        }
+    };
+    if (first)
+        for (int64_t e = tid; e < g.head; e += nc)
+            term(E::load(row + e), e);
+    if (last)
+        for (int64_t e = g.tail0 + tid; e < V; e += nc)
+            term(E::load(row + e), e);
+    const uint4 *body = reinterpret_cast<const uint4 *>(row + g.head);
+    for (int64_t vb = v0 + tid; vb < v1; vb += nc) {
+        float f[VEC];
+        E::unpack(body[vb], f);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e)
+            term(f[e], g.head + vb * VEC + e);
+    }
+    return h;
 }
 
 // Per-row constants of the gradient pass.  The exponent carries an offset
@@ -319,6 +359,33 @@ __device__ __forceinline__ float logp_with_targets(float mS, float sS, const int
     return finalize_logp(m, s, xt[k], T);
 }
 
+// Entropy of a row from the state (mS, sS, hS) of every column outside the
+// target set S: the distinct members of S other than the first index are
+// folded in, and the first index is the reference column of
+// finalize_entropy (a confident row's sampled token is its dominant column).
+// NaN when the first index is out of range.
+template <int KMAX>
+__device__ __forceinline__ float entropy_with_targets(float mS, float sS, float hS,
+                                                      const int32_t *tg, const float *xt, int K,
+                                                      float c, float T)
+{
+    const int32_t t0 = tg[0];
+    if (t0 < 0)
+        return __int_as_float(0x7fc00000);
+    float m = mS, s = sS, h = hS;
+    for (int j = 1; j < K; ++j) {
+        const int32_t tj = tg[j];
+        if (tj < 0 || tj == t0)
+            continue;
+        bool dup = false;
+        for (int i = 1; i < j; ++i)
+            dup |= (tg[i] == tj);
+        if (!dup)
+            merge_max_sum_h(m, s, h, xt[j], 1.0f, 0.0f, c);
+    }
+    return finalize_entropy(m, s, h, xt[0], T);
+}
+
 __device__ __forceinline__ float upstream_grad(const RowParams &p, int64_t r)
 {
     if (p.reduction == 0)
@@ -360,7 +427,8 @@ __device__ void fill_row_slice(T *drow, int64_t V, int split, int splits, float 
 }
 
 template <typename T, int MODE, int KMAX>
-__global__ void __launch_bounds__(kRowThreads, 2) row_kernel(const RowParams p)
+__global__ void __launch_bounds__(kRowThreads, (MODE == kModeLogpEnt && KMAX <= 4) ? 3 : 2)
+    row_kernel(const RowParams p)
 {
     using E = Elem<T>;
     constexpr int VEC = E::kVec;
@@ -371,7 +439,9 @@ __global__ void __launch_bounds__(kRowThreads, 2) row_kernel(const RowParams p)
     static_assert(CV % NC == 0, "chunk must split evenly over consumer threads");
     constexpr bool kStats = (MODE != kModeGrad && MODE != kModeLogpGrad);
     constexpr bool kGrad = (MODE == kModeGrad || MODE == kModeFused || MODE == kModeLogpGrad);
-    constexpr bool kGather = (MODE == kModeLogp || MODE == kModeLogpGrad);  // K indices
+    constexpr bool kEnt = (MODE == kModeLogpEnt);                  // + row entropy
+    constexpr bool kLogpFwd = (MODE == kModeLogp || kEnt);         // log p of K indices
+    constexpr bool kGather = (kLogpFwd || MODE == kModeLogpGrad);  // K indices
     constexpr int kPasses = (MODE == kModeFused) ? 2 : 1;
 
     extern __shared__ __align__(128) uint8_t dyn_smem[];
@@ -379,12 +449,12 @@ __global__ void __launch_bounds__(kRowThreads, 2) row_kernel(const RowParams p)
         (reinterpret_cast<uintptr_t>(dyn_smem) + (kRingAlign - 1)) & ~uintptr_t(kRingAlign - 1));
     __shared__ uint64_t full_bar[kStages];
     __shared__ uint64_t empty_bar[kStages];
-    __shared__ float red_m[NCW], red_s[NCW];
+    __shared__ float red_m[NCW], red_s[NCW], red_h[NCW];
     __shared__ float s_xt[KMAX];
     __shared__ float s_dt[KMAX];       // kModeLogpGrad: gradient at each gathered column
     __shared__ float s_G, s_lp0;       // kModeLogpGrad: sum of upstream, log p of index 0
     __shared__ int32_t s_tg[KMAX];
-    __shared__ float bc_m, bc_s, bc_logp;
+    __shared__ float bc_m, bc_s, bc_h, bc_logp;
     __shared__ uint64_t xbar;                   // fused, cluster of CTAs per row
     __shared__ float2 xchg[kMaxClusterCtas];    // every CTA's (max, sum) partial
 
@@ -433,9 +503,11 @@ __global__ void __launch_bounds__(kRowThreads, 2) row_kernel(const RowParams p)
         const float fill = state == 1 ? 0.0f : __int_as_float(0x7fc00000);
         // direct: this launch writes the row's outputs (no separate merge)
         const bool direct = (p.splits == 1) || MODE == kModeFused;
-        if (MODE == kModeLogp) {
+        if (kLogpFwd) {
             if (direct && tid < p.k)
                 p.logp_out[r * p.k + tid] = 0.0f;
+            if (kEnt && direct && tid == 0)
+                p.entropy_out[r] = 0.0f;
         } else if (MODE == kModeLogpGrad) {
             if (tid == 0 && split == 0 && state == 2)
                 report(p.dev_status, GBCE_DEV_BAD_INDEX);
@@ -560,7 +632,15 @@ __global__ void __launch_bounds__(kRowThreads, 2) row_kernel(const RowParams p)
     float logp = 0.0f, xy = 0.0f;
 
     if (kStats) {
-        OnlineMaxSum st;
+        OnlineStats<kEnt> st;
+        // Every body vector vb this thread sweeps has (vb - v0) % NC == tid,
+        // so a warp none of whose threads holds a target vector skips the
+        // per-vector target test (warp-uniform branch).
+        bool mine = false;
+#pragma unroll
+        for (int k = 0; k < KMAX; ++k)
+            mine |= tv[k] >= v0 && tv[k] < v1 && (tv[k] - v0) % NC == tid;
+        const bool wcheck = __any_sync(0xffffffffu, mine);
         if (split == 0)
             for (int64_t e = tid; e < g.head; e += NC) {
                 const float x = E::load(row + e);
@@ -590,13 +670,13 @@ __global__ void __launch_bounds__(kRowThreads, 2) row_kernel(const RowParams p)
 #pragma unroll
                     for (int u = 0; u + 1 < PER_THREAD; u += 2)
                         stats_two<T, KMAX>(st, raw[u], raw[u + 1], vb0 + tid + u * NC,
-                                        vb0 + tid + (u + 1) * NC, col0, tv, tg, c);
+                                        vb0 + tid + (u + 1) * NC, col0, tv, tg, c, wcheck);
                     if (PER_THREAD & 1)
                         stats_one<T, KMAX>(st, raw[PER_THREAD - 1], vb0 + tid + (PER_THREAD - 1) * NC,
-                                        col0, tv, tg, c);
+                                        col0, tv, tg, c, wcheck);
                 } else {
                     for (int v = tid; v < nv; v += NC)
-                        stats_one<T, KMAX>(st, chunk[v], vb0 + v, col0, tv, tg, c);
+                        stats_one<T, KMAX>(st, chunk[v], vb0 + v, col0, tv, tg, c, wcheck);
                 }
             }
             __syncwarp();
@@ -604,28 +684,34 @@ __global__ void __launch_bounds__(kRowThreads, 2) row_kernel(const RowParams p)
                 mbar_arrive(&empty_bar[slot]);
         }
 
-        // CTA-wide merge of the per-thread (max, sum) in a fixed order
-        float m = st.m, s = st.sum();
+        // CTA-wide merge of the per-thread (max, sum[, h]) in a fixed order
+        float m = st.m, s = st.sum(), h = kEnt ? st.hsum() : 0.0f;
+        if (kEnt && alive && isnan(h) && !isnan(s))
+            h = rescan_entropy_moment<T, KMAX>(row, g, V, v0, v1, split == 0,
+                                               split == p.splits - 1, tg, c, st.nmc, tid, NC);
+        const auto merge_lanes = [&]() {
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
-            const float s2 = __shfl_xor_sync(0xffffffffu, s, off);
-            merge_max_sum(m, s, m2, s2, c);
-        }
+            for (int off = 16; off > 0; off >>= 1) {
+                const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
+                const float s2 = __shfl_xor_sync(0xffffffffu, s, off);
+                if (kEnt)
+                    merge_max_sum_h(m, s, h, m2, s2, __shfl_xor_sync(0xffffffffu, h, off), c);
+                else
+                    merge_max_sum(m, s, m2, s2, c);
+            }
+        };
+        merge_lanes();
         if (lane == 0) {
             red_m[warp] = m;
             red_s[warp] = s;
+            red_h[warp] = h;
         }
         named_sync(1, NC);
         if (warp == 0) {
             m = lane < NCW ? red_m[lane] : kNegInf;
             s = lane < NCW ? red_s[lane] : 0.0f;
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
-                const float s2 = __shfl_xor_sync(0xffffffffu, s, off);
-                merge_max_sum(m, s, m2, s2, c);
-            }
+            h = lane < NCW ? red_h[lane] : 0.0f;
+            merge_lanes();
             if (lane == 0) {
                 if (exchange) {
                     const uint32_t C = static_cast<uint32_t>(p.splits);
@@ -636,9 +722,12 @@ __global__ void __launch_bounds__(kRowThreads, 2) row_kernel(const RowParams p)
                         st_async_pair(map_to_rank(slot, t), m, s, map_to_rank(bar, t));
                 } else if (p.splits > 1) {
                     p.partials[unit] = make_float2(m, s);
-                } else if (MODE == kModeLogp) {
+                    if (kEnt)
+                        p.partials_h[unit] = h;
+                } else if (kLogpFwd) {
                     bc_m = m;
                     bc_s = s;
+                    bc_h = h;
                 } else {
                     xy = s_xt[0];
                     logp = finalize_logp(m, s, xy, p.T);
@@ -651,8 +740,11 @@ __global__ void __launch_bounds__(kRowThreads, 2) row_kernel(const RowParams p)
                 }
             }
         }
-        if (MODE == kModeLogp && p.splits == 1) {
+        if (kLogpFwd && p.splits == 1) {
             named_sync(1, NC);
+            if (kEnt && tid == NC - 1)
+                p.entropy_out[r] = entropy_with_targets<KMAX>(bc_m, bc_s, bc_h, s_tg, s_xt,
+                                                              static_cast<int>(p.k), c, p.T);
             if (tid < p.k) {
                 float out;
                 if (s_tg[tid] < 0) {
@@ -827,11 +919,15 @@ __global__ void combine_kernel(const RowParams p)
     const int64_t V = p.vocab;
     const float c = p.c;
     const float nan = __int_as_float(0x7fc00000);
+    constexpr bool kEnt = (MODE == kModeLogpEnt);
+    constexpr bool kLogpFwd = (MODE == kModeLogp || kEnt);
 
-    if (MODE == kModeLogp) {
+    if (kLogpFwd) {
         if (p.row_mask != nullptr && p.row_mask[r] == 0) {
             for (int64_t k = 0; k < p.k; ++k)
                 p.logp_out[r * p.k + k] = 0.0f;
+            if (kEnt)
+                p.entropy_out[r] = 0.0f;
             return;
         }
     } else {
@@ -849,13 +945,16 @@ __global__ void combine_kernel(const RowParams p)
         }
     }
 
-    float m = kNegInf, s = 0.0f;
+    float m = kNegInf, s = 0.0f, h = 0.0f;
     for (int i = 0; i < p.splits; ++i) {
         const float2 part = p.partials[r * p.splits + i];
-        merge_max_sum(m, s, part.x, part.y, c);
+        if (kEnt)
+            merge_max_sum_h(m, s, h, part.x, part.y, p.partials_h[r * p.splits + i], c);
+        else
+            merge_max_sum(m, s, part.x, part.y, c);
     }
 
-    if (MODE == kModeLogp) {
+    if (kLogpFwd) {
         int32_t tg[GBCE_MAX_K];
         float xt[GBCE_MAX_K];
         const int K = static_cast<int>(p.k);
@@ -874,6 +973,8 @@ __global__ void combine_kernel(const RowParams p)
             }
             p.logp_out[r * p.k + k] = out;
         }
+        if (kEnt)
+            p.entropy_out[r] = entropy_with_targets<GBCE_MAX_K>(m, s, h, tg, xt, K, c, p.T);
     } else {
         const float xy = E::load(row + p.targets[r]);
         const float logp = finalize_logp(m, s, xy, p.T);
@@ -966,6 +1067,12 @@ cudaError_t launch_rows_per_unit(const RowParams &p, int mode, cudaStream_t stre
         if (p.k <= 4)
             return launch_row_kernel<T, kModeLogp, 4>(p, stream);
         return launch_row_kernel<T, kModeLogp, GBCE_MAX_K>(p, stream);
+    case kModeLogpEnt:
+        if (p.k <= 1)
+            return launch_row_kernel<T, kModeLogpEnt, 1>(p, stream);
+        if (p.k <= 4)
+            return launch_row_kernel<T, kModeLogpEnt, 4>(p, stream);
+        return launch_row_kernel<T, kModeLogpEnt, GBCE_MAX_K>(p, stream);
     case kModeCe:
         return launch_row_kernel<T, kModeCe, 1>(p, stream);
     case kModeGrad:
@@ -992,6 +1099,8 @@ cudaError_t launch_combine(const RowParams &p, int mode, cudaStream_t stream)
     const unsigned blocks = static_cast<unsigned>((p.rows + threads - 1) / threads);
     if (mode == kModeLogp)
         combine_kernel<T, kModeLogp><<<blocks, threads, 0, stream>>>(p);
+    else if (mode == kModeLogpEnt)
+        combine_kernel<T, kModeLogpEnt><<<blocks, threads, 0, stream>>>(p);
     else
         combine_kernel<T, kModeCe><<<blocks, threads, 0, stream>>>(p);
     note_launches(1);

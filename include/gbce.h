@@ -89,30 +89,39 @@ uint64_t gbce_kernel_launches(void);
 /*
  * Selective log-softmax: logp_out[r, k] = log p_{index[r, k]} of row r at
  * temperature T, for rows with row_mask[r] != 0 (or all rows when row_mask
- * is NULL); masked-out rows are not read and get 0.
+ * is NULL); masked-out rows are not read and get 0.  With entropy_out, the
+ * same sweep also gives the entropy of each row's softmax,
+ * entropy_out[r] = -sum_j p_j log p_j (0 log 0 = 0; 0 for masked rows),
+ * with the first index as the reference column whose probability may be
+ * near 1: its 1 - p comes from its accurate log p, so a confident row keeps
+ * its small positive entropy.
  *
  * Source: "perf(rlhf): chunk selective_log_softmax instead of looping per
  * token" (ms-swift PR #10337), "PR information": the naive
  * gather(logits.log_softmax(-1)) with top-K indices, temperature and a row
  * mask, here in one launch over all rows; accurate log-probs as in "Fix
- * softmax collapse ..." (Liger-Kernel PR #1555), "Summary", second bullet.
+ * softmax collapse ..." (Liger-Kernel PR #1555), "Summary", second bullet;
+ * the entropy taking the others' sum from the same term as the target's
+ * log p: the unsloth-zoo #2080 commit quoted there, "Fix", forward bullet.
  *
  *   logits     [rows, row_stride] fp32/bf16
  *   index      [rows, k] int64, 1 <= k <= GBCE_MAX_K; duplicates allowed
  *   row_mask   [rows] uint8 or NULL
  *   logp_out   [rows, k] fp32
+ *   entropy_out [rows] fp32 or NULL (NULL: the sweep skips the entropy)
  *   workspace  >= gbce_workspace_size(rows, vocab, k) bytes (may be NULL
  *              when that size is 0), 16-byte aligned
  * Errors: GBCE_EINVAL for NULL logits/index/logp_out with rows > 0,
  * vocab < 1, row_stride < vocab, k outside [1, GBCE_MAX_K], temperature not
  * finite and > 0; GBCE_EDTYPE; GBCE_EWORKSPACE.  Out-of-range indices of
- * live rows: GBCE_DEV_BAD_INDEX and a NaN output for that (r, k).
+ * live rows: GBCE_DEV_BAD_INDEX and a NaN output for that (r, k); the
+ * entropy of a row whose first index is out of range is NaN.
  */
 gbce_status selective_logsoftmax(const void *logits, gbce_dtype dtype, int64_t rows,
                                  int64_t vocab, int64_t row_stride, const int64_t *index,
                                  int64_t k, float temperature, const uint8_t *row_mask,
-                                 float *logp_out, void *workspace, size_t workspace_bytes,
-                                 int32_t *dev_status, void *stream);
+                                 float *logp_out, float *entropy_out, void *workspace,
+                                 size_t workspace_bytes, int32_t *dev_status, void *stream);
 
 /*
  * Selective log-softmax backward: the gradient of sum_k g[r, k] *

@@ -6,6 +6,9 @@ Tolerances (floating point, against the fp64 oracle):
   dlogits, per row ||got - ref||_2 / ||ref||_2: 2e-5 fp32, 4e-3 bf16;
     ignored rows exactly zero.
   reduced loss, relative: 2e-5.
+  row entropy, element-wise relative: 2e-5 for either logit type (the sums
+    behind it are fp32 whatever the input type); exactly 0 where the oracle
+    gives exactly 0; never negative.
   zero-sum rows: |sum_j dx_j| <= tol * sum_j |dx_j| (fp64 host sums), tol
     1e-5 fp32 / 4e-3 bf16.
 Integer results (item counts, skipped rows) are compared exactly.
@@ -19,6 +22,7 @@ import torch
 LOGP_TOL = {torch.float32: 2e-5, torch.bfloat16: 1e-5}
 GRAD_TOL = {torch.float32: 2e-5, torch.bfloat16: 4e-3}
 LOSS_TOL = 2e-5
+ENTROPY_TOL = 2e-5
 ZERO_SUM_TOL = {torch.float32: 1e-5, torch.bfloat16: 4e-3}
 
 
@@ -79,3 +83,19 @@ def assert_loss_close(got: float, ref: float, what="loss"):
         assert got == 0.0, f"{what}: {got} != 0"
         return
     assert abs(got - ref) <= LOSS_TOL * abs(ref), f"{what}: {got} vs {ref}"
+
+
+def assert_entropy_close(got, ref, what="entropy"):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    assert np.all(np.isnan(got) == np.isnan(ref)), f"{what}: NaN pattern differs"
+    ok = ~np.isnan(ref)
+    g, r = got[ok], ref[ok]
+    assert np.all(g >= 0.0), f"{what}: negative entropy {g.min()}"
+    zero = r == 0.0
+    assert np.all(g[zero] == 0.0), f"{what}: nonzero where the oracle is exactly 0"
+    rel = np.abs(g[~zero] - r[~zero]) / r[~zero]
+    worst = rel.max() if rel.size else 0.0
+    assert worst <= ENTROPY_TOL, f"{what}: worst relative error {worst:.3e} > {ENTROPY_TOL:.0e}"
+    return worst

@@ -73,11 +73,13 @@ FAKE = 0x10000  # never dereferenced: every case fails host validation first
 
 def _logp(lib, **kw):
     a = dict(logits=FAKE, dtype=1, rows=4, vocab=100, stride=100, index=FAKE, k=1, T=1.0,
-             mask=None, out=FAKE, ws=FAKE, ws_bytes=1 << 20, status=None, stream=None)
+             mask=None, out=FAKE, entropy=None, ws=FAKE, ws_bytes=1 << 20, status=None,
+             stream=None)
     a.update(kw)
     return lib.selective_logsoftmax(a["logits"], a["dtype"], a["rows"], a["vocab"], a["stride"],
-                                    a["index"], a["k"], a["T"], a["mask"], a["out"], a["ws"],
-                                    a["ws_bytes"], a["status"], a["stream"])
+                                    a["index"], a["k"], a["T"], a["mask"], a["out"],
+                                    a["entropy"], a["ws"], a["ws_bytes"], a["status"],
+                                    a["stream"])
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -97,6 +99,7 @@ def _logp(lib, **kw):
     (dict(ws=None), 4),
     (dict(ws_bytes=16), 4),
     (dict(ws=FAKE + 8), 4),
+    (dict(entropy=FAKE, ws=None), 4),
 ])
 def test_selective_logsoftmax_host_checks(lib, kw, code):
     assert _logp(lib, **kw) == code
