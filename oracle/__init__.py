@@ -17,7 +17,8 @@ Functions and the passages they follow:
   gather(log_softmax(logits / T)) at K indices per row with a row mask,
   computed in the collapse-safe form of "Fix softmax collapse in CE, GRPO,
   KL/JSD and softmax" (Liger-Kernel PR #1555), "Details".
-* :func:`selective_logsoftmax_backward` -- the gradient of sum_k g_k log p_{t_k}:
+* :func:`selective_logsoftmax_backward` -- the gradient of sum_k g_k log p_{t_k}
+  (plus g_H H, the row entropy, when given):
   (1/T)(sum_{k: t_k = j} g_k - G p_j), with the gathered columns in the
   -expm1(log p_t) form of the same page's "Summary" (second bullet).
 * :func:`entropy` -- -sum_j p_j log p_j per row, the reference column's term
@@ -86,7 +87,8 @@ def _load():
             dp, dp, dp, ip, ctypes.c_void_p, i64]
         lib.oracle_selective_logsoftmax_backward.restype = i64
         lib.oracle_selective_logsoftmax_backward.argtypes = [
-            dp, i64, i64, i64, ip, i64, ctypes.c_double, ctypes.c_void_p, dp, dp, i64]
+            dp, i64, i64, i64, ip, i64, ctypes.c_double, ctypes.c_void_p, dp, ctypes.c_void_p,
+            dp, i64]
         lib.oracle_entropy.restype = i64
         lib.oracle_entropy.argtypes = [dp, i64, i64, i64, ip, ctypes.c_double, ctypes.c_void_p, dp]
         lib.oracle_num_threads.restype = ctypes.c_int
@@ -145,9 +147,12 @@ def selective_logsoftmax(x, index, temperature: float = 1.0, row_mask=None):
     return out, int(bad)
 
 
-def selective_logsoftmax_backward(x, index, grad, temperature: float = 1.0, row_mask=None):
+def selective_logsoftmax_backward(x, index, grad, temperature: float = 1.0, row_mask=None,
+                                  grad_entropy=None):
     """dL/dx for upstream grad[r, k] = dL/d log p_{index[r, k]}; masked rows 0.
 
+    ``grad_entropy`` [rows] (optional) is dL/dH_r for the row entropy H_r
+    (:func:`entropy` with reference column index[r, 0]).
     Returns ``(dx[rows, V] float64, n_bad_rows)``.
     """
     lib = _load()
@@ -161,10 +166,15 @@ def selective_logsoftmax_backward(x, index, grad, temperature: float = 1.0, row_
     if row_mask is not None:
         mask_arr = np.ascontiguousarray(np.asarray(row_mask).reshape(rows).astype(np.uint8))
         mask_ptr = mask_arr.ctypes.data
+    gh_arr = None
+    gh_ptr = None
+    if grad_entropy is not None:
+        gh_arr = np.ascontiguousarray(np.asarray(grad_entropy, dtype=np.float64).reshape(rows))
+        gh_ptr = gh_arr.ctypes.data
     dx = np.empty((rows, V), dtype=np.float64)
     bad = lib.oracle_selective_logsoftmax_backward(
         _ptr(x, ctypes.c_double), rows, V, x.strides[0] // 8, _ptr(idx, ctypes.c_int64), K,
-        exact_temperature(temperature), mask_ptr, _ptr(g, ctypes.c_double),
+        exact_temperature(temperature), mask_ptr, _ptr(g, ctypes.c_double), gh_ptr,
         _ptr(dx, ctypes.c_double), V)
     return dx, int(bad)
 

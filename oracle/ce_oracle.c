@@ -318,19 +318,25 @@ int64_t oracle_cross_entropy(const double *x, int64_t rows, int64_t V, int64_t l
     return bad;
 }
 
+/* Forward declaration: the entropy term of the backward below uses it. */
+static double row_entropy(const double *x, int64_t V, int64_t t, double T);
+
 /*
- * Selective log-softmax backward.
+ * Selective log-softmax backward, optionally with an entropy term.
  *   x         [rows, ld] fp64
  *   idx       [rows, K] int64
  *   row_mask  [rows] uint8 or NULL
  *   grad      [rows, K] fp64: dL/d out[r, k]
+ *   grad_ent  [rows] fp64 or NULL: dL/d H_r, H_r = -sum_j p_j log p_j; it
+ *             adds -(grad_ent / T) p_j (log p_j + H_r) to column j (the
+ *             derivative of the entropy, written out), 0 where p_j = 0
  *   dx        [rows, ldx] out
  * Returns the number of rows with an out-of-range index (their rows NaN).
  */
 int64_t oracle_selective_logsoftmax_backward(const double *x, int64_t rows, int64_t V,
                                              int64_t ld, const int64_t *idx, int64_t K, double T,
                                              const uint8_t *row_mask, const double *grad,
-                                             double *dx, int64_t ldx)
+                                             const double *grad_ent, double *dx, int64_t ldx)
 {
     int64_t bad = 0;
 #pragma omp parallel for schedule(dynamic, 1) reduction(+ : bad)
@@ -365,8 +371,15 @@ int64_t oracle_selective_logsoftmax_backward(const double *x, int64_t rows, int6
         for (int64_t k = 0; k < K; ++k)
             sum_add(&G, grad[r * K + k]);
         const double Gv = sum_value(&G);
-        for (int64_t j = 0; j < V; ++j)
-            dr[j] = -(Gv / T) * exp(xr[j] / T - lse);
+        const double gH = grad_ent ? grad_ent[r] : 0.0;
+        const double H = grad_ent ? row_entropy(xr, V, idx[r * K], T) : 0.0;
+        for (int64_t j = 0; j < V; ++j) {
+            const double lpj = xr[j] / T - lse;
+            const double pj = exp(lpj);
+            dr[j] = -(Gv / T) * pj;
+            if (gH != 0.0 && pj != 0.0)
+                dr[j] -= (gH / T) * pj * (lpj + H);
+        }
         /* gathered columns, each once, in the collapse-safe form */
         for (int64_t k = 0; k < K; ++k) {
             const int64_t t = idx[r * K + k];
@@ -383,6 +396,8 @@ int64_t oracle_selective_logsoftmax_backward(const double *x, int64_t rows, int6
             const double g_t = sum_value(&gt);
             const double lp = row_logp(xr, V, t, T);
             dr[t] = (-g_t * expm1(lp) - (Gv - g_t) * exp(lp)) / T;
+            if (gH != 0.0 && exp(lp) != 0.0)
+                dr[t] -= (gH / T) * exp(lp) * (lp + H);
         }
     }
     return bad;

@@ -41,8 +41,10 @@ MUTANTS = {
                                       "                if (i == k)\n                    sum_add(&gt"),
     "entropy_target_term_dropped": ("    sum_add(&h, neg_plogp(lp_t));\n", ""),
     "entropy_lse_sign": (": x[t] / T - lp_t;", ": x[t] / T + lp_t;"),
-    "sel_bwd_missing_inverse_T": ("dr[j] = -(Gv / T) * exp(xr[j] / T - lse);",
-                                  "dr[j] = -Gv * exp(xr[j] / T - lse);"),
+    "ent_bwd_sign": ("dr[j] -= (gH / T) * pj * (lpj + H);", "dr[j] += (gH / T) * pj * (lpj + H);"),
+    "ent_bwd_target_drops_H": ("* exp(lp) * (lp + H);", "* exp(lp) * lp;"),
+    "sel_bwd_missing_inverse_T": ("dr[j] = -(Gv / T) * pj;",
+                                  "dr[j] = -Gv * pj;"),
 }
 
 

@@ -510,3 +510,82 @@ def test_entropy_ignores_zero_probability_columns():
     for ref in (5, 40, 42):
         got, bad = oracle.entropy(x, [ref], 0.9)
         assert bad == 0 and got[0] == pytest.approx(want, rel=1e-13), ref
+
+
+# ----------------------------------------------- entropy term of the backward
+
+def brute_entropy_grad(row, T):
+    """dH/dx_j = -(1/T) p_j (log p_j + H) at 120 digits, and the size
+    max_j p_j (|log p_j| + H) / T of the terms it takes the difference of."""
+    logps, _ = brute_row(row, 0, T)
+    h = Decimal(0)
+    for lp in logps:
+        h = CTX.subtract(h, CTX.multiply(CTX.exp(lp), lp))
+    Td = Decimal(T)
+    grad = [float(-CTX.divide(CTX.multiply(CTX.exp(lp), CTX.add(lp, h)), Td)) for lp in logps]
+    size = max(float(CTX.divide(CTX.multiply(CTX.exp(lp), CTX.add(abs(lp), h)), Td))
+               for lp in logps)
+    return np.array(grad), size
+
+
+@pytest.mark.parametrize("V", [2, 5, 33])
+@pytest.mark.parametrize("T", [1.0, 0.7])
+def test_entropy_backward_brute_force(V, T):
+    margins = [0.0, 17.0, 30.0, 50.0]
+    w = workloads.peaked_rows_tiny(V, margins, seed=500 + V)
+    x = w.logits.numpy()
+    y = w.labels.numpy()
+    gh = np.array([1.0, -0.5, 2.0, 0.25])
+    zero = np.zeros((len(margins), 1))
+    dx, bad = oracle.selective_logsoftmax_backward(x, y[:, None], zero, T, grad_entropy=gh)
+    assert bad == 0
+    Te = oracle.exact_temperature(T)
+    for r in range(len(margins)):
+        grad, size = brute_entropy_grad(x[r], Te)
+        want = gh[r] * grad
+        # log p_j + H cancels near a uniform row: the bound scales with the terms
+        assert np.max(np.abs(dx[r] - want)) <= 1e-13 * abs(gh[r]) * size, (r, margins[r])
+        # the dominant column's tiny entry keeps its relative accuracy
+        assert dx[r, y[r]] == pytest.approx(want[y[r]], rel=1e-9, abs=1e-300)
+
+
+def test_entropy_backward_finite_difference_with_logp_terms():
+    rng = np.random.default_rng(41)
+    V, rows, K = 9, 3, 2
+    x = rng.normal(scale=2.0, size=(rows, V))
+    idx = np.array([[1, 4], [2, 2], [8, 0]])
+    g = rng.normal(size=(rows, K))
+    gh = rng.normal(size=rows)
+    T = 0.8
+    dx, _ = oracle.selective_logsoftmax_backward(x, idx, g, T, grad_entropy=gh)
+    h = 1e-6
+    num = np.zeros_like(x)
+    for r in range(rows):
+        for j in range(V):
+            xp, xm = x.copy(), x.copy()
+            xp[r, j] += h
+            xm[r, j] -= h
+            fp, _ = oracle.selective_logsoftmax(xp, idx, T)
+            fm, _ = oracle.selective_logsoftmax(xm, idx, T)
+            hp, _ = oracle.entropy(xp, idx[:, 0], T)
+            hm, _ = oracle.entropy(xm, idx[:, 0], T)
+            num[r, j] = (np.sum(g[r] * (fp[r] - fm[r])) + gh[r] * (hp[r] - hm[r])) / (2 * h)
+    np.testing.assert_allclose(dx, num, rtol=2e-6, atol=1e-9)
+
+
+def test_entropy_backward_invariants():
+    # uniform rows sit at the entropy maximum: zero entropy gradient; rows sum
+    # to zero; a column at -inf gets exactly 0
+    V = 50
+    x = np.full((1, V), 1.5)
+    dx, _ = oracle.selective_logsoftmax_backward(x, [[3]], [[0.0]], 0.9, grad_entropy=[2.0])
+    assert np.max(np.abs(dx)) <= 1e-15
+    rng = np.random.default_rng(3)
+    x = rng.normal(scale=3, size=(4, 60))
+    x[1, 7] = -np.inf
+    dx, _ = oracle.selective_logsoftmax_backward(x, rng.integers(0, 60, (4, 2)),
+                                                 rng.normal(size=(4, 2)), 0.7,
+                                                 grad_entropy=rng.normal(size=4))
+    assert dx[1, 7] == 0.0
+    for r in range(4):
+        assert abs(math.fsum(dx[r])) <= 1e-14 * math.fsum(np.abs(dx[r]))
