@@ -380,7 +380,7 @@ def op_bytes(w, op, k=1):
     of every row written once, int64 labels / indices and fp32 outputs."""
     es = w.logits.element_size()
     rows, V = w.rows, w.vocab
-    if op in ("logp", "logp_ent", "logp_bwd"):
+    if op in ("logp", "logp_ent", "logp_bwd", "logp_ent_bwd"):
         live = rows if w.row_mask is None else int(w.row_mask.sum().item())
         mask = 0 if w.row_mask is None else rows
         if op == "logp":
@@ -388,7 +388,9 @@ def op_bytes(w, op, k=1):
         if op == "logp_ent":  # + one fp32 entropy per row
             return live * V * es + rows * k * 8 + rows * k * 4 + rows * 4 + mask
         # logits in, dlogits out, index + upstream gradient + saved log-probs
-        return live * V * es + rows * V * es + rows * k * (8 + 4 + 4) + mask
+        # (+ dL/dH and the saved entropy per row)
+        ent = rows * 8 if op == "logp_ent_bwd" else 0
+        return live * V * es + rows * V * es + rows * k * (8 + 4 + 4) + mask + ent
     live = int((w.labels != workloads.IGNORE_INDEX).sum().item())
     read = live * V * es + rows * 8
     if op == "ce_fwd":
@@ -477,6 +479,12 @@ def measure_configs(gbce, dev, stream, peak):
             record(f"{tag}/selective_logsoftmax_bwd", w, "logp_bwd", time_op(
                 lambda: gbce.selective_logsoftmax_bwd(x, idx, g, o, T, mask, dlogits=d),
                 stream, 10, fl), k=K_)
+            if entropy:
+                gh = torch.full((w.rows,), 0.01, device=dev)
+                record(f"{tag}/selective_logsoftmax_bwd+entropy", w, "logp_ent_bwd", time_op(
+                    lambda: gbce.selective_logsoftmax_bwd(x, idx, g, o, T, mask, grad_entropy=gh,
+                                                          saved_entropy=h, dlogits=d),
+                    stream, 10, fl), k=K_)
 
     w = workloads.ce_small_fp32(device=dev)
     ce_ops("ce_small_fp32_64x4096", w, 1.0, "mean", torch.ones(1, device=dev))

@@ -47,7 +47,7 @@ _SIGNATURES = {
     "selective_logsoftmax": (_i32, [_vp, _i32, _i64, _i64, _i64, _vp, _i64, _f32, _vp, _vp,
                                     _vp, _vp, _sz, _vp, _vp]),
     "selective_logsoftmax_bwd": (_i32, [_vp, _i32, _i64, _i64, _i64, _vp, _i64, _f32, _vp, _vp,
-                                        _vp, _vp, _i64, _vp, _vp]),
+                                        _vp, _vp, _vp, _vp, _i64, _vp, _vp]),
     "ce_fwd": (_i32, [_vp, _i32, _i64, _i64, _i64, _vp, _i64, _f32, _i32, _vp, _vp, _vp, _vp,
                       _vp, _sz, _vp, _vp]),
     "ce_bwd": (_i32, [_vp, _i32, _i64, _i64, _i64, _vp, _i64, _f32, _i32, _vp, _vp, _vp, _vp,
@@ -197,13 +197,16 @@ def selective_logsoftmax(logits: torch.Tensor, index, temperature: float = 1.0,
 
 def selective_logsoftmax_bwd(logits: torch.Tensor, index, grad_logp, saved_logp,
                              temperature: float = 1.0, row_mask: Optional[torch.Tensor] = None,
-                             *, dlogits: Optional[torch.Tensor] = None,
+                             *, grad_entropy=None, saved_entropy: Optional[torch.Tensor] = None,
+                             dlogits: Optional[torch.Tensor] = None,
                              dev_status: Optional[torch.Tensor] = None,
                              stream=None) -> torch.Tensor:
     """dL/dlogits for upstream grad_logp = dL/d selective_logsoftmax(...).
 
     ``index``, ``grad_logp`` and ``saved_logp`` have the forward's output
-    shape ([..., K], or [...] for K = 1); masked-out rows get zero.
+    shape ([..., K], or [...] for K = 1); masked-out rows get zero.  With
+    ``grad_entropy`` = dL/d entropy ([...], one per row) the gradient of the
+    forward's entropy output is added; ``saved_entropy`` is that output.
     """
     lib = load_library()
     lead_shape = logits.shape[:-1]
@@ -218,13 +221,21 @@ def selective_logsoftmax_bwd(logits: torch.Tensor, index, grad_logp, saved_logp,
     mask = None
     if row_mask is not None:
         mask = row_mask.to(device=x.device, dtype=torch.uint8).reshape(rows).contiguous()
+    gh = hs = None
+    if (grad_entropy is None) != (saved_entropy is None):
+        raise ValueError("grad_entropy and saved_entropy go together")
+    if grad_entropy is not None:
+        gh = torch.as_tensor(grad_entropy, dtype=torch.float32,
+                             device=x.device).reshape(rows).contiguous()
+        hs = saved_entropy.to(torch.float32).reshape(rows).contiguous()
     if dlogits is None:
         dlogits = torch.empty_like(logits)
     d = _rows_view(dlogits)
     st = lib.selective_logsoftmax_bwd(x.data_ptr(), _dtype_code(x), rows, V, x.stride(0),
                                       idx.data_ptr(), K, float(temperature), _ptr(mask),
-                                      g.data_ptr(), lp.data_ptr(), d.data_ptr(), d.stride(0),
-                                      _ptr(dev_status), _stream_ptr(stream))
+                                      g.data_ptr(), lp.data_ptr(), _ptr(gh), _ptr(hs),
+                                      d.data_ptr(), d.stride(0), _ptr(dev_status),
+                                      _stream_ptr(stream))
     _check(st, "selective_logsoftmax_bwd")
     return dlogits
 

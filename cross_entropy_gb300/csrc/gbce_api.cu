@@ -257,6 +257,7 @@ gbce_status selective_logsoftmax_bwd(const void *logits, gbce_dtype dtype, int64
                                      int64_t vocab, int64_t row_stride, const int64_t *index,
                                      int64_t k, float temperature, const uint8_t *row_mask,
                                      const float *grad_logp, const float *saved_logp,
+                                     const float *grad_entropy, const float *saved_entropy,
                                      void *dlogits, int64_t dlogits_row_stride,
                                      int32_t *dev_status, void *stream)
 {
@@ -268,6 +269,8 @@ gbce_status selective_logsoftmax_bwd(const void *logits, gbce_dtype dtype, int64
     if (rows == 0)
         return GBCE_OK;
     if (index == nullptr || grad_logp == nullptr || saved_logp == nullptr)
+        return GBCE_EINVAL;
+    if ((grad_entropy == nullptr) != (saved_entropy == nullptr))
         return GBCE_EINVAL;
     if ((st = check_dlogits(logits, dtype, rows, vocab, row_stride, dlogits,
                             dlogits_row_stride)) != GBCE_OK)
@@ -282,8 +285,10 @@ gbce_status selective_logsoftmax_bwd(const void *logits, gbce_dtype dtype, int64
     p.vec_store = same_vector_phase(logits, row_stride, dlogits, dlogits_row_stride, dtype);
     p.grad_out = grad_logp;
     p.saved_logp = saved_logp;
-    return cuda_status(
-        launch_rows(p, dtype, gbce::kModeLogpGrad, static_cast<cudaStream_t>(stream)));
+    p.grad_entropy = grad_entropy;
+    p.saved_entropy = saved_entropy;
+    const int mode = grad_entropy != nullptr ? gbce::kModeLogpEntGrad : gbce::kModeLogpGrad;
+    return cuda_status(launch_rows(p, dtype, mode, static_cast<cudaStream_t>(stream)));
 }
 
 gbce_status ce_fwd(const void *logits, gbce_dtype dtype, int64_t rows, int64_t vocab,

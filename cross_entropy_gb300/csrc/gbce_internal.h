@@ -18,6 +18,7 @@ enum Mode : int {
     kModeFused = 3,  // statistics then gradient of the same row (one launch)
     kModeLogpGrad = 4,  // selective log-softmax gradient from saved log p (K indices)
     kModeLogpEnt = 5,   // kModeLogp plus the entropy of each row
+    kModeLogpEntGrad = 6,  // kModeLogpGrad plus the gradient of the row entropy
 };
 
 struct RowParams {
@@ -47,6 +48,8 @@ struct RowParams {
     int reduction;  // 0 none, 1 sum, 2 mean
     const int64_t *n_items;
     const float *saved_logp;  // kModeGrad: [rows]; kModeLogpGrad: [rows, k]
+    const float *grad_entropy;   // kModeLogpEntGrad: [rows] dL/dH
+    const float *saved_entropy;  // kModeLogpEntGrad: [rows] H from the forward
 
     int32_t *dev_status;
 };

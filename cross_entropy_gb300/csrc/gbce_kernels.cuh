@@ -240,6 +240,8 @@ struct GradConsts {
     float kbx;  // kb - x_y * c: the bf16 path's exponent is x * c + kbx
     float gs;   // g / T * 2^-offset
     float dy;   // g / T * expm1(log p), the label column
+    // entropy gradient: an element is 2^z (ea + eb z) instead of gs 2^z
+    float ea, eb;
 };
 
 __device__ __forceinline__ GradConsts grad_consts(float xy, float c, float logp, float gscale)
@@ -255,10 +257,37 @@ __device__ __forceinline__ GradConsts grad_consts(float xy, float c, float logp,
     return k;
 }
 
+// Constants for a gradient whose element j != gathered columns is
+// p_j (A + B log p_j) -- the selective log-softmax gradient (A = -G/T, B = 0)
+// plus the entropy's (A -= gH H / T, B = -gH / T).  With z = log2 p_j + off
+// (the exponent the element evaluates), log p_j = (z - off) ln 2, so the
+// element is 2^z * 2^-off (A - B off ln2 + B ln2 z) = 2^z (ea + eb z).
+__device__ __forceinline__ GradConsts grad_consts_ent(float xy, float c, float logp, float A,
+                                                      float B)
+{
+    // same offset rule as grad_consts, on the larger coefficient
+    const float big = fmaxf(fabsf(A), fabsf(B));
+    GradConsts k = grad_consts(xy, c, logp, big);
+    const bool offset = big >= 0x1p-90f;
+    const float off = offset ? 32.0f : 0.0f, scale = offset ? 0x1p-32f : 1.0f;
+    constexpr float kLn2 = 0.69314718055994531f;
+    k.ea = scale * fmaf(-B * kLn2, off, A);
+    k.eb = scale * (B * kLn2);
+    return k;
+}
+
 // dlogits of one element j != y: g/T * exp((x_j - x_y)/T + log p).
 __device__ __forceinline__ float grad_scalar(float x, const GradConsts &k)
 {
     return k.gs * ex2(fmaf(x + k.nxy, k.c, k.kb));
+}
+
+// The same element with the entropy term: 2^z (ea + eb z); a -inf logit
+// (2^z = 0) gives 0, not 0 * inf.
+__device__ __forceinline__ float grad_scalar_ent(float x, const GradConsts &k)
+{
+    const float z = fmaf(x + k.nxy, k.c, k.kb);
+    return ex2(z) * fmaf(k.eb, OnlineStats<true>::zfin(z), k.ea);
 }
 
 // dlogits of one 16-byte vector.  yoff = label column - first column of
@@ -270,13 +299,21 @@ template <typename T> struct GradVec;
 template <> struct GradVec<__nv_bfloat16> {
     // bf16 logits are exact in fp32 and |x c| is small, so x c + (kb - x_y c)
     // in one fused multiply-add stays within a few fp32 ulps of the exponent.
+    template <bool ENT = false>
     __device__ static __forceinline__ uint4 run(const uint4 &raw, int32_t yoff, const GradConsts &k)
     {
         const float2 cc = make_float2(k.c, k.c), kk = make_float2(k.kbx, k.kbx);
         const float2 gg = make_float2(k.gs, k.gs);
+        const float2 ea = make_float2(k.ea, k.ea), eb = make_float2(k.eb, k.eb);
         const auto one = [&](uint32_t w) {
             const float2 z = ffma2(bf16x2_to_float2(w), cc, kk);
-            return float2_to_bf16x2(fmul2(make_float2(ex2(z.x), ex2(z.y)), gg));
+            const float2 e = make_float2(ex2(z.x), ex2(z.y));
+            if (ENT) {
+                using S = OnlineStats<true>;
+                const float2 wv = ffma2(make_float2(S::zfin(z.x), S::zfin(z.y)), eb, ea);
+                return float2_to_bf16x2(fmul2(e, wv));
+            }
+            return float2_to_bf16x2(fmul2(e, gg));
         };
         uint4 o = make_uint4(one(raw.x), one(raw.y), one(raw.z), one(raw.w));
         if (static_cast<uint32_t>(yoff) < 8u) {
@@ -293,18 +330,24 @@ template <> struct GradVec<__nv_bfloat16> {
         }
         return o;
     }
+    template <bool ENT = false>
     __device__ static __forceinline__ void run_unpacked(const uint4 &raw, int32_t yoff,
                                                         const GradConsts &k, float (&d)[8])
     {
         float f[8];
         Elem<__nv_bfloat16>::unpack(raw, f);
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-            d[e] = (e == yoff) ? k.dy : k.gs * ex2(fmaf(f[e], k.c, k.kbx));
+        for (int e = 0; e < 8; ++e) {
+            const float z = fmaf(f[e], k.c, k.kbx);
+            const float v = ENT ? ex2(z) * fmaf(k.eb, OnlineStats<true>::zfin(z), k.ea)
+                                : k.gs * ex2(z);
+            d[e] = (e == yoff) ? k.dy : v;
+        }
     }
 };
 
 template <> struct GradVec<float> {
+    template <bool ENT = false>
     __device__ static __forceinline__ uint4 run(const uint4 &raw, int32_t yoff, const GradConsts &k)
     {
         const float2 nn = make_float2(k.nxy, k.nxy), cc = make_float2(k.c, k.c);
@@ -312,8 +355,15 @@ template <> struct GradVec<float> {
         const float2 p0 = make_float2(__uint_as_float(raw.x), __uint_as_float(raw.y));
         const float2 p1 = make_float2(__uint_as_float(raw.z), __uint_as_float(raw.w));
         const float2 z0 = ffma2(fadd2(p0, nn), cc, kk), z1 = ffma2(fadd2(p1, nn), cc, kk);
-        const float2 d0 = fmul2(make_float2(ex2(z0.x), ex2(z0.y)), gg);
-        const float2 d1 = fmul2(make_float2(ex2(z1.x), ex2(z1.y)), gg);
+        float2 g0 = gg, g1 = gg;
+        if (ENT) {
+            using S = OnlineStats<true>;
+            const float2 ea = make_float2(k.ea, k.ea), eb = make_float2(k.eb, k.eb);
+            g0 = ffma2(make_float2(S::zfin(z0.x), S::zfin(z0.y)), eb, ea);
+            g1 = ffma2(make_float2(S::zfin(z1.x), S::zfin(z1.y)), eb, ea);
+        }
+        const float2 d0 = fmul2(make_float2(ex2(z0.x), ex2(z0.y)), g0);
+        const float2 d1 = fmul2(make_float2(ex2(z1.x), ex2(z1.y)), g1);
         uint4 o = make_uint4(__float_as_uint(d0.x), __float_as_uint(d0.y), __float_as_uint(d1.x),
                              __float_as_uint(d1.y));
         if (static_cast<uint32_t>(yoff) < 4u) {
@@ -325,6 +375,7 @@ template <> struct GradVec<float> {
         }
         return o;
     }
+    template <bool ENT = false>
     __device__ static __forceinline__ void run_unpacked(const uint4 &raw, int32_t yoff,
                                                         const GradConsts &k, float (&d)[4])
     {
@@ -332,7 +383,7 @@ template <> struct GradVec<float> {
         Elem<float>::unpack(raw, f);
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-            d[e] = (e == yoff) ? k.dy : grad_scalar(f[e], k);
+            d[e] = (e == yoff) ? k.dy : (ENT ? grad_scalar_ent(f[e], k) : grad_scalar(f[e], k));
     }
 };
 
@@ -437,11 +488,13 @@ __global__ void __launch_bounds__(kRowThreads, (MODE == kModeLogpEnt && KMAX <= 
     constexpr int CV = kChunkBytes / 16;  // vectors per full chunk
     constexpr int PER_THREAD = CV / NC;
     static_assert(CV % NC == 0, "chunk must split evenly over consumer threads");
-    constexpr bool kStats = (MODE != kModeGrad && MODE != kModeLogpGrad);
-    constexpr bool kGrad = (MODE == kModeGrad || MODE == kModeFused || MODE == kModeLogpGrad);
+    constexpr bool kSelGrad = (MODE == kModeLogpGrad || MODE == kModeLogpEntGrad);
+    constexpr bool kEntGrad = (MODE == kModeLogpEntGrad);
+    constexpr bool kStats = (MODE != kModeGrad && !kSelGrad);
+    constexpr bool kGrad = (MODE == kModeGrad || MODE == kModeFused || kSelGrad);
     constexpr bool kEnt = (MODE == kModeLogpEnt);                  // + row entropy
     constexpr bool kLogpFwd = (MODE == kModeLogp || kEnt);         // log p of K indices
-    constexpr bool kGather = (kLogpFwd || MODE == kModeLogpGrad);  // K indices
+    constexpr bool kGather = (kLogpFwd || kSelGrad);  // K indices
     constexpr int kPasses = (MODE == kModeFused) ? 2 : 1;
 
     extern __shared__ __align__(128) uint8_t dyn_smem[];
@@ -453,6 +506,7 @@ __global__ void __launch_bounds__(kRowThreads, (MODE == kModeLogpEnt && KMAX <= 
     __shared__ float s_xt[KMAX];
     __shared__ float s_dt[KMAX];       // kModeLogpGrad: gradient at each gathered column
     __shared__ float s_G, s_lp0;       // kModeLogpGrad: sum of upstream, log p of index 0
+    __shared__ float s_gH, s_H;        // kModeLogpEntGrad: dL/dH and H of the row
     __shared__ int32_t s_tg[KMAX];
     __shared__ float bc_m, bc_s, bc_h, bc_logp;
     __shared__ uint64_t xbar;                   // fused, cluster of CTAs per row
@@ -485,7 +539,7 @@ __global__ void __launch_bounds__(kRowThreads, (MODE == kModeLogpEnt && KMAX <= 
             tg[k] = (t >= 0 && t < V) ? static_cast<int32_t>(t) : -1;
         }
         // the forward NaNs just the bad (r, k); its gradient NaNs the row
-        if (MODE == kModeLogpGrad && any_bad)
+        if (kSelGrad && any_bad)
             state = 2;
     } else {
         const int64_t lab = p.targets[r];
@@ -508,7 +562,7 @@ __global__ void __launch_bounds__(kRowThreads, (MODE == kModeLogpEnt && KMAX <= 
                 p.logp_out[r * p.k + tid] = 0.0f;
             if (kEnt && direct && tid == 0)
                 p.entropy_out[r] = 0.0f;
-        } else if (MODE == kModeLogpGrad) {
+        } else if (kSelGrad) {
             if (tid == 0 && split == 0 && state == 2)
                 report(p.dev_status, GBCE_DEV_BAD_INDEX);
             fill_row_slice<T>(drow, V, split, p.splits, fill);
@@ -550,10 +604,11 @@ __global__ void __launch_bounds__(kRowThreads, (MODE == kModeLogpEnt && KMAX <= 
             mbar_init(&xbar, 1);
         fence_barrier_init();
     }
-    if (MODE == kModeLogpGrad) {
+    if (kSelGrad) {
         // gathered column t: (1/T)(-g_t expm1(log p_t) - (G - g_t) exp(log p_t)),
         // g_t the upstream of every k that gathers t; every other column j:
-        // -(G/T) exp((x_j - x_{t0})/T + log p_{t0})
+        // -(G/T) exp((x_j - x_{t0})/T + log p_{t0}).  The entropy term adds
+        // -(gH/T) p_j (log p_j + H) to every column (0 where p_j = 0).
         if (tid < p.k) {
             const float *gr = p.grad_out + r * p.k;
             float G = 0.0f, gt = 0.0f;
@@ -571,10 +626,21 @@ __global__ void __launch_bounds__(kRowThreads, (MODE == kModeLogpEnt && KMAX <= 
                         gt += gk;
                 }
             const float lp = p.saved_logp[r * p.k + tid];
-            s_dt[tid] = (-gt * expm1f(lp) - (G - gt) * expf(lp)) / p.T;
+            float dt = (-gt * expm1f(lp) - (G - gt) * expf(lp)) / p.T;
+            float gH = 0.0f, H = 0.0f;
+            if (kEntGrad) {
+                gH = p.grad_entropy[r];
+                H = p.saved_entropy[r];
+                const float pt = expf(lp);
+                if (pt > 0.0f)
+                    dt -= (gH / p.T) * pt * (lp + H);
+            }
+            s_dt[tid] = dt;
             if (tid == 0) {
                 s_G = G;
                 s_lp0 = lp;
+                s_gH = gH;
+                s_H = H;
                 s_xt[0] = E::load(row + mine);
             }
         }
@@ -793,8 +859,13 @@ __global__ void __launch_bounds__(kRowThreads, (MODE == kModeLogpEnt && KMAX <= 
         }
     }
 
-    if (MODE == kModeLogpGrad) {
-        const GradConsts gk = grad_consts(s_xt[0], c, s_lp0, -s_G / p.T);
+    if (kSelGrad) {
+        const GradConsts gk =
+            kEntGrad ? grad_consts_ent(s_xt[0], c, s_lp0, -fmaf(s_gH, s_H, s_G) / p.T, -s_gH / p.T)
+                     : grad_consts(s_xt[0], c, s_lp0, -s_G / p.T);
+        const auto elem = [&](float x) {
+            return kEntGrad ? grad_scalar_ent(x, gk) : grad_scalar(x, gk);
+        };
         float dtv[KMAX];
 #pragma unroll
         for (int k = 0; k < KMAX; ++k)
@@ -809,12 +880,10 @@ __global__ void __launch_bounds__(kRowThreads, (MODE == kModeLogpEnt && KMAX <= 
         constexpr int32_t kNoLabel = 0x7fffffff;
         if (split == 0)
             for (int64_t e = tid; e < g.head; e += NC)
-                E::store(drow + e, at_target(static_cast<int32_t>(e),
-                                             grad_scalar(E::load(row + e), gk)));
+                E::store(drow + e, at_target(static_cast<int32_t>(e), elem(E::load(row + e))));
         if (split == p.splits - 1)
             for (int64_t e = g.tail0 + tid; e < V; e += NC)
-                E::store(drow + e, at_target(static_cast<int32_t>(e),
-                                             grad_scalar(E::load(row + e), gk)));
+                E::store(drow + e, at_target(static_cast<int32_t>(e), elem(E::load(row + e))));
         for (int64_t i = 0; i < nchunks; ++i, ++seq) {
             const int slot = static_cast<int>(seq % kStages);
             if (alive && !mbar_wait(&full_bar[slot], static_cast<uint32_t>((seq / kStages) & 1))) {
@@ -830,11 +899,12 @@ __global__ void __launch_bounds__(kRowThreads, (MODE == kModeLogpEnt && KMAX <= 
                     const uint4 raw = chunk[v];
                     const int32_t vb = static_cast<int32_t>(vbase + v);
                     if (!vector_has_target<KMAX>(tv, vb) && p.vec_store) {
-                        st_cs_v4(dbase + v * VEC, GradVec<T>::run(raw, kNoLabel, gk));
+                        st_cs_v4(dbase + v * VEC,
+                                 GradVec<T>::template run<kEntGrad>(raw, kNoLabel, gk));
                         continue;
                     }
                     float d[VEC];
-                    GradVec<T>::run_unpacked(raw, kNoLabel, gk, d);
+                    GradVec<T>::template run_unpacked<kEntGrad>(raw, kNoLabel, gk, d);
                     const int32_t col0v = static_cast<int32_t>(g.head) + vb * VEC;
 #pragma unroll
                     for (int e = 0; e < VEC; ++e)
@@ -1085,6 +1155,12 @@ cudaError_t launch_rows_per_unit(const RowParams &p, int mode, cudaStream_t stre
         if (p.k <= 4)
             return launch_row_kernel<T, kModeLogpGrad, 4>(p, stream);
         return launch_row_kernel<T, kModeLogpGrad, GBCE_MAX_K>(p, stream);
+    case kModeLogpEntGrad:
+        if (p.k <= 1)
+            return launch_row_kernel<T, kModeLogpEntGrad, 1>(p, stream);
+        if (p.k <= 4)
+            return launch_row_kernel<T, kModeLogpEntGrad, 4>(p, stream);
+        return launch_row_kernel<T, kModeLogpEntGrad, GBCE_MAX_K>(p, stream);
     default:
         return cudaErrorInvalidValue;
     }

@@ -130,7 +130,11 @@ gbce_status selective_logsoftmax(const void *logits, gbce_dtype dtype, int64_t r
  * G_r = sum_k g[r, k], with every gathered column t evaluated as
  *   (1/T) * ( -g_t * expm1(log p_t) - (G_r - g_t) * exp(log p_t) )
  * (g_t = the upstream of every k that gathers t) so that 1 - p_t keeps its
- * value when p_t rounds to 1; masked-out rows get a zero row.
+ * value when p_t rounds to 1; masked-out rows get a zero row.  With
+ * grad_entropy, the gradient of gH_r * H_r (H_r the row entropy of the
+ * forward's entropy_out) is added:
+ *   - (gH_r / T) * p_j * (log p_j + H_r)   for every column j,
+ * 0 where p_j = 0, with log p of the gathered columns from saved_logp.
  *
  * Source: the gradient a GRPO-style loss sends back through the accurate
  * log-probs of "Fix softmax collapse in CE, GRPO, KL/JSD and softmax"
@@ -144,6 +148,9 @@ gbce_status selective_logsoftmax(const void *logits, gbce_dtype dtype, int64_t r
  *   grad_logp   [rows, k] fp32, device: dL/d logp_out
  *   saved_logp  [rows, k] fp32: selective_logsoftmax's output for the same
  *               logits, index and temperature
+ *   grad_entropy  [rows] fp32 or NULL: dL/d entropy_out
+ *   saved_entropy [rows] fp32: the forward's entropy_out; NULL exactly when
+ *               grad_entropy is NULL
  *   dlogits     [rows, dlogits_row_stride], the logits' dtype; must not
  *               overlap the logits
  * Errors: as ce_bwd; a row with an index outside [0, vocab) sets
@@ -153,6 +160,7 @@ gbce_status selective_logsoftmax_bwd(const void *logits, gbce_dtype dtype, int64
                                      int64_t vocab, int64_t row_stride, const int64_t *index,
                                      int64_t k, float temperature, const uint8_t *row_mask,
                                      const float *grad_logp, const float *saved_logp,
+                                     const float *grad_entropy, const float *saved_entropy,
                                      void *dlogits, int64_t dlogits_row_stride,
                                      int32_t *dev_status, void *stream);
 

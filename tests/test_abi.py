@@ -158,3 +158,11 @@ def test_missing_library_fails_loudly(tmp_path):
 
     with pytest.raises(RuntimeError, match="not found"):
         gbce.load_library(str(tmp_path / "libgbce.so"))
+
+
+def test_selective_backward_entropy_pointers_go_together(lib):
+    def call(gh, hs):
+        return lib.selective_logsoftmax_bwd(FAKE, 0, 4, 100, 100, FAKE, 1, 1.0, None, FAKE, FAKE,
+                                            gh, hs, FAKE * 16, 100, None, None)
+    assert call(FAKE, None) == 1
+    assert call(None, FAKE) == 1

@@ -135,3 +135,99 @@ def test_bad_index_gives_nan_row_and_status():
     assert int(status.item()) == gbce.DEV_BAD_INDEX
     assert torch.isnan(d[1]).all() and torch.isnan(d[2]).all()
     assert torch.isfinite(d[0]).all() and torch.isfinite(d[3]).all()
+
+
+# ------------------------------------------------ with the row entropy's term
+
+def run_ent_case(x_cpu, idx, g, gh, T, mask=None, rows_sel=None):
+    """GPU forward (log p + entropy) and backward with dL/dH; oracle backward."""
+    x = x_cpu.to(DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    m_dev = None if mask is None else mask.to(DEV)
+    lp, h = gbce.selective_logsoftmax(x, idx.to(DEV), T, m_dev, with_entropy=True,
+                                      dev_status=status)
+    d = gbce.selective_logsoftmax_bwd(x, idx.to(DEV), g.to(DEV), lp, T, m_dev,
+                                      grad_entropy=gh.to(DEV), saved_entropy=h,
+                                      dev_status=status)
+    torch.cuda.synchronize()
+    sel = np.arange(x_cpu.shape[0]) if rows_sel is None else np.asarray(rows_sel)
+    st = torch.as_tensor(sel)
+    ref, bad = oracle.selective_logsoftmax_backward(
+        workloads.to_numpy_f64(x_cpu[st]), idx.numpy()[sel], g.double().numpy()[sel], T,
+        None if mask is None else mask.numpy()[sel], grad_entropy=gh.double().numpy()[sel])
+    return to_f64(d[st.to(DEV)]), ref, int(status.item()), bad
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("K", [1, 4])
+def test_entropy_term_matches_oracle(dtype, K):
+    gen = torch.Generator().manual_seed(60 + K)
+    rows, V = 560, 24001
+    w = workloads.collapse_stress(dtype=dtype, rows=rows, V=V, seed=30 + K)
+    idx = torch.randint(0, V, (rows, K), generator=gen)
+    idx[:, 0] = torch.where(w.labels >= 0, w.labels, idx[:, 0])
+    if K > 1:
+        idx[::4, 1] = idx[::4, 0]
+    mask = (torch.rand(rows, generator=gen) > 0.1).to(torch.uint8)
+    g = torch.randn((rows, K), generator=gen)
+    gh = torch.randn(rows, generator=gen)
+    sel = np.arange(0, rows, 5)
+    got, ref, status, bad = run_ent_case(w.logits, idx, g, gh, 0.9, mask, rows_sel=sel)
+    assert status == 0 and bad == 0
+    assert_grad_rows_close(got, ref, dtype, "selective_logsoftmax_bwd + entropy")
+    assert_zero_sum_rows(got, dtype)
+    assert np.all(got[mask.numpy()[sel] == 0] == 0.0)
+
+
+def test_entropy_only_gradient_of_confident_rows():
+    # g = 0: the gradient of the entropy alone; a confident row's dominant
+    # column has d H / d x_t = -(p_t / T)(log p_t + H) < 0, tiny but not 0
+    rows, V = 520, 151936
+    w = workloads.collapse_stress(dtype=torch.float32, rows=rows, V=V, seed=13)
+    idx = torch.where(w.labels >= 0, w.labels, 0)[:, None]
+    g = torch.zeros((rows, 1))
+    gh = torch.ones(rows)
+    pk = w.peaked_rows.numpy()
+    sel = pk[w.labels.numpy()[pk] >= 0][:32]
+    got, ref, status, _ = run_ent_case(w.logits, idx, g, gh, 1.0, rows_sel=sel)
+    assert status == 0
+    assert_grad_rows_close(got, ref, torch.float32)
+    cols = idx.numpy()[sel, 0]
+    assert np.all(got[np.arange(len(sel)), cols] < 0.0)
+    assert_zero_sum_rows(got, torch.float32)
+
+
+def test_entropy_term_with_minus_infinity_and_split_path():
+    gen = torch.Generator().manual_seed(70)
+    for rows, V in ((3, 152064), (530, 7003)):
+        x = torch.randn((rows, V), generator=gen).mul(2.0)
+        x[:, ::97] = float("-inf")
+        idx = torch.randint(0, V, (rows, 2), generator=gen)
+        idx[:, 0] = (idx[:, 0] // 97) * 97 + 1           # a finite reference column
+        g = torch.randn((rows, 2), generator=gen)
+        gh = torch.randn(rows, generator=gen)
+        sel = np.arange(0, rows, max(1, rows // 40))
+        got, ref, status, _ = run_ent_case(x, idx, g, gh, 0.8, rows_sel=sel)
+        assert status == 0
+        assert_grad_rows_close(got, ref, torch.float32)
+        assert np.all(got[:, ::97] == 0.0)
+
+
+def test_full_size_grpo_k4_with_entropy():
+    w = workloads.grpo_bf16(device=DEV)
+    gen = torch.Generator(device=DEV).manual_seed(2)
+    g = torch.randn((w.rows, 4), device=DEV, generator=gen)
+    gh = torch.randn(w.rows, device=DEV, generator=gen)
+    lp, h = gbce.selective_logsoftmax(w.logits, w.index, 0.9, with_entropy=True)
+    d = gbce.selective_logsoftmax_bwd(w.logits, w.index, g, lp, 0.9, grad_entropy=gh,
+                                      saved_entropy=h)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(5)
+    sel = np.sort(np.concatenate([rng.choice(w.rows, 16, replace=False),
+                                  w.peaked_rows.cpu().numpy()[:8]]))
+    st = torch.as_tensor(sel, device=DEV)
+    ref, _ = oracle.selective_logsoftmax_backward(workloads.to_numpy_f64(w.logits[st]),
+                                                  w.index[st].cpu().numpy(),
+                                                  g[st].double().cpu().numpy(), 0.9,
+                                                  grad_entropy=gh[st].double().cpu().numpy())
+    assert_grad_rows_close(to_f64(d[st]), ref, torch.bfloat16)
