@@ -27,7 +27,9 @@ Functions and the passages they follow:
 * :func:`cross_entropy` -- the same page's "Summary" (loss from the sum that
   excludes the target) with ms-swift PR #10353's "PR information" (analytic
   backward g*softmax - g*onehot, zero weight on ignored labels) and the
-  unsloth-zoo #2080 "Fix" section's -expm1(log p_t) target gradient.
+  unsloth-zoo #2080 "Fix" section's -expm1(log p_t) target gradient (label
+  smoothing included there); the DFT variant weights each row by p_y, held
+  constant in the backward (ms-swift PR #10353, "PR information").
 
 Pins: closed forms, 120-digit brute force, invariants and the pages' collapse
 thresholds, in ``tests/test_oracle_pins.py``.
@@ -83,8 +85,8 @@ def _load():
             dp, i64, i64, i64, ip, i64, ctypes.c_double, ctypes.c_void_p, dp]
         lib.oracle_cross_entropy.restype = i64
         lib.oracle_cross_entropy.argtypes = [
-            dp, i64, i64, i64, ip, i64, ctypes.c_double, ctypes.c_int, ctypes.c_void_p,
-            dp, dp, dp, ip, ctypes.c_void_p, i64]
+            dp, i64, i64, i64, ip, i64, ctypes.c_double, ctypes.c_int, ctypes.c_double,
+            ctypes.c_int, ctypes.c_void_p, dp, dp, dp, ip, ctypes.c_void_p, i64]
         lib.oracle_selective_logsoftmax_backward.restype = i64
         lib.oracle_selective_logsoftmax_backward.argtypes = [
             dp, i64, i64, i64, ip, i64, ctypes.c_double, ctypes.c_void_p, dp, ctypes.c_void_p,
@@ -201,8 +203,12 @@ def entropy(x, ref, temperature: float = 1.0, live=None):
 
 
 def cross_entropy(x, labels, ignore_index: int = -100, temperature: float = 1.0,
-                  reduction: str = "mean", grad_out=None, want_grad: bool = True):
+                  reduction: str = "mean", grad_out=None, want_grad: bool = True,
+                  label_smoothing: float = 0.0, dft: bool = False):
     """Token CE forward (and backward when ``want_grad``).
+
+    ``label_smoothing`` eps puts 1 - eps on the label and eps / V on every
+    class; ``dft`` weights each row's loss and gradient by its detached p_y.
 
     ``grad_out`` is the upstream gradient: [rows] for reduction 'none', a
     scalar otherwise (default 1).  Returns a dict with ``logp`` [rows],
@@ -230,7 +236,8 @@ def cross_entropy(x, labels, ignore_index: int = -100, temperature: float = 1.0,
     dx = np.empty((rows, V), dtype=np.float64) if want_grad else None
     bad = lib.oracle_cross_entropy(
         _ptr(x, ctypes.c_double), rows, V, x.strides[0] // 8, _ptr(lab, ctypes.c_int64),
-        int(ignore_index), exact_temperature(temperature), red, g_ptr,
+        int(ignore_index), exact_temperature(temperature), red, float(label_smoothing),
+        int(bool(dft)), g_ptr,
         _ptr(logp, ctypes.c_double), _ptr(loss_rows, ctypes.c_double),
         _ptr(loss, ctypes.c_double), _ptr(n_items, ctypes.c_int64),
         dx.ctypes.data if dx is not None else None, V)

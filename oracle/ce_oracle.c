@@ -230,13 +230,22 @@ int64_t oracle_selective_logsoftmax(const double *x, int64_t rows, int64_t V, in
 }
 
 /*
- * Token cross-entropy, forward and (when dx != NULL) backward.
+ * Token cross-entropy, forward and (when dx != NULL) backward, with optional
+ * label smoothing and DFT weighting.  For a kept row with label y,
+ *   loss_r = w_r * ((1 - eps) * (-log p_y) + eps * mean_j(-log p_j))
+ * (the smoothed target puts 1 - eps on y and eps / V on every class), and
+ *   dz_j = g_r * w_r * (p_j - (1 - eps) [j == y] - eps / V),  dx = dz / T,
+ * where w_r = p_y, held constant (the detached DFT weight), when dft != 0,
+ * else 1.  The label column of the gradient is written with expm1(log p_y)
+ * for p_y - 1.
  *   x          [rows, ld] fp64
  *   labels     [rows] int64, ignore_index marks rows to skip
  *   reduction  0 = none, 1 = sum, 2 = mean
+ *   eps        label smoothing in [0, 1]
+ *   dft        nonzero: weight each row by its detached p_y
  *   grad_out   [rows] for none, [1] otherwise; may be NULL when dx == NULL
  *   logp_y     [rows] out: log p of the label (0 for ignored rows)
- *   loss_rows  [rows] out: -log p of the label (0 for ignored rows)
+ *   loss_rows  [rows] out: the row's loss above (0 for ignored rows)
  *   loss       [1] out: the reduced loss (sum for none, for reference)
  *   n_items    [1] out: number of rows whose label is not ignore_index
  *   dx         [rows, ldx] out or NULL
@@ -244,7 +253,8 @@ int64_t oracle_selective_logsoftmax(const double *x, int64_t rows, int64_t V, in
  */
 int64_t oracle_cross_entropy(const double *x, int64_t rows, int64_t V, int64_t ld,
                              const int64_t *labels, int64_t ignore_index, double T,
-                             int reduction, const double *grad_out, double *logp_y,
+                             int reduction, double eps, int dft, const double *grad_out,
+                             double *logp_y,
                              double *loss_rows, double *loss, int64_t *n_items,
                              double *dx, int64_t ldx)
 {
@@ -267,8 +277,20 @@ int64_t oracle_cross_entropy(const double *x, int64_t rows, int64_t V, int64_t l
             loss_rows[r] = NAN;
             ++bad;
         } else {
-            logp_y[r] = row_logp(xr, V, y, T);
-            loss_rows[r] = -logp_y[r];
+            const double lp = row_logp(xr, V, y, T);
+            logp_y[r] = lp;
+            double loss_r = -lp;
+            if (eps != 0.0) {
+                /* mean over all classes of -log p_j, -log p_j = lse - z_j */
+                const double lse = xr[y] / T - lp;
+                oracle_sum nl = {0.0, 0.0};
+                sum_add(&nl, -lp);
+                for (int64_t j = 0; j < V; ++j)
+                    if (j != y)
+                        sum_add(&nl, lse - xr[j] / T);
+                loss_r = (1.0 - eps) * (-lp) + eps * (sum_value(&nl) / (double)V);
+            }
+            loss_rows[r] = dft ? exp(lp) * loss_r : loss_r;
         }
     }
 
@@ -305,14 +327,15 @@ int64_t oracle_cross_entropy(const double *x, int64_t rows, int64_t V, int64_t l
             g = grad_out[0];
         else
             g = count > 0 ? grad_out[0] / (double)count : 0.0;
-        double scale = g / T;
         double lp = logp_y[r];
+        double scale = (dft ? exp(lp) * g : g) / T;
         double zy = xr[y] / T;
+        const double u = eps / (double)V;
         for (int64_t j = 0; j < V; ++j) {
             if (j == y)
-                dr[j] = scale * expm1(lp);
+                dr[j] = scale * (expm1(lp) + (eps - u));
             else
-                dr[j] = scale * exp(xr[j] / T - zy + lp);
+                dr[j] = scale * (exp(xr[j] / T - zy + lp) - u);
         }
     }
     return bad;

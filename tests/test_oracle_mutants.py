@@ -20,18 +20,19 @@ MUTANTS = {
     "softplus_sign": ("fmax(a, 0.0) + log1p(", "fmax(a, 0.0) - log1p("),
     "target_left_in_others": ("        if (j == skip)\n            continue;\n        sum_add",
                               "        sum_add"),
-    "target_grad_exp_minus_one": ("scale * expm1(lp)", "scale * (exp(lp) - 1.0)"),
-    "grad_missing_inverse_T": ("double scale = g / T;", "double scale = g;"),
+    "target_grad_exp_minus_one": ("scale * (expm1(lp)", "scale * ((exp(lp) - 1.0)"),
+    "grad_missing_inverse_T": ("double scale = (dft ? exp(lp) * g : g) / T;",
+                               "double scale = (dft ? exp(lp) * g : g);"),
     "mean_grad_not_divided": ("g = count > 0 ? grad_out[0] / (double)count : 0.0;",
                               "g = grad_out[0];"),
     "mean_loss_not_divided": ("*loss = count > 0 ? sum_value(&total) / (double)count : 0.0;",
                               "*loss = sum_value(&total);"),
     "ignored_rows_counted": ("if (labels[r] != ignore_index)\n            ++count;",
                              "++count;"),
-    "grad_sign_flipped": ("dr[j] = scale * exp(xr[j] / T - zy + lp);",
-                          "dr[j] = -scale * exp(xr[j] / T - zy + lp);"),
-    "other_logit_target_swap": ("scale * exp(xr[j] / T - zy + lp)",
-                                "scale * exp(zy - xr[j] / T + lp)"),
+    "grad_sign_flipped": ("dr[j] = scale * (exp(xr[j] / T - zy + lp) - u);",
+                          "dr[j] = -scale * (exp(xr[j] / T - zy + lp) - u);"),
+    "other_logit_target_swap": ("scale * (exp(xr[j] / T - zy + lp)",
+                                "scale * (exp(zy - xr[j] / T + lp)"),
     "masked_rows_computed": ("if (row_mask && row_mask[r] == 0) {\n                *o = 0.0;",
                              "if (0) {\n                *o = 0.0;"),
     "sel_bwd_target_term_sign": ("dr[t] = (-g_t * expm1(lp) - (Gv - g_t) * exp(lp)) / T;",
@@ -43,6 +44,11 @@ MUTANTS = {
     "entropy_lse_sign": (": x[t] / T - lp_t;", ": x[t] / T + lp_t;"),
     "ent_bwd_sign": ("dr[j] -= (gH / T) * pj * (lpj + H);", "dr[j] += (gH / T) * pj * (lpj + H);"),
     "ent_bwd_target_drops_H": ("* exp(lp) * (lp + H);", "* exp(lp) * lp;"),
+    "smoothing_off_by_one_class": ("const double u = eps / (double)V;",
+                                   "const double u = eps / (double)(V - 1);"),
+    "smoothing_mean_not_over_V": ("eps * (sum_value(&nl) / (double)V)", "eps * sum_value(&nl)"),
+    "dft_weight_missing_in_gradient": ("double scale = (dft ? exp(lp) * g : g) / T;",
+                                       "double scale = g / T;"),
     "sel_bwd_missing_inverse_T": ("dr[j] = -(Gv / T) * pj;",
                                   "dr[j] = -Gv * pj;"),
 }

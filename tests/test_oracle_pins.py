@@ -589,3 +589,99 @@ def test_entropy_backward_invariants():
     assert dx[1, 7] == 0.0
     for r in range(4):
         assert abs(math.fsum(dx[r])) <= 1e-14 * math.fsum(np.abs(dx[r]))
+
+
+# ------------------------------------------- label smoothing and DFT on the CE
+
+def brute_smoothed_loss(row, y, T, eps, dft):
+    logps, lpy = brute_row(row, y, T)
+    V = len(row)
+    mean_nl = CTX.divide(-sum(logps, Decimal(0)), Decimal(V))
+    loss = CTX.add(CTX.multiply(Decimal(1) - Decimal(eps), -lpy),
+                   CTX.multiply(Decimal(eps), mean_nl))
+    if dft:
+        loss = CTX.multiply(CTX.exp(lpy), loss)
+    return float(loss)
+
+
+@pytest.mark.parametrize("V", [2, 5, 33])
+@pytest.mark.parametrize("eps,dft", [(0.1, False), (0.0, True), (0.25, True)])
+def test_smoothed_and_dft_loss_brute_force(V, eps, dft):
+    margins = [0.0, 17.0, 30.0, 50.0]
+    w = workloads.peaked_rows_tiny(V, margins, seed=700 + V)
+    x = w.logits.numpy()
+    y = w.labels.numpy()
+    for T in (1.0, 0.7):
+        out = oracle.cross_entropy(x, y, temperature=T, reduction="none", want_grad=False,
+                                   label_smoothing=eps, dft=dft)
+        Te = oracle.exact_temperature(T)
+        for r in range(len(margins)):
+            want = brute_smoothed_loss(x[r], y[r], Te, eps, dft)
+            assert out["loss_rows"][r] == pytest.approx(want, rel=1e-12, abs=1e-300), (r, T)
+
+
+def test_smoothed_ce_matches_torch_fp64():
+    rng = np.random.default_rng(12)
+    x = rng.normal(scale=2.5, size=(40, 300))
+    y = rng.integers(0, 300, 40)
+    y[[3, 17]] = -100
+    g = 0.37
+    for eps in (0.05, 0.3):
+        for red in ("mean", "sum", "none"):
+            out = oracle.cross_entropy(x, y, temperature=0.8, reduction=red, label_smoothing=eps,
+                                       grad_out=np.full(40, g) if red == "none" else [g])
+            xt = torch.tensor(x, requires_grad=True)
+            Te = oracle.exact_temperature(0.8)
+            ref = torch.nn.functional.cross_entropy(xt / Te, torch.tensor(y), ignore_index=-100,
+                                                    reduction=red, label_smoothing=eps)
+            (ref * g).sum().backward()
+            if red == "none":
+                np.testing.assert_allclose(out["loss_rows"], ref.detach().numpy(), rtol=1e-13)
+            else:
+                assert out["loss"] == pytest.approx(float(ref.detach()), rel=1e-13)
+            np.testing.assert_allclose(out["dlogits"], xt.grad.numpy(), rtol=1e-11, atol=1e-17)
+
+
+def test_smoothing_and_dft_closed_forms():
+    V = 64
+    x = np.full((2, V), -0.4)
+    # uniform row: every -log p_j is log V, so any eps gives log V; DFT scales by 1/V
+    for eps in (0.0, 0.2, 1.0):
+        out = oracle.cross_entropy(x, [1, 60], reduction="none", label_smoothing=eps)
+        np.testing.assert_allclose(out["loss_rows"], math.log(V), rtol=1e-14)
+        d = oracle.cross_entropy(x, [1, 60], reduction="none", label_smoothing=eps, dft=True)
+        np.testing.assert_allclose(d["loss_rows"], math.log(V) / V, rtol=1e-14)
+        # and a uniform row's smoothed gradient: (1 - eps)(1/V - 1) at y,
+        # 1/V - eps/V = (1 - eps)/V at every other column
+        np.testing.assert_allclose(out["dlogits"][0, 1], (1 - eps) * (1.0 / V - 1.0),
+                                   rtol=1e-12, atol=1e-16)
+        others = np.delete(out["dlogits"][0], 1)
+        np.testing.assert_allclose(others, (1 - eps) / V, rtol=1e-12, atol=1e-16)
+
+
+def test_smoothed_gradient_finite_difference_and_dft_relation():
+    rng = np.random.default_rng(77)
+    V, rows = 11, 3
+    x = rng.normal(scale=2.0, size=(rows, V))
+    y = np.array([2, 9, 0])
+    eps, T, h = 0.15, 0.9, 1e-6
+    out = oracle.cross_entropy(x, y, temperature=T, reduction="sum", label_smoothing=eps)
+    num = np.zeros_like(x)
+    for r in range(rows):
+        for j in range(V):
+            xp, xm = x.copy(), x.copy()
+            xp[r, j] += h
+            xm[r, j] -= h
+            fp = oracle.cross_entropy(xp, y, temperature=T, reduction="sum", want_grad=False,
+                                      label_smoothing=eps)["loss"]
+            fm = oracle.cross_entropy(xm, y, temperature=T, reduction="sum", want_grad=False,
+                                      label_smoothing=eps)["loss"]
+            num[r, j] = (fp - fm) / (2 * h)
+    np.testing.assert_allclose(out["dlogits"], num, rtol=2e-6, atol=1e-9)
+    # DFT: the weight p_y is held constant, so the gradient is p_y times the plain one
+    d = oracle.cross_entropy(x, y, temperature=T, reduction="sum", label_smoothing=eps, dft=True)
+    py = np.exp(out["logp"])
+    np.testing.assert_allclose(d["dlogits"], py[:, None] * out["dlogits"], rtol=1e-14)
+    np.testing.assert_allclose(d["loss_rows"], py * out["loss_rows"], rtol=1e-14)
+    for r in range(rows):
+        assert abs(math.fsum(d["dlogits"][r])) <= 1e-14 * math.fsum(np.abs(d["dlogits"][r]))
