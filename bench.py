@@ -442,7 +442,7 @@ def measure_configs(gbce, dev, stream, peak):
         out[name] = {"ms": round(ms, 5), "rows_per_s": round(w.rows / (ms * 1e-3)),
                      "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4), "bytes": nb}
 
-    def ce_ops(tag, w, T, red, g):
+    def ce_ops(tag, w, T, red, g, options=False):
         x, lab = w.logits, w.labels
         d = torch.empty_like(x)
         ws = gbce.new_workspace(w.rows, w.vocab, 1, device=dev)
@@ -457,6 +457,13 @@ def measure_configs(gbce, dev, stream, peak):
         record(f"{tag}/ce_bwd", w, "ce_bwd", time_op(
             lambda: gbce.ce_bwd(x, lab, g, fwd.logp, fwd.n_items, temperature=T, reduction=red,
                                 dlogits=d), stream, 10, fl))
+        if options:  # label smoothing 0.1 with DFT weights: the smoothing sum in the sweep
+            kw = dict(temperature=T, reduction=red, label_smoothing=0.1, dft=True)
+            record(f"{tag}/ce_fwd_bwd_fused+smooth+dft", w, "fused", time_op(
+                lambda: gbce.ce_fwd_bwd_fused(x, lab, g, dlogits=d, workspace=ws, **kw),
+                stream, 10, fl))
+            record(f"{tag}/ce_fwd+smooth+dft", w, "ce_fwd", time_op(
+                lambda: gbce.ce_fwd(x, lab, workspace=ws, **kw), stream, 10, fl))
 
     def logp_op(tag, w, T, backward=False, k=None, entropy=False):
         x, idx = w.logits, (w.index if k is None else w.index[:, :k].contiguous())
@@ -504,7 +511,8 @@ def measure_configs(gbce, dev, stream, peak):
     ce_ops("split_bf16_64x152064", w, TEMPERATURE, "mean", torch.ones(1, device=dev))
     logp_op("split_bf16_64x152064", w, TEMPERATURE, entropy=True)
     w = workloads.grpo_bf16(device=dev, rows=ROWS)
-    ce_ops(f"grpo_bf16_{ROWS}x{VOCAB}", w, TEMPERATURE, "mean", torch.ones(1, device=dev))
+    ce_ops(f"grpo_bf16_{ROWS}x{VOCAB}", w, TEMPERATURE, "mean", torch.ones(1, device=dev),
+           options=True)
     logp_op(f"grpo_bf16_{ROWS}x{VOCAB}_k4", w, TEMPERATURE, backward=True, entropy=True)
     logp_op(f"grpo_bf16_{ROWS}x{VOCAB}_k1", w, TEMPERATURE, backward=True, k=1, entropy=True)
     del w, flush

@@ -49,11 +49,11 @@ _SIGNATURES = {
     "selective_logsoftmax_bwd": (_i32, [_vp, _i32, _i64, _i64, _i64, _vp, _i64, _f32, _vp, _vp,
                                         _vp, _vp, _vp, _vp, _i64, _vp, _vp]),
     "ce_fwd": (_i32, [_vp, _i32, _i64, _i64, _i64, _vp, _i64, _f32, _i32, _vp, _vp, _vp, _vp,
-                      _vp, _sz, _vp, _vp]),
+                      _vp, _vp, _sz, _vp, _vp]),
     "ce_bwd": (_i32, [_vp, _i32, _i64, _i64, _i64, _vp, _i64, _f32, _i32, _vp, _vp, _vp, _vp,
-                      _i64, _vp, _vp]),
+                      _vp, _i64, _vp, _vp]),
     "ce_fwd_bwd_fused": (_i32, [_vp, _i32, _i64, _i64, _i64, _vp, _i64, _f32, _i32, _vp, _vp,
-                                _vp, _vp, _vp, _vp, _i64, _vp, _sz, _vp, _vp]),
+                                _vp, _vp, _vp, _vp, _vp, _i64, _vp, _sz, _vp, _vp]),
     "ce_fwd_bwd_fused_noalloc": (_i32, [_vp, _i32, _i64, _i64, _i64, _vp, _i64, _f32, _i32,
                                         _vp, _vp, _vp, _vp, _vp, _vp, _i64, _vp, _vp]),
 }
@@ -240,6 +240,19 @@ def selective_logsoftmax_bwd(logits: torch.Tensor, index, grad_logp, saved_logp,
     return dlogits
 
 
+class CeOptions(ctypes.Structure):
+    """gbce_ce_options: label smoothing eps and the DFT row weight."""
+
+    _fields_ = [("label_smoothing", ctypes.c_float), ("dft", ctypes.c_int32)]
+
+
+def _ce_options(label_smoothing: float, dft: bool):
+    """A CeOptions to pass by reference, or None for plain CE."""
+    if label_smoothing == 0.0 and not dft:
+        return None
+    return ctypes.byref(CeOptions(float(label_smoothing), 1 if dft else 0))
+
+
 class CeForward(NamedTuple):
     loss: torch.Tensor              # [rows] for 'none', [] otherwise
     logp: Optional[torch.Tensor]    # [rows] log p of the label (0 for ignored rows)
@@ -256,10 +269,14 @@ class CeFused(NamedTuple):
 
 
 def ce_fwd(logits: torch.Tensor, labels, ignore_index: int = -100, temperature: float = 1.0,
-           reduction: str = "mean", *, want_lse: bool = False,
-           workspace: Optional[torch.Tensor] = None, dev_status: Optional[torch.Tensor] = None,
-           stream=None) -> CeForward:
-    """Cross-entropy forward; returns loss, saved log p (for ce_bwd), lse, n_items."""
+           reduction: str = "mean", *, label_smoothing: float = 0.0, dft: bool = False,
+           want_lse: bool = False, workspace: Optional[torch.Tensor] = None,
+           dev_status: Optional[torch.Tensor] = None, stream=None) -> CeForward:
+    """Cross-entropy forward; returns loss, saved log p (for ce_bwd), lse, n_items.
+
+    ``label_smoothing`` eps and ``dft`` (rows weighted by their detached p_y)
+    change the loss; ce_bwd must be given the same two.
+    """
     lib = load_library()
     x = _rows_view(logits)
     rows, V = x.shape
@@ -271,7 +288,8 @@ def ce_fwd(logits: torch.Tensor, labels, ignore_index: int = -100, temperature: 
     n_items = torch.empty(1, dtype=torch.int64, device=x.device)
     ws, ws_ptr, ws_bytes = _workspace(workspace, rows, V, 1, x.device)
     st = lib.ce_fwd(x.data_ptr(), _dtype_code(x), rows, V, x.stride(0), lab.data_ptr(),
-                    int(ignore_index), float(temperature), red, loss.data_ptr(), logp.data_ptr(),
+                    int(ignore_index), float(temperature), red,
+                    _ce_options(label_smoothing, dft), loss.data_ptr(), logp.data_ptr(),
                     _ptr(lse), n_items.data_ptr(), ws_ptr, ws_bytes, _ptr(dev_status),
                     _stream_ptr(stream))
     _check(st, "ce_fwd")
@@ -280,9 +298,11 @@ def ce_fwd(logits: torch.Tensor, labels, ignore_index: int = -100, temperature: 
 
 def ce_bwd(logits: torch.Tensor, labels, grad_out, saved_logp: torch.Tensor, n_items=None,
            ignore_index: int = -100, temperature: float = 1.0, reduction: str = "mean", *,
+           label_smoothing: float = 0.0, dft: bool = False,
            dlogits: Optional[torch.Tensor] = None, dev_status: Optional[torch.Tensor] = None,
            stream=None) -> torch.Tensor:
-    """dlogits = g * (softmax - onehot) / T from ce_fwd's saved log p."""
+    """dlogits = g * (softmax - onehot) / T from ce_fwd's saved log p (smoothed /
+    DFT-weighted with the same options as the forward)."""
     lib = load_library()
     x = _rows_view(logits)
     rows, V = x.shape
@@ -297,7 +317,8 @@ def ce_bwd(logits: torch.Tensor, labels, grad_out, saved_logp: torch.Tensor, n_i
     d = _rows_view(dlogits)
     lp = saved_logp.reshape(rows).contiguous()
     st = lib.ce_bwd(x.data_ptr(), _dtype_code(x), rows, V, x.stride(0), lab.data_ptr(),
-                    int(ignore_index), float(temperature), red, g.data_ptr(), lp.data_ptr(),
+                    int(ignore_index), float(temperature), red,
+                    _ce_options(label_smoothing, dft), g.data_ptr(), lp.data_ptr(),
                     _ptr(n), d.data_ptr(), d.stride(0), _ptr(dev_status), _stream_ptr(stream))
     _check(st, "ce_bwd")
     return dlogits
@@ -305,6 +326,7 @@ def ce_bwd(logits: torch.Tensor, labels, grad_out, saved_logp: torch.Tensor, n_i
 
 def ce_fwd_bwd_fused(logits: torch.Tensor, labels, grad_out=None, ignore_index: int = -100,
                      temperature: float = 1.0, reduction: str = "mean", *,
+                     label_smoothing: float = 0.0, dft: bool = False,
                      dlogits: Optional[torch.Tensor] = None, want_logp: bool = True,
                      want_lse: bool = False, workspace: Optional[torch.Tensor] = None,
                      dev_status: Optional[torch.Tensor] = None, stream=None) -> CeFused:
@@ -328,7 +350,8 @@ def ce_fwd_bwd_fused(logits: torch.Tensor, labels, grad_out=None, ignore_index: 
     d = _rows_view(dlogits)
     ws, ws_ptr, ws_bytes = _workspace(workspace, rows, V, 1, x.device)
     st = lib.ce_fwd_bwd_fused(x.data_ptr(), _dtype_code(x), rows, V, x.stride(0), lab.data_ptr(),
-                              int(ignore_index), float(temperature), red, g.data_ptr(),
+                              int(ignore_index), float(temperature), red,
+                              _ce_options(label_smoothing, dft), g.data_ptr(),
                               loss.data_ptr(), _ptr(logp), _ptr(lse), n_items.data_ptr(),
                               d.data_ptr(), d.stride(0), ws_ptr, ws_bytes, _ptr(dev_status),
                               _stream_ptr(stream))

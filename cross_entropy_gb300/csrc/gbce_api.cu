@@ -50,7 +50,7 @@ struct WsLayout {
     size_t loss = 0;      // float [rows] per-row losses
     size_t logp = 0;      // float [rows] per-row log p (split path)
     size_t partials = 0;  // float2 [rows * splits]
-    size_t partials_h = 0;  // float [rows * splits]: selective_logsoftmax's entropy moments
+    size_t partials_h = 0;  // float [rows * splits]: entropy moments or sums of logits
     size_t total = 0;
 };
 
@@ -148,6 +148,21 @@ int same_vector_phase(const void *logits, int64_t row_stride, const void *dlogit
     return ((l & 15u) == (d & 15u)) &&
            (((static_cast<uint64_t>(row_stride) * es) & 15u) ==
             ((static_cast<uint64_t>(d_stride) * es) & 15u));
+}
+
+// Host check of gbce_ce_options; fills the CE option fields of p.
+gbce_status apply_ce_options(const gbce_ce_options *opt, RowParams &p)
+{
+    p.ls_eps = 0.0f;
+    p.dft = 0;
+    if (opt == nullptr)
+        return GBCE_OK;
+    const float eps = opt->label_smoothing;
+    if (!(eps >= 0.0f && eps <= 1.0f))  // also rejects NaN
+        return GBCE_EINVAL;
+    p.ls_eps = eps;
+    p.dft = opt->dft != 0 ? 1 : 0;
+    return GBCE_OK;
 }
 
 RowParams base_params(const void *logits, gbce_dtype, int64_t rows, int64_t vocab,
@@ -293,10 +308,14 @@ gbce_status selective_logsoftmax_bwd(const void *logits, gbce_dtype dtype, int64
 
 gbce_status ce_fwd(const void *logits, gbce_dtype dtype, int64_t rows, int64_t vocab,
                    int64_t row_stride, const int64_t *labels, int64_t ignore_index,
-                   float temperature, gbce_reduction reduction, float *loss_out,
-                   float *logp_out, float *lse_out, int64_t *n_items_out, void *workspace,
+                   float temperature, gbce_reduction reduction,
+                   const gbce_ce_options *options, float *loss_out, float *logp_out,
+                   float *lse_out, int64_t *n_items_out, void *workspace,
                    size_t workspace_bytes, int32_t *dev_status, void *stream)
 {
+    RowParams opt_probe{};
+    if (apply_ce_options(options, opt_probe) != GBCE_OK)
+        return GBCE_EINVAL;
     gbce_status st = check_logits(logits, dtype, rows, vocab, row_stride, temperature);
     if (st != GBCE_OK)
         return st;
@@ -322,9 +341,12 @@ gbce_status ce_fwd(const void *logits, gbce_dtype dtype, int64_t rows, int64_t v
         p.logp_out = logp_out;
         p.lse_out = lse_out;
         p.partials = ws_at<float2>(workspace, w.partials);
-        e = launch_rows(p, dtype, gbce::kModeCe, s);
+        p.partials_h = ws_at<float>(workspace, w.partials_h);
+        apply_ce_options(options, p);
+        const int mode = p.ls_eps != 0.0f ? gbce::kModeCeSmooth : gbce::kModeCe;
+        e = launch_rows(p, dtype, mode, s);
         if (e == cudaSuccess && p.splits > 1)
-            e = launch_combine(p, dtype, gbce::kModeCe, s);
+            e = launch_combine(p, dtype, mode, s);
     }
     int64_t *n_ptr = n_items_out;
     if (n_ptr == nullptr && rows > 0)
@@ -339,10 +361,14 @@ gbce_status ce_fwd(const void *logits, gbce_dtype dtype, int64_t rows, int64_t v
 
 gbce_status ce_bwd(const void *logits, gbce_dtype dtype, int64_t rows, int64_t vocab,
                    int64_t row_stride, const int64_t *labels, int64_t ignore_index,
-                   float temperature, gbce_reduction reduction, const float *grad_out,
+                   float temperature, gbce_reduction reduction,
+                   const gbce_ce_options *options, const float *grad_out,
                    const float *saved_logp, const int64_t *n_items, void *dlogits,
                    int64_t dlogits_row_stride, int32_t *dev_status, void *stream)
 {
+    RowParams opt_probe{};
+    if (apply_ce_options(options, opt_probe) != GBCE_OK)
+        return GBCE_EINVAL;
     gbce_status st = check_logits(logits, dtype, rows, vocab, row_stride, temperature);
     if (st != GBCE_OK)
         return st;
@@ -367,17 +393,22 @@ gbce_status ce_bwd(const void *logits, gbce_dtype dtype, int64_t rows, int64_t v
     p.reduction = static_cast<int>(reduction);
     p.n_items = n_items;
     p.saved_logp = saved_logp;
+    apply_ce_options(options, p);
     return cuda_status(launch_rows(p, dtype, gbce::kModeGrad, static_cast<cudaStream_t>(stream)));
 }
 
 gbce_status ce_fwd_bwd_fused(const void *logits, gbce_dtype dtype, int64_t rows,
                              int64_t vocab, int64_t row_stride, const int64_t *labels,
                              int64_t ignore_index, float temperature,
-                             gbce_reduction reduction, const float *grad_out, float *loss_out,
-                             float *logp_out, float *lse_out, int64_t *n_items_out,
-                             void *dlogits, int64_t dlogits_row_stride, void *workspace,
+                             gbce_reduction reduction, const gbce_ce_options *options,
+                             const float *grad_out, float *loss_out, float *logp_out,
+                             float *lse_out, int64_t *n_items_out, void *dlogits,
+                             int64_t dlogits_row_stride, void *workspace,
                              size_t workspace_bytes, int32_t *dev_status, void *stream)
 {
+    RowParams opt_probe{};
+    if (apply_ce_options(options, opt_probe) != GBCE_OK)
+        return GBCE_EINVAL;
     gbce_status st = check_logits(logits, dtype, rows, vocab, row_stride, temperature);
     if (st != GBCE_OK)
         return st;
@@ -425,6 +456,8 @@ gbce_status ce_fwd_bwd_fused(const void *logits, gbce_dtype dtype, int64_t rows,
     p.grad_out = grad_out;
     p.reduction = static_cast<int>(reduction);
     p.n_items = n_ptr;
+    p.partials_h = ws_at<float>(workspace, w.partials_h);
+    apply_ce_options(options, p);
 
     if (e == cudaSuccess && p.splits == 1) {
         e = launch_rows(p, dtype, gbce::kModeFused, s);
@@ -432,9 +465,10 @@ gbce_status ce_fwd_bwd_fused(const void *logits, gbce_dtype dtype, int64_t rows,
         // few rows: split statistics, merge, then a split gradient pass
         float *logp_buf = logp_out != nullptr ? logp_out : ws_at<float>(workspace, w.logp);
         p.logp_out = logp_buf;
-        e = launch_rows(p, dtype, gbce::kModeCe, s);
+        const int mode = p.ls_eps != 0.0f ? gbce::kModeCeSmooth : gbce::kModeCe;
+        e = launch_rows(p, dtype, mode, s);
         if (e == cudaSuccess)
-            e = launch_combine(p, dtype, gbce::kModeCe, s);
+            e = launch_combine(p, dtype, mode, s);
         p.saved_logp = logp_buf;
         if (e == cudaSuccess)
             e = launch_rows(p, dtype, gbce::kModeGrad, s);

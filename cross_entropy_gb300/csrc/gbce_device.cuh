@@ -363,8 +363,9 @@ template <> struct Elem<__nv_bfloat16> {
 //   m = max x_j,   s = sum_j 2^{(x_j - m) c},   c = log2(e) / T,
 // so that s = sum_j exp((x_j - m) / T).  Excluded columns are fed as -inf.
 // The sum is kept in two packed pairs (four independent accumulators).
-template <bool ENT>
+template <bool ENT, bool SUMX = false>
 struct OnlineStats {
+    static constexpr bool kSumx = SUMX;
     float m = kNegInf;
     float nmc = __builtin_huge_valf();  // -m * c, the shift added to every x * c
     float2 sa = make_float2(0.0f, 0.0f);
@@ -372,6 +373,17 @@ struct OnlineStats {
     // ENT: sums of 2^z * z, z = (x - m) c <= 0 (the entropy's first moment)
     float2 ha = make_float2(0.0f, 0.0f);
     float2 hb = make_float2(0.0f, 0.0f);
+    // SUMX: plain sums of the raw logits, every column including targets
+    float2 xa = make_float2(0.0f, 0.0f);
+    float2 xb = make_float2(0.0f, 0.0f);
+
+    // SUMX: add raw logits that the exp sums do not see as themselves
+    // (target columns, masked to -inf there; vectors that are all -inf).
+    __device__ __forceinline__ void sumx_add(float x)
+    {
+        if (SUMX)
+            xa.x += x;
+    }
 
     // New running maximum `vmax` for the values about to be added; returns
     // false when there is nothing to add (all of them are -inf).
@@ -411,6 +423,10 @@ struct OnlineStats {
         const float2 eq = make_float2(ex2(zq.x), ex2(zq.y));
         sa = fadd2(sa, ep);
         sb = fadd2(sb, eq);
+        if (SUMX) {
+            xa = fadd2(xa, p);
+            xb = fadd2(xb, q);
+        }
         if (ENT) {
             ha = ffma2(ep, zp, ha);
             hb = ffma2(eq, zq, hb);
@@ -462,6 +478,11 @@ struct OnlineStats {
     __device__ __forceinline__ float hsum() const
     {
         return __fadd_rn(__fadd_rn(ha.x, ha.y), __fadd_rn(hb.x, hb.y));
+    }
+    // SUMX: the thread's sum of raw logits.
+    __device__ __forceinline__ float xsum() const
+    {
+        return __fadd_rn(__fadd_rn(xa.x, xa.y), __fadd_rn(xb.x, xb.y));
     }
 };
 

@@ -21,11 +21,21 @@ int fused_cluster_size(int64_t vocab)
 }
 
 // Kernel choice for a row launch: a fused cross-entropy call over many rows
-// runs one cluster of CTAs per row (partials swapped through distributed
-// shared memory); everything else runs one CTA per (row, vocab slice).
+// runs the persistent kernel (one CTA per SM walking rows); build options
+// select instead a cluster of CTAs per row (partials swapped through
+// distributed shared memory) or one CTA per row.  Everything else runs one
+// CTA per (row, vocab slice).
 template <typename T>
 cudaError_t launch_rows_dispatch(const RowParams &p, int mode, cudaStream_t stream)
 {
+    if (mode == kModeFused && p.splits == 1 && p.ls_eps != 0.0f) {
+        // label smoothing needs each row's sum of logits, which only the
+        // persistent kernel carries among the fused designs
+        const int sms = device_sm_count();
+        if (sms <= 0)
+            return cudaErrorInvalidDevice;
+        return launch_persistent_fused<T>(p, static_cast<int>(p.rows < sms ? p.rows : sms), stream);
+    }
     if (mode == kModeFused && p.splits == 1) {
 #if defined(GBCE_FUSED_CLUSTER)  // build option: a cluster of CTAs per row
         const int C = fused_cluster_size<T>(p.vocab);

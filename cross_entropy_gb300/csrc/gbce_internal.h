@@ -19,6 +19,7 @@ enum Mode : int {
     kModeLogpGrad = 4,  // selective log-softmax gradient from saved log p (K indices)
     kModeLogpEnt = 5,   // kModeLogp plus the entropy of each row
     kModeLogpEntGrad = 6,  // kModeLogpGrad plus the gradient of the row entropy
+    kModeCeSmooth = 7,     // kModeCe plus the sum of each row's logits (label smoothing)
 };
 
 struct RowParams {
@@ -32,6 +33,8 @@ struct RowParams {
 
     float T;  // temperature
     float c;  // log2(e) / T
+    float ls_eps;  // CE label smoothing (0: none)
+    int dft;       // CE: weight each row's loss and gradient by its detached p_y
     int splits;  // vocab slices per row (1 = the CTA finalizes the row itself)
 
     float *logp_out;   // kModeLogp: [rows, k]; CE modes: [rows] or null
@@ -39,7 +42,8 @@ struct RowParams {
     float *lse_out;    // CE modes: [rows] or null
     float2 *partials;  // [rows * splits] (max, sum) when splits > 1
     float *entropy_out;  // kModeLogpEnt: [rows]
-    float *partials_h;   // kModeLogpEnt, splits > 1: [rows * splits] sum 2^z z
+    float *partials_h;   // splits > 1: [rows * splits] sum 2^z z (kModeLogpEnt) or
+                         // sum of logits (kModeCeSmooth)
 
     void *dlogits;  // kModeGrad / kModeFused
     int64_t d_stride;

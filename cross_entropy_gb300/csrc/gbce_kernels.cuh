@@ -94,6 +94,26 @@ __device__ __forceinline__ bool vector_has_target(const int32_t (&tv)[KMAX], int
     return hit;
 }
 
+// The sweep hands body vector vb of a slice [v0, v1) to consumer thread
+// (vb - v0) % nc, so each thread knows in advance which of its vectors hold a
+// target.  Returns the first such vector of this thread after `after`, or
+// INT32_MAX: the sweep then tests one cursor per vector pair instead of K
+// indices per vector.
+template <int KMAX>
+__device__ __forceinline__ int32_t next_target_vector(const int32_t (&tv)[KMAX], int64_t v0,
+                                                      int64_t v1, int tid, int nc, int32_t after)
+{
+    int32_t next = INT32_MAX;
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k) {
+        const int32_t t = tv[k];
+        const bool mine = t >= v0 && t < v1 && (t - v0) % nc == tid;
+        if (mine && t > after && t < next)
+            next = t;
+    }
+    return next;
+}
+
 // Fold one 16-byte vector of logits, masking target columns (slow path).
 template <typename T, int KMAX, typename S>
 __device__ __forceinline__ void stats_vector(S &st, const uint4 &raw, int32_t col0,
@@ -102,6 +122,10 @@ __device__ __forceinline__ void stats_vector(S &st, const uint4 &raw, int32_t co
     constexpr int VEC = Elem<T>::kVec;
     float f[VEC];
     Elem<T>::unpack(raw, f);
+    if (S::kSumx)
+#pragma unroll
+        for (int e = 0; e < VEC; ++e)
+            st.sumx_add(f[e]);
 #pragma unroll
     for (int e = 0; e < VEC; ++e)
         if (is_target<KMAX>(tg, col0 + e))
@@ -158,36 +182,46 @@ template <> struct FastVec<float> {
     }
 };
 
-// Fold body vectors va (and vb) of a row; col0 = first column of vector 0.
+// Fold body vectors va (and vb, the same thread's next vector) of a row;
+// col0 = first column of vector 0; nt = this thread's next target vector
+// (next_target_vector), advanced past the vectors a hit folds.
 template <typename T, int KMAX, typename S>
-__device__ __forceinline__ void stats_one(S &st, const uint4 &a, int32_t va,
-                                          int32_t col0, const int32_t (&tv)[KMAX],
-                                          const int32_t (&tg)[KMAX], float c, bool check = true)
+__device__ __forceinline__ void stats_one(S &st, const uint4 &a, int32_t va, int32_t col0,
+                                          int32_t &nt, const int32_t (&tg)[KMAX], float c,
+                                          const int32_t (&tv)[KMAX], int64_t v0, int64_t v1,
+                                          int tid, int nc, bool check = true)
 {
     constexpr int VEC = Elem<T>::kVec;
-    if (check && vector_has_target<KMAX>(tv, va)) {
+    if (check && nt == va) {
         stats_vector<T, KMAX>(st, a, col0 + va * VEC, tg, c);
+        nt = next_target_vector<KMAX>(tv, v0, v1, tid, nc, va);
         return;
     }
     if (st.raise_to(FastVec<T>::vmax(a), c))
         FastVec<T>::add(st, a, c);
+    else
+        st.sumx_add(kNegInf);  // the whole vector is -inf
 }
 
 template <typename T, int KMAX, typename S>
-__device__ __forceinline__ void stats_two(S &st, const uint4 &a, const uint4 &b,
-                                          int32_t va, int32_t vb, int32_t col0,
-                                          const int32_t (&tv)[KMAX], const int32_t (&tg)[KMAX],
-                                          float c, bool check = true)
+__device__ __forceinline__ void stats_two(S &st, const uint4 &a, const uint4 &b, int32_t va,
+                                          int32_t vb, int32_t col0, int32_t &nt,
+                                          const int32_t (&tg)[KMAX], float c,
+                                          const int32_t (&tv)[KMAX], int64_t v0, int64_t v1,
+                                          int tid, int nc, bool check = true)
 {
     constexpr int VEC = Elem<T>::kVec;
-    if (check && (vector_has_target<KMAX>(tv, va) || vector_has_target<KMAX>(tv, vb))) {
+    if (check && static_cast<uint32_t>(nt - va) <= static_cast<uint32_t>(vb - va)) {
         stats_vector<T, KMAX>(st, a, col0 + va * VEC, tg, c);
         stats_vector<T, KMAX>(st, b, col0 + vb * VEC, tg, c);
+        nt = next_target_vector<KMAX>(tv, v0, v1, tid, nc, vb);
         return;
     }
     if (st.raise_to(FastVec<T>::vmax(a, b), c)) {
         FastVec<T>::add(st, a, c);
         FastVec<T>::add(st, b, c);
+    } else {
+        st.sumx_add(kNegInf);  // both vectors are -inf
     }
 }
 
@@ -240,6 +274,7 @@ struct GradConsts {
     float kbx;  // kb - x_y * c: the bf16 path's exponent is x * c + kbx
     float gs;   // g / T * 2^-offset
     float dy;   // g / T * expm1(log p), the label column
+    float c0;   // constant added to every non-label element (label smoothing)
     // entropy gradient: an element is 2^z (ea + eb z) instead of gs 2^z
     float ea, eb;
 };
@@ -254,6 +289,39 @@ __device__ __forceinline__ GradConsts grad_consts(float xy, float c, float logp,
     k.kbx = fmaf(-xy, c, k.kb);
     k.gs = offset ? gscale * 0x1p-32f : gscale;
     k.dy = gscale * expm1f(logp);
+    k.c0 = 0.0f;
+    k.ea = k.eb = 0.0f;
+    return k;
+}
+
+// Loss of one kept row of the token CE from log p_y, x_y and (label
+// smoothing) the row's sum of logits: w ((1 - eps)(-log p_y) + eps (lse -
+// mean_j z_j)), lse = x_y / T - log p_y, w = p_y under DFT, else 1.
+__device__ __forceinline__ float ce_row_loss(float lp, float xy, float sumx, float T, float eps,
+                                             int dft, int64_t V)
+{
+    float loss = -lp;
+    if (eps != 0.0f) {
+        const float lse = xy / T - lp;
+        const float mean_z = sumx / (T * static_cast<float>(V));
+        loss = fmaf(1.0f - eps, -lp, eps * (lse - mean_z));
+    }
+    return dft ? expf(lp) * loss : loss;
+}
+
+// Gradient constants of a kept CE row with upstream g: every element is
+// (g w / T)(p_j - eps / V), the label's (g w / T)(expm1(log p_y) + eps - eps / V),
+// w = p_y under DFT (held constant), else 1.
+__device__ __forceinline__ GradConsts grad_consts_ce(float xy, float c, float logp, float g,
+                                                     float T, float eps, int dft, int64_t V)
+{
+    const float gscale = (dft ? g * expf(logp) : g) / T;
+    GradConsts k = grad_consts(xy, c, logp, gscale);
+    if (eps != 0.0f) {
+        const float u = eps / static_cast<float>(V);
+        k.c0 = -gscale * u;
+        k.dy = gscale * (expm1f(logp) + (eps - u));
+    }
     return k;
 }
 
@@ -279,7 +347,7 @@ __device__ __forceinline__ GradConsts grad_consts_ent(float xy, float c, float l
 // dlogits of one element j != y: g/T * exp((x_j - x_y)/T + log p).
 __device__ __forceinline__ float grad_scalar(float x, const GradConsts &k)
 {
-    return k.gs * ex2(fmaf(x + k.nxy, k.c, k.kb));
+    return fmaf(k.gs, ex2(fmaf(x + k.nxy, k.c, k.kb)), k.c0);
 }
 
 // The same element with the entropy term: 2^z (ea + eb z); a -inf logit
@@ -303,7 +371,7 @@ template <> struct GradVec<__nv_bfloat16> {
     __device__ static __forceinline__ uint4 run(const uint4 &raw, int32_t yoff, const GradConsts &k)
     {
         const float2 cc = make_float2(k.c, k.c), kk = make_float2(k.kbx, k.kbx);
-        const float2 gg = make_float2(k.gs, k.gs);
+        const float2 gg = make_float2(k.gs, k.gs), c0 = make_float2(k.c0, k.c0);
         const float2 ea = make_float2(k.ea, k.ea), eb = make_float2(k.eb, k.eb);
         const auto one = [&](uint32_t w) {
             const float2 z = ffma2(bf16x2_to_float2(w), cc, kk);
@@ -313,7 +381,7 @@ template <> struct GradVec<__nv_bfloat16> {
                 const float2 wv = ffma2(make_float2(S::zfin(z.x), S::zfin(z.y)), eb, ea);
                 return float2_to_bf16x2(fmul2(e, wv));
             }
-            return float2_to_bf16x2(fmul2(e, gg));
+            return float2_to_bf16x2(ffma2(e, gg, c0));
         };
         uint4 o = make_uint4(one(raw.x), one(raw.y), one(raw.z), one(raw.w));
         if (static_cast<uint32_t>(yoff) < 8u) {
@@ -340,7 +408,7 @@ template <> struct GradVec<__nv_bfloat16> {
         for (int e = 0; e < 8; ++e) {
             const float z = fmaf(f[e], k.c, k.kbx);
             const float v = ENT ? ex2(z) * fmaf(k.eb, OnlineStats<true>::zfin(z), k.ea)
-                                : k.gs * ex2(z);
+                                : fmaf(k.gs, ex2(z), k.c0);
             d[e] = (e == yoff) ? k.dy : v;
         }
     }
@@ -356,14 +424,15 @@ template <> struct GradVec<float> {
         const float2 p1 = make_float2(__uint_as_float(raw.z), __uint_as_float(raw.w));
         const float2 z0 = ffma2(fadd2(p0, nn), cc, kk), z1 = ffma2(fadd2(p1, nn), cc, kk);
         float2 g0 = gg, g1 = gg;
+        const float2 c0 = make_float2(k.c0, k.c0);
         if (ENT) {
             using S = OnlineStats<true>;
             const float2 ea = make_float2(k.ea, k.ea), eb = make_float2(k.eb, k.eb);
             g0 = ffma2(make_float2(S::zfin(z0.x), S::zfin(z0.y)), eb, ea);
             g1 = ffma2(make_float2(S::zfin(z1.x), S::zfin(z1.y)), eb, ea);
         }
-        const float2 d0 = fmul2(make_float2(ex2(z0.x), ex2(z0.y)), g0);
-        const float2 d1 = fmul2(make_float2(ex2(z1.x), ex2(z1.y)), g1);
+        const float2 d0 = ffma2(make_float2(ex2(z0.x), ex2(z0.y)), g0, c0);
+        const float2 d1 = ffma2(make_float2(ex2(z1.x), ex2(z1.y)), g1, c0);
         uint4 o = make_uint4(__float_as_uint(d0.x), __float_as_uint(d0.y), __float_as_uint(d1.x),
                              __float_as_uint(d1.y));
         if (static_cast<uint32_t>(yoff) < 4u) {
@@ -478,7 +547,7 @@ __device__ void fill_row_slice(T *drow, int64_t V, int split, int splits, float 
 }
 
 template <typename T, int MODE, int KMAX>
-__global__ void __launch_bounds__(kRowThreads, (MODE == kModeLogpEnt && KMAX <= 4) ? 3 : 2)
+__global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4) ? 3 : 2)
     row_kernel(const RowParams p)
 {
     using E = Elem<T>;
@@ -495,6 +564,7 @@ __global__ void __launch_bounds__(kRowThreads, (MODE == kModeLogpEnt && KMAX <= 
     constexpr bool kEnt = (MODE == kModeLogpEnt);                  // + row entropy
     constexpr bool kLogpFwd = (MODE == kModeLogp || kEnt);         // log p of K indices
     constexpr bool kGather = (kLogpFwd || kSelGrad);  // K indices
+    constexpr bool kSumx = (MODE == kModeCeSmooth);  // + the row's sum of logits
     constexpr int kPasses = (MODE == kModeFused) ? 2 : 1;
 
     extern __shared__ __align__(128) uint8_t dyn_smem[];
@@ -698,24 +768,22 @@ __global__ void __launch_bounds__(kRowThreads, (MODE == kModeLogpEnt && KMAX <= 
     float logp = 0.0f, xy = 0.0f;
 
     if (kStats) {
-        OnlineStats<kEnt> st;
-        // Every body vector vb this thread sweeps has (vb - v0) % NC == tid,
-        // so a warp none of whose threads holds a target vector skips the
-        // per-vector target test (warp-uniform branch).
-        bool mine = false;
-#pragma unroll
-        for (int k = 0; k < KMAX; ++k)
-            mine |= tv[k] >= v0 && tv[k] < v1 && (tv[k] - v0) % NC == tid;
-        const bool wcheck = __any_sync(0xffffffffu, mine);
+        OnlineStats<kEnt, kSumx> st;
+        // each thread's next target vector; a warp none of whose threads
+        // holds one skips even the cursor test (warp-uniform branch)
+        int32_t nt = next_target_vector<KMAX>(tv, v0, v1, tid, NC, -1);
+        const bool wcheck = __any_sync(0xffffffffu, nt != INT32_MAX);
         if (split == 0)
             for (int64_t e = tid; e < g.head; e += NC) {
                 const float x = E::load(row + e);
                 st.add1(is_target<KMAX>(tg, static_cast<int32_t>(e)) ? kNegInf : x, c);
+                st.sumx_add(x);
             }
         if (split == p.splits - 1)
             for (int64_t e = g.tail0 + tid; e < V; e += NC) {
                 const float x = E::load(row + e);
                 st.add1(is_target<KMAX>(tg, static_cast<int32_t>(e)) ? kNegInf : x, c);
+                st.sumx_add(x);
             }
         for (int64_t i = 0; i < nchunks; ++i, ++seq) {
             const int slot = static_cast<int>(seq % kStages);
@@ -736,13 +804,16 @@ __global__ void __launch_bounds__(kRowThreads, (MODE == kModeLogpEnt && KMAX <= 
 #pragma unroll
                     for (int u = 0; u + 1 < PER_THREAD; u += 2)
                         stats_two<T, KMAX>(st, raw[u], raw[u + 1], vb0 + tid + u * NC,
-                                        vb0 + tid + (u + 1) * NC, col0, tv, tg, c, wcheck);
+                                           vb0 + tid + (u + 1) * NC, col0, nt, tg, c, tv, v0, v1,
+                                           tid, NC, wcheck);
                     if (PER_THREAD & 1)
-                        stats_one<T, KMAX>(st, raw[PER_THREAD - 1], vb0 + tid + (PER_THREAD - 1) * NC,
-                                        col0, tv, tg, c, wcheck);
+                        stats_one<T, KMAX>(st, raw[PER_THREAD - 1],
+                                           vb0 + tid + (PER_THREAD - 1) * NC, col0, nt, tg, c, tv,
+                                           v0, v1, tid, NC, wcheck);
                 } else {
                     for (int v = tid; v < nv; v += NC)
-                        stats_one<T, KMAX>(st, chunk[v], vb0 + v, col0, tv, tg, c, wcheck);
+                        stats_one<T, KMAX>(st, chunk[v], vb0 + v, col0, nt, tg, c, tv, v0, v1,
+                                           tid, NC, wcheck);
                 }
             }
             __syncwarp();
@@ -750,8 +821,9 @@ __global__ void __launch_bounds__(kRowThreads, (MODE == kModeLogpEnt && KMAX <= 
                 mbar_arrive(&empty_bar[slot]);
         }
 
-        // CTA-wide merge of the per-thread (max, sum[, h]) in a fixed order
-        float m = st.m, s = st.sum(), h = kEnt ? st.hsum() : 0.0f;
+        // CTA-wide merge of the per-thread (max, sum[, h]) in a fixed order;
+        // h is the entropy moment (kEnt) or the sum of logits (kSumx)
+        float m = st.m, s = st.sum(), h = kEnt ? st.hsum() : (kSumx ? st.xsum() : 0.0f);
         if (kEnt && alive && isnan(h) && !isnan(s))
             h = rescan_entropy_moment<T, KMAX>(row, g, V, v0, v1, split == 0,
                                                split == p.splits - 1, tg, c, st.nmc, tid, NC);
@@ -764,6 +836,8 @@ __global__ void __launch_bounds__(kRowThreads, (MODE == kModeLogpEnt && KMAX <= 
                     merge_max_sum_h(m, s, h, m2, s2, __shfl_xor_sync(0xffffffffu, h, off), c);
                 else
                     merge_max_sum(m, s, m2, s2, c);
+                if (kSumx)
+                    h = __fadd_rn(h, __shfl_xor_sync(0xffffffffu, h, off));
             }
         };
         merge_lanes();
@@ -788,7 +862,7 @@ __global__ void __launch_bounds__(kRowThreads, (MODE == kModeLogpEnt && KMAX <= 
                         st_async_pair(map_to_rank(slot, t), m, s, map_to_rank(bar, t));
                 } else if (p.splits > 1) {
                     p.partials[unit] = make_float2(m, s);
-                    if (kEnt)
+                    if (kEnt || kSumx)
                         p.partials_h[unit] = h;
                 } else if (kLogpFwd) {
                     bc_m = m;
@@ -797,7 +871,7 @@ __global__ void __launch_bounds__(kRowThreads, (MODE == kModeLogpEnt && KMAX <= 
                 } else {
                     xy = s_xt[0];
                     logp = finalize_logp(m, s, xy, p.T);
-                    p.loss_rows[r] = -logp;
+                    p.loss_rows[r] = ce_row_loss(logp, xy, h, p.T, p.ls_eps, p.dft, V);
                     if (p.logp_out)
                         p.logp_out[r] = logp;
                     if (p.lse_out)
@@ -841,7 +915,8 @@ __global__ void __launch_bounds__(kRowThreads, (MODE == kModeLogpEnt && KMAX <= 
                     const float lp = finalize_logp(M, Ssum, x_y, p.T);
                     bc_logp = lp;
                     if (split == 0) {
-                        p.loss_rows[r] = -lp;
+                        // (smoothing never takes this path: no sum of logits)
+                        p.loss_rows[r] = ce_row_loss(lp, x_y, 0.0f, p.T, 0.0f, p.dft, V);
                         if (p.logp_out)
                             p.logp_out[r] = lp;
                         if (p.lse_out)
@@ -927,7 +1002,8 @@ __global__ void __launch_bounds__(kRowThreads, (MODE == kModeLogpEnt && KMAX <= 
             logp = p.saved_logp[r];
             xy = E::load(row + y);
         }
-        const GradConsts gk = grad_consts(xy, c, logp, upstream_grad(p, r) / p.T);
+        const GradConsts gk =
+            grad_consts_ce(xy, c, logp, upstream_grad(p, r), p.T, p.ls_eps, p.dft, V);
         if (split == 0)
             for (int64_t e = tid; e < g.head; e += NC)
                 E::store(drow + e, e == y ? gk.dy : grad_scalar(E::load(row + e), gk));
@@ -991,6 +1067,7 @@ __global__ void combine_kernel(const RowParams p)
     const float nan = __int_as_float(0x7fc00000);
     constexpr bool kEnt = (MODE == kModeLogpEnt);
     constexpr bool kLogpFwd = (MODE == kModeLogp || kEnt);
+    constexpr bool kSumx = (MODE == kModeCeSmooth);
 
     if (kLogpFwd) {
         if (p.row_mask != nullptr && p.row_mask[r] == 0) {
@@ -1022,6 +1099,8 @@ __global__ void combine_kernel(const RowParams p)
             merge_max_sum_h(m, s, h, part.x, part.y, p.partials_h[r * p.splits + i], c);
         else
             merge_max_sum(m, s, part.x, part.y, c);
+        if (kSumx)
+            h += p.partials_h[r * p.splits + i];
     }
 
     if (kLogpFwd) {
@@ -1048,7 +1127,7 @@ __global__ void combine_kernel(const RowParams p)
     } else {
         const float xy = E::load(row + p.targets[r]);
         const float logp = finalize_logp(m, s, xy, p.T);
-        p.loss_rows[r] = -logp;
+        p.loss_rows[r] = ce_row_loss(logp, xy, h, p.T, p.ls_eps, p.dft, V);
         if (p.logp_out)
             p.logp_out[r] = logp;
         if (p.lse_out)
@@ -1145,6 +1224,8 @@ cudaError_t launch_rows_per_unit(const RowParams &p, int mode, cudaStream_t stre
         return launch_row_kernel<T, kModeLogpEnt, GBCE_MAX_K>(p, stream);
     case kModeCe:
         return launch_row_kernel<T, kModeCe, 1>(p, stream);
+    case kModeCeSmooth:
+        return launch_row_kernel<T, kModeCeSmooth, 1>(p, stream);
     case kModeGrad:
         return launch_row_kernel<T, kModeGrad, 1>(p, stream);
     case kModeFused:
@@ -1177,6 +1258,8 @@ cudaError_t launch_combine(const RowParams &p, int mode, cudaStream_t stream)
         combine_kernel<T, kModeLogp><<<blocks, threads, 0, stream>>>(p);
     else if (mode == kModeLogpEnt)
         combine_kernel<T, kModeLogpEnt><<<blocks, threads, 0, stream>>>(p);
+    else if (mode == kModeCeSmooth)
+        combine_kernel<T, kModeCeSmooth><<<blocks, threads, 0, stream>>>(p);
     else
         combine_kernel<T, kModeCe><<<blocks, threads, 0, stream>>>(p);
     note_launches(1);

@@ -73,7 +73,7 @@ extern "C" gbce_status ce_fwd_bwd_fused_noalloc(
             return GBCE_ECUDA;
     }
     return ce_fwd_bwd_fused(logits, dtype, rows, vocab, row_stride, labels, ignore_index,
-                            temperature, reduction, grad_out, loss_out, logp_out, lse_out,
+                            temperature, reduction, nullptr, grad_out, loss_out, logp_out, lse_out,
                             n_items_out, dlogits, dlogits_row_stride, scratch,
                             GBCE_NOALLOC_SCRATCH_BYTES, dev_status, stream);
 }

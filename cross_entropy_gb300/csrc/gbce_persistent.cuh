@@ -48,7 +48,8 @@ constexpr int kPersistStages = GBCE_PERSIST_STAGES;  // 192 KB ring: one CTA per
 constexpr int kPersistThreads = (kPersistWarps + 1) * 32;
 constexpr int kPersistDynSmem = kPersistStages * kPersistChunk + kRingAlign;
 
-template <typename T>
+// SMOOTH: label smoothing, which also needs each row's sum of logits.
+template <typename T, bool SMOOTH>
 __global__ void __launch_bounds__(kPersistThreads, 1) persistent_fused_kernel(const RowParams p)
 {
     using E = Elem<T>;
@@ -67,7 +68,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persistent_fused_kernel(co
         (reinterpret_cast<uintptr_t>(dyn_smem) + (kRingAlign - 1)) & ~uintptr_t(kRingAlign - 1));
     __shared__ uint64_t full_bar[S];
     __shared__ uint64_t empty_bar[S];
-    __shared__ float red_m[NCW], red_s[NCW];
+    __shared__ float red_m[NCW], red_s[NCW], red_x[NCW];
     __shared__ float bc_logp;
 
     const int tid = threadIdx.x;
@@ -172,14 +173,22 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persistent_fused_kernel(co
         // the label logit and the upstream gradient are read now (every thread,
         // one cached address each), so their latency hides under pass 1
         const float xy = E::load(row + y);
-        const float gscale = upstream_grad(p, r) / p.T;
+        const float gup = upstream_grad(p, r);
 
         // pass 1: statistics
-        OnlineMaxSum st;
-        for (int64_t e = tid; e < g.head; e += NC)
-            st.add1(e == y ? kNegInf : E::load(row + e), c);
-        for (int64_t e = g.tail0 + tid; e < V; e += NC)
-            st.add1(e == y ? kNegInf : E::load(row + e), c);
+        OnlineStats<false, SMOOTH> st;
+        int32_t nt = next_target_vector<1>(tv, 0, g.nvec, tid, NC, -1);
+        const bool wcheck = __any_sync(0xffffffffu, nt != INT32_MAX);
+        for (int64_t e = tid; e < g.head; e += NC) {
+            const float x = E::load(row + e);
+            st.add1(e == y ? kNegInf : x, c);
+            st.sumx_add(x);
+        }
+        for (int64_t e = g.tail0 + tid; e < V; e += NC) {
+            const float x = E::load(row + e);
+            st.add1(e == y ? kNegInf : x, c);
+            st.sumx_add(x);
+        }
         for (int64_t i = 0; i < nchunks; ++i) {
             if (alive && !mbar_wait(&full_bar[slot], lap & 1)) {
                 alive = false;
@@ -197,10 +206,12 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persistent_fused_kernel(co
 #pragma unroll
                     for (int u = 0; u < PER_THREAD; u += 2)
                         stats_two<T, 1>(st, raw[u], raw[u + 1], vb0 + tid + u * NC,
-                                        vb0 + tid + (u + 1) * NC, col0, tv, tg, c);
+                                        vb0 + tid + (u + 1) * NC, col0, nt, tg, c, tv, 0, g.nvec,
+                                        tid, NC, wcheck);
                 } else {
                     for (int v = tid; v < nv; v += NC)
-                        stats_one<T, 1>(st, chunk[v], vb0 + v, col0, tv, tg, c);
+                        stats_one<T, 1>(st, chunk[v], vb0 + v, col0, nt, tg, c, tv, 0, g.nvec,
+                                        tid, NC, wcheck);
                 }
             }
             __syncwarp();
@@ -213,31 +224,37 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persistent_fused_kernel(co
         }
 
         // merge: warp shuffles, then warp 0 over the warps, then finalize
-        float m = st.m, s = st.sum();
+        float m = st.m, s = st.sum(), sx = SMOOTH ? st.xsum() : 0.0f;
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
             const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
             const float s2 = __shfl_xor_sync(0xffffffffu, s, off);
             merge_max_sum(m, s, m2, s2, c);
+            if (SMOOTH)
+                sx = __fadd_rn(sx, __shfl_xor_sync(0xffffffffu, sx, off));
         }
         if (lane == 0) {
             red_m[warp] = m;
             red_s[warp] = s;
+            red_x[warp] = sx;
         }
         named_sync(1, NC);
         if (warp == 0) {
             m = lane < NCW ? red_m[lane] : kNegInf;
             s = lane < NCW ? red_s[lane] : 0.0f;
+            sx = lane < NCW ? red_x[lane] : 0.0f;
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) {
                 const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
                 const float s2 = __shfl_xor_sync(0xffffffffu, s, off);
                 merge_max_sum(m, s, m2, s2, c);
+                if (SMOOTH)
+                    sx = __fadd_rn(sx, __shfl_xor_sync(0xffffffffu, sx, off));
             }
             if (lane == 0) {
                 const float lp = finalize_logp(m, s, xy, p.T);
                 bc_logp = lp;
-                p.loss_rows[r] = -lp;
+                p.loss_rows[r] = ce_row_loss(lp, xy, sx, p.T, p.ls_eps, p.dft, V);
                 if (p.logp_out)
                     p.logp_out[r] = lp;
                 if (p.lse_out)
@@ -245,7 +262,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persistent_fused_kernel(co
             }
         }
         named_sync(1, NC);
-        const GradConsts gk = grad_consts(xy, c, bc_logp, gscale);
+        const GradConsts gk = grad_consts_ce(xy, c, bc_logp, gup, p.T, p.ls_eps, p.dft, V);
 
         // pass 2: gradient
         for (int64_t e = tid; e < g.head; e += NC)
@@ -317,17 +334,24 @@ inline int device_sm_count()
     return n;
 }
 
-template <typename T>
-cudaError_t launch_persistent_fused(const RowParams &p, int grid, cudaStream_t stream)
+template <typename T, bool SMOOTH>
+cudaError_t launch_persistent_fused_as(const RowParams &p, int grid, cudaStream_t stream)
 {
     static std::atomic<uint64_t> attr_done{0};
-    auto kernel = persistent_fused_kernel<T>;
+    auto kernel = persistent_fused_kernel<T, SMOOTH>;
     cudaError_t err = ensure_smem_attr(kernel, kPersistDynSmem, attr_done);
     if (err != cudaSuccess)
         return err;
     kernel<<<grid, kPersistThreads, kPersistDynSmem, stream>>>(p);
     note_launches(1);
     return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_persistent_fused(const RowParams &p, int grid, cudaStream_t stream)
+{
+    return p.ls_eps != 0.0f ? launch_persistent_fused_as<T, true>(p, grid, stream)
+                            : launch_persistent_fused_as<T, false>(p, grid, stream);
 }
 
 }  // namespace gbce

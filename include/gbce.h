@@ -165,6 +165,30 @@ gbce_status selective_logsoftmax_bwd(const void *logits, gbce_dtype dtype, int64
                                      int32_t *dev_status, void *stream);
 
 /*
+ * Options of the token cross-entropy calls (ce_fwd, ce_bwd,
+ * ce_fwd_bwd_fused).  A NULL pointer means all defaults (plain CE).
+ *
+ *   label_smoothing  eps in [0, 1]: the target distribution puts 1 - eps on
+ *                    the label and eps / vocab on every class, so a kept
+ *                    row's loss is (1 - eps)(-log p_y) + eps * mean_j(-log p_j)
+ *                    and its gradient (g/T)(p_j - (1 - eps)[j == y] - eps/vocab),
+ *                    the label column in the expm1(log p_y) form ("Fix
+ *                    softmax collapse ...", the unsloth-zoo #2080 commit's
+ *                    "Fix", backward bullet).  A row with a -inf logit has
+ *                    an infinite smoothed loss, as the definition gives.
+ *   dft              nonzero: weight each kept row's loss and gradient by its
+ *                    own p_y, held constant in the backward (the DFT loss
+ *                    -p_y log p_y of ms-swift PR #10353, "PR information").
+ *                    Combines with label_smoothing (the weight multiplies
+ *                    the smoothed row loss).
+ * ce_bwd must be given the same options as the ce_fwd whose log p it takes.
+ */
+typedef struct gbce_ce_options {
+    float label_smoothing;
+    int32_t dft;
+} gbce_ce_options;
+
+/*
  * Token cross-entropy forward.  For rows whose label is not ignore_index:
  * loss_r = -log p_{labels[r]} at temperature T; ignored rows are skipped
  * before any read of their logits and get loss 0.
@@ -174,6 +198,7 @@ gbce_status selective_logsoftmax_bwd(const void *logits, gbce_dtype dtype, int64
  * before any vocabulary work from ms-swift PR #10353, "PR information".
  *
  *   labels      [rows] int64
+ *   options     gbce_ce_options or NULL (plain CE)
  *   reduction   GBCE_NONE: loss_out[rows] = loss_r;
  *               GBCE_SUM:  loss_out[0] = sum_r loss_r;
  *               GBCE_MEAN: loss_out[0] = sum_r loss_r / n_items, 0 when
@@ -189,7 +214,8 @@ gbce_status selective_logsoftmax_bwd(const void *logits, gbce_dtype dtype, int64
  */
 gbce_status ce_fwd(const void *logits, gbce_dtype dtype, int64_t rows, int64_t vocab,
                    int64_t row_stride, const int64_t *labels, int64_t ignore_index,
-                   float temperature, gbce_reduction reduction, float *loss_out,
+                   float temperature, gbce_reduction reduction,
+                   const gbce_ce_options *options, float *loss_out,
                    float *logp_out, float *lse_out, int64_t *n_items_out, void *workspace,
                    size_t workspace_bytes, int32_t *dev_status, void *stream);
 
@@ -198,7 +224,9 @@ gbce_status ce_fwd(const void *logits, gbce_dtype dtype, int64_t rows, int64_t v
  *   dlogits[r, j] = (g_r / T) * exp(z_j - z_y + log p_y)   for j != y,
  *   dlogits[r, y] = (g_r / T) * expm1(log p_y),
  * i.e. g_r * (softmax - onehot) / T with the target term in the form that
- * does not round to zero; ignored rows get a zero row.  g_r = grad_out[r]
+ * does not round to zero (with options: the smoothed and DFT-weighted
+ * gradient described at gbce_ce_options); ignored rows get a zero row.
+ * g_r = grad_out[r]
  * (NONE), grad_out[0] (SUM) or grad_out[0] / n_items (MEAN, 0 when
  * n_items == 0).
  *
@@ -218,7 +246,8 @@ gbce_status ce_fwd(const void *logits, gbce_dtype dtype, int64_t rows, int64_t v
  */
 gbce_status ce_bwd(const void *logits, gbce_dtype dtype, int64_t rows, int64_t vocab,
                    int64_t row_stride, const int64_t *labels, int64_t ignore_index,
-                   float temperature, gbce_reduction reduction, const float *grad_out,
+                   float temperature, gbce_reduction reduction,
+                   const gbce_ce_options *options, const float *grad_out,
                    const float *saved_logp, const int64_t *n_items, void *dlogits,
                    int64_t dlogits_row_stride, int32_t *dev_status, void *stream);
 
@@ -238,7 +267,8 @@ gbce_status ce_bwd(const void *logits, gbce_dtype dtype, int64_t rows, int64_t v
 gbce_status ce_fwd_bwd_fused(const void *logits, gbce_dtype dtype, int64_t rows,
                              int64_t vocab, int64_t row_stride, const int64_t *labels,
                              int64_t ignore_index, float temperature,
-                             gbce_reduction reduction, const float *grad_out, float *loss_out,
+                             gbce_reduction reduction, const gbce_ce_options *options,
+                             const float *grad_out, float *loss_out,
                              float *logp_out, float *lse_out, int64_t *n_items_out,
                              void *dlogits, int64_t dlogits_row_stride, void *workspace,
                              size_t workspace_bytes, int32_t *dev_status, void *stream);

@@ -107,11 +107,19 @@ def test_selective_logsoftmax_host_checks(lib, kw, code):
 
 def _bwd(lib, **kw):
     a = dict(logits=FAKE, dtype=0, rows=4, vocab=100, stride=100, labels=FAKE, ignore=-100,
-             T=1.0, red=2, grad=FAKE, logp=FAKE, n=FAKE, d=FAKE * 16, dstride=100)
+             T=1.0, red=2, opt=None, grad=FAKE, logp=FAKE, n=FAKE, d=FAKE * 16, dstride=100)
     a.update(kw)
     return lib.ce_bwd(a["logits"], a["dtype"], a["rows"], a["vocab"], a["stride"], a["labels"],
-                      a["ignore"], a["T"], a["red"], a["grad"], a["logp"], a["n"], a["d"],
-                      a["dstride"], None, None)
+                      a["ignore"], a["T"], a["red"], a["opt"], a["grad"], a["logp"], a["n"],
+                      a["d"], a["dstride"], None, None)
+
+
+def _opts(eps, dft=0):
+    import ctypes
+
+    import cross_entropy_gb300 as gbce
+
+    return ctypes.byref(gbce.CeOptions(eps, dft))
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -128,17 +136,27 @@ def test_ce_bwd_host_checks(lib, kw, code):
     assert _bwd(lib, **kw) == code
 
 
+@pytest.mark.parametrize("eps", [-0.1, 1.5, float("nan"), float("inf")])
+def test_ce_options_out_of_range_are_refused(lib, eps):
+    assert _bwd(lib, opt=_opts(eps)) == 1
+    args = [FAKE, 1, 4, 100, 100, FAKE, -100, 1.0, 2, _opts(eps, 1), FAKE, FAKE, None, None,
+            None, FAKE * 16, 100, FAKE * 64, 1 << 20, None, None]
+    assert lib.ce_fwd_bwd_fused(*args) == 1
+    assert lib.ce_fwd(FAKE, 1, 4, 100, 100, FAKE, -100, 1.0, 2, _opts(eps), FAKE, None, None,
+                      None, FAKE * 64, 1 << 20, None, None) == 1
+
+
 def test_fused_host_checks(lib):
-    args = [FAKE, 1, 4, 100, 100, FAKE, -100, 1.0, 2, FAKE, FAKE, None, None, None,
+    args = [FAKE, 1, 4, 100, 100, FAKE, -100, 1.0, 2, None, FAKE, FAKE, None, None, None,
             FAKE * 16, 100, FAKE * 64, 1 << 20, None, None]
     a = list(args)
-    a[14] = FAKE          # dlogits == logits
+    a[15] = FAKE          # dlogits == logits
     assert lib.ce_fwd_bwd_fused(*a) == 1
     a = list(args)
-    a[9] = None           # no upstream gradient
+    a[10] = None          # no upstream gradient
     assert lib.ce_fwd_bwd_fused(*a) == 1
     a = list(args)
-    a[17] = 8             # workspace too small
+    a[18] = 8             # workspace too small
     assert lib.ce_fwd_bwd_fused(*a) == 4
 
 

@@ -1,0 +1,123 @@
+"""GPU parity of the token CE with label smoothing and DFT weighting
+(ce_fwd, ce_bwd, ce_fwd_bwd_fused) against the fp64 oracle, through the C ABI."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from helpers import (assert_grad_rows_close, assert_logp_close, assert_loss_close,
+                     assert_zero_sum_rows, to_f64)
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    import cross_entropy_gb300 as gbce
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    import __graft_entry__
+
+    __graft_entry__.build()
+    gbce.load_library()
+
+
+def check_rows_loss(got_rows, ref_rows, dtype, what):
+    # row losses are >= 0: compare them as (negated) log-probs, same bound
+    assert_logp_close(-to_f64(got_rows), -np.asarray(ref_rows), dtype, what)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("eps,dft", [(0.1, False), (0.0, True), (0.2, True)])
+@pytest.mark.parametrize("reduction", ["mean", "none"])
+def test_fwd_bwd_and_fused_match_oracle(dtype, eps, dft, reduction):
+    w = workloads.collapse_stress(dtype=dtype, rows=640, V=32003, seed=90)
+    x, lab = w.logits.to(DEV), w.labels.to(DEV)
+    T = 0.9
+    g = (torch.randn(640, generator=torch.Generator().manual_seed(1)) if reduction == "none"
+         else torch.tensor([0.75]))
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    kw = dict(temperature=T, reduction=reduction, label_smoothing=eps, dft=dft)
+    fwd = gbce.ce_fwd(x, lab, dev_status=status, **kw)
+    d_sep = gbce.ce_bwd(x, lab, g.to(DEV), fwd.logp, fwd.n_items, dev_status=status, **kw)
+    fused = gbce.ce_fwd_bwd_fused(x, lab, g.to(DEV), dev_status=status, **kw)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref = oracle.cross_entropy(workloads.to_numpy_f64(w.logits), w.labels.numpy(),
+                               temperature=T, reduction=reduction, grad_out=g.double().numpy(),
+                               label_smoothing=eps, dft=dft)
+    assert int(fwd.n_items.item()) == ref["n_items"] == int(fused.n_items.item())
+    if reduction == "none":
+        check_rows_loss(fwd.loss, ref["loss_rows"], dtype, "ce_fwd rows")
+        check_rows_loss(fused.loss, ref["loss_rows"], dtype, "fused rows")
+    else:
+        assert_loss_close(float(fwd.loss.item()), ref["loss"], "ce_fwd")
+        assert_loss_close(float(fused.loss.item()), ref["loss"], "fused")
+    sel = np.arange(0, 640, 4)
+    st = torch.as_tensor(sel, device=DEV)
+    for d, name in ((d_sep, "ce_bwd"), (fused.dlogits, "fused")):
+        got = to_f64(d[st])
+        assert_grad_rows_close(got, ref["dlogits"][sel], dtype, name)
+        assert_zero_sum_rows(got, dtype)
+    # confident rows keep a nonzero label gradient (negative for g > 0, eps small)
+    pk = w.peaked_rows.numpy()
+    pk = pk[w.labels.numpy()[pk] >= 0][:20]
+    col = w.labels.numpy()[pk]
+    gl = to_f64(fused.dlogits[torch.as_tensor(pk, device=DEV)])[np.arange(len(pk)), col]
+    want = ref["dlogits"][pk, col]
+    assert np.all(np.sign(gl) == np.sign(want)) and np.all(gl != 0.0)
+
+
+@pytest.mark.parametrize("rows", [2, 100])
+def test_split_path_with_smoothing(rows):
+    V = 152064
+    w = workloads.collapse_stress(dtype=torch.bfloat16, rows=rows, V=V, seed=rows + 3)
+    x, lab = w.logits.to(DEV), w.labels.to(DEV)
+    fused = gbce.ce_fwd_bwd_fused(x, lab, torch.ones(1, device=DEV), temperature=0.8,
+                                  reduction="sum", label_smoothing=0.05, dft=True)
+    fwd = gbce.ce_fwd(x, lab, temperature=0.8, reduction="none", label_smoothing=0.05, dft=True)
+    torch.cuda.synchronize()
+    ref = oracle.cross_entropy(workloads.to_numpy_f64(w.logits), w.labels.numpy(),
+                               temperature=0.8, reduction="sum", label_smoothing=0.05, dft=True)
+    assert_loss_close(float(fused.loss.item()), ref["loss"], "fused sum")
+    check_rows_loss(fwd.loss, ref["loss_rows"], torch.bfloat16, "ce_fwd rows")
+    sel = np.arange(0, rows, max(1, rows // 20))
+    assert_grad_rows_close(to_f64(fused.dlogits[torch.as_tensor(sel, device=DEV)]),
+                           ref["dlogits"][sel], torch.bfloat16)
+
+
+def test_minus_infinity_logit_gives_infinite_smoothed_loss():
+    x = torch.randn((2, 4099), device=DEV)
+    x[0, 17] = float("-inf")
+    lab = torch.tensor([3, 5], device=DEV)
+    fwd = gbce.ce_fwd(x, lab, reduction="none", label_smoothing=0.1)
+    plain = gbce.ce_fwd(x, lab, reduction="none")
+    torch.cuda.synchronize()
+    assert torch.isinf(fwd.loss[0]) and torch.isfinite(fwd.loss[1])
+    assert torch.isfinite(plain.loss).all()
+
+
+def test_full_size_grpo_smoothed_dft_fused():
+    w = workloads.grpo_bf16(device=DEV)
+    out = gbce.ce_fwd_bwd_fused(w.logits, w.labels, torch.ones(1, device=DEV), temperature=0.9,
+                                reduction="mean", label_smoothing=0.1, dft=True)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(9)
+    sel = np.sort(np.concatenate([rng.choice(w.rows, 16, replace=False),
+                                  w.peaked_rows.cpu().numpy()[:8]]))
+    st = torch.as_tensor(sel, device=DEV)
+    ref = oracle.cross_entropy(workloads.to_numpy_f64(w.logits[st]), w.labels[st].cpu().numpy(),
+                               temperature=0.9, reduction="none", label_smoothing=0.1, dft=True,
+                               grad_out=np.full(len(sel), 1.0 / w.rows))
+    assert_grad_rows_close(to_f64(out.dlogits[st]), ref["dlogits"], torch.bfloat16)
+    # the mean over all rows: each sampled row's loss also checked through ce_fwd
+    rows_loss = gbce.ce_fwd(w.logits, w.labels, temperature=0.9, reduction="none",
+                            label_smoothing=0.1, dft=True).loss
+    check_rows_loss(rows_loss[st], ref["loss_rows"], torch.bfloat16, "rows")
+    assert_loss_close(float(out.loss.item()), float(rows_loss.double().mean().item()), "mean")
