@@ -49,13 +49,15 @@ FALLBACK_HBM_GBS = 6800.0
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "fused_ce_bf16_8192x152064.txt")
 
 
-def algorithmic_bytes(rows=None, vocab=VOCAB, k=K, esize=2):
+def algorithmic_bytes(rows=None, vocab=VOCAB, k=K, esize=2, entropy=False):
     """Bytes each op must move at least once: per row, the logits read once per
     op, the dlogits row written once, the K indices, the label and the K fp32
-    log-probs."""
+    log-probs (and the fp32 row entropy with --entropy)."""
     rows = ROWS if rows is None else rows
     logits = rows * vocab * esize
     logp = logits + rows * k * 8 + rows * k * 4          # logits + index + fp32 out
+    if entropy:
+        logp += rows * 4
     ce = 2 * logits + rows * 8                           # logits in, dlogits out, labels
     return {"selective_logsoftmax": logp, "ce_fwd_bwd_fused": ce, "step": logp + ce}
 
@@ -258,10 +260,11 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
-def workload_config(world):
+def workload_config(world, entropy=False):
+    ops = ["selective_logsoftmax" + ("+entropy" if entropy else ""), "ce_fwd_bwd_fused"]
     return {"workload": f"grpo_bf16_{ROWS}x{VOCAB}_k{K}", "rows": ROWS, "vocab": VOCAB,
             "k": K, "temperature": TEMPERATURE, "logits_dtype": "bf16",
-            "ops": ["selective_logsoftmax", "ce_fwd_bwd_fused"], "reduction": "mean",
+            "ops": ops, "reduction": "mean",
             "peaked_rows": "5% with target +8..12", "l2": "inputs larger than L2 (2.49 GB "
             "logits per op), no flush", "parallelism": f"replicas x{world}"}
 
@@ -281,6 +284,7 @@ def run_gbce(args):
     x, idx, lab = w.logits, w.index, w.labels
     grad = torch.ones(1, device=dev)
     logp_out = torch.empty((ROWS, K), dtype=torch.float32, device=dev)
+    ent_out = torch.empty(ROWS, dtype=torch.float32, device=dev) if args.entropy else None
     dlogits = torch.empty_like(x)
     ws = gbce.new_workspace(ROWS, VOCAB, K, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -289,8 +293,8 @@ def run_gbce(args):
     def step(evs=None):
         if evs is not None:
             evs[0].record(stream)
-        gbce.selective_logsoftmax(x, idx, TEMPERATURE, out=logp_out, workspace=ws,
-                                  dev_status=status)
+        gbce.selective_logsoftmax(x, idx, TEMPERATURE, out=logp_out, entropy_out=ent_out,
+                                  workspace=ws, dev_status=status)
         if evs is not None:
             evs[1].record(stream)
         out = gbce.ce_fwd_bwd_fused(x, lab, grad, temperature=TEMPERATURE, reduction="mean",
@@ -326,7 +330,7 @@ def run_gbce(args):
     ce_ms = [e[1].elapsed_time(e[2]) for e in evs]
     total_ms = max_over_ranks(total_ms, world, dev)
 
-    nbytes = algorithmic_bytes()
+    nbytes = algorithmic_bytes(entropy=args.entropy)
     ms_per_step = total_ms / args.steps
     value = aggregate_gbs(world, nbytes["step"], args.steps, total_ms)
     peak, peak_kind = measured_peak()
@@ -353,7 +357,7 @@ def run_gbce(args):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": workload_config(world),
+        "config": workload_config(world, args.entropy),
         "frac_of_peak": value / world / peak,
         "ops": {
             "selective_logsoftmax": {"ms": lp_avg,
@@ -589,6 +593,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the per-workload, per-op timings")
+    ap.add_argument("--entropy", action="store_true",
+                    help="the step's selective log-softmax also writes each row's entropy")
     ap.add_argument("--rows", type=int, default=ROWS,
                     help="rows of the workload (a smaller case for profiling captures)")
     args = ap.parse_args()
