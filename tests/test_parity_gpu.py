@@ -429,3 +429,34 @@ def test_persistent_stats_many_rows_k16_and_masks():
                                          0.8, mask.numpy()[sel])
     assert_logp_close(to_f64(got)[sel], ref, torch.bfloat16)
     assert np.all(to_f64(got)[mask.numpy() == 0] == 0.0)
+
+
+# ---------------------------------------------------------- size extremes
+
+def test_huge_vocab_few_rows_split_path():
+    # 2 rows of 2^25 + 3 columns: the split path at 64 slices of ~524K
+    # columns, an odd tail, one confident row
+    V = (1 << 25) + 3
+    w = workloads.collapse_stress(dtype=torch.bfloat16, rows=2, V=V, seed=101)
+    w.labels[:] = torch.tensor([7, V - 1])
+    workloads.set_target_margin(w.logits, torch.tensor([1]), torch.tensor([V - 1]),
+                                torch.tensor([30.0]))
+    w.index = w.labels[:, None].clone()
+    w.row_mask = None
+    res, ref, sel = run_all(w, temperature=0.9, reduction="sum", grad_out=torch.ones(1))
+    check_all(w, res, ref, sel, reduction="sum", T=0.9)
+
+
+def test_million_column_rows_persistent_path():
+    # 520 rows of 1,000,003 fp32 columns (4 MB a row): the persistent fused
+    # kernel's rows no longer all fit L2 at once; K = 16 gathered indices
+    V, rows = 1_000_003, 520
+    g = torch.Generator().manual_seed(5)
+    w = workloads.collapse_stress(dtype=torch.float32, rows=rows, V=V, seed=55)
+    idx = torch.randint(0, V, (rows, 16), generator=g)
+    idx[:, 0] = torch.where(w.labels >= 0, w.labels, idx[:, 0])
+    w.index = idx
+    sel = np.concatenate([np.arange(0, rows, 53), w.peaked_rows.numpy()[:6]])
+    res, ref, sel = run_all(w, temperature=1.0, reduction="mean", grad_out=torch.ones(1),
+                            rows_sel=np.sort(sel))
+    check_all(w, res, ref, sel, reduction="mean", check_scalar_vs_oracle=False, T=1.0)
