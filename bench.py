@@ -516,6 +516,10 @@ def measure_configs(gbce, dev, stream, peak):
     w = workloads.grpo_bf16(device=dev, rows=64, seed=7)
     ce_ops("split_bf16_64x152064", w, TEMPERATURE, "mean", torch.ones(1, device=dev))
     logp_op("split_bf16_64x152064", w, TEMPERATURE, entropy=True)
+    # sparse supervision at full size: 25% of the rows carry a label
+    w = workloads.sft_sparse_bf16(device=dev)
+    ce_ops(w.name, w, 1.0, "mean", torch.ones(1, device=dev))
+    del w
     w = workloads.grpo_bf16(device=dev, rows=ROWS)
     ce_ops(f"grpo_bf16_{ROWS}x{VOCAB}", w, TEMPERATURE, "mean", torch.ones(1, device=dev),
            options=True)

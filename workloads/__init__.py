@@ -105,12 +105,10 @@ def ce_small_fp32(device="cpu", seed: int = 0) -> Workload:
                     margins=margins)
 
 
-def ce_sparse_bf16(device="cpu", seed: int = 0) -> Workload:
-    """1922 x 4096 bf16 ~N(0,2^2): two 961-row samples, four 32-row supervised spans each."""
-    samples, per_sample, spans, span_len, V = 2, 961, 4, 32, 4096
+def _span_labels(samples, per_sample, spans, span_len, V, g, device):
+    """Labels that are IGNORE_INDEX except in `spans` non-overlapping runs of
+    `span_len` rows per sample, at seeded offsets."""
     rows = samples * per_sample
-    g = _gen(seed, device)
-    logits = _normal(rows, V, 2.0, torch.bfloat16, g, device)
     labels = torch.full((rows,), IGNORE_INDEX, dtype=torch.int64, device=device)
     free = per_sample - spans * span_len
     for s in range(samples):
@@ -121,6 +119,34 @@ def ce_sparse_bf16(device="cpu", seed: int = 0) -> Workload:
             start = s * per_sample + int(offs[k]) + k * span_len
             labels[start:start + span_len] = torch.randint(
                 0, V, (span_len,), generator=g, device=device)
+    return labels
+
+
+def sft_sparse_bf16(device="cpu", seed: int = 0, samples: int = 8, per_sample: int = 1024,
+                    spans: int = 4, span_len: int = 64, V: int = 152064) -> Workload:
+    """8192 x 152064 bf16 ~N(0,2.5^2): 8 samples of 1024 rows, four 64-row
+    supervised spans each (2048 supervised rows, 25%), mean over them.
+
+    The sparse-supervision structure of ms-swift PR #10353 at the packed
+    workload's size and vocabulary.
+    """
+    rows = samples * per_sample
+    g = _gen(seed, device)
+    logits = _normal(rows, V, 2.5, torch.bfloat16, g, device)
+    labels = _span_labels(samples, per_sample, spans, span_len, V, g, device)
+    mask = (labels != IGNORE_INDEX).to(torch.uint8)
+    return Workload(f"sft_sparse_bf16_{rows}x{V}", logits, labels, _index_from_labels(labels),
+                    mask, 1.0, "mean", torch.ones(1, device=device),
+                    meta={"supervised": samples * spans * span_len})
+
+
+def ce_sparse_bf16(device="cpu", seed: int = 0) -> Workload:
+    """1922 x 4096 bf16 ~N(0,2^2): two 961-row samples, four 32-row supervised spans each."""
+    samples, per_sample, spans, span_len, V = 2, 961, 4, 32, 4096
+    rows = samples * per_sample
+    g = _gen(seed, device)
+    logits = _normal(rows, V, 2.0, torch.bfloat16, g, device)
+    labels = _span_labels(samples, per_sample, spans, span_len, V, g, device)
     n_sup = samples * spans * span_len
     grad = torch.full((rows,), 1.0 / n_sup, device=device)
     mask = (labels != IGNORE_INDEX).to(torch.uint8)
