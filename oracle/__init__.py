@@ -86,7 +86,7 @@ def _load():
         lib.oracle_cross_entropy.restype = i64
         lib.oracle_cross_entropy.argtypes = [
             dp, i64, i64, i64, ip, i64, ctypes.c_double, ctypes.c_int, ctypes.c_double,
-            ctypes.c_int, ctypes.c_void_p, dp, dp, dp, ip, ctypes.c_void_p, i64]
+            ctypes.c_int, ctypes.c_double, ctypes.c_void_p, dp, dp, dp, ip, ctypes.c_void_p, i64]
         lib.oracle_selective_logsoftmax_backward.restype = i64
         lib.oracle_selective_logsoftmax_backward.argtypes = [
             dp, i64, i64, i64, ip, i64, ctypes.c_double, ctypes.c_void_p, dp, ctypes.c_void_p,
@@ -204,11 +204,12 @@ def entropy(x, ref, temperature: float = 1.0, live=None):
 
 def cross_entropy(x, labels, ignore_index: int = -100, temperature: float = 1.0,
                   reduction: str = "mean", grad_out=None, want_grad: bool = True,
-                  label_smoothing: float = 0.0, dft: bool = False):
+                  label_smoothing: float = 0.0, dft: bool = False, softcap: float = 0.0):
     """Token CE forward (and backward when ``want_grad``).
 
     ``label_smoothing`` eps puts 1 - eps on the label and eps / V on every
-    class; ``dft`` weights each row's loss and gradient by its detached p_y.
+    class; ``dft`` weights each row's loss and gradient by its detached p_y;
+    ``softcap`` > 0 caps every logit as softcap * tanh(x / softcap) first.
 
     ``grad_out`` is the upstream gradient: [rows] for reduction 'none', a
     scalar otherwise (default 1).  Returns a dict with ``logp`` [rows],
@@ -237,7 +238,7 @@ def cross_entropy(x, labels, ignore_index: int = -100, temperature: float = 1.0,
     bad = lib.oracle_cross_entropy(
         _ptr(x, ctypes.c_double), rows, V, x.strides[0] // 8, _ptr(lab, ctypes.c_int64),
         int(ignore_index), exact_temperature(temperature), red, float(label_smoothing),
-        int(bool(dft)), g_ptr,
+        int(bool(dft)), float(softcap), g_ptr,
         _ptr(logp, ctypes.c_double), _ptr(loss_rows, ctypes.c_double),
         _ptr(loss, ctypes.c_double), _ptr(n_items, ctypes.c_int64),
         dx.ctypes.data if dx is not None else None, V)

@@ -67,6 +67,7 @@
 #include <math.h>
 #include <stddef.h>
 #include <stdint.h>
+#include <stdlib.h>
 #ifdef _OPENMP
 #include <omp.h>
 #endif
@@ -251,12 +252,11 @@ int64_t oracle_selective_logsoftmax(const double *x, int64_t rows, int64_t V, in
  *   dx         [rows, ldx] out or NULL
  * Returns the number of rows whose label is out of range.
  */
-int64_t oracle_cross_entropy(const double *x, int64_t rows, int64_t V, int64_t ld,
-                             const int64_t *labels, int64_t ignore_index, double T,
-                             int reduction, double eps, int dft, const double *grad_out,
-                             double *logp_y,
-                             double *loss_rows, double *loss, int64_t *n_items,
-                             double *dx, int64_t ldx)
+static int64_t ce_core(const double *x, int64_t rows, int64_t V, int64_t ld,
+                       const int64_t *labels, int64_t ignore_index, double T, int reduction,
+                       double eps, int dft, const double *grad_out, double *logp_y,
+                       double *loss_rows, double *loss, int64_t *n_items, double *dx,
+                       int64_t ldx)
 {
     int64_t count = 0;
     for (int64_t r = 0; r < rows; ++r)
@@ -338,6 +338,42 @@ int64_t oracle_cross_entropy(const double *x, int64_t rows, int64_t V, int64_t l
                 dr[j] = scale * (exp(xr[j] / T - zy + lp) - u);
         }
     }
+    return bad;
+}
+
+/*
+ * The exported cross-entropy: ce_core above, with optional logit soft-capping.
+ * softcap > 0 replaces every logit x by cap * tanh(x / cap) before the
+ * temperature and the softmax (a per-element transform of the logits), and
+ * the gradient with respect to x takes the chain factor 1 - tanh^2(x / cap).
+ */
+int64_t oracle_cross_entropy(const double *x, int64_t rows, int64_t V, int64_t ld,
+                             const int64_t *labels, int64_t ignore_index, double T,
+                             int reduction, double eps, int dft, double softcap,
+                             const double *grad_out, double *logp_y, double *loss_rows,
+                             double *loss, int64_t *n_items, double *dx, int64_t ldx)
+{
+    if (!(softcap > 0.0))
+        return ce_core(x, rows, V, ld, labels, ignore_index, T, reduction, eps, dft, grad_out,
+                       logp_y, loss_rows, loss, n_items, dx, ldx);
+    double *z = (double *)malloc((size_t)rows * (size_t)V * sizeof(double));
+    if (z == NULL)
+        return -1;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t j = 0; j < V; ++j)
+            z[r * V + j] = softcap * tanh(x[r * ld + j] / softcap);
+    const int64_t bad = ce_core(z, rows, V, V, labels, ignore_index, T, reduction, eps, dft,
+                                grad_out, logp_y, loss_rows, loss, n_items, dx, ldx);
+    if (dx != NULL) {
+#pragma omp parallel for schedule(static)
+        for (int64_t r = 0; r < rows; ++r)
+            for (int64_t j = 0; j < V; ++j) {
+                const double t = tanh(x[r * ld + j] / softcap);
+                dx[r * ldx + j] *= 1.0 - t * t;
+            }
+    }
+    free(z);
     return bad;
 }
 

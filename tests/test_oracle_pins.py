@@ -685,3 +685,58 @@ def test_smoothed_gradient_finite_difference_and_dft_relation():
     np.testing.assert_allclose(d["loss_rows"], py * out["loss_rows"], rtol=1e-14)
     for r in range(rows):
         assert abs(math.fsum(d["dlogits"][r])) <= 1e-14 * math.fsum(np.abs(d["dlogits"][r]))
+
+
+# -------------------------------------------------- logit soft-capping on the CE
+
+@pytest.mark.parametrize("eps", [0.0, 0.1])
+def test_softcapped_ce_matches_torch_fp64(eps):
+    rng = np.random.default_rng(33)
+    x = rng.normal(scale=20.0, size=(24, 200))      # many logits past the cap's knee
+    y = rng.integers(0, 200, 24)
+    y[5] = -100
+    cap, T = 30.0, 0.8
+    out = oracle.cross_entropy(x, y, temperature=T, reduction="sum", label_smoothing=eps,
+                               softcap=cap, grad_out=[0.5])
+    xt = torch.tensor(x, requires_grad=True)
+    Te = oracle.exact_temperature(T)
+    z = cap * torch.tanh(xt / cap)
+    ref = torch.nn.functional.cross_entropy(z / Te, torch.tensor(y), ignore_index=-100,
+                                            reduction="sum", label_smoothing=eps)
+    (0.5 * ref).backward()
+    assert out["loss"] == pytest.approx(float(ref.detach()), rel=1e-13)
+    np.testing.assert_allclose(out["dlogits"], xt.grad.numpy(), rtol=1e-10, atol=1e-16)
+
+
+def test_softcap_limits_closed_form_and_finite_differences():
+    rng = np.random.default_rng(4)
+    x = rng.normal(scale=3.0, size=(5, 50))
+    y = rng.integers(0, 50, 5)
+    plain = oracle.cross_entropy(x, y, reduction="none")
+    huge = oracle.cross_entropy(x, y, reduction="none", softcap=1e7)
+    np.testing.assert_allclose(huge["loss_rows"], plain["loss_rows"], rtol=1e-10)
+    np.testing.assert_allclose(huge["dlogits"], plain["dlogits"], rtol=1e-8, atol=1e-18)
+    # V = 2: log p_y = -softplus((z_o - z_y) / T), z = cap tanh(x / cap)
+    x2 = np.array([[41.0, -7.5]])
+    cap, T = 25.0, 0.9
+    zo, zy = cap * math.tanh(-7.5 / cap), cap * math.tanh(41.0 / cap)
+    Te = oracle.exact_temperature(T)
+    a = (zo - zy) / Te
+    want = max(a, 0.0) + math.log1p(math.exp(-abs(a)))
+    got = oracle.cross_entropy(x2, [0], temperature=T, reduction="none", softcap=cap)
+    assert got["loss_rows"][0] == pytest.approx(want, rel=1e-13)
+    # finite differences through the cap
+    x3 = rng.normal(scale=15.0, size=(2, 9))
+    y3 = np.array([4, 0])
+    d = oracle.cross_entropy(x3, y3, reduction="sum", softcap=cap)["dlogits"]
+    h = 1e-6
+    for r in range(2):
+        for j in range(9):
+            xp, xm = x3.copy(), x3.copy()
+            xp[r, j] += h
+            xm[r, j] -= h
+            fp = oracle.cross_entropy(xp, y3, reduction="sum", softcap=cap, want_grad=False)
+            fm = oracle.cross_entropy(xm, y3, reduction="sum", softcap=cap, want_grad=False)
+            # abs: one ulp of a loss of order 10 over 2h is about 1e-9
+            assert d[r, j] == pytest.approx((fp["loss"] - fm["loss"]) / (2 * h),
+                                            rel=2e-6, abs=5e-9)
