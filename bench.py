@@ -470,6 +470,14 @@ def measure_configs(gbce, dev, stream, peak):
                 stream, 10, fl))
             record(f"{tag}/ce_fwd+smooth+dft", w, "ce_fwd", time_op(
                 lambda: gbce.ce_fwd(x, lab, workspace=ws, **kw), stream, 10, fl))
+            # logit soft-capping at 30: a tanh per element (and the fused
+            # call as two passes)
+            kc = dict(temperature=T, reduction=red, softcap=30.0)
+            record(f"{tag}/ce_fwd_bwd_fused+softcap30", w, "fused", time_op(
+                lambda: gbce.ce_fwd_bwd_fused(x, lab, g, dlogits=d, workspace=ws, **kc),
+                stream, 10, fl))
+            record(f"{tag}/ce_fwd+softcap30", w, "ce_fwd", time_op(
+                lambda: gbce.ce_fwd(x, lab, workspace=ws, **kc), stream, 10, fl))
 
     def logp_op(tag, w, T, backward=False, k=None, entropy=False):
         x, idx = w.logits, (w.index if k is None else w.index[:, :k].contiguous())

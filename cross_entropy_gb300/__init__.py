@@ -243,14 +243,15 @@ def selective_logsoftmax_bwd(logits: torch.Tensor, index, grad_logp, saved_logp,
 class CeOptions(ctypes.Structure):
     """gbce_ce_options: label smoothing eps and the DFT row weight."""
 
-    _fields_ = [("label_smoothing", ctypes.c_float), ("dft", ctypes.c_int32)]
+    _fields_ = [("label_smoothing", ctypes.c_float), ("dft", ctypes.c_int32),
+                ("softcap", ctypes.c_float)]
 
 
-def _ce_options(label_smoothing: float, dft: bool):
+def _ce_options(label_smoothing: float, dft: bool, softcap: float = 0.0):
     """A CeOptions to pass by reference, or None for plain CE."""
-    if label_smoothing == 0.0 and not dft:
+    if label_smoothing == 0.0 and not dft and softcap == 0.0:
         return None
-    return ctypes.byref(CeOptions(float(label_smoothing), 1 if dft else 0))
+    return ctypes.byref(CeOptions(float(label_smoothing), 1 if dft else 0, float(softcap)))
 
 
 class CeForward(NamedTuple):
@@ -270,12 +271,14 @@ class CeFused(NamedTuple):
 
 def ce_fwd(logits: torch.Tensor, labels, ignore_index: int = -100, temperature: float = 1.0,
            reduction: str = "mean", *, label_smoothing: float = 0.0, dft: bool = False,
+           softcap: float = 0.0,
            want_lse: bool = False, workspace: Optional[torch.Tensor] = None,
            dev_status: Optional[torch.Tensor] = None, stream=None) -> CeForward:
     """Cross-entropy forward; returns loss, saved log p (for ce_bwd), lse, n_items.
 
-    ``label_smoothing`` eps and ``dft`` (rows weighted by their detached p_y)
-    change the loss; ce_bwd must be given the same two.
+    ``label_smoothing`` eps, ``dft`` (rows weighted by their detached p_y) and
+    ``softcap`` (logits capped as softcap * tanh(x / softcap)) change the loss;
+    ce_bwd must be given the same three.
     """
     lib = load_library()
     x = _rows_view(logits)
@@ -289,7 +292,7 @@ def ce_fwd(logits: torch.Tensor, labels, ignore_index: int = -100, temperature: 
     ws, ws_ptr, ws_bytes = _workspace(workspace, rows, V, 1, x.device)
     st = lib.ce_fwd(x.data_ptr(), _dtype_code(x), rows, V, x.stride(0), lab.data_ptr(),
                     int(ignore_index), float(temperature), red,
-                    _ce_options(label_smoothing, dft), loss.data_ptr(), logp.data_ptr(),
+                    _ce_options(label_smoothing, dft, softcap), loss.data_ptr(), logp.data_ptr(),
                     _ptr(lse), n_items.data_ptr(), ws_ptr, ws_bytes, _ptr(dev_status),
                     _stream_ptr(stream))
     _check(st, "ce_fwd")
@@ -298,7 +301,7 @@ def ce_fwd(logits: torch.Tensor, labels, ignore_index: int = -100, temperature: 
 
 def ce_bwd(logits: torch.Tensor, labels, grad_out, saved_logp: torch.Tensor, n_items=None,
            ignore_index: int = -100, temperature: float = 1.0, reduction: str = "mean", *,
-           label_smoothing: float = 0.0, dft: bool = False,
+           label_smoothing: float = 0.0, dft: bool = False, softcap: float = 0.0,
            dlogits: Optional[torch.Tensor] = None, dev_status: Optional[torch.Tensor] = None,
            stream=None) -> torch.Tensor:
     """dlogits = g * (softmax - onehot) / T from ce_fwd's saved log p (smoothed /
@@ -318,7 +321,7 @@ def ce_bwd(logits: torch.Tensor, labels, grad_out, saved_logp: torch.Tensor, n_i
     lp = saved_logp.reshape(rows).contiguous()
     st = lib.ce_bwd(x.data_ptr(), _dtype_code(x), rows, V, x.stride(0), lab.data_ptr(),
                     int(ignore_index), float(temperature), red,
-                    _ce_options(label_smoothing, dft), g.data_ptr(), lp.data_ptr(),
+                    _ce_options(label_smoothing, dft, softcap), g.data_ptr(), lp.data_ptr(),
                     _ptr(n), d.data_ptr(), d.stride(0), _ptr(dev_status), _stream_ptr(stream))
     _check(st, "ce_bwd")
     return dlogits
@@ -326,7 +329,7 @@ def ce_bwd(logits: torch.Tensor, labels, grad_out, saved_logp: torch.Tensor, n_i
 
 def ce_fwd_bwd_fused(logits: torch.Tensor, labels, grad_out=None, ignore_index: int = -100,
                      temperature: float = 1.0, reduction: str = "mean", *,
-                     label_smoothing: float = 0.0, dft: bool = False,
+                     label_smoothing: float = 0.0, dft: bool = False, softcap: float = 0.0,
                      dlogits: Optional[torch.Tensor] = None, want_logp: bool = True,
                      want_lse: bool = False, workspace: Optional[torch.Tensor] = None,
                      dev_status: Optional[torch.Tensor] = None, stream=None) -> CeFused:
@@ -351,7 +354,7 @@ def ce_fwd_bwd_fused(logits: torch.Tensor, labels, grad_out=None, ignore_index: 
     ws, ws_ptr, ws_bytes = _workspace(workspace, rows, V, 1, x.device)
     st = lib.ce_fwd_bwd_fused(x.data_ptr(), _dtype_code(x), rows, V, x.stride(0), lab.data_ptr(),
                               int(ignore_index), float(temperature), red,
-                              _ce_options(label_smoothing, dft), g.data_ptr(),
+                              _ce_options(label_smoothing, dft, softcap), g.data_ptr(),
                               loss.data_ptr(), _ptr(logp), _ptr(lse), n_items.data_ptr(),
                               d.data_ptr(), d.stride(0), ws_ptr, ws_bytes, _ptr(dev_status),
                               _stream_ptr(stream))

@@ -155,14 +155,34 @@ gbce_status apply_ce_options(const gbce_ce_options *opt, RowParams &p)
 {
     p.ls_eps = 0.0f;
     p.dft = 0;
+    p.softcap = 0.0f;
+    p.inv_cap = 0.0f;
     if (opt == nullptr)
         return GBCE_OK;
     const float eps = opt->label_smoothing;
     if (!(eps >= 0.0f && eps <= 1.0f))  // also rejects NaN
         return GBCE_EINVAL;
+    const float cap = opt->softcap;
+    if (!(cap >= 0.0f && std::isfinite(cap)))
+        return GBCE_EINVAL;
     p.ls_eps = eps;
     p.dft = opt->dft != 0 ? 1 : 0;
+    p.softcap = cap;
+    p.inv_cap = cap > 0.0f ? 1.0f / cap : 0.0f;
     return GBCE_OK;
+}
+
+// Statistics and gradient modes of a CE call with these options.
+int ce_stats_mode(const RowParams &p)
+{
+    if (p.softcap > 0.0f)
+        return gbce::kModeCeCap;
+    return p.ls_eps != 0.0f ? gbce::kModeCeSmooth : gbce::kModeCe;
+}
+
+int ce_grad_mode(const RowParams &p)
+{
+    return p.softcap > 0.0f ? gbce::kModeGradCap : gbce::kModeGrad;
 }
 
 RowParams base_params(const void *logits, gbce_dtype, int64_t rows, int64_t vocab,
@@ -343,7 +363,7 @@ gbce_status ce_fwd(const void *logits, gbce_dtype dtype, int64_t rows, int64_t v
         p.partials = ws_at<float2>(workspace, w.partials);
         p.partials_h = ws_at<float>(workspace, w.partials_h);
         apply_ce_options(options, p);
-        const int mode = p.ls_eps != 0.0f ? gbce::kModeCeSmooth : gbce::kModeCe;
+        const int mode = ce_stats_mode(p);
         e = launch_rows(p, dtype, mode, s);
         if (e == cudaSuccess && p.splits > 1)
             e = launch_combine(p, dtype, mode, s);
@@ -394,7 +414,7 @@ gbce_status ce_bwd(const void *logits, gbce_dtype dtype, int64_t rows, int64_t v
     p.n_items = n_items;
     p.saved_logp = saved_logp;
     apply_ce_options(options, p);
-    return cuda_status(launch_rows(p, dtype, gbce::kModeGrad, static_cast<cudaStream_t>(stream)));
+    return cuda_status(launch_rows(p, dtype, ce_grad_mode(p), static_cast<cudaStream_t>(stream)));
 }
 
 gbce_status ce_fwd_bwd_fused(const void *logits, gbce_dtype dtype, int64_t rows,
@@ -459,19 +479,21 @@ gbce_status ce_fwd_bwd_fused(const void *logits, gbce_dtype dtype, int64_t rows,
     p.partials_h = ws_at<float>(workspace, w.partials_h);
     apply_ce_options(options, p);
 
-    if (e == cudaSuccess && p.splits == 1) {
+    if (e == cudaSuccess && p.splits == 1 && p.softcap == 0.0f) {
         e = launch_rows(p, dtype, gbce::kModeFused, s);
     } else if (e == cudaSuccess) {
-        // few rows: split statistics, merge, then a split gradient pass
+        // few rows, or soft-capped logits (where tanh per element, not the
+        // second read, sets the pace): statistics (split and merged when
+        // the rows are few), then a gradient pass
         float *logp_buf = logp_out != nullptr ? logp_out : ws_at<float>(workspace, w.logp);
         p.logp_out = logp_buf;
-        const int mode = p.ls_eps != 0.0f ? gbce::kModeCeSmooth : gbce::kModeCe;
+        const int mode = ce_stats_mode(p);
         e = launch_rows(p, dtype, mode, s);
-        if (e == cudaSuccess)
+        if (e == cudaSuccess && p.splits > 1)
             e = launch_combine(p, dtype, mode, s);
         p.saved_logp = logp_buf;
         if (e == cudaSuccess)
-            e = launch_rows(p, dtype, gbce::kModeGrad, s);
+            e = launch_rows(p, dtype, ce_grad_mode(p), s);
     }
     if (e == cudaSuccess && reduction != GBCE_NONE)
         e = gbce::launch_reduce_loss(loss_rows, labels, rows, ignore_index,

@@ -20,6 +20,8 @@ enum Mode : int {
     kModeLogpEnt = 5,   // kModeLogp plus the entropy of each row
     kModeLogpEntGrad = 6,  // kModeLogpGrad plus the gradient of the row entropy
     kModeCeSmooth = 7,     // kModeCe plus the sum of each row's logits (label smoothing)
+    kModeCeCap = 8,        // kModeCeSmooth on soft-capped logits cap * tanh(x / cap)
+    kModeGradCap = 9,      // kModeGrad on soft-capped logits, with the chain factor
 };
 
 struct RowParams {
@@ -35,6 +37,7 @@ struct RowParams {
     float c;  // log2(e) / T
     float ls_eps;  // CE label smoothing (0: none)
     int dft;       // CE: weight each row's loss and gradient by its detached p_y
+    float softcap, inv_cap;  // CE logit soft-capping (kModeCeCap / kModeGradCap)
     int splits;  // vocab slices per row (1 = the CTA finalizes the row itself)
 
     float *logp_out;   // kModeLogp: [rows, k]; CE modes: [rows] or null

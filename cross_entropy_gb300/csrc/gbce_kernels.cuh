@@ -559,12 +559,16 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
     static_assert(CV % NC == 0, "chunk must split evenly over consumer threads");
     constexpr bool kSelGrad = (MODE == kModeLogpGrad || MODE == kModeLogpEntGrad);
     constexpr bool kEntGrad = (MODE == kModeLogpEntGrad);
-    constexpr bool kStats = (MODE != kModeGrad && !kSelGrad);
-    constexpr bool kGrad = (MODE == kModeGrad || MODE == kModeFused || kSelGrad);
+    constexpr bool kCeGrad = (MODE == kModeGrad || MODE == kModeGradCap);  // ce_bwd
+    constexpr bool kCap = (MODE == kModeCeCap || MODE == kModeGradCap);    // soft-capped
+    constexpr bool kStats = (!kCeGrad && !kSelGrad);
+    constexpr bool kGrad = (kCeGrad || MODE == kModeFused || kSelGrad);
     constexpr bool kEnt = (MODE == kModeLogpEnt);                  // + row entropy
     constexpr bool kLogpFwd = (MODE == kModeLogp || kEnt);         // log p of K indices
     constexpr bool kGather = (kLogpFwd || kSelGrad);  // K indices
-    constexpr bool kSumx = (MODE == kModeCeSmooth);  // + the row's sum of logits
+    constexpr bool kSumx = (MODE == kModeCeSmooth || MODE == kModeCeCap);  // + sum of logits
+    // a logit as the softmax sees it (soft-capped in the capped modes)
+    const auto capped = [&](float x) { return kCap ? p.softcap * tanh_acc(x * p.inv_cap) : x; };
     constexpr int kPasses = (MODE == kModeFused) ? 2 : 1;
 
     extern __shared__ __align__(128) uint8_t dyn_smem[];
@@ -637,9 +641,9 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
                 report(p.dev_status, GBCE_DEV_BAD_INDEX);
             fill_row_slice<T>(drow, V, split, p.splits, fill);
         } else {
-            if (tid == 0 && (direct || MODE == kModeGrad) && split == 0 && state == 2)
+            if (tid == 0 && (direct || kCeGrad) && split == 0 && state == 2)
                 report(p.dev_status, GBCE_DEV_BAD_LABEL);
-            if (tid == 0 && direct && split == 0 && MODE != kModeGrad) {
+            if (tid == 0 && direct && split == 0 && !kCeGrad) {
                 p.loss_rows[r] = fill;
                 if (p.logp_out)
                     p.logp_out[r] = fill;
@@ -721,7 +725,7 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
         for (int k = 0; k < KMAX; ++k)
             if (tid == k) {
                 s_tg[k] = tg[k];
-                s_xt[k] = tg[k] >= 0 ? E::load(row + tg[k]) : 0.0f;
+                s_xt[k] = tg[k] >= 0 ? capped(E::load(row + tg[k])) : 0.0f;
             }
     }
     __syncthreads();
@@ -775,13 +779,13 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
         const bool wcheck = __any_sync(0xffffffffu, nt != INT32_MAX);
         if (split == 0)
             for (int64_t e = tid; e < g.head; e += NC) {
-                const float x = E::load(row + e);
+                const float x = capped(E::load(row + e));
                 st.add1(is_target<KMAX>(tg, static_cast<int32_t>(e)) ? kNegInf : x, c);
                 st.sumx_add(x);
             }
         if (split == p.splits - 1)
             for (int64_t e = g.tail0 + tid; e < V; e += NC) {
-                const float x = E::load(row + e);
+                const float x = capped(E::load(row + e));
                 st.add1(is_target<KMAX>(tg, static_cast<int32_t>(e)) ? kNegInf : x, c);
                 st.sumx_add(x);
             }
@@ -796,7 +800,24 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
                 const int64_t nv = (v1 - v0 - i * CV) < CV ? (v1 - v0 - i * CV) : CV;
                 const int32_t vb0 = static_cast<int32_t>(v0 + i * CV);  // body vector of chunk[0]
                 const int32_t col0 = static_cast<int32_t>(g.head);
-                if (nv == CV) {
+                if (kCap) {
+                    // soft-capped: every element through tanh, unpacked
+                    for (int v = tid; v < nv; v += NC) {
+                        float f[VEC];
+                        E::unpack(chunk[v], f);
+                        const int32_t colv = col0 + (vb0 + v) * VEC;
+                        float vm = kNegInf;
+#pragma unroll
+                        for (int e = 0; e < VEC; ++e) {
+                            f[e] = capped(f[e]);
+                            st.sumx_add(f[e]);
+                            if (is_target<KMAX>(tg, colv + e))
+                                f[e] = kNegInf;
+                            vm = fmaxf(vm, f[e]);
+                        }
+                        st.template add<VEC>(f, vm, c);
+                    }
+                } else if (nv == CV) {
                     uint4 raw[PER_THREAD];
 #pragma unroll
                     for (int u = 0; u < PER_THREAD; ++u)
@@ -998,12 +1019,62 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
                 mbar_arrive(&empty_bar[slot]);
         }
     } else if (kGrad) {
-        if (MODE == kModeGrad) {
+        if (kCeGrad) {
             logp = p.saved_logp[r];
-            xy = E::load(row + y);
+            xy = capped(E::load(row + y));
         }
         const GradConsts gk =
             grad_consts_ce(xy, c, logp, upstream_grad(p, r), p.T, p.ls_eps, p.dft, V);
+        if (kCap) {
+            // soft-capped: element j is (its plain value on z = cap tanh(x / cap))
+            // times the chain factor 1 - tanh^2(x / cap)
+            const auto elem = [&](float x, bool is_y) {
+                const float t = tanh_acc(x * p.inv_cap);
+                const float chain = fmaf(-t, t, 1.0f);
+                const float z = p.softcap * t;
+                const float d = is_y ? gk.dy : fmaf(gk.gs, ex2(fmaf(z + gk.nxy, gk.c, gk.kb)), gk.c0);
+                return d * chain;
+            };
+            if (split == 0)
+                for (int64_t e = tid; e < g.head; e += NC)
+                    E::store(drow + e, elem(E::load(row + e), e == y));
+            if (split == p.splits - 1)
+                for (int64_t e = g.tail0 + tid; e < V; e += NC)
+                    E::store(drow + e, elem(E::load(row + e), e == y));
+            for (int64_t i = 0; i < nchunks; ++i, ++seq) {
+                const int slot = static_cast<int>(seq % kStages);
+                if (alive &&
+                    !mbar_wait(&full_bar[slot], static_cast<uint32_t>((seq / kStages) & 1))) {
+                    alive = false;
+                    report(p.dev_status, GBCE_DEV_TIMEOUT);
+                }
+                if (alive) {
+                    const uint4 *chunk = reinterpret_cast<const uint4 *>(ring + slot * kChunkBytes);
+                    const int64_t nv = (v1 - v0 - i * CV) < CV ? (v1 - v0 - i * CV) : CV;
+                    const int64_t vbase = v0 + i * CV;
+                    const int64_t col_base = g.head + vbase * VEC;
+                    T *dbase = drow + col_base;
+                    for (int v = tid; v < nv; v += NC) {
+                        float f[VEC];
+                        E::unpack(chunk[v], f);
+#pragma unroll
+                        for (int e = 0; e < VEC; ++e)
+                            f[e] = elem(f[e], col_base + v * VEC + e == y);
+                        if (p.vec_store) {
+                            st_cs_v4(dbase + v * VEC, E::pack(f));
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < VEC; ++e)
+                                E::store(dbase + v * VEC + e, f[e]);
+                        }
+                    }
+                }
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&empty_bar[slot]);
+            }
+            return;
+        }
         if (split == 0)
             for (int64_t e = tid; e < g.head; e += NC)
                 E::store(drow + e, e == y ? gk.dy : grad_scalar(E::load(row + e), gk));
@@ -1067,7 +1138,7 @@ __global__ void combine_kernel(const RowParams p)
     const float nan = __int_as_float(0x7fc00000);
     constexpr bool kEnt = (MODE == kModeLogpEnt);
     constexpr bool kLogpFwd = (MODE == kModeLogp || kEnt);
-    constexpr bool kSumx = (MODE == kModeCeSmooth);
+    constexpr bool kSumx = (MODE == kModeCeSmooth || MODE == kModeCeCap);
 
     if (kLogpFwd) {
         if (p.row_mask != nullptr && p.row_mask[r] == 0) {
@@ -1125,7 +1196,9 @@ __global__ void combine_kernel(const RowParams p)
         if (kEnt)
             p.entropy_out[r] = entropy_with_targets<GBCE_MAX_K>(m, s, h, tg, xt, K, c, p.T);
     } else {
-        const float xy = E::load(row + p.targets[r]);
+        float xy = E::load(row + p.targets[r]);
+        if (MODE == kModeCeCap)
+            xy = p.softcap * tanh_acc(xy * p.inv_cap);
         const float logp = finalize_logp(m, s, xy, p.T);
         p.loss_rows[r] = ce_row_loss(logp, xy, h, p.T, p.ls_eps, p.dft, V);
         if (p.logp_out)
@@ -1226,6 +1299,10 @@ cudaError_t launch_rows_per_unit(const RowParams &p, int mode, cudaStream_t stre
         return launch_row_kernel<T, kModeCe, 1>(p, stream);
     case kModeCeSmooth:
         return launch_row_kernel<T, kModeCeSmooth, 1>(p, stream);
+    case kModeCeCap:
+        return launch_row_kernel<T, kModeCeCap, 1>(p, stream);
+    case kModeGradCap:
+        return launch_row_kernel<T, kModeGradCap, 1>(p, stream);
     case kModeGrad:
         return launch_row_kernel<T, kModeGrad, 1>(p, stream);
     case kModeFused:
@@ -1260,6 +1337,8 @@ cudaError_t launch_combine(const RowParams &p, int mode, cudaStream_t stream)
         combine_kernel<T, kModeLogpEnt><<<blocks, threads, 0, stream>>>(p);
     else if (mode == kModeCeSmooth)
         combine_kernel<T, kModeCeSmooth><<<blocks, threads, 0, stream>>>(p);
+    else if (mode == kModeCeCap)
+        combine_kernel<T, kModeCeCap><<<blocks, threads, 0, stream>>>(p);
     else
         combine_kernel<T, kModeCe><<<blocks, threads, 0, stream>>>(p);
     note_launches(1);

@@ -181,11 +181,20 @@ gbce_status selective_logsoftmax_bwd(const void *logits, gbce_dtype dtype, int64
  *                    -p_y log p_y of ms-swift PR #10353, "PR information").
  *                    Combines with label_smoothing (the weight multiplies
  *                    the smoothed row loss).
+ *   softcap          cap >= 0 (0: off): every logit x becomes cap * tanh(x / cap)
+ *                    before the temperature and the softmax; the gradient
+ *                    with respect to x takes the factor 1 - tanh^2(x / cap).
+ *                    Its tanh per element makes these calls ALU-bound, and
+ *                    the fused call then runs as a statistics pass and a
+ *                    gradient pass.  Logit soft-capping is named among the
+ *                    options of the fused losses on "Fix softmax collapse
+ *                    ..." (the unsloth-zoo #2080 commit, "Accuracy" tests).
  * ce_bwd must be given the same options as the ce_fwd whose log p it takes.
  */
 typedef struct gbce_ce_options {
     float label_smoothing;
     int32_t dft;
+    float softcap;
 } gbce_ce_options;
 
 /*

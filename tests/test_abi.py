@@ -114,12 +114,12 @@ def _bwd(lib, **kw):
                       a["d"], a["dstride"], None, None)
 
 
-def _opts(eps, dft=0):
+def _opts(eps, dft=0, cap=0.0):
     import ctypes
 
     import cross_entropy_gb300 as gbce
 
-    return ctypes.byref(gbce.CeOptions(eps, dft))
+    return ctypes.byref(gbce.CeOptions(eps, dft, cap))
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -184,3 +184,8 @@ def test_selective_backward_entropy_pointers_go_together(lib):
                                             gh, hs, FAKE * 16, 100, None, None)
     assert call(FAKE, None) == 1
     assert call(None, FAKE) == 1
+
+
+@pytest.mark.parametrize("cap", [-1.0, float("nan"), float("inf")])
+def test_softcap_out_of_range_is_refused(lib, cap):
+    assert _bwd(lib, opt=_opts(0.0, 0, cap)) == 1

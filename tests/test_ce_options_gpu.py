@@ -121,3 +121,66 @@ def test_full_size_grpo_smoothed_dft_fused():
                             label_smoothing=0.1, dft=True).loss
     check_rows_loss(rows_loss[st], ref["loss_rows"], torch.bfloat16, "rows")
     assert_loss_close(float(out.loss.item()), float(rows_loss.double().mean().item()), "mean")
+
+
+# ------------------------------------------------------ logit soft-capping
+
+def cap_tolerances(dtype, cap, T):
+    """The kernels' tanh is within 2.2e-7 relative, so a capped logit is
+    within cap * 2.2e-7 and a log-prob (a difference of two of them over T)
+    within 2 cap 2.2e-7 / T more than the uncapped bound."""
+    extra = 2.0 * cap * 2.2e-7 / T
+    from helpers import GRAD_TOL, LOGP_TOL
+    return LOGP_TOL[dtype] + extra, GRAD_TOL[dtype] + extra
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("eps,dft,scale", [(0.0, False, 1.0), (0.1, True, 1.0), (0.0, False, 12.0)])
+def test_softcap_fwd_bwd_fused_match_oracle(dtype, eps, dft, scale):
+    # scale 12 pushes most logits past the cap's knee (|x| / cap ~ 0.4 .. 2)
+    rows, V, cap, T = 560, 24001, 30.0, 0.9
+    w = workloads.collapse_stress(dtype=torch.float32, rows=rows, V=V, seed=70)
+    x_cpu = (w.logits * scale).to(dtype)
+    x, lab = x_cpu.to(DEV), w.labels.to(DEV)
+    g = torch.tensor([0.5])
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    kw = dict(temperature=T, reduction="sum", label_smoothing=eps, dft=dft, softcap=cap)
+    fwd = gbce.ce_fwd(x, lab, dev_status=status, **kw)
+    rows_fwd = gbce.ce_fwd(x, lab, dev_status=status, **dict(kw, reduction="none"))
+    d_sep = gbce.ce_bwd(x, lab, g.to(DEV), fwd.logp, fwd.n_items, dev_status=status, **kw)
+    fused = gbce.ce_fwd_bwd_fused(x, lab, g.to(DEV), dev_status=status, **kw)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref = oracle.cross_entropy(workloads.to_numpy_f64(x_cpu), w.labels.numpy(), temperature=T,
+                               reduction="sum", grad_out=[0.5], label_smoothing=eps, dft=dft,
+                               softcap=cap)
+    lp_tol, g_tol = cap_tolerances(dtype, cap, T)
+    live = w.labels.numpy() != -100
+    assert_logp_close(to_f64(fwd.logp), ref["logp"], dtype, "capped log p", tol=lp_tol)
+    assert_logp_close(-to_f64(rows_fwd.loss), -ref["loss_rows"], dtype, "capped rows", tol=lp_tol)
+    assert abs(float(fused.loss.item()) - ref["loss"]) <= lp_tol * abs(ref["loss"])
+    sel = np.arange(0, rows, 4)
+    st = torch.as_tensor(sel, device=DEV)
+    for d, name in ((d_sep, "ce_bwd"), (fused.dlogits, "fused")):
+        got = to_f64(d[st])
+        assert_grad_rows_close(got, ref["dlogits"][sel], dtype, name, tol=g_tol)
+    assert np.all(to_f64(fused.dlogits)[~live] == 0.0)
+
+
+def test_softcap_split_path_and_saturated_logits():
+    # few rows take the split statistics + merge; logits up to 1e4 saturate
+    V, cap = 152064, 50.0
+    gen = torch.Generator().manual_seed(8)
+    x_cpu = torch.randn((3, V), generator=gen) * 40.0
+    x_cpu[0, 17] = 1e4
+    x_cpu[1, 5] = -1e4
+    lab = torch.tensor([17, 5, 100])
+    x = x_cpu.to(DEV)
+    out = gbce.ce_fwd_bwd_fused(x, lab.to(DEV), torch.ones(3, device=DEV), reduction="none",
+                                softcap=cap)
+    torch.cuda.synchronize()
+    ref = oracle.cross_entropy(x_cpu.double().numpy(), lab.numpy(), reduction="none",
+                               grad_out=np.ones(3), softcap=cap)
+    lp_tol, g_tol = cap_tolerances(torch.float32, cap, 1.0)
+    assert_logp_close(-to_f64(out.loss), -ref["loss_rows"], torch.float32, "rows", tol=lp_tol)
+    assert_grad_rows_close(to_f64(out.dlogits), ref["dlogits"], torch.float32, tol=g_tol)
