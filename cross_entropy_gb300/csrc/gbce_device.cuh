@@ -300,6 +300,38 @@ __device__ __forceinline__ float2 fmul2(float2 a, float2 b)
 }
 
 // Exact max of two packed bf16 pairs (a NaN operand yields the other one).
+// 1 / x to about 1 ulp (0 for +inf).
+__device__ __forceinline__ float rcp_approx(float x)
+{
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// tanh_acc on a packed pair: the same two branches in f32x2 arithmetic (the
+// exponential one only when a lane needs it), one selected per lane.
+__device__ __forceinline__ float2 tanh_acc2(float2 u)
+{
+    const float2 a = make_float2(fabsf(u.x), fabsf(u.y));
+    const float2 s = fmul2(a, a);
+    const auto k2 = [](float v) { return make_float2(v, v); };
+    float2 p = k2(-929569.0f / 638512875.0f);
+    p = ffma2(p, s, k2(21844.0f / 6081075.0f));
+    p = ffma2(p, s, k2(-1382.0f / 155925.0f));
+    p = ffma2(p, s, k2(62.0f / 2835.0f));
+    p = ffma2(p, s, k2(-17.0f / 315.0f));
+    p = ffma2(p, s, k2(2.0f / 15.0f));
+    p = ffma2(p, s, k2(-1.0f / 3.0f));
+    const float2 small = ffma2(fmul2(a, s), p, a);
+    if (fmaxf(a.x, a.y) < 0.55f)  // both lanes on the series: skip the exponential
+        return make_float2(copysignf(small.x, u.x), copysignf(small.y, u.y));
+    const float2 e = fmul2(a, k2(2.0f * 1.4426950408889634f));
+    const float2 d = fadd2(make_float2(ex2(e.x), ex2(e.y)), k2(1.0f));
+    const float2 big = ffma2(k2(-2.0f), make_float2(rcp_approx(d.x), rcp_approx(d.y)), k2(1.0f));
+    return make_float2(copysignf(a.x < 0.55f ? small.x : big.x, u.x),
+                       copysignf(a.y < 0.55f ? small.y : big.y, u.y));
+}
+
 __device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b)
 {
     uint32_t d;

@@ -182,6 +182,54 @@ template <> struct FastVec<float> {
     }
 };
 
+// Soft-capped vectors: z = cap * tanh(x / cap) for a whole 16-byte vector in
+// packed pairs.  capped_pairs returns the vector's transformed pairs (4 for
+// bf16, 2 for fp32); the caller adds them or writes their gradient.
+template <typename T> struct CapVec;
+
+template <> struct CapVec<__nv_bfloat16> {
+    static constexpr int kPairs = 4;
+    __device__ static __forceinline__ void pairs(const uint4 &a, float2 (&x)[4])
+    {
+        x[0] = bf16x2_to_float2(a.x);
+        x[1] = bf16x2_to_float2(a.y);
+        x[2] = bf16x2_to_float2(a.z);
+        x[3] = bf16x2_to_float2(a.w);
+    }
+};
+
+template <> struct CapVec<float> {
+    static constexpr int kPairs = 2;
+    __device__ static __forceinline__ void pairs(const uint4 &a, float2 (&x)[2])
+    {
+        x[0] = make_float2(__uint_as_float(a.x), __uint_as_float(a.y));
+        x[1] = make_float2(__uint_as_float(a.z), __uint_as_float(a.w));
+    }
+};
+
+// Fold one soft-capped vector that holds no target: the running max comes
+// from the raw vector's exact max (tanh is increasing, so the capped max is
+// the cap of the raw max, taken only when the raw running max mraw rises),
+// the exponentials and the sum of capped logits from packed pairs.
+template <typename T, typename S>
+__device__ __forceinline__ void stats_capped(S &st, float &mraw, const uint4 &a, float c,
+                                             float cap, float inv_cap)
+{
+    constexpr int NP = CapVec<T>::kPairs;
+    const float vmax = FastVec<T>::vmax(a);
+    if (vmax > mraw || mraw != mraw) {  // (a NaN max keeps re-raising: NaN results)
+        mraw = vmax;
+        st.raise_to(cap * tanh_acc(vmax * inv_cap), c);  // >= -cap, never -inf
+    }
+    float2 x[NP];
+    CapVec<T>::pairs(a, x);
+    const float2 ic = make_float2(inv_cap, inv_cap), cc = make_float2(cap, cap);
+#pragma unroll
+    for (int i = 0; i < NP; i += 2)
+        st.add_pairs(fmul2(tanh_acc2(fmul2(x[i], ic)), cc),
+                     fmul2(tanh_acc2(fmul2(x[i + 1], ic)), cc), c);
+}
+
 // Fold body vectors va (and vb, the same thread's next vector) of a row;
 // col0 = first column of vector 0; nt = this thread's next target vector
 // (next_target_vector), advanced past the vectors a hit folds.
@@ -455,6 +503,57 @@ template <> struct GradVec<float> {
             d[e] = (e == yoff) ? k.dy : (ENT ? grad_scalar_ent(f[e], k) : grad_scalar(f[e], k));
     }
 };
+
+// Gradient of one soft-capped vector that does not hold the label, packed:
+// element j is fma(gs, 2^z', c0) * (1 - t^2), t = tanh(x / cap), z' the
+// exponent of the uncapped formula on the capped logit cap * t.
+template <typename T>
+__device__ __forceinline__ uint4 grad_capped(const uint4 &a, const GradConsts &k, float cap,
+                                             float inv_cap);
+
+template <>
+__device__ __forceinline__ uint4 grad_capped<__nv_bfloat16>(const uint4 &a, const GradConsts &k,
+                                                           float cap, float inv_cap)
+{
+    float2 x[4];
+    CapVec<__nv_bfloat16>::pairs(a, x);
+    const float2 ic = make_float2(inv_cap, inv_cap), cc = make_float2(cap, cap);
+    const float2 nn = make_float2(k.nxy, k.nxy), kc = make_float2(k.c, k.c);
+    const float2 kb = make_float2(k.kb, k.kb), gs = make_float2(k.gs, k.gs);
+    const float2 c0 = make_float2(k.c0, k.c0), one = make_float2(1.0f, 1.0f);
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 t = tanh_acc2(fmul2(x[i], ic));
+        const float2 chain = ffma2(make_float2(-t.x, -t.y), t, one);
+        const float2 z = ffma2(fadd2(fmul2(t, cc), nn), kc, kb);
+        const float2 d = ffma2(make_float2(ex2(z.x), ex2(z.y)), gs, c0);
+        o[i] = float2_to_bf16x2(fmul2(d, chain));
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+template <>
+__device__ __forceinline__ uint4 grad_capped<float>(const uint4 &a, const GradConsts &k, float cap,
+                                                   float inv_cap)
+{
+    float2 x[2];
+    CapVec<float>::pairs(a, x);
+    const float2 ic = make_float2(inv_cap, inv_cap), cc = make_float2(cap, cap);
+    const float2 nn = make_float2(k.nxy, k.nxy), kc = make_float2(k.c, k.c);
+    const float2 kb = make_float2(k.kb, k.kb), gs = make_float2(k.gs, k.gs);
+    const float2 c0 = make_float2(k.c0, k.c0), one = make_float2(1.0f, 1.0f);
+    float2 d[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const float2 t = tanh_acc2(fmul2(x[i], ic));
+        const float2 chain = ffma2(make_float2(-t.x, -t.y), t, one);
+        const float2 z = ffma2(fadd2(fmul2(t, cc), nn), kc, kb);
+        d[i] = fmul2(ffma2(make_float2(ex2(z.x), ex2(z.y)), gs, c0), chain);
+    }
+    return make_uint4(__float_as_uint(d[0].x), __float_as_uint(d[0].y), __float_as_uint(d[1].x),
+                      __float_as_uint(d[1].y));
+}
 
 // log p of target k, whose "others" are every column outside the target set
 // S (already folded into (mS, sS)) plus the distinct members of S other
@@ -777,6 +876,7 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
         // holds one skips even the cursor test (warp-uniform branch)
         int32_t nt = next_target_vector<KMAX>(tv, v0, v1, tid, NC, -1);
         const bool wcheck = __any_sync(0xffffffffu, nt != INT32_MAX);
+        float mraw = kNegInf;  // soft-capped sweep: the raw max behind st.m
         if (split == 0)
             for (int64_t e = tid; e < g.head; e += NC) {
                 const float x = capped(E::load(row + e));
@@ -801,11 +901,17 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
                 const int32_t vb0 = static_cast<int32_t>(v0 + i * CV);  // body vector of chunk[0]
                 const int32_t col0 = static_cast<int32_t>(g.head);
                 if (kCap) {
-                    // soft-capped: every element through tanh, unpacked
+                    // soft-capped: packed pairs, a vector holding a target
+                    // unpacked with that column masked
                     for (int v = tid; v < nv; v += NC) {
+                        const int32_t vb = vb0 + v;
+                        if (!(wcheck && nt == vb)) {
+                            stats_capped<T>(st, mraw, chunk[v], c, p.softcap, p.inv_cap);
+                            continue;
+                        }
                         float f[VEC];
                         E::unpack(chunk[v], f);
-                        const int32_t colv = col0 + (vb0 + v) * VEC;
+                        const int32_t colv = col0 + vb * VEC;
                         float vm = kNegInf;
 #pragma unroll
                         for (int e = 0; e < VEC; ++e) {
@@ -816,6 +922,7 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
                             vm = fmaxf(vm, f[e]);
                         }
                         st.template add<VEC>(f, vm, c);
+                        nt = next_target_vector<KMAX>(tv, v0, v1, tid, NC, vb);
                     }
                 } else if (nv == CV) {
                     uint4 raw[PER_THREAD];
@@ -1055,6 +1162,12 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
                     const int64_t col_base = g.head + vbase * VEC;
                     T *dbase = drow + col_base;
                     for (int v = tid; v < nv; v += NC) {
+                        const int64_t yoff = y - (col_base + v * VEC);
+                        if (p.vec_store && (yoff < 0 || yoff >= VEC)) {
+                            st_cs_v4(dbase + v * VEC,
+                                     grad_capped<T>(chunk[v], gk, p.softcap, p.inv_cap));
+                            continue;
+                        }
                         float f[VEC];
                         E::unpack(chunk[v], f);
 #pragma unroll
