@@ -23,7 +23,11 @@
 //    logits, and the gradient is g*softmax - g*onehot in a separate buffer:
 //    ms-swift PR #10353, "PR information";
 //  * a slice split with a later merge of (max, sum) partials: the split
-//    partial/combine kernels of the unsloth-zoo #2080 commit ("Fix").
+//    partial/combine kernels of the unsloth-zoo #2080 commit ("Fix");
+//  * the row entropy taken around the same others' sum, its gradient, label
+//    smoothing (the -expm1 label term covers it) and the soft-capped logits
+//    of the fused losses' options: the unsloth-zoo #2080 commit ("Fix",
+//    "Accuracy"); the DFT row weight: ms-swift PR #10353, "PR information".
 #pragma once
 
 #include <atomic>

@@ -190,6 +190,8 @@ gbce_status selective_logsoftmax_bwd(const void *logits, gbce_dtype dtype, int64
  *                    options of the fused losses on "Fix softmax collapse
  *                    ..." (the unsloth-zoo #2080 commit, "Accuracy" tests).
  * ce_bwd must be given the same options as the ce_fwd whose log p it takes.
+ * An eps outside [0, 1] (or NaN), or a negative or non-finite softcap, makes
+ * the call return GBCE_EINVAL before any GPU work.
  */
 typedef struct gbce_ce_options {
     float label_smoothing;
