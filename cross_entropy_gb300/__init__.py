@@ -11,12 +11,19 @@ Functions (same names as the C ABI):
 
 * :func:`selective_logsoftmax` -- log p at K gathered indices per row, with
   temperature and row mask ("perf(rlhf): chunk selective_log_softmax instead
-  of looping per token", "PR information"); :func:`selective_logsoftmax_bwd`
-  its gradient, the one a GRPO-style loss sends back.
+  of looping per token", "PR information"), and optionally each row's softmax
+  entropy from the same sweep; :func:`selective_logsoftmax_bwd` its gradient
+  (the one a GRPO-style loss sends back), optionally with the entropy's.
 * :func:`ce_fwd`, :func:`ce_bwd`, :func:`ce_fwd_bwd_fused` -- token
   cross-entropy in the collapse-safe form of "Fix softmax collapse in CE,
   GRPO, KL/JSD and softmax" ("Summary"), with the analytic backward
-  g*softmax - g*onehot of ms-swift PR #10353 ("PR information").
+  g*softmax - g*onehot of ms-swift PR #10353 ("PR information"), optional
+  label smoothing, DFT row weights and logit soft-capping.
+* :func:`ce_fwd_bwd_fused_noalloc` -- the fused call without a workspace.
+
+Caller-supplied output, scratch and status tensors are checked for device,
+dtype and size before any GPU work: the kernels write through their data
+pointers.
 """
 
 from __future__ import annotations
@@ -114,9 +121,36 @@ def _rows_view(logits: torch.Tensor) -> torch.Tensor:
     return logits
 
 
-def _stream_ptr(stream) -> int:
-    s = stream if stream is not None else torch.cuda.current_stream()
+def _stream_ptr(stream, device=None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream(device)
     return int(s.cuda_stream)
+
+
+def _check_buffer(t: Optional[torch.Tensor], name: str, dtype, numel: int, device) -> None:
+    """A caller-supplied output or scratch tensor: the kernels write exactly
+    `numel` elements of `dtype` through its data pointer, so anything else is
+    refused here, before any GPU work."""
+    if t is None:
+        return
+    if t.device != device:
+        raise ValueError(f"{name} must be on {device}, got {t.device}")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous() or t.numel() != numel:
+        raise ValueError(f"{name} must be a contiguous tensor of {numel} elements, "
+                         f"got shape {tuple(t.shape)}")
+
+
+def _check_dlogits(d: torch.Tensor, x: torch.Tensor) -> None:
+    if d.device != x.device or d.dtype != x.dtype or tuple(d.shape) != tuple(x.shape):
+        raise ValueError(f"dlogits must be a {x.dtype} tensor of shape {tuple(x.shape)} on "
+                         f"{x.device} (rows x vocab, unit vocab stride)")
+
+
+def _check_status(st: Optional[torch.Tensor], device) -> None:
+    if st is not None and (st.device != device or st.dtype != torch.int32 or st.numel() < 1):
+        raise ValueError("dev_status must be an int32 tensor of at least 1 element on "
+                         "the logits' device")
 
 
 def _dev_int64(x, device) -> torch.Tensor:
@@ -142,6 +176,8 @@ def new_workspace(rows: int, vocab: int, k: int = 1, device=None) -> torch.Tenso
 def _workspace(ws, rows, vocab, k, device):
     if ws is None:
         ws = new_workspace(rows, vocab, k, device)
+    elif ws.device != device or not ws.is_contiguous():
+        raise ValueError(f"workspace must be a contiguous tensor on {device}")
     return ws, int(ws.data_ptr()), int(ws.numel() * ws.element_size())
 
 
@@ -176,17 +212,18 @@ def selective_logsoftmax(logits: torch.Tensor, index, temperature: float = 1.0,
         mask = row_mask.to(device=x.device, dtype=torch.uint8).reshape(rows).contiguous()
     if out is None:
         out = torch.empty((rows, K), dtype=torch.float32, device=x.device)
+    _check_buffer(out, "out", torch.float32, rows * K, x.device)
+    _check_status(dev_status, x.device)
     ent = entropy_out
     if ent is None and with_entropy:
         ent = torch.empty(rows, dtype=torch.float32, device=x.device)
-    if ent is not None and (ent.dtype != torch.float32 or not ent.is_contiguous()
-                            or ent.numel() != rows):
-        raise ValueError("entropy_out must be a contiguous fp32 tensor with one value per row")
+    _check_buffer(ent, "entropy_out", torch.float32, rows, x.device)
     ws, ws_ptr, ws_bytes = _workspace(workspace, rows, V, K, x.device)
-    st = lib.selective_logsoftmax(x.data_ptr(), _dtype_code(x), rows, V, x.stride(0),
-                                  idx.data_ptr(), K, float(temperature), _ptr(mask),
-                                  out.data_ptr(), _ptr(ent), ws_ptr, ws_bytes, _ptr(dev_status),
-                                  _stream_ptr(stream))
+    with torch.cuda.device(x.device):  # the library launches on the current device
+        st = lib.selective_logsoftmax(x.data_ptr(), _dtype_code(x), rows, V, x.stride(0),
+                                      idx.data_ptr(), K, float(temperature), _ptr(mask),
+                                      out.data_ptr(), _ptr(ent), ws_ptr, ws_bytes, _ptr(dev_status),
+                                      _stream_ptr(stream, x.device))
     _check(st, "selective_logsoftmax")
     res = out.view(*lead_shape, K)
     res = res.squeeze(-1) if squeeze else res
@@ -217,7 +254,7 @@ def selective_logsoftmax_bwd(logits: torch.Tensor, index, grad_logp, saved_logp,
     idx = idx.reshape(rows, K)
     g = torch.as_tensor(grad_logp, dtype=torch.float32, device=x.device).reshape(rows, K)
     g = g.contiguous()
-    lp = saved_logp.to(torch.float32).reshape(rows, K).contiguous()
+    lp = saved_logp.to(device=x.device, dtype=torch.float32).reshape(rows, K).contiguous()
     mask = None
     if row_mask is not None:
         mask = row_mask.to(device=x.device, dtype=torch.uint8).reshape(rows).contiguous()
@@ -227,15 +264,18 @@ def selective_logsoftmax_bwd(logits: torch.Tensor, index, grad_logp, saved_logp,
     if grad_entropy is not None:
         gh = torch.as_tensor(grad_entropy, dtype=torch.float32,
                              device=x.device).reshape(rows).contiguous()
-        hs = saved_entropy.to(torch.float32).reshape(rows).contiguous()
+        hs = saved_entropy.to(device=x.device, dtype=torch.float32).reshape(rows).contiguous()
     if dlogits is None:
         dlogits = torch.empty_like(logits)
     d = _rows_view(dlogits)
-    st = lib.selective_logsoftmax_bwd(x.data_ptr(), _dtype_code(x), rows, V, x.stride(0),
-                                      idx.data_ptr(), K, float(temperature), _ptr(mask),
-                                      g.data_ptr(), lp.data_ptr(), _ptr(gh), _ptr(hs),
-                                      d.data_ptr(), d.stride(0), _ptr(dev_status),
-                                      _stream_ptr(stream))
+    _check_dlogits(d, x)
+    _check_status(dev_status, x.device)
+    with torch.cuda.device(x.device):  # the library launches on the current device
+        st = lib.selective_logsoftmax_bwd(x.data_ptr(), _dtype_code(x), rows, V, x.stride(0),
+                                          idx.data_ptr(), K, float(temperature), _ptr(mask),
+                                          g.data_ptr(), lp.data_ptr(), _ptr(gh), _ptr(hs),
+                                          d.data_ptr(), d.stride(0), _ptr(dev_status),
+                                          _stream_ptr(stream, x.device))
     _check(st, "selective_logsoftmax_bwd")
     return dlogits
 
@@ -290,11 +330,14 @@ def ce_fwd(logits: torch.Tensor, labels, ignore_index: int = -100, temperature: 
     lse = torch.empty(rows, dtype=torch.float32, device=x.device) if want_lse else None
     n_items = torch.empty(1, dtype=torch.int64, device=x.device)
     ws, ws_ptr, ws_bytes = _workspace(workspace, rows, V, 1, x.device)
-    st = lib.ce_fwd(x.data_ptr(), _dtype_code(x), rows, V, x.stride(0), lab.data_ptr(),
-                    int(ignore_index), float(temperature), red,
-                    _ce_options(label_smoothing, dft, softcap), loss.data_ptr(), logp.data_ptr(),
-                    _ptr(lse), n_items.data_ptr(), ws_ptr, ws_bytes, _ptr(dev_status),
-                    _stream_ptr(stream))
+    _check_status(dev_status, x.device)
+    with torch.cuda.device(x.device):  # the library launches on the current device
+        st = lib.ce_fwd(x.data_ptr(), _dtype_code(x), rows, V, x.stride(0), lab.data_ptr(),
+                        int(ignore_index), float(temperature), red,
+                        _ce_options(label_smoothing, dft, softcap), loss.data_ptr(),
+                        logp.data_ptr(),
+                        _ptr(lse), n_items.data_ptr(), ws_ptr, ws_bytes, _ptr(dev_status),
+                        _stream_ptr(stream, x.device))
     _check(st, "ce_fwd")
     return CeForward(loss if red == 0 else loss[0], logp, lse, n_items[0])
 
@@ -318,11 +361,15 @@ def ce_bwd(logits: torch.Tensor, labels, grad_out, saved_logp: torch.Tensor, n_i
     if dlogits is None:
         dlogits = torch.empty((rows, V), dtype=x.dtype, device=x.device)
     d = _rows_view(dlogits)
-    lp = saved_logp.reshape(rows).contiguous()
-    st = lib.ce_bwd(x.data_ptr(), _dtype_code(x), rows, V, x.stride(0), lab.data_ptr(),
-                    int(ignore_index), float(temperature), red,
-                    _ce_options(label_smoothing, dft, softcap), g.data_ptr(), lp.data_ptr(),
-                    _ptr(n), d.data_ptr(), d.stride(0), _ptr(dev_status), _stream_ptr(stream))
+    _check_dlogits(d, x)
+    _check_status(dev_status, x.device)
+    lp = saved_logp.to(device=x.device, dtype=torch.float32).reshape(rows).contiguous()
+    with torch.cuda.device(x.device):  # the library launches on the current device
+        st = lib.ce_bwd(x.data_ptr(), _dtype_code(x), rows, V, x.stride(0), lab.data_ptr(),
+                        int(ignore_index), float(temperature), red,
+                        _ce_options(label_smoothing, dft, softcap), g.data_ptr(), lp.data_ptr(),
+                        _ptr(n), d.data_ptr(), d.stride(0), _ptr(dev_status),
+                        _stream_ptr(stream, x.device))
     _check(st, "ce_bwd")
     return dlogits
 
@@ -351,13 +398,17 @@ def ce_fwd_bwd_fused(logits: torch.Tensor, labels, grad_out=None, ignore_index: 
     if dlogits is None:
         dlogits = torch.empty((rows, V), dtype=x.dtype, device=x.device)
     d = _rows_view(dlogits)
+    _check_dlogits(d, x)
+    _check_status(dev_status, x.device)
     ws, ws_ptr, ws_bytes = _workspace(workspace, rows, V, 1, x.device)
-    st = lib.ce_fwd_bwd_fused(x.data_ptr(), _dtype_code(x), rows, V, x.stride(0), lab.data_ptr(),
-                              int(ignore_index), float(temperature), red,
-                              _ce_options(label_smoothing, dft, softcap), g.data_ptr(),
-                              loss.data_ptr(), _ptr(logp), _ptr(lse), n_items.data_ptr(),
-                              d.data_ptr(), d.stride(0), ws_ptr, ws_bytes, _ptr(dev_status),
-                              _stream_ptr(stream))
+    with torch.cuda.device(x.device):  # the library launches on the current device
+        st = lib.ce_fwd_bwd_fused(x.data_ptr(), _dtype_code(x), rows, V, x.stride(0),
+                                  lab.data_ptr(),
+                                  int(ignore_index), float(temperature), red,
+                                  _ce_options(label_smoothing, dft, softcap), g.data_ptr(),
+                                  loss.data_ptr(), _ptr(logp), _ptr(lse), n_items.data_ptr(),
+                                  d.data_ptr(), d.stride(0), ws_ptr, ws_bytes, _ptr(dev_status),
+                                  _stream_ptr(stream, x.device))
     _check(st, "ce_fwd_bwd_fused")
     return CeFused(loss if red == 0 else loss[0], dlogits, logp, lse, n_items[0])
 
@@ -389,10 +440,14 @@ def ce_fwd_bwd_fused_noalloc(logits: torch.Tensor, labels, grad_out=None,
     if dlogits is None:
         dlogits = torch.empty((rows, V), dtype=x.dtype, device=x.device)
     d = _rows_view(dlogits)
-    st = lib.ce_fwd_bwd_fused_noalloc(x.data_ptr(), _dtype_code(x), rows, V, x.stride(0),
-                                      lab.data_ptr(), int(ignore_index), float(temperature), red,
-                                      g.data_ptr(), loss.data_ptr(), logp.data_ptr(), None,
-                                      n_items.data_ptr(), d.data_ptr(), d.stride(0),
-                                      _ptr(dev_status), _stream_ptr(stream))
+    _check_dlogits(d, x)
+    _check_status(dev_status, x.device)
+    with torch.cuda.device(x.device):  # the library launches on the current device
+        st = lib.ce_fwd_bwd_fused_noalloc(x.data_ptr(), _dtype_code(x), rows, V, x.stride(0),
+                                          lab.data_ptr(), int(ignore_index), float(temperature),
+                                          red,
+                                          g.data_ptr(), loss.data_ptr(), logp.data_ptr(), None,
+                                          n_items.data_ptr(), d.data_ptr(), d.stride(0),
+                                          _ptr(dev_status), _stream_ptr(stream, x.device))
     _check(st, "ce_fwd_bwd_fused_noalloc")
     return CeFused(loss if red == 0 else loss[0], dlogits, logp, None, n_items[0])

@@ -460,3 +460,30 @@ def test_million_column_rows_persistent_path():
     res, ref, sel = run_all(w, temperature=1.0, reduction="mean", grad_out=torch.ones(1),
                             rows_sel=np.sort(sel))
     check_all(w, res, ref, sel, reduction="mean", check_scalar_vs_oracle=False, T=1.0)
+
+
+def test_binding_refuses_bad_output_buffers_before_any_launch():
+    x = torch.randn((6, 300), device=DEV)
+    lab = torch.zeros(6, dtype=torch.int64, device=DEV)
+    idx = torch.zeros((6, 2), dtype=torch.int64, device=DEV)
+    before = gbce.kernel_launches()
+    bad_calls = [
+        lambda: gbce.selective_logsoftmax(x, idx, out=torch.empty((5, 2), device=DEV)),
+        lambda: gbce.selective_logsoftmax(x, idx, out=torch.empty((6, 2), dtype=torch.float64,
+                                                                  device=DEV)),
+        lambda: gbce.selective_logsoftmax(x, idx, entropy_out=torch.empty(5, device=DEV)),
+        lambda: gbce.ce_fwd_bwd_fused(x, lab, dlogits=torch.empty((5, 300), device=DEV)),
+        lambda: gbce.ce_fwd_bwd_fused(x, lab, dlogits=torch.empty((6, 300), dtype=torch.bfloat16,
+                                                                  device=DEV)),
+        lambda: gbce.ce_bwd(x, lab, torch.ones(1), torch.zeros(6), torch.tensor(6),
+                            dlogits=torch.empty((6, 299), device=DEV)),
+        lambda: gbce.selective_logsoftmax_bwd(x, idx, torch.ones((6, 2)), torch.zeros((6, 2)),
+                                              dlogits=torch.empty((6, 300), device=DEV)[:, :299]),
+        lambda: gbce.ce_fwd(x, lab, dev_status=torch.zeros(1, dtype=torch.int64, device=DEV)),
+        lambda: gbce.ce_fwd(x, lab, workspace=torch.empty(1 << 16, dtype=torch.uint8)),
+    ]
+    for call in bad_calls:
+        with pytest.raises(ValueError):
+            call()
+    torch.cuda.synchronize()
+    assert gbce.kernel_launches() == before
