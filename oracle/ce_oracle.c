@@ -132,16 +132,33 @@ static double neg_plogp(double lp)
     return p == 0.0 ? 0.0 : -p * lp;
 }
 
-/* -sum_j p_j log p_j of one row, with column t's term from its accurate log p. */
-static double row_entropy(const double *x, int64_t V, int64_t t, double T)
+/* The first column holding a row's largest logit (its dominant column). */
+static int64_t row_argmax(const double *x, int64_t V)
 {
-    const double lp_t = row_logp(x, V, t, T);
-    /* logsumexp of all columns; the others' alone when p_t is exactly 0 */
-    const double lse = lp_t == -INFINITY ? lse_excluding(x, V, t, T) : x[t] / T - lp_t;
+    int64_t d = 0;
+    for (int64_t j = 1; j < V; ++j)
+        if (x[j] > x[d])
+            d = j;
+    return d;
+}
+
+/*
+ * -sum_j p_j log p_j of one row.  The dominant column d enters with its
+ * accurate log p (the collapse-safe form), every other column with
+ * z_j - lse, lse = z_d - log p_d.  A row whose mass sits almost all on one
+ * column thus keeps its small entropy, whichever column that is: the value
+ * depends on the row alone.
+ */
+static double row_entropy(const double *x, int64_t V, double T)
+{
+    const int64_t d = row_argmax(x, V);
+    const double lp_d = row_logp(x, V, d, T);
+    /* logsumexp of all columns; the others' alone when p_d is exactly 0 */
+    const double lse = lp_d == -INFINITY ? lse_excluding(x, V, d, T) : x[d] / T - lp_d;
     oracle_sum h = {0.0, 0.0};
-    sum_add(&h, neg_plogp(lp_t));
+    sum_add(&h, neg_plogp(lp_d));
     for (int64_t j = 0; j < V; ++j) {
-        if (j == t)
+        if (j == d)
             continue;
         sum_add(&h, neg_plogp(x[j] / T - lse));
     }
@@ -151,7 +168,9 @@ static double row_entropy(const double *x, int64_t V, int64_t t, double T)
 /*
  * Row entropy.
  *   x        [rows, ld] fp64
- *   ref      [rows] int64: the reference column of each row
+ *   ref      [rows] int64: a column of each row (the sampled token); the
+ *            entropy does not depend on it, but a row whose column is out
+ *            of range gets NaN, as its log-prob does
  *   live     [rows] uint8 or NULL: rows with 0 are skipped (entropy 0)
  *   out      [rows] fp64
  * Returns the number of live rows whose reference column is out of range.
@@ -172,7 +191,7 @@ int64_t oracle_entropy(const double *x, int64_t rows, int64_t V, int64_t ld, con
             ++bad;
             continue;
         }
-        out[r] = row_entropy(x + r * ld, V, t, T);
+        out[r] = row_entropy(x + r * ld, V, T);
     }
     return bad;
 }
@@ -377,8 +396,9 @@ int64_t oracle_cross_entropy(const double *x, int64_t rows, int64_t V, int64_t l
     return bad;
 }
 
-/* Forward declaration: the entropy term of the backward below uses it. */
-static double row_entropy(const double *x, int64_t V, int64_t t, double T);
+/* Forward declarations: the entropy term of the backward below uses them. */
+static double row_entropy(const double *x, int64_t V, double T);
+static int64_t row_argmax(const double *x, int64_t V);
 
 /*
  * Selective log-softmax backward, optionally with an entropy term.
@@ -388,7 +408,11 @@ static double row_entropy(const double *x, int64_t V, int64_t t, double T);
  *   grad      [rows, K] fp64: dL/d out[r, k]
  *   grad_ent  [rows] fp64 or NULL: dL/d H_r, H_r = -sum_j p_j log p_j; it
  *             adds -(grad_ent / T) p_j (log p_j + H_r) to column j (the
- *             derivative of the entropy, written out), 0 where p_j = 0
+ *             derivative of the entropy, written out), 0 where p_j = 0.
+ *             For the row's dominant column d, log p_d + H_r is taken as
+ *             sum_{j != d} p_j (z_d - z_j), the same number (H_r = lse -
+ *             sum_j p_j z_j) as a sum of non-negative terms: the difference
+ *             itself cancels when p_d is near 1.
  *   dx        [rows, ldx] out
  * Returns the number of rows with an out-of-range index (their rows NaN).
  */
@@ -431,13 +455,22 @@ int64_t oracle_selective_logsoftmax_backward(const double *x, int64_t rows, int6
             sum_add(&G, grad[r * K + k]);
         const double Gv = sum_value(&G);
         const double gH = grad_ent ? grad_ent[r] : 0.0;
-        const double H = grad_ent ? row_entropy(xr, V, idx[r * K], T) : 0.0;
+        const double H = grad_ent ? row_entropy(xr, V, T) : 0.0;
+        const int64_t d = row_argmax(xr, V);
+        oracle_sum q = {0.0, 0.0};
+        if (gH != 0.0)
+            for (int64_t j = 0; j < V; ++j) {
+                const double pj = exp(xr[j] / T - lse);
+                if (j != d && pj != 0.0)
+                    sum_add(&q, pj * ((xr[d] - xr[j]) / T));
+            }
+        const double Hd = sum_value(&q); /* log p_d + H */
         for (int64_t j = 0; j < V; ++j) {
             const double lpj = xr[j] / T - lse;
             const double pj = exp(lpj);
             dr[j] = -(Gv / T) * pj;
             if (gH != 0.0 && pj != 0.0)
-                dr[j] -= (gH / T) * pj * (lpj + H);
+                dr[j] -= (gH / T) * pj * (j == d ? Hd : lpj + H);
         }
         /* gathered columns, each once, in the collapse-safe form */
         for (int64_t k = 0; k < K; ++k) {
@@ -456,7 +489,7 @@ int64_t oracle_selective_logsoftmax_backward(const double *x, int64_t rows, int6
             const double lp = row_logp(xr, V, t, T);
             dr[t] = (-g_t * expm1(lp) - (Gv - g_t) * exp(lp)) / T;
             if (gH != 0.0 && exp(lp) != 0.0)
-                dr[t] -= (gH / T) * exp(lp) * (lp + H);
+                dr[t] -= (gH / T) * exp(lp) * (t == d ? Hd : lp + H);
         }
     }
     return bad;

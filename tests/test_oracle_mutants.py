@@ -40,10 +40,17 @@ MUTANTS = {
     "sel_bwd_others_use_all_of_G": ("- (Gv - g_t) * exp(lp)) / T;", "- Gv * exp(lp)) / T;"),
     "sel_bwd_duplicates_not_summed": ("                if (idx[r * K + i] == t)\n                    sum_add(&gt",
                                       "                if (i == k)\n                    sum_add(&gt"),
-    "entropy_target_term_dropped": ("    sum_add(&h, neg_plogp(lp_t));\n", ""),
-    "entropy_lse_sign": (": x[t] / T - lp_t;", ": x[t] / T + lp_t;"),
-    "ent_bwd_sign": ("dr[j] -= (gH / T) * pj * (lpj + H);", "dr[j] += (gH / T) * pj * (lpj + H);"),
-    "ent_bwd_target_drops_H": ("* exp(lp) * (lp + H);", "* exp(lp) * lp;"),
+    "entropy_target_term_dropped": ("    sum_add(&h, neg_plogp(lp_d));\n", ""),
+    "entropy_lse_sign": (": x[d] / T - lp_d;", ": x[d] / T + lp_d;"),
+    "entropy_reference_not_dominant": ("    const int64_t d = row_argmax(x, V);\n    const double lp_d",
+                                       "    const int64_t d = 0;\n    const double lp_d"),
+    "ent_bwd_sign": ("dr[j] -= (gH / T) * pj * (j == d ? Hd : lpj + H);",
+                     "dr[j] += (gH / T) * pj * (j == d ? Hd : lpj + H);"),
+    "ent_bwd_dominant_by_difference": ("dr[j] -= (gH / T) * pj * (j == d ? Hd : lpj + H);",
+                                       "dr[j] -= (gH / T) * pj * (lpj + H);"),
+    "ent_bwd_gap_sign": ("sum_add(&q, pj * ((xr[d] - xr[j]) / T));",
+                         "sum_add(&q, pj * ((xr[j] - xr[d]) / T));"),
+    "ent_bwd_target_drops_H": ("* exp(lp) * (t == d ? Hd : lp + H);", "* exp(lp) * (t == d ? Hd : lp);"),
     "smoothing_off_by_one_class": ("const double u = eps / (double)V;",
                                    "const double u = eps / (double)(V - 1);"),
     "smoothing_mean_not_over_V": ("eps * (sum_value(&nl) / (double)V)", "eps * sum_value(&nl)"),

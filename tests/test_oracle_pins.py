@@ -471,6 +471,25 @@ def test_entropy_brute_force(V, T):
         assert h[r] > 0.0          # never collapses to 0 for a finite margin
 
 
+@pytest.mark.parametrize("V", [5, 33])
+@pytest.mark.parametrize("T", [1.0, 0.7])
+def test_entropy_brute_force_when_another_column_dominates(V, T):
+    # the sampled column (the reference passed in) is not the row's dominant
+    # one: the dominant column's 1 - p must still not round away
+    margins = [17.0, 30.0, 50.0]
+    w = workloads.peaked_rows_tiny(V, margins, seed=700 + V)
+    x = w.logits.numpy()
+    y = w.labels.numpy()
+    other = (y + 1 + np.arange(len(margins))) % V
+    assert np.all(other != y)
+    h, bad = oracle.entropy(x, other, T)
+    assert bad == 0
+    Te = oracle.exact_temperature(T)
+    for r in range(len(margins)):
+        want = brute_entropy(x[r], Te)
+        assert h[r] == pytest.approx(want, rel=1e-11, abs=1e-300), (r, margins[r])
+
+
 def test_entropy_closed_forms_and_bounds():
     V = 1000
     x = np.full((2, V), 0.25)
@@ -547,6 +566,35 @@ def test_entropy_backward_brute_force(V, T):
         assert np.max(np.abs(dx[r] - want)) <= 1e-13 * abs(gh[r]) * size, (r, margins[r])
         # the dominant column's tiny entry keeps its relative accuracy
         assert dx[r, y[r]] == pytest.approx(want[y[r]], rel=1e-9, abs=1e-300)
+
+
+@pytest.mark.parametrize("V", [5, 33])
+@pytest.mark.parametrize("T", [1.0, 0.7])
+def test_entropy_backward_brute_force_dominant_column_not_gathered(V, T):
+    # gathered columns other than the dominant one, with and without log-prob
+    # upstream: the dominant column's entry still keeps its relative accuracy
+    margins = [17.0, 30.0, 50.0]
+    w = workloads.peaked_rows_tiny(V, margins, seed=900 + V)
+    x = w.logits.numpy()
+    y = w.labels.numpy()
+    idx = np.stack([(y + 1) % V, (y + 2) % V], axis=1)
+    g = np.array([[0.0, 0.0], [0.5, -1.0], [0.0, 0.0]])
+    gh = np.array([1.0, -0.75, 0.5])
+    dx, bad = oracle.selective_logsoftmax_backward(x, idx, g, T, grad_entropy=gh)
+    assert bad == 0
+    Te = oracle.exact_temperature(T)
+    for r in range(len(margins)):
+        grad, size = brute_entropy_grad(x[r], Te)
+        want = gh[r] * grad
+        logps, _ = brute_row(x[r], 0, Te)
+        for k in range(2):
+            t = idx[r, k]
+            want[t] += g[r, k] / Te
+        want -= g[r].sum() / Te * np.array([float(CTX.exp(lp)) for lp in logps])
+        d = y[r]
+        assert dx[r, d] == pytest.approx(want[d], rel=1e-9, abs=1e-300), (r, margins[r])
+        scale = abs(gh[r]) * size + np.abs(g[r]).sum() / Te
+        assert np.max(np.abs(dx[r] - want)) <= 1e-13 * scale, (r, margins[r])
 
 
 def test_entropy_backward_finite_difference_with_logp_terms():
