@@ -21,25 +21,49 @@ std::atomic<uint64_t> g_launches{0};
 
 void gbce::note_launches(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 
+int gbce::device_sm_count()
+{
+    static std::atomic<int> cache[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return 0;
+    if (dev >= 0 && dev < 64) {
+        const int v = cache[dev].load(std::memory_order_relaxed);
+        if (v > 0)
+            return v;
+    }
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 0;
+    if (dev >= 0 && dev < 64)
+        cache[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
+
 namespace {
 
-// Few-row problems are split along the vocabulary so that the grid still
-// has about kSplitTargetUnits work units; a slice keeps >= kMinSplitElems.
-constexpr int64_t kSplitTargetUnits = 512;
+// Few-row problems split the vocabulary so that the row kernel's grid still
+// fills the GPU in one wave: rows x splits <= the resident CTAs (3 per SM),
+// at most kMaxClusterSplits slices (the portable cluster size, since a split
+// row's CTAs form one cluster) of at least kMinSplitElems columns each.
+constexpr int kRowCtasPerSm = 3;
 constexpr int64_t kMinSplitElems = 8192;
-constexpr int64_t kMaxSplits = 64;
+constexpr int64_t kMaxClusterSplits = 8;
 constexpr int64_t kMaxVocab = INT32_MAX - 64;  // columns are int32 on the device
 
 int split_count(int64_t rows, int64_t vocab)
 {
-    if (rows <= 0 || rows >= kSplitTargetUnits)
+    if (rows <= 0)
         return 1;
-    int64_t s = (kSplitTargetUnits + rows - 1) / rows;
-    const int64_t by_vocab = vocab / kMinSplitElems;
-    if (s > by_vocab)
-        s = by_vocab;
-    if (s > kMaxSplits)
-        s = kMaxSplits;
+    const int sms = gbce::device_sm_count();
+    const int64_t slots = static_cast<int64_t>(kRowCtasPerSm) * (sms > 0 ? sms : 152);
+    if (rows * 2 > slots)
+        return 1;
+    int64_t s = slots / rows;
+    if (s > vocab / kMinSplitElems)
+        s = vocab / kMinSplitElems;
+    if (s > kMaxClusterSplits)
+        s = kMaxClusterSplits;
     return s < 1 ? 1 : static_cast<int>(s);
 }
 
@@ -47,33 +71,27 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct WsLayout {
     size_t count = 0;     // int64 n_items scratch
+    size_t ticket = 0;    // int32 row ticket of the persistent fused kernel
     size_t loss = 0;      // float [rows] per-row losses
-    size_t logp = 0;      // float [rows] per-row log p (split path)
-    size_t partials = 0;  // float2 [rows * splits]
-    size_t partials_h = 0;  // float [rows * splits]: entropy moments or sums of logits
+    size_t logp = 0;      // float [rows] per-row log p (two-pass fused calls)
     size_t total = 0;
 };
 
 WsLayout ws_layout(int64_t rows, int64_t vocab)
 {
+    (void)vocab;  // split rows swap their partials on chip, not through the workspace
     WsLayout w;
     if (rows <= 0)
         return w;
-    const int splits = split_count(rows, vocab);
     const size_t r = static_cast<size_t>(rows);
     size_t off = 0;
     w.count = off;
+    w.ticket = off + 8;
     off += 256;
     w.loss = off;
     off += align_up(r * sizeof(float), 256);
     w.logp = off;
     off += align_up(r * sizeof(float), 256);
-    w.partials = off;
-    if (splits > 1)
-        off += align_up(r * static_cast<size_t>(splits) * 2 * sizeof(float), 256);
-    w.partials_h = off;
-    if (splits > 1)
-        off += align_up(r * static_cast<size_t>(splits) * sizeof(float), 256);
     w.total = off;
     return w;
 }
@@ -97,7 +115,7 @@ gbce_status check_logits(const void *logits, gbce_dtype dtype, int64_t rows, int
         return GBCE_EDTYPE;
     if (row_stride > (INT64_MAX / 8) / rows)
         return GBCE_EINVAL;
-    if (rows * static_cast<int64_t>(split_count(rows, vocab)) > INT32_MAX)
+    if (rows > INT32_MAX / kMaxClusterSplits)  // grid size: rows x slices CTAs
         return GBCE_EINVAL;
     return GBCE_OK;
 }
@@ -176,7 +194,7 @@ gbce_status apply_ce_options(const gbce_ce_options *opt, RowParams &p)
 int ce_stats_mode(const RowParams &p)
 {
     if (p.softcap > 0.0f)
-        return gbce::kModeCeCap;
+        return p.ls_eps != 0.0f ? gbce::kModeCeCapSmooth : gbce::kModeCeCap;
     return p.ls_eps != 0.0f ? gbce::kModeCeSmooth : gbce::kModeCe;
 }
 
@@ -208,12 +226,6 @@ cudaError_t launch_rows(const RowParams &p, gbce_dtype dt, int mode, cudaStream_
                            : gbce::launch_rows<float>(p, mode, s);
 }
 
-cudaError_t launch_combine(const RowParams &p, gbce_dtype dt, int mode, cudaStream_t s)
-{
-    return dt == GBCE_BF16 ? gbce::launch_combine<__nv_bfloat16>(p, mode, s)
-                           : gbce::launch_combine<float>(p, mode, s);
-}
-
 template <typename P>
 P *ws_at(void *ws, size_t off)
 {
@@ -228,7 +240,7 @@ extern "C" {
 
 size_t gbce_workspace_size(int64_t rows, int64_t vocab, int64_t k)
 {
-    (void)k;  // the split partials hold one (max, sum) pair per slice for any k
+    (void)k;  // the workspace holds per-row values only, for any k
     if (rows <= 0 || vocab < 1)
         return 0;
     return ws_layout(rows, vocab).total;
@@ -270,7 +282,6 @@ gbce_status selective_logsoftmax(const void *logits, gbce_dtype dtype, int64_t r
         return GBCE_EINVAL;
     if ((st = check_workspace(workspace, workspace_bytes, rows, vocab)) != GBCE_OK)
         return st;
-    const WsLayout w = ws_layout(rows, vocab);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
     RowParams p = base_params(logits, dtype, rows, vocab, row_stride, temperature, dev_status);
@@ -279,13 +290,8 @@ gbce_status selective_logsoftmax(const void *logits, gbce_dtype dtype, int64_t r
     p.row_mask = row_mask;
     p.logp_out = logp_out;
     p.entropy_out = entropy_out;
-    p.partials = ws_at<float2>(workspace, w.partials);
-    p.partials_h = ws_at<float>(workspace, w.partials_h);
     const int mode = entropy_out != nullptr ? gbce::kModeLogpEnt : gbce::kModeLogp;
-    cudaError_t e = launch_rows(p, dtype, mode, s);
-    if (e == cudaSuccess && p.splits > 1)
-        e = launch_combine(p, dtype, mode, s);
-    return cuda_status(e);
+    return cuda_status(launch_rows(p, dtype, mode, s));
 }
 
 gbce_status selective_logsoftmax_bwd(const void *logits, gbce_dtype dtype, int64_t rows,
@@ -360,13 +366,8 @@ gbce_status ce_fwd(const void *logits, gbce_dtype dtype, int64_t rows, int64_t v
         p.loss_rows = loss_rows;
         p.logp_out = logp_out;
         p.lse_out = lse_out;
-        p.partials = ws_at<float2>(workspace, w.partials);
-        p.partials_h = ws_at<float>(workspace, w.partials_h);
         apply_ce_options(options, p);
-        const int mode = ce_stats_mode(p);
-        e = launch_rows(p, dtype, mode, s);
-        if (e == cudaSuccess && p.splits > 1)
-            e = launch_combine(p, dtype, mode, s);
+        e = launch_rows(p, dtype, ce_stats_mode(p), s);
     }
     int64_t *n_ptr = n_items_out;
     if (n_ptr == nullptr && rows > 0)
@@ -375,7 +376,7 @@ gbce_status ce_fwd(const void *logits, gbce_dtype dtype, int64_t rows, int64_t v
         e = gbce::launch_reduce_loss(loss_rows, labels, rows, ignore_index,
                                      static_cast<int>(reduction), nullptr, n_ptr, loss_out, s);
     else if (e == cudaSuccess && n_items_out != nullptr)
-        e = gbce::launch_count_items(labels, rows, ignore_index, n_items_out, s);
+        e = gbce::launch_count_items(labels, rows, ignore_index, n_items_out, nullptr, s);
     return cuda_status(e);
 }
 
@@ -444,7 +445,7 @@ gbce_status ce_fwd_bwd_fused(const void *logits, gbce_dtype dtype, int64_t rows,
                                          static_cast<int>(reduction), nullptr, n_items_out,
                                          loss_out, s);
         else if (n_items_out != nullptr)
-            e = gbce::launch_count_items(labels, 0, ignore_index, n_items_out, s);
+            e = gbce::launch_count_items(labels, 0, ignore_index, n_items_out, nullptr, s);
         return cuda_status(e);
     }
     if (labels == nullptr || loss_out == nullptr || grad_out == nullptr)
@@ -459,38 +460,38 @@ gbce_status ce_fwd_bwd_fused(const void *logits, gbce_dtype dtype, int64_t rows,
     int64_t *n_ptr = n_items_out != nullptr ? n_items_out : ws_at<int64_t>(workspace, w.count);
     float *loss_rows = reduction == GBCE_NONE ? loss_out : ws_at<float>(workspace, w.loss);
 
-    cudaError_t e = cudaSuccess;
-    if (reduction == GBCE_MEAN || n_items_out != nullptr)
-        e = gbce::launch_count_items(labels, rows, ignore_index, n_ptr, s);
-
     RowParams p = base_params(logits, dtype, rows, vocab, row_stride, temperature, dev_status);
+    // the persistent kernel (all calls but few-row ones) hands out rows from
+    // a ticket that the item count zeroes first
+    const bool persistent = p.splits == 1;
+    p.row_ticket = persistent ? ws_at<int32_t>(workspace, w.ticket) : nullptr;
+    cudaError_t e = cudaSuccess;
+    if (reduction == GBCE_MEAN || n_items_out != nullptr || persistent)
+        e = gbce::launch_count_items(labels, rows, ignore_index, n_ptr, p.row_ticket, s);
+
     p.targets = labels;
     p.ignore_index = ignore_index;
     p.loss_rows = loss_rows;
     p.logp_out = logp_out;
     p.lse_out = lse_out;
-    p.partials = ws_at<float2>(workspace, w.partials);
     p.dlogits = dlogits;
     p.d_stride = dlogits_row_stride;
     p.vec_store = same_vector_phase(logits, row_stride, dlogits, dlogits_row_stride, dtype);
     p.grad_out = grad_out;
     p.reduction = static_cast<int>(reduction);
     p.n_items = n_ptr;
-    p.partials_h = ws_at<float>(workspace, w.partials_h);
     apply_ce_options(options, p);
 
-    if (e == cudaSuccess && p.splits == 1 && p.softcap == 0.0f) {
+    if (e == cudaSuccess && (p.softcap == 0.0f || persistent)) {
+        // many rows: the persistent kernel (soft-capped or not); few rows:
+        // one cluster per row
         e = launch_rows(p, dtype, gbce::kModeFused, s);
     } else if (e == cudaSuccess) {
-        // few rows, or soft-capped logits (where tanh per element, not the
-        // second read, sets the pace): statistics (split and merged when
-        // the rows are few), then a gradient pass
+        // few rows with soft-capped logits: a (split) statistics pass, then
+        // a gradient pass
         float *logp_buf = logp_out != nullptr ? logp_out : ws_at<float>(workspace, w.logp);
         p.logp_out = logp_buf;
-        const int mode = ce_stats_mode(p);
-        e = launch_rows(p, dtype, mode, s);
-        if (e == cudaSuccess && p.splits > 1)
-            e = launch_combine(p, dtype, mode, s);
+        e = launch_rows(p, dtype, ce_stats_mode(p), s);
         p.saved_logp = logp_buf;
         if (e == cudaSuccess)
             e = launch_rows(p, dtype, ce_grad_mode(p), s);

@@ -177,16 +177,22 @@ __device__ __forceinline__ uint32_t cluster_count()
     return r;
 }
 
-// All threads of all CTAs of the cluster; used once, right after barrier
-// initialisation (whose fence.mbarrier_init makes the barriers visible to
-// the cluster), so that no CTA stores into a peer's shared memory before the
-// peer's mbarriers exist.  Every CTA of a cluster is co-scheduled and
-// reaches it without waiting on any data.  The arrive is relaxed: nothing
-// but the barrier initialisation has to be ordered, and that has its fence.
-__device__ __forceinline__ void cluster_sync_all()
+// The cluster barrier in two halves.  Every thread of every CTA arrives
+// once, right after its CTA's mbarriers are initialised (whose
+// fence.mbarrier_init makes them visible to the cluster); the relaxed arrive
+// orders nothing else.  A thread that is about to store into a peer's shared
+// memory first waits, which returns once every non-exited thread of the
+// cluster has arrived -- so no store reaches a peer before the peer's
+// mbarriers exist.  The CTAs of a cluster are co-scheduled and arrive at
+// their start, so the wait does not depend on any data.
+__device__ __forceinline__ void cluster_arrive_relaxed()
 {
-    asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\t"
-                 "barrier.cluster.wait.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait()
+{
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
 }
 
 // Address of the same shared-memory location in CTA `rank` of the cluster.
@@ -197,15 +203,15 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t smem_address, uint32_t 
     return r;
 }
 
-// Store two floats into a peer CTA's shared memory; completion is counted
-// as 8 transaction bytes on the peer's mbarrier at `remote_bar`.
-__device__ __forceinline__ void st_async_pair(uint32_t remote_addr, float a, float b,
-                                              uint32_t remote_bar)
+// Store four floats into a peer CTA's shared memory (16-byte aligned);
+// completion is counted as 16 transaction bytes on the peer's mbarrier at
+// `remote_bar`.
+__device__ __forceinline__ void st_async_v4(uint32_t remote_addr, float4 v, uint32_t remote_bar)
 {
     asm volatile(
-        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(
-            remote_addr),
-        "f"(a), "f"(b), "r"(remote_bar)
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, "
+        "[%5];" ::"r"(remote_addr),
+        "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(remote_bar)
         : "memory");
 }
 
@@ -236,26 +242,6 @@ __device__ __forceinline__ float ex2(float x)
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
-}
-
-// tanh to about 2e-7 relative (the hardware's tanh.approx is good to about
-// 2^-11, far too coarse for a log-probability): below |u| = 0.55 the odd
-// Taylor series of tanh through u^15 (truncation < 5e-8 there), above it
-// 1 - 2 / (e^{2|u|} + 1), which is >= 0.5 there and so loses no digits.
-__device__ __forceinline__ float tanh_acc(float u)
-{
-    const float a = fabsf(u), s = a * a;
-    float p = -929569.0f / 638512875.0f;
-    p = fmaf(p, s, 21844.0f / 6081075.0f);
-    p = fmaf(p, s, -1382.0f / 155925.0f);
-    p = fmaf(p, s, 62.0f / 2835.0f);
-    p = fmaf(p, s, -17.0f / 315.0f);
-    p = fmaf(p, s, 2.0f / 15.0f);
-    p = fmaf(p, s, -1.0f / 3.0f);
-    const float small = fmaf(a * s, p, a);
-    const float e2a = ex2(2.0f * 1.4426950408889634f * a);  // +inf far out: big = 1
-    const float big = 1.0f - __fdividef(2.0f, e2a + 1.0f);
-    return copysignf(a < 0.55f ? small : big, u);
 }
 
 __device__ __forceinline__ float softplus(float a)
@@ -299,7 +285,6 @@ __device__ __forceinline__ float2 fmul2(float2 a, float2 b)
     return d;
 }
 
-// Exact max of two packed bf16 pairs (a NaN operand yields the other one).
 // 1 / x to about 1 ulp (0 for +inf).
 __device__ __forceinline__ float rcp_approx(float x)
 {
@@ -308,30 +293,77 @@ __device__ __forceinline__ float rcp_approx(float x)
     return y;
 }
 
-// tanh_acc on a packed pair: the same two branches in f32x2 arithmetic (the
-// exponential one only when a lane needs it), one selected per lane.
-__device__ __forceinline__ float2 tanh_acc2(float2 u)
+// ------------------------------------------------------------ soft-capping
+//
+// A soft-capped logit is cap * tanh(x / cap).  The few values that set a
+// row's log p to full accuracy -- the row max and the target -- use CUDA's
+// tanhf.  The bulk of a row goes through tanh_pair below, in packed pairs.
+// Written as t = tanh(u), u = x / cap, the capped logit cap * t enters the
+// softmax through the exponent t * (cap * log2(e) / T) + shift, so cap
+// costs no extra multiply.
+
+// Range of the series form: |u| < kCapSeriesBound.
+constexpr float kCapSeriesBound = 0.55f;
+
+// tanh(u) = u P(s), s = u^2, for |u| < kCapSeriesBound, with P(s) = 1 +
+// s Q(s) and Q the cubic fitted to (tanh(u) / u - 1) / s on that range by
+// weighted least squares in relative error (near-minimax): 3.7e-8 relative
+// in exact arithmetic, about 1.5 ulp evaluated in fp32.  The form is odd in
+// u: no abs and no sign fix-up.
+constexpr float kTanhQ0 = -0.3333294657493646f, kTanhQ1 = 0.13320723563804557f,
+                kTanhQ2 = -0.052671713622700365f, kTanhQ3 = 0.016437383467281172f;
+
+// scale * P(s) by Horner in packed pairs, from the pre-scaled coefficients
+// sq[k] = scale * kTanhQk and s0 = scale (4 fused multiply-adds).
+__device__ __forceinline__ float2 tanh_poly_pair(float2 s, const float (&sq)[4], float s0)
 {
-    const float2 a = make_float2(fabsf(u.x), fabsf(u.y));
-    const float2 s = fmul2(a, a);
-    const auto k2 = [](float v) { return make_float2(v, v); };
-    float2 p = k2(-929569.0f / 638512875.0f);
-    p = ffma2(p, s, k2(21844.0f / 6081075.0f));
-    p = ffma2(p, s, k2(-1382.0f / 155925.0f));
-    p = ffma2(p, s, k2(62.0f / 2835.0f));
-    p = ffma2(p, s, k2(-17.0f / 315.0f));
-    p = ffma2(p, s, k2(2.0f / 15.0f));
-    p = ffma2(p, s, k2(-1.0f / 3.0f));
-    const float2 small = ffma2(fmul2(a, s), p, a);
-    if (fmaxf(a.x, a.y) < 0.55f)  // both lanes on the series: skip the exponential
-        return make_float2(copysignf(small.x, u.x), copysignf(small.y, u.y));
-    const float2 e = fmul2(a, k2(2.0f * 1.4426950408889634f));
-    const float2 d = fadd2(make_float2(ex2(e.x), ex2(e.y)), k2(1.0f));
-    const float2 big = ffma2(k2(-2.0f), make_float2(rcp_approx(d.x), rcp_approx(d.y)), k2(1.0f));
-    return make_float2(copysignf(a.x < 0.55f ? small.x : big.x, u.x),
-                       copysignf(a.y < 0.55f ? small.y : big.y, u.y));
+    float2 h = make_float2(sq[3], sq[3]);
+    h = ffma2(h, s, make_float2(sq[2], sq[2]));
+    h = ffma2(h, s, make_float2(sq[1], sq[1]));
+    h = ffma2(h, s, make_float2(sq[0], sq[0]));
+    return ffma2(h, s, make_float2(s0, s0));
 }
 
+__device__ __forceinline__ float2 tanh_series_pair(float2 u)
+{
+    const float q[4] = {kTanhQ0, kTanhQ1, kTanhQ2, kTanhQ3};
+    return fmul2(u, tanh_poly_pair(fmul2(u, u), q, 1.0f));
+}
+
+// tanh(u) for any u, one lane at a time: the series below kCapSeriesBound,
+// else t = 1 - 2 r with r = 1 / (e + 1), e = e^{2|u|} (t >= 0.5 there, so
+// nothing cancels; e = +inf gives t = 1).  *chain receives 1 - t^2, as
+// 4 e r^2 beyond the series range: it keeps its relative accuracy when t
+// nears 1.
+__device__ __forceinline__ float tanh_lane(float u, float &chain)
+{
+    const float a = fabsf(u);
+    if (a < kCapSeriesBound) {
+        const float2 t = tanh_series_pair(make_float2(u, u));
+        chain = fmaf(-t.x, t.x, 1.0f);
+        return t.x;
+    }
+    const float e = ex2(2.0f * 1.4426950408889634f * a);
+    const float r = rcp_approx(e + 1.0f);
+    chain = e < 1e30f ? 4.0f * e * r * r : 0.0f;
+    return copysignf(fmaf(-2.0f, r, 1.0f), u);
+}
+
+__device__ __forceinline__ uint32_t bf16x2_min(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("min.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+__device__ __forceinline__ float fmin3(float a, float b, float c)
+{
+    float d;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// Exact max / min of two packed bf16 pairs (a NaN operand yields the other one).
 __device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b)
 {
     uint32_t d;
@@ -485,6 +517,22 @@ struct OnlineStats {
         }
     }
 
+    // Add 2^z for four precomputed exponents z = x c - m c in two pairs.
+    __device__ __forceinline__ void add_exponent_pairs(float2 zp, float2 zq)
+    {
+        sa = fadd2(sa, make_float2(ex2(zp.x), ex2(zp.y)));
+        sb = fadd2(sb, make_float2(ex2(zq.x), ex2(zq.y)));
+    }
+
+    // SUMX: add two pairs of logits to the plain sums.
+    __device__ __forceinline__ void sumx_pairs(float2 p, float2 q)
+    {
+        if (SUMX) {
+            xa = fadd2(xa, p);
+            xb = fadd2(xb, q);
+        }
+    }
+
     // Fold N unpacked values (masked columns already -inf).
     template <int N>
     __device__ __forceinline__ void add(const float (&f)[N], float vmax, float c)
@@ -585,6 +633,39 @@ __device__ __forceinline__ void merge_max_sum_h(float &m, float &s, float &h, fl
     s = __fadd_rn(sa, sb);
     h = __fadd_rn(ha, hb);
     m = M;
+}
+
+// What the third accumulator h of a row state (m, s, h) holds: nothing, the
+// entropy moment sum 2^z z (rescaled with the max), or a plain sum (of raw
+// logits, for label smoothing).
+enum StateH : int { kHNone = 0, kHMoment = 1, kHSum = 2 };
+
+// Merge two row states with the same scale c; exactly commutative.
+template <int HK>
+__device__ __forceinline__ void merge_state(float &m, float &s, float &h, float m2, float s2,
+                                            float h2, float c)
+{
+    if (HK == kHMoment) {
+        merge_max_sum_h(m, s, h, m2, s2, h2, c);
+    } else {
+        merge_max_sum(m, s, m2, s2, c);
+        if (HK == kHSum)
+            h = __fadd_rn(h, h2);
+    }
+}
+
+// Butterfly merge over the 32 lanes of a warp.  Because merge_state is
+// exactly commutative, every lane ends with the same bits.
+template <int HK>
+__device__ __forceinline__ void warp_merge_state(float &m, float &s, float &h, float c)
+{
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
+        const float s2 = __shfl_xor_sync(0xffffffffu, s, off);
+        const float h2 = HK != kHNone ? __shfl_xor_sync(0xffffffffu, h, off) : 0.0f;
+        merge_state<HK>(m, s, h, m2, s2, h2, c);
+    }
 }
 
 // log p_t from the others' (m, s) and the target logit, all in raw logit

@@ -10,6 +10,10 @@ namespace gbce {
 // Counts every kernel the library enqueues (see gbce_kernel_launches()).
 void note_launches(int n);
 
+// Streaming multiprocessors of the current device (cached per device; 0 if
+// the runtime cannot say).
+int device_sm_count();
+
 // What a row-kernel launch does with each (row, vocab slice) work unit.
 enum Mode : int {
     kModeLogp = 0,   // selective log-softmax statistics (K gathered indices)
@@ -20,8 +24,9 @@ enum Mode : int {
     kModeLogpEnt = 5,   // kModeLogp plus the entropy of each row
     kModeLogpEntGrad = 6,  // kModeLogpGrad plus the gradient of the row entropy
     kModeCeSmooth = 7,     // kModeCe plus the sum of each row's logits (label smoothing)
-    kModeCeCap = 8,        // kModeCeSmooth on soft-capped logits cap * tanh(x / cap)
+    kModeCeCap = 8,        // kModeCe on soft-capped logits cap * tanh(x / cap)
     kModeGradCap = 9,      // kModeGrad on soft-capped logits, with the chain factor
+    kModeCeCapSmooth = 10,  // kModeCeCap plus the sum of each row's capped logits
 };
 
 struct RowParams {
@@ -38,15 +43,12 @@ struct RowParams {
     float ls_eps;  // CE label smoothing (0: none)
     int dft;       // CE: weight each row's loss and gradient by its detached p_y
     float softcap, inv_cap;  // CE logit soft-capping (kModeCeCap / kModeGradCap)
-    int splits;  // vocab slices per row (1 = the CTA finalizes the row itself)
+    int splits;  // vocab slices per row: 1, or the CTAs of a row's cluster (<= 8)
 
     float *logp_out;   // kModeLogp: [rows, k]; CE modes: [rows] or null
     float *loss_rows;  // CE modes: [rows]
     float *lse_out;    // CE modes: [rows] or null
-    float2 *partials;  // [rows * splits] (max, sum) when splits > 1
     float *entropy_out;  // kModeLogpEnt: [rows]
-    float *partials_h;   // splits > 1: [rows * splits] sum 2^z z (kModeLogpEnt) or
-                         // sum of logits (kModeCeSmooth)
 
     void *dlogits;  // kModeGrad / kModeFused
     int64_t d_stride;
@@ -59,19 +61,17 @@ struct RowParams {
     const float *saved_entropy;  // kModeLogpEntGrad: [rows] H from the forward
 
     int32_t *dev_status;
+    int32_t *row_ticket;  // persistent fused kernel: rows handed out beyond the first wave
 };
 
 // Row kernel (one CTA per work unit) for logit type T (float / bf16).
 template <typename T>
 cudaError_t launch_rows(const RowParams &p, int mode, cudaStream_t stream);
 
-// Merge per-slice partials and finalize the row outputs (splits > 1).
-template <typename T>
-cudaError_t launch_combine(const RowParams &p, int mode, cudaStream_t stream);
-
-// n_items = #(labels != ignore_index) into *n_out (one CTA).
+// n_items = #(labels != ignore_index) into *n_out (one CTA); also zeroes
+// *zero_out when it is non-null (the persistent kernel's row ticket).
 cudaError_t launch_count_items(const int64_t *labels, int64_t rows, int64_t ignore_index,
-                               int64_t *n_out, cudaStream_t stream);
+                               int64_t *n_out, int32_t *zero_out, cudaStream_t stream);
 
 // loss_out[0] = sum (SUM) or sum / n (MEAN, 0 when n == 0) of loss_rows in a
 // fixed order with fp64 accumulation; when count_into is non-null the item

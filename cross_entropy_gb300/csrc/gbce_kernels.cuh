@@ -23,7 +23,9 @@
 //    logits, and the gradient is g*softmax - g*onehot in a separate buffer:
 //    ms-swift PR #10353, "PR information";
 //  * a slice split with a later merge of (max, sum) partials: the split
-//    partial/combine kernels of the unsloth-zoo #2080 commit ("Fix");
+//    partial/combine kernels of the unsloth-zoo #2080 commit ("Fix"), here
+//    the CTAs of one thread-block cluster swapping their partials through
+//    distributed shared memory instead of a second kernel;
 //  * the row entropy taken around the same others' sum, its gradient, label
 //    smoothing (the -expm1 label term covers it) and the soft-capped logits
 //    of the fused losses' options: the unsloth-zoo #2080 commit ("Fix",
@@ -154,6 +156,11 @@ template <> struct FastVec<__nv_bfloat16> {
         return fmaxf(__uint_as_float(m << 16), __uint_as_float(m & 0xffff0000u));
     }
     __device__ static __forceinline__ float vmax(const uint4 &a) { return unpack_max(pmax(a)); }
+    __device__ static __forceinline__ float vmin(const uint4 &a)
+    {
+        const uint32_t m = bf16x2_min(bf16x2_min(a.x, a.y), bf16x2_min(a.z, a.w));
+        return fminf(__uint_as_float(m << 16), __uint_as_float(m & 0xffff0000u));
+    }
     __device__ static __forceinline__ float vmax(const uint4 &a, const uint4 &b)
     {
         return unpack_max(bf16x2_max(pmax(a), pmax(b)));
@@ -170,6 +177,11 @@ template <> struct FastVec<float> {
     __device__ static __forceinline__ float vmax(const uint4 &a)
     {
         return fmaxf(fmax3(__uint_as_float(a.x), __uint_as_float(a.y), __uint_as_float(a.z)),
+                     __uint_as_float(a.w));
+    }
+    __device__ static __forceinline__ float vmin(const uint4 &a)
+    {
+        return fminf(fmin3(__uint_as_float(a.x), __uint_as_float(a.y), __uint_as_float(a.z)),
                      __uint_as_float(a.w));
     }
     __device__ static __forceinline__ float vmax(const uint4 &a, const uint4 &b)
@@ -200,6 +212,11 @@ template <> struct CapVec<__nv_bfloat16> {
         x[2] = bf16x2_to_float2(a.z);
         x[3] = bf16x2_to_float2(a.w);
     }
+    __device__ static __forceinline__ uint4 pack(const float2 (&d)[4])
+    {
+        return make_uint4(float2_to_bf16x2(d[0]), float2_to_bf16x2(d[1]), float2_to_bf16x2(d[2]),
+                          float2_to_bf16x2(d[3]));
+    }
 };
 
 template <> struct CapVec<float> {
@@ -209,29 +226,144 @@ template <> struct CapVec<float> {
         x[0] = make_float2(__uint_as_float(a.x), __uint_as_float(a.y));
         x[1] = make_float2(__uint_as_float(a.z), __uint_as_float(a.w));
     }
+    __device__ static __forceinline__ uint4 pack(const float2 (&d)[2])
+    {
+        return make_uint4(__float_as_uint(d[0].x), __float_as_uint(d[0].y),
+                          __float_as_uint(d[1].x), __float_as_uint(d[1].y));
+    }
 };
 
-// Fold one soft-capped vector that holds no target: the running max comes
-// from the raw vector's exact max (tanh is increasing, so the capped max is
-// the cap of the raw max, taken only when the raw running max mraw rises),
-// the exponentials and the sum of capped logits from packed pairs.
-template <typename T, typename S>
-__device__ __forceinline__ void stats_capped(S &st, float &mraw, const uint4 &a, float c,
-                                             float cap, float inv_cap)
+// Soft-capping constants of a row pass: cap, 1 / cap, the exponent scale
+// capc = cap * c (c = log2(e) / T; a capped logit cap * t enters the
+// exponent as t * capc), and capc * kTanhQ, the coefficients that give the
+// capped logit's exponent as u * (capc P(s)) in one polynomial.
+struct CapConsts {
+    float cap, inv_cap, capc;
+    float aq[4];
+};
+
+__device__ __forceinline__ CapConsts cap_consts(float cap, float inv_cap, float c)
+{
+    CapConsts k;
+    k.cap = cap;
+    k.inv_cap = inv_cap;
+    k.capc = cap * c;
+    k.aq[0] = k.capc * kTanhQ0;
+    k.aq[1] = k.capc * kTanhQ1;
+    k.aq[2] = k.capc * kTanhQ2;
+    k.aq[3] = k.capc * kTanhQ3;
+    return k;
+}
+
+// Whether every logit of a 16-byte vector is inside the series range of
+// tanh_poly_pair (|x| < kCapSeriesBound * cap), from its raw max and min.
+template <typename T>
+__device__ __forceinline__ bool vector_in_series_range(const uint4 &a, float vmax, float cap)
+{
+    return fmaxf(vmax, -FastVec<T>::vmin(a)) < kCapSeriesBound * cap;
+}
+
+// Fold NV soft-capped vectors that hold no target (one, or a thread's two
+// consecutive vectors): the running max comes from the raw vectors' exact
+// max (tanh is increasing, so the capped max is the cap of the raw max,
+// taken only when the raw running max mraw rises); in the series range each
+// pair's exponent is u * (capc P(s)) - m c, one polynomial (u = x / cap,
+// s = u^2); outside it, tanh one lane at a time.
+template <typename T, int NV, typename S>
+__device__ __forceinline__ void stats_capped(S &st, float &mraw, const uint4 (&a)[NV], float c,
+                                             const CapConsts &k)
 {
     constexpr int NP = CapVec<T>::kPairs;
-    const float vmax = FastVec<T>::vmax(a);
+    const float vmax = NV == 2 ? FastVec<T>::vmax(a[0], a[NV - 1]) : FastVec<T>::vmax(a[0]);
     if (vmax > mraw || mraw != mraw) {  // (a NaN max keeps re-raising: NaN results)
         mraw = vmax;
-        st.raise_to(cap * tanh_acc(vmax * inv_cap), c);  // >= -cap, never -inf
+        st.raise_to(k.cap * tanhf(vmax * k.inv_cap), c);  // >= -cap, never -inf
     }
-    float2 x[NP];
-    CapVec<T>::pairs(a, x);
-    const float2 ic = make_float2(inv_cap, inv_cap), cc = make_float2(cap, cap);
+    float vmin = FastVec<T>::vmin(a[0]);
+    if (NV == 2)
+        vmin = fminf(vmin, FastVec<T>::vmin(a[NV - 1]));
+    const float2 ic = make_float2(k.inv_cap, k.inv_cap);
+    const float2 kk = make_float2(st.nmc, st.nmc);
+    const bool series = fmaxf(vmax, -vmin) < kCapSeriesBound * k.cap;
 #pragma unroll
-    for (int i = 0; i < NP; i += 2)
-        st.add_pairs(fmul2(tanh_acc2(fmul2(x[i], ic)), cc),
-                     fmul2(tanh_acc2(fmul2(x[i + 1], ic)), cc), c);
+    for (int v = 0; v < NV; ++v) {
+        float2 x[NP];
+        CapVec<T>::pairs(a[v], x);
+#pragma unroll
+        for (int i = 0; i < NP; i += 2) {
+            float2 z[2];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const float2 u = fmul2(x[i + j], ic);
+                if (series) {
+                    const float2 A = tanh_poly_pair(fmul2(u, u), k.aq, k.capc);
+                    if (S::kSumx) {
+                        const float2 zc = fmul2(u, A);  // capc * t
+                        z[j] = fadd2(zc, kk);
+                        st.sumx_pairs(fmul2(zc, make_float2(1.0f / c, 1.0f / c)),
+                                      make_float2(0.0f, 0.0f));
+                    } else {
+                        z[j] = ffma2(u, A, kk);
+                    }
+                } else {
+                    float cx, cy;
+                    const float2 t = make_float2(tanh_lane(u.x, cx), tanh_lane(u.y, cy));
+                    z[j] = ffma2(t, make_float2(k.capc, k.capc), kk);
+                    if (S::kSumx)
+                        st.sumx_pairs(fmul2(t, make_float2(k.cap, k.cap)), make_float2(0.0f, 0.0f));
+                }
+            }
+            st.add_exponent_pairs(z[0], z[1]);
+        }
+    }
+}
+
+// Fold one soft-capped vector that holds a target column (masked), unpacked.
+template <typename T, int KMAX, typename S>
+__device__ __forceinline__ void stats_capped_target(S &st, const uint4 &raw, int32_t col0,
+                                                    const int32_t (&tg)[KMAX], float c,
+                                                    const CapConsts &k)
+{
+    constexpr int VEC = Elem<T>::kVec;
+    float f[VEC];
+    Elem<T>::unpack(raw, f);
+    float vm = kNegInf;
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) {
+        f[e] = k.cap * tanhf(f[e] * k.inv_cap);
+        st.sumx_add(f[e]);
+        if (is_target<KMAX>(tg, col0 + e))
+            f[e] = kNegInf;
+        vm = fmaxf(vm, f[e]);
+    }
+    st.template add<VEC>(f, vm, c);
+}
+
+// One thread's NPT vectors of a full chunk (thread tid's vectors vb0 + tid +
+// u * nc), soft-capped: two at a time, the pair that holds a target (nt) one
+// at a time with the target masked.
+template <typename T, int KMAX, int NPT, typename S>
+__device__ __forceinline__ void stats_capped_chunk(S &st, float &mraw, const uint4 (&raw)[NPT],
+                                                   int32_t vb0, int32_t col0, int32_t &nt,
+                                                   const int32_t (&tg)[KMAX],
+                                                   const int32_t (&tv)[KMAX], int64_t v0,
+                                                   int64_t v1, int tid, int nc, bool check,
+                                                   float c, const CapConsts &k)
+{
+    constexpr int VEC = Elem<T>::kVec;
+    static_assert(NPT % 2 == 0, "vectors go in pairs");
+#pragma unroll
+    for (int u = 0; u < NPT; u += 2) {
+        const int32_t va = vb0 + tid + u * nc, vb = va + nc;
+        if (check && static_cast<uint32_t>(nt - va) <= static_cast<uint32_t>(vb - va)) {
+            stats_capped_target<T, KMAX>(st, raw[u], col0 + va * VEC, tg, c, k);
+            stats_capped_target<T, KMAX>(st, raw[u + 1], col0 + vb * VEC, tg, c, k);
+            nt = next_target_vector<KMAX>(tv, v0, v1, tid, nc, vb);
+            continue;
+        }
+        const uint4 two[2] = {raw[u], raw[u + 1]};
+        stats_capped<T, 2>(st, mraw, two, c, k);
+    }
 }
 
 // Fold body vectors va (and vb, the same thread's next vector) of a row;
@@ -313,6 +445,162 @@ __device__ __forceinline__ float rescan_entropy_moment(const T *row, const RowGe
             term(f[e], g.head + vb * VEC + e);
     }
     return h;
+}
+
+// ------------------------------------------- whole-row passes (off the hot path)
+//
+// A few rows need a second look at all of their columns after (or before)
+// the pipelined sweep: the entropy of a confident row whose dominant column
+// is not the reference column.  These passes read the row from global
+// memory (16-byte vectors for the aligned body) with every consumer thread
+// of the CTA and synchronize on named barrier 1; they never run for the
+// other rows.
+
+// Calls f(x, col) for every column that consumer thread `tid` of `nc` owns
+// in a whole-row pass: its share of the scalar head and tail, and the body
+// vectors tid, tid + nc, ...
+template <typename T, typename F>
+__device__ __forceinline__ void for_each_own_column(const T *row, const RowGeom &g, int64_t V,
+                                                    int tid, int nc, F &&f)
+{
+    using E = Elem<T>;
+    constexpr int VEC = E::kVec;
+    for (int64_t e = tid; e < g.head; e += nc)
+        f(E::load(row + e), e);
+    for (int64_t e = g.tail0 + tid; e < V; e += nc)
+        f(E::load(row + e), e);
+    const uint4 *body = reinterpret_cast<const uint4 *>(row + g.head);
+    for (int64_t vb = tid; vb < g.nvec; vb += nc) {
+        float v[VEC];
+        E::unpack(ld_nc_v4(body + vb), v);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e)
+            f(v[e], g.head + vb * VEC + e);
+    }
+}
+
+// The largest logit M of a row and the first column d holding it, found by
+// NCW consumer warps together (NCW == 1: one warp, no shared memory or
+// barrier); every participating thread gets both.
+template <typename T, int NCW>
+__device__ void row_argmax(const T *row, const RowGeom &g, int64_t V, int tid, float *red_m,
+                           int32_t *red_i, float &M, int32_t &d)
+{
+    constexpr int NC = NCW * 32;
+    const int warp = tid >> 5, lane = tid & 31;
+    const auto better = [](float xa, int32_t ia, float xb, int32_t ib) {
+        return xb > xa || (xb == xa && ib < ia);
+    };
+    float bm = kNegInf;
+    int32_t bi = INT32_MAX;
+    for_each_own_column<T>(row, g, V, tid, NC, [&](float x, int64_t col) {
+        if (better(bm, bi, x, static_cast<int32_t>(col))) {
+            bm = x;
+            bi = static_cast<int32_t>(col);
+        }
+    });
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, bm, off);
+        const int32_t i2 = __shfl_xor_sync(0xffffffffu, bi, off);
+        if (better(bm, bi, m2, i2)) {
+            bm = m2;
+            bi = i2;
+        }
+    }
+    if (NCW == 1) {
+        M = bm;
+        d = bi;
+        return;
+    }
+    if (lane == 0) {
+        red_m[warp] = bm;
+        red_i[warp] = bi;
+    }
+    named_sync(1, NC);
+    bm = kNegInf;
+    bi = INT32_MAX;
+    for (int w = 0; w < NCW; ++w)
+        if (better(bm, bi, red_m[w], red_i[w])) {
+            bm = red_m[w];
+            bi = red_i[w];
+        }
+    named_sync(1, NC);  // the scratch arrays are free again
+    M = bm;
+    d = bi;
+}
+
+// Entropy of a row with column d (logit xd) as the reference column of
+// finalize_entropy: the state (m, s, h) of every other column from a
+// whole-row pass by NCW warps (NCW == 1: one warp, no shared memory or
+// barrier).  For a confident row whose dominant column d is not the column
+// the sweep left out, this is what keeps 1 - p_d (and so the entropy) from
+// rounding: the sweep's s = 1 + (everything else) cannot hold the rest when
+// it is below fp32's resolution at 1.  Valid in thread 0 of the group.
+template <typename T, int NCW>
+__device__ float entropy_around(const T *row, const RowGeom &g, int64_t V, int32_t d, float xd,
+                                float c, float temperature, int tid, float *red_m, float *red_s,
+                                float *red_h)
+{
+    constexpr int NC = NCW * 32;
+    const int warp = tid >> 5, lane = tid & 31;
+    OnlineStats<true> st;
+    for_each_own_column<T>(row, g, V, tid, NC,
+                           [&](float x, int64_t col) { st.add1(col == d ? kNegInf : x, c); });
+    float m = st.m, s = st.sum(), h = st.hsum();
+    warp_merge_state<kHMoment>(m, s, h, c);
+    if (NCW == 1)
+        return finalize_entropy(m, s, h, xd, temperature);
+    if (lane == 0) {
+        red_m[warp] = m;
+        red_s[warp] = s;
+        red_h[warp] = h;
+    }
+    named_sync(1, NC);
+    float H = 0.0f;
+    if (warp == 0) {
+        m = lane < NCW ? red_m[lane] : kNegInf;
+        s = lane < NCW ? red_s[lane] : 0.0f;
+        h = lane < NCW ? red_h[lane] : 0.0f;
+        warp_merge_state<kHMoment>(m, s, h, c);
+        H = finalize_entropy(m, s, h, xd, temperature);
+    }
+    named_sync(1, NC);
+    return H;
+}
+
+// Q = sum_{j != d} p_j (x_d - x_j) / T over a row, with p_j = exp((x_j - x_t)/T
+// + log p_t) taken from a column t whose log p is known accurately.  For the
+// dominant column d, Q equals H + log p_d (H the row entropy), but as a sum
+// of non-negative terms: the gradient of the entropy at d needs that value,
+// and H + log p_d cancels when p_d is near 1.  Every consumer thread gets Q.
+template <typename T, int NCW>
+__device__ float entropy_gap(const T *row, const RowGeom &g, int64_t V, int32_t d, float xd,
+                             float xt, float lpt, float c, float inv_t, int tid, float *red)
+{
+    constexpr int NC = NCW * 32;
+    const int warp = tid >> 5, lane = tid & 31;
+    // 2^(z + 32), z = log2 p_j: p_j down to 2^-158 although ex2 flushes below 2^-126
+    const float kb = fmaf(lpt, kLog2e, 32.0f);
+    float acc = 0.0f;
+    for_each_own_column<T>(row, g, V, tid, NC, [&](float x, int64_t col) {
+        if (col != d) {
+            const float pj = ex2(fmaf(x - xt, c, kb));
+            if (pj > 0.0f || pj != pj)  // a -inf logit adds 0 (not 0 * inf); NaN stays
+                acc = fmaf(pj, (xd - x) * inv_t, acc);
+        }
+    });
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, off));
+    if (lane == 0)
+        red[warp] = acc;
+    named_sync(1, NC);
+    float q = 0.0f;
+    for (int w = 0; w < NCW; ++w)
+        q += red[w];
+    named_sync(1, NC);
+    return q * 0x1p-32f;
 }
 
 // Per-row constants of the gradient pass.  The exponent carries an offset
@@ -509,54 +797,45 @@ template <> struct GradVec<float> {
 };
 
 // Gradient of one soft-capped vector that does not hold the label, packed:
-// element j is fma(gs, 2^z', c0) * (1 - t^2), t = tanh(x / cap), z' the
-// exponent of the uncapped formula on the capped logit cap * t.
+// element j is fma(gs, 2^z, c0) * (1 - t^2), t = tanh(x_j / cap), with the
+// exponent z = t * capc + kbx of the uncapped formula on the capped logit
+// (kbx from the capped label logit).  In the series range it is evaluated
+// as (-gs 2^z - c0)(t^2 - 1): the sign goes into the constants, so the chain
+// factor is one fused multiply-add.
 template <typename T>
-__device__ __forceinline__ uint4 grad_capped(const uint4 &a, const GradConsts &k, float cap,
-                                             float inv_cap);
-
-template <>
-__device__ __forceinline__ uint4 grad_capped<__nv_bfloat16>(const uint4 &a, const GradConsts &k,
-                                                           float cap, float inv_cap)
+__device__ __forceinline__ uint4 grad_capped(const uint4 &a, const GradConsts &k,
+                                             const CapConsts &cp)
 {
-    float2 x[4];
-    CapVec<__nv_bfloat16>::pairs(a, x);
-    const float2 ic = make_float2(inv_cap, inv_cap), cc = make_float2(cap, cap);
-    const float2 nn = make_float2(k.nxy, k.nxy), kc = make_float2(k.c, k.c);
-    const float2 kb = make_float2(k.kb, k.kb), gs = make_float2(k.gs, k.gs);
-    const float2 c0 = make_float2(k.c0, k.c0), one = make_float2(1.0f, 1.0f);
-    uint32_t o[4];
+    constexpr int NP = CapVec<T>::kPairs;
+    float2 x[NP];
+    CapVec<T>::pairs(a, x);
+    const float2 ic = make_float2(cp.inv_cap, cp.inv_cap);
+    const float2 cc = make_float2(cp.capc, cp.capc), kk = make_float2(k.kbx, k.kbx);
+    float2 d[NP];
+    if (vector_in_series_range<T>(a, FastVec<T>::vmax(a), cp.cap)) {
+        const float q[4] = {kTanhQ0, kTanhQ1, kTanhQ2, kTanhQ3};
+        const float2 ngs = make_float2(-k.gs, -k.gs), nc0 = make_float2(-k.c0, -k.c0);
+        const float2 m1 = make_float2(-1.0f, -1.0f);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float2 t = tanh_acc2(fmul2(x[i], ic));
-        const float2 chain = ffma2(make_float2(-t.x, -t.y), t, one);
-        const float2 z = ffma2(fadd2(fmul2(t, cc), nn), kc, kb);
-        const float2 d = ffma2(make_float2(ex2(z.x), ex2(z.y)), gs, c0);
-        o[i] = float2_to_bf16x2(fmul2(d, chain));
-    }
-    return make_uint4(o[0], o[1], o[2], o[3]);
-}
-
-template <>
-__device__ __forceinline__ uint4 grad_capped<float>(const uint4 &a, const GradConsts &k, float cap,
-                                                   float inv_cap)
-{
-    float2 x[2];
-    CapVec<float>::pairs(a, x);
-    const float2 ic = make_float2(inv_cap, inv_cap), cc = make_float2(cap, cap);
-    const float2 nn = make_float2(k.nxy, k.nxy), kc = make_float2(k.c, k.c);
-    const float2 kb = make_float2(k.kb, k.kb), gs = make_float2(k.gs, k.gs);
-    const float2 c0 = make_float2(k.c0, k.c0), one = make_float2(1.0f, 1.0f);
-    float2 d[2];
+        for (int i = 0; i < NP; ++i) {
+            const float2 u = fmul2(x[i], ic);
+            const float2 t = fmul2(u, tanh_poly_pair(fmul2(u, u), q, 1.0f));
+            const float2 z = ffma2(t, cc, kk);
+            const float2 e = make_float2(ex2(z.x), ex2(z.y));
+            d[i] = fmul2(ffma2(e, ngs, nc0), ffma2(t, t, m1));
+        }
+    } else {
+        const float2 gs = make_float2(k.gs, k.gs), c0 = make_float2(k.c0, k.c0);
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const float2 t = tanh_acc2(fmul2(x[i], ic));
-        const float2 chain = ffma2(make_float2(-t.x, -t.y), t, one);
-        const float2 z = ffma2(fadd2(fmul2(t, cc), nn), kc, kb);
-        d[i] = fmul2(ffma2(make_float2(ex2(z.x), ex2(z.y)), gs, c0), chain);
+        for (int i = 0; i < NP; ++i) {
+            const float2 u = fmul2(x[i], ic);
+            float cx, cy;
+            const float2 t = make_float2(tanh_lane(u.x, cx), tanh_lane(u.y, cy));
+            const float2 z = ffma2(t, cc, kk);
+            d[i] = fmul2(ffma2(make_float2(ex2(z.x), ex2(z.y)), gs, c0), make_float2(cx, cy));
+        }
     }
-    return make_uint4(__float_as_uint(d[0].x), __float_as_uint(d[0].y), __float_as_uint(d[1].x),
-                      __float_as_uint(d[1].y));
+    return CapVec<T>::pack(d);
 }
 
 // log p of target k, whose "others" are every column outside the target set
@@ -585,14 +864,21 @@ __device__ __forceinline__ float logp_with_targets(float mS, float sS, const int
 // Entropy of a row from the state (mS, sS, hS) of every column outside the
 // target set S: the distinct members of S other than the first index are
 // folded in, and the first index is the reference column of
-// finalize_entropy (a confident row's sampled token is its dominant column).
-// NaN when the first index is out of range.
+// finalize_entropy.  That is accurate to fp32 rounding unless the row is
+// confident in another column d: the others' max m lies above x_t0 and the
+// others' sum s = 1 + rest (d's own term is the 1) has rest < 2^-5.  Then
+// 1 + rest keeps only the rest's leading digits, the entropy (about rest *
+// log(1/rest)) inherits their loss, and the caller recomputes it around d
+// (entropy_around).  With rest >= 2^-5 the absolute error of log s, about
+// 1e-7, stays below 1e-5 of the entropy.  NaN when the first index is out
+// of range.
 template <int KMAX>
 __device__ __forceinline__ float entropy_with_targets(float mS, float sS, float hS,
                                                       const int32_t *tg, const float *xt, int K,
-                                                      float c, float T)
+                                                      float c, float T, bool &rescan)
 {
     const int32_t t0 = tg[0];
+    rescan = false;
     if (t0 < 0)
         return __int_as_float(0x7fc00000);
     float m = mS, s = sS, h = hS;
@@ -606,6 +892,7 @@ __device__ __forceinline__ float entropy_with_targets(float mS, float sS, float 
         if (!dup)
             merge_max_sum_h(m, s, h, xt[j], 1.0f, 0.0f, c);
     }
+    rescan = m > xt[0] && s < 1.03125f && isfinite(m);
     return finalize_entropy(m, s, h, xt[0], T);
 }
 
@@ -663,15 +950,21 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
     constexpr bool kSelGrad = (MODE == kModeLogpGrad || MODE == kModeLogpEntGrad);
     constexpr bool kEntGrad = (MODE == kModeLogpEntGrad);
     constexpr bool kCeGrad = (MODE == kModeGrad || MODE == kModeGradCap);  // ce_bwd
-    constexpr bool kCap = (MODE == kModeCeCap || MODE == kModeGradCap);    // soft-capped
+    constexpr bool kCap = (MODE == kModeCeCap || MODE == kModeCeCapSmooth ||
+                           MODE == kModeGradCap);  // soft-capped logits
     constexpr bool kStats = (!kCeGrad && !kSelGrad);
     constexpr bool kGrad = (kCeGrad || MODE == kModeFused || kSelGrad);
     constexpr bool kEnt = (MODE == kModeLogpEnt);                  // + row entropy
     constexpr bool kLogpFwd = (MODE == kModeLogp || kEnt);         // log p of K indices
     constexpr bool kGather = (kLogpFwd || kSelGrad);  // K indices
-    constexpr bool kSumx = (MODE == kModeCeSmooth || MODE == kModeCeCap);  // + sum of logits
+    // + sum of logits (label smoothing; the fused mode runs only for few rows,
+    // where the extra add costs nothing)
+    constexpr bool kSumx =
+        (MODE == kModeCeSmooth || MODE == kModeCeCapSmooth || MODE == kModeFused);
+    constexpr int kH = kEnt ? kHMoment : (kSumx ? kHSum : kHNone);  // what h holds
     // a logit as the softmax sees it (soft-capped in the capped modes)
-    const auto capped = [&](float x) { return kCap ? p.softcap * tanh_acc(x * p.inv_cap) : x; };
+    const auto capped = [&](float x) { return kCap ? p.softcap * tanhf(x * p.inv_cap) : x; };
+    const CapConsts capk = cap_consts(p.softcap, p.inv_cap, p.c);
     constexpr int kPasses = (MODE == kModeFused) ? 2 : 1;
 
     extern __shared__ __align__(128) uint8_t dyn_smem[];
@@ -680,14 +973,15 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
     __shared__ uint64_t full_bar[kStages];
     __shared__ uint64_t empty_bar[kStages];
     __shared__ float red_m[NCW], red_s[NCW], red_h[NCW];
+    __shared__ int32_t red_i[NCW];
     __shared__ float s_xt[KMAX];
     __shared__ float s_dt[KMAX];       // kModeLogpGrad: gradient at each gathered column
     __shared__ float s_G, s_lp0;       // kModeLogpGrad: sum of upstream, log p of index 0
     __shared__ float s_gH, s_H;        // kModeLogpEntGrad: dL/dH and H of the row
     __shared__ int32_t s_tg[KMAX];
     __shared__ float bc_m, bc_s, bc_h, bc_logp;
-    __shared__ uint64_t xbar;                   // fused, cluster of CTAs per row
-    __shared__ float2 xchg[kMaxClusterCtas];    // every CTA's (max, sum) partial
+    __shared__ uint64_t xbar;                   // cluster of CTAs per row: partials landed
+    __shared__ __align__(16) float4 xchg[kMaxClusterCtas];  // every CTA's (m, s, h) partial
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -703,17 +997,20 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
     int32_t y = -1;
     int state = 0;  // 0 live, 1 skipped (ignored label / masked row), 2 bad label / index
     if (kGather) {
-        if (p.row_mask != nullptr && p.row_mask[r] == 0)
-            state = 1;
+        // (the mask and the indices are read together: one memory latency)
         bool any_bad = false;
 #pragma unroll
         for (int k = 0; k < KMAX; ++k) {
-            int64_t t = -1;
-            if (state == 0 && k < p.k) {
-                t = p.targets[r * p.k + k];
-                any_bad |= (t < 0 || t >= V);
-            }
+            const int64_t t = k < p.k ? p.targets[r * p.k + k] : -1;
+            any_bad |= k < p.k && (t < 0 || t >= V);
             tg[k] = (t >= 0 && t < V) ? static_cast<int32_t>(t) : -1;
+        }
+        if (p.row_mask != nullptr && p.row_mask[r] == 0) {
+            state = 1;
+            any_bad = false;
+#pragma unroll
+            for (int k = 0; k < KMAX; ++k)
+                tg[k] = -1;
         }
         // the forward NaNs just the bad (r, k); its gradient NaNs the row
         if (kSelGrad && any_bad)
@@ -731,9 +1028,11 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
     }
 
     if (state != 0) {
+        // (every CTA of a row's cluster takes this exit together: nothing is
+        // exchanged for the row)
         const float fill = state == 1 ? 0.0f : __int_as_float(0x7fc00000);
-        // direct: this launch writes the row's outputs (no separate merge)
-        const bool direct = (p.splits == 1) || MODE == kModeFused;
+        // the first slice's CTA writes the row's outputs
+        const bool direct = split == 0;
         if (kLogpFwd) {
             if (direct && tid < p.k)
                 p.logp_out[r * p.k + tid] = 0.0f;
@@ -744,9 +1043,9 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
                 report(p.dev_status, GBCE_DEV_BAD_INDEX);
             fill_row_slice<T>(drow, V, split, p.splits, fill);
         } else {
-            if (tid == 0 && (direct || kCeGrad) && split == 0 && state == 2)
+            if (tid == 0 && direct && state == 2)
                 report(p.dev_status, GBCE_DEV_BAD_LABEL);
-            if (tid == 0 && direct && split == 0 && !kCeGrad) {
+            if (tid == 0 && direct && !kCeGrad) {
                 p.loss_rows[r] = fill;
                 if (p.logp_out)
                     p.logp_out[r] = fill;
@@ -769,8 +1068,11 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
     const char *body = reinterpret_cast<const char *>(row + g.head) + v0 * 16;
     const int64_t body_bytes = (v1 - v0) * 16;
 
-    // fused with a cluster of CTAs per row: the CTAs swap (max, sum) partials
-    const bool exchange = (MODE == kModeFused && p.splits > 1);
+    // statistics over a vocabulary split: the row's CTAs form a cluster and
+    // send their (m, s, h) partials through distributed shared memory to the
+    // first CTA (to every CTA in the fused mode, which needs log p for its
+    // gradient slice)
+    const bool exchange = (kStats && p.splits > 1);
     if (tid == 0) {
 #pragma unroll
         for (int s = 0; s < kStages; ++s) {
@@ -781,6 +1083,45 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
             mbar_init(&xbar, 1);
         fence_barrier_init();
     }
+    __syncthreads();  // the mbarriers exist before anyone uses them
+    if (exchange)
+        cluster_arrive_relaxed();
+
+    // ------------------------------------------------------------ producer
+    if (warp == NCW) {
+        if (lane == 0 && total > 0) {
+            const uint64_t keep = policy_evict_last();
+            const uint64_t stream = policy_evict_first();
+            int64_t i = 0;
+            bool ok = true;
+            for (; i < total; ++i) {
+                const int slot = static_cast<int>(i % kStages);
+                if (i >= kStages &&
+                    !mbar_wait(&empty_bar[slot], static_cast<uint32_t>((i / kStages - 1) & 1))) {
+                    ok = false;
+                    break;
+                }
+                const int64_t ci = i % nchunks;
+                const int64_t off = ci * kChunkBytes;
+                const int64_t left = body_bytes - off;
+                const uint32_t bytes =
+                    static_cast<uint32_t>(left < kChunkBytes ? left : kChunkBytes);
+                const bool first_of_two = (kPasses == 2 && i < nchunks);
+                mbar_arrive_expect_tx(&full_bar[slot], bytes);
+                bulk_load(ring + slot * kChunkBytes, body + off, bytes, &full_bar[slot],
+                          first_of_two ? keep : stream);
+            }
+            if (!ok)
+                report(p.dev_status, GBCE_DEV_TIMEOUT);
+            // no copy may still be in flight when the CTA exits
+            for (int64_t j = (i > kStages ? i - kStages : 0); j < i; ++j)
+                mbar_wait(&full_bar[j % kStages], static_cast<uint32_t>((j / kStages) & 1));
+        }
+        return;
+    }
+
+    // ------------------------------------------------------------ consumers
+    // Per-row constants, computed while the producer already streams.
     if (kSelGrad) {
         // gathered column t: (1/T)(-g_t expm1(log p_t) - (G - g_t) exp(log p_t)),
         // g_t the upstream of every k that gathers t; every other column j:
@@ -823,7 +1164,8 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
         }
     }
     if (kStats) {
-        // target logits, for the finalize step (loaded while the sweep runs)
+        // target logits, for the finalize step (read after the merge's
+        // barrier; their load latency hides under the sweep)
 #pragma unroll
         for (int k = 0; k < KMAX; ++k)
             if (tid == k) {
@@ -831,44 +1173,9 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
                 s_xt[k] = tg[k] >= 0 ? capped(E::load(row + tg[k])) : 0.0f;
             }
     }
-    __syncthreads();
-    if (exchange)
-        cluster_sync_all();  // every peer's xbar exists before any partial is sent
+    if (kSelGrad)
+        named_sync(1, NC);  // the gradient constants before the sweep uses them
 
-    // ------------------------------------------------------------ producer
-    if (warp == NCW) {
-        if (lane == 0 && total > 0) {
-            const uint64_t keep = policy_evict_last();
-            const uint64_t stream = policy_evict_first();
-            int64_t i = 0;
-            bool ok = true;
-            for (; i < total; ++i) {
-                const int slot = static_cast<int>(i % kStages);
-                if (i >= kStages &&
-                    !mbar_wait(&empty_bar[slot], static_cast<uint32_t>((i / kStages - 1) & 1))) {
-                    ok = false;
-                    break;
-                }
-                const int64_t ci = i % nchunks;
-                const int64_t off = ci * kChunkBytes;
-                const int64_t left = body_bytes - off;
-                const uint32_t bytes =
-                    static_cast<uint32_t>(left < kChunkBytes ? left : kChunkBytes);
-                const bool first_of_two = (kPasses == 2 && i < nchunks);
-                mbar_arrive_expect_tx(&full_bar[slot], bytes);
-                bulk_load(ring + slot * kChunkBytes, body + off, bytes, &full_bar[slot],
-                          first_of_two ? keep : stream);
-            }
-            if (!ok)
-                report(p.dev_status, GBCE_DEV_TIMEOUT);
-            // no copy may still be in flight when the CTA exits
-            for (int64_t j = (i > kStages ? i - kStages : 0); j < i; ++j)
-                mbar_wait(&full_bar[j % kStages], static_cast<uint32_t>((j / kStages) & 1));
-        }
-        return;
-    }
-
-    // ------------------------------------------------------------ consumers
     const float c = p.c;
     int64_t seq = 0;  // chunk sequence number across passes (slot, parity)
     bool alive = true;
@@ -904,29 +1211,24 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
                 const int64_t nv = (v1 - v0 - i * CV) < CV ? (v1 - v0 - i * CV) : CV;
                 const int32_t vb0 = static_cast<int32_t>(v0 + i * CV);  // body vector of chunk[0]
                 const int32_t col0 = static_cast<int32_t>(g.head);
-                if (kCap) {
-                    // soft-capped: packed pairs, a vector holding a target
-                    // unpacked with that column masked
+                if (kCap && nv == CV) {
+                    uint4 raw[PER_THREAD];
+#pragma unroll
+                    for (int u = 0; u < PER_THREAD; ++u)
+                        raw[u] = chunk[tid + u * NC];
+                    stats_capped_chunk<T, KMAX, PER_THREAD>(st, mraw, raw, vb0, col0, nt, tg, tv,
+                                                           v0, v1, tid, NC, wcheck, c, capk);
+                } else if (kCap) {
                     for (int v = tid; v < nv; v += NC) {
                         const int32_t vb = vb0 + v;
-                        if (!(wcheck && nt == vb)) {
-                            stats_capped<T>(st, mraw, chunk[v], c, p.softcap, p.inv_cap);
+                        if (wcheck && nt == vb) {
+                            stats_capped_target<T, KMAX>(st, chunk[v], col0 + vb * VEC, tg, c,
+                                                         capk);
+                            nt = next_target_vector<KMAX>(tv, v0, v1, tid, NC, vb);
                             continue;
                         }
-                        float f[VEC];
-                        E::unpack(chunk[v], f);
-                        const int32_t colv = col0 + vb * VEC;
-                        float vm = kNegInf;
-#pragma unroll
-                        for (int e = 0; e < VEC; ++e) {
-                            f[e] = capped(f[e]);
-                            st.sumx_add(f[e]);
-                            if (is_target<KMAX>(tg, colv + e))
-                                f[e] = kNegInf;
-                            vm = fmaxf(vm, f[e]);
-                        }
-                        st.template add<VEC>(f, vm, c);
-                        nt = next_target_vector<KMAX>(tv, v0, v1, tid, NC, vb);
+                        const uint4 one[1] = {chunk[v]};
+                        stats_capped<T, 1>(st, mraw, one, c, capk);
                     }
                 } else if (nv == CV) {
                     uint4 raw[PER_THREAD];
@@ -959,20 +1261,7 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
         if (kEnt && alive && isnan(h) && !isnan(s))
             h = rescan_entropy_moment<T, KMAX>(row, g, V, v0, v1, split == 0,
                                                split == p.splits - 1, tg, c, st.nmc, tid, NC);
-        const auto merge_lanes = [&]() {
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
-                const float s2 = __shfl_xor_sync(0xffffffffu, s, off);
-                if (kEnt)
-                    merge_max_sum_h(m, s, h, m2, s2, __shfl_xor_sync(0xffffffffu, h, off), c);
-                else
-                    merge_max_sum(m, s, m2, s2, c);
-                if (kSumx)
-                    h = __fadd_rn(h, __shfl_xor_sync(0xffffffffu, h, off));
-            }
-        };
-        merge_lanes();
+        warp_merge_state<kH>(m, s, h, c);
         if (lane == 0) {
             red_m[warp] = m;
             red_s[warp] = s;
@@ -983,40 +1272,80 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
             m = lane < NCW ? red_m[lane] : kNegInf;
             s = lane < NCW ? red_s[lane] : 0.0f;
             h = lane < NCW ? red_h[lane] : 0.0f;
-            merge_lanes();
-            if (lane == 0) {
-                if (exchange) {
-                    const uint32_t C = static_cast<uint32_t>(p.splits);
-                    mbar_arrive_expect_tx(&xbar, C * static_cast<uint32_t>(sizeof(float2)));
-                    const uint32_t slot = smem_addr(&xchg[split]);
-                    const uint32_t bar = smem_addr(&xbar);
-                    for (uint32_t t = 0; t < C; ++t)
-                        st_async_pair(map_to_rank(slot, t), m, s, map_to_rank(bar, t));
-                } else if (p.splits > 1) {
-                    p.partials[unit] = make_float2(m, s);
-                    if (kEnt || kSumx)
-                        p.partials_h[unit] = h;
-                } else if (kLogpFwd) {
-                    bc_m = m;
-                    bc_s = s;
-                    bc_h = h;
-                } else {
-                    xy = s_xt[0];
-                    logp = finalize_logp(m, s, xy, p.T);
+            warp_merge_state<kH>(m, s, h, c);
+            if (exchange)
+                cluster_wait();  // every peer's mbarriers exist
+            if (exchange && lane == 0) {
+                const uint32_t C = static_cast<uint32_t>(p.splits);
+                const bool all = (MODE == kModeFused);
+                if (all || split == 0)
+                    mbar_arrive_expect_tx(&xbar, C * static_cast<uint32_t>(sizeof(float4)));
+                const uint32_t slot = smem_addr(&xchg[split]);
+                const uint32_t bar = smem_addr(&xbar);
+                const float4 part = make_float4(m, s, h, 0.0f);
+                for (uint32_t t = 0; t < (all ? C : 1u); ++t)
+                    st_async_v4(map_to_rank(slot, t), part, map_to_rank(bar, t));
+            }
+        }
+        // a statistics-only CTA of a split row is done once its partial is sent
+        if (exchange && MODE != kModeFused && split != 0)
+            return;
+        if (exchange && warp == 0) {
+            // the partials of every slice, merged in slice order
+            if (!mbar_wait_cluster(&xbar, 0)) {
+                alive = false;
+                report(p.dev_status, GBCE_DEV_TIMEOUT);
+            }
+            m = kNegInf;
+            s = 0.0f;
+            h = 0.0f;
+            for (int t = 0; t < p.splits; ++t) {
+                const float4 part = xchg[t];
+                merge_state<kH>(m, s, h, part.x, part.y, part.z, c);
+            }
+        }
+        if (warp == 0 && lane == 0) {
+            if (kLogpFwd) {
+                bc_m = m;
+                bc_s = s;
+                bc_h = h;
+            } else {
+                xy = s_xt[0];
+                logp = finalize_logp(m, s, xy, p.T);
+                if (split == 0) {
                     p.loss_rows[r] = ce_row_loss(logp, xy, h, p.T, p.ls_eps, p.dft, V);
                     if (p.logp_out)
                         p.logp_out[r] = logp;
                     if (p.lse_out)
                         p.lse_out[r] = xy / p.T - logp;
-                    bc_logp = logp;
                 }
+                bc_logp = logp;
             }
         }
-        if (kLogpFwd && p.splits == 1) {
+        if (kLogpFwd) {
             named_sync(1, NC);
-            if (kEnt && tid == NC - 1)
-                p.entropy_out[r] = entropy_with_targets<KMAX>(bc_m, bc_s, bc_h, s_tg, s_xt,
-                                                              static_cast<int>(p.k), c, p.T);
+            // the last warp finalizes the entropy while warp 0 writes the
+            // log-probs; a row that needs the second look gets it from that
+            // warp alone, so no other warp waits for it
+            if (kEnt && warp == NCW - 1) {
+                bool rescan = false;
+                float H = 0.0f;
+                if (lane == 0)
+                    H = entropy_with_targets<KMAX>(bc_m, bc_s, bc_h, s_tg, s_xt,
+                                                   static_cast<int>(p.k), c, p.T, rescan);
+                if (__shfl_sync(0xffffffffu, rescan, 0)) {
+                    // confident in a column other than the first index: the
+                    // entropy again, around that column, from the whole row
+                    const RowGeom gr = row_geom<T>(row, V);
+                    float M;
+                    int32_t d;
+                    row_argmax<T, 1>(row, gr, V, lane, nullptr, nullptr, M, d);
+                    H = entropy_around<T, 1>(row, gr, V, d, M, c, p.T, lane, nullptr, nullptr,
+                                             nullptr);
+                }
+                if (lane == 0)
+                    p.entropy_out[r] = H;
+            }
             if (tid < p.k) {
                 float out;
                 if (s_tg[tid] < 0) {
@@ -1029,37 +1358,7 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
                 p.logp_out[r * p.k + tid] = out;
             }
         }
-        if (MODE == kModeFused && exchange) {
-            // warp 0 waits for the cluster's partials and finalizes; the
-            // other warps wait on the named barrier, issuing nothing
-            if (warp == 0) {
-                if (!mbar_wait_cluster(&xbar, 0)) {
-                    alive = false;
-                    report(p.dev_status, GBCE_DEV_TIMEOUT);
-                }
-                if (lane == 0) {
-                    float M = kNegInf, Ssum = 0.0f;
-                    for (int t = 0; t < p.splits; ++t) {
-                        const float2 part = xchg[t];
-                        merge_max_sum(M, Ssum, part.x, part.y, c);
-                    }
-                    const float x_y = s_xt[0];
-                    const float lp = finalize_logp(M, Ssum, x_y, p.T);
-                    bc_logp = lp;
-                    if (split == 0) {
-                        // (smoothing never takes this path: no sum of logits)
-                        p.loss_rows[r] = ce_row_loss(lp, x_y, 0.0f, p.T, 0.0f, p.dft, V);
-                        if (p.logp_out)
-                            p.logp_out[r] = lp;
-                        if (p.lse_out)
-                            p.lse_out[r] = x_y / p.T - lp;
-                    }
-                }
-            }
-            named_sync(1, NC);
-            logp = bc_logp;
-            xy = s_xt[0];
-        } else if (MODE == kModeFused) {
+        if (MODE == kModeFused) {
             named_sync(1, NC);
             logp = bc_logp;
             xy = s_xt[0];
@@ -1077,8 +1376,32 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
 #pragma unroll
         for (int k = 0; k < KMAX; ++k)
             dtv[k] = s_dt[k];
+        // With the entropy term, a row confident in a column d outside the
+        // gathered set (p_t0 < 1/2 and H < 1/16) gets d's element from a
+        // whole-row pass first: there the term needs H + log p_d, which the
+        // per-element formula would take as a difference of nearly equal
+        // numbers.  Its value then patches d like a gathered column.
+        int32_t dcol = -1, dvec = -1;
+        float dval = 0.0f;
+        if (kEntGrad && s_gH != 0.0f && s_H < 0.0625f && s_lp0 < -0.69314718f) {
+            float M;
+            int32_t d;
+            row_argmax<T, NCW>(row, g, V, tid, red_m, red_i, M, d);
+            bool gathered = false;
+#pragma unroll
+            for (int k = 0; k < KMAX; ++k)
+                gathered |= (tg[k] == d);
+            if (!gathered && d < V) {
+                const float Q = entropy_gap<T, NCW>(row, g, V, d, M, s_xt[0], s_lp0, c,
+                                                    1.0f / p.T, tid, red_m);
+                const float pd = ex2(fmaf(M - s_xt[0], c, s_lp0 * kLog2e));
+                dval = pd * (-(s_G / p.T) - (s_gH / p.T) * Q);
+                dcol = d;
+                dvec = (d >= g.head && d < g.tail0) ? static_cast<int32_t>((d - g.head) / VEC) : -1;
+            }
+        }
         const auto at_target = [&](int32_t col, float dflt) {
-            float v = dflt;
+            float v = col == dcol ? dval : dflt;
 #pragma unroll
             for (int k = 0; k < KMAX; ++k)
                 v = (tg[k] == col) ? dtv[k] : v;
@@ -1105,7 +1428,7 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
                 for (int v = tid; v < nv; v += NC) {
                     const uint4 raw = chunk[v];
                     const int32_t vb = static_cast<int32_t>(vbase + v);
-                    if (!vector_has_target<KMAX>(tv, vb) && p.vec_store) {
+                    if (!vector_has_target<KMAX>(tv, vb) && vb != dvec && p.vec_store) {
                         st_cs_v4(dbase + v * VEC,
                                  GradVec<T>::template run<kEntGrad>(raw, kNoLabel, gk));
                         continue;
@@ -1140,8 +1463,8 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
             // soft-capped: element j is (its plain value on z = cap tanh(x / cap))
             // times the chain factor 1 - tanh^2(x / cap)
             const auto elem = [&](float x, bool is_y) {
-                const float t = tanh_acc(x * p.inv_cap);
-                const float chain = fmaf(-t, t, 1.0f);
+                const float t = tanhf(x * p.inv_cap);
+                const float chain = (1.0f - t) * (1.0f + t);
                 const float z = p.softcap * t;
                 const float d = is_y ? gk.dy : fmaf(gk.gs, ex2(fmaf(z + gk.nxy, gk.c, gk.kb)), gk.c0);
                 return d * chain;
@@ -1169,7 +1492,7 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
                         const int64_t yoff = y - (col_base + v * VEC);
                         if (p.vec_store && (yoff < 0 || yoff >= VEC)) {
                             st_cs_v4(dbase + v * VEC,
-                                     grad_capped<T>(chunk[v], gk, p.softcap, p.inv_cap));
+                                     grad_capped<T>(chunk[v], gk, capk));
                             continue;
                         }
                         float f[VEC];
@@ -1240,91 +1563,6 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
     }
 }
 
-// Merge the slices' (max, sum) partials of each row in slice order and write
-// the row's outputs.  One thread per row.
-template <typename T, int MODE>
-__global__ void combine_kernel(const RowParams p)
-{
-    using E = Elem<T>;
-    const int64_t r = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (r >= p.rows)
-        return;
-    const T *row = static_cast<const T *>(p.logits) + r * p.row_stride;
-    const int64_t V = p.vocab;
-    const float c = p.c;
-    const float nan = __int_as_float(0x7fc00000);
-    constexpr bool kEnt = (MODE == kModeLogpEnt);
-    constexpr bool kLogpFwd = (MODE == kModeLogp || kEnt);
-    constexpr bool kSumx = (MODE == kModeCeSmooth || MODE == kModeCeCap);
-
-    if (kLogpFwd) {
-        if (p.row_mask != nullptr && p.row_mask[r] == 0) {
-            for (int64_t k = 0; k < p.k; ++k)
-                p.logp_out[r * p.k + k] = 0.0f;
-            if (kEnt)
-                p.entropy_out[r] = 0.0f;
-            return;
-        }
-    } else {
-        const int64_t lab = p.targets[r];
-        if (lab == p.ignore_index || lab < 0 || lab >= V) {
-            const float fill = lab == p.ignore_index ? 0.0f : nan;
-            if (lab != p.ignore_index)
-                report(p.dev_status, GBCE_DEV_BAD_LABEL);
-            p.loss_rows[r] = fill;
-            if (p.logp_out)
-                p.logp_out[r] = fill;
-            if (p.lse_out)
-                p.lse_out[r] = fill;
-            return;
-        }
-    }
-
-    float m = kNegInf, s = 0.0f, h = 0.0f;
-    for (int i = 0; i < p.splits; ++i) {
-        const float2 part = p.partials[r * p.splits + i];
-        if (kEnt)
-            merge_max_sum_h(m, s, h, part.x, part.y, p.partials_h[r * p.splits + i], c);
-        else
-            merge_max_sum(m, s, part.x, part.y, c);
-        if (kSumx)
-            h += p.partials_h[r * p.splits + i];
-    }
-
-    if (kLogpFwd) {
-        int32_t tg[GBCE_MAX_K];
-        float xt[GBCE_MAX_K];
-        const int K = static_cast<int>(p.k);
-        for (int k = 0; k < K; ++k) {
-            const int64_t t = p.targets[r * p.k + k];
-            tg[k] = (t >= 0 && t < V) ? static_cast<int32_t>(t) : -1;
-            xt[k] = tg[k] >= 0 ? E::load(row + tg[k]) : 0.0f;
-        }
-        for (int k = 0; k < K; ++k) {
-            float out;
-            if (tg[k] < 0) {
-                out = nan;
-                report(p.dev_status, GBCE_DEV_BAD_INDEX);
-            } else {
-                out = logp_with_targets<GBCE_MAX_K>(m, s, tg, xt, K, k, c, p.T);
-            }
-            p.logp_out[r * p.k + k] = out;
-        }
-        if (kEnt)
-            p.entropy_out[r] = entropy_with_targets<GBCE_MAX_K>(m, s, h, tg, xt, K, c, p.T);
-    } else {
-        float xy = E::load(row + p.targets[r]);
-        if (MODE == kModeCeCap)
-            xy = p.softcap * tanh_acc(xy * p.inv_cap);
-        const float logp = finalize_logp(m, s, xy, p.T);
-        p.loss_rows[r] = ce_row_loss(logp, xy, h, p.T, p.ls_eps, p.dft, V);
-        if (p.logp_out)
-            p.logp_out[r] = logp;
-        if (p.lse_out)
-            p.lse_out[r] = xy / p.T - logp;
-    }
-}
-
 // The opt-in to more than 48 KB of dynamic shared memory is an attribute of
 // the function in each device's context: set it once per device.
 template <typename Kernel>
@@ -1343,48 +1581,84 @@ static cudaError_t ensure_smem_attr(Kernel kernel, int bytes, std::atomic<uint64
     return err;
 }
 
-template <typename T>
-cudaError_t launch_rows_dispatch(const RowParams &p, int mode, cudaStream_t stream);
-
-// Fused mode with a cluster of p.splits CTAs per row (one per vocab slice).
-template <typename T>
-static cudaError_t launch_fused_row_cluster(const RowParams &p, cudaStream_t stream)
-{
-    static std::atomic<uint64_t> attr_done{0};
-    auto kernel = row_kernel<T, kModeFused, 1>;
-    cudaError_t err = ensure_smem_attr(kernel, kDynSmemBytes, attr_done);
-    if (err != cudaSuccess)
-        return err;
+// Launch configuration of `units` row-kernel CTAs in clusters of C.
+struct ClusterLaunch {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(p.rows * p.splits), 1, 1);
-    cfg.blockDim = dim3(kRowThreads, 1, 1);
-    cfg.dynamicSmemBytes = kDynSmemBytes;
-    cfg.stream = stream;
     cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(p.splits);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    err = cudaLaunchKernelEx(&cfg, kernel, p);
-    note_launches(1);
-    return err;
+    ClusterLaunch(int64_t units, int C, cudaStream_t stream)
+    {
+        cfg.gridDim = dim3(static_cast<unsigned>(units), 1, 1);
+        cfg.blockDim = dim3(kRowThreads, 1, 1);
+        cfg.dynamicSmemBytes = kDynSmemBytes;
+        cfg.stream = stream;
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = static_cast<unsigned>(C);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+};
+
+// The largest cluster size C <= want for which `rows` clusters of this
+// kernel are all resident at once (one wave; a cluster must fit in one GPC,
+// so this is below rows x C <= the CTA slots), 1 if none is.  The occupancy
+// query runs once per device and size.
+template <typename Kernel>
+static int one_wave_cluster_size(Kernel kernel, int want, int64_t rows,
+                                 std::atomic<int> (&cache)[64][kMaxClusterCtas + 1])
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return want;
+    for (int C = want; C > 1; --C) {
+        int n = cache[dev][C].load(std::memory_order_relaxed);
+        if (n == 0) {
+            ClusterLaunch l(static_cast<int64_t>(C) * rows, C, nullptr);
+            if (cudaOccupancyMaxActiveClusters(&n, kernel, &l.cfg) != cudaSuccess || n < 1) {
+                (void)cudaGetLastError();
+                return want;  // no answer: keep the requested split
+            }
+            cache[dev][C].store(n, std::memory_order_relaxed);
+        }
+        if (n >= rows)
+            return C;
+    }
+    return 1;
 }
 
+// One CTA per work unit.  Split statistics (p.splits > 1 in a statistics or
+// fused mode) run each row's slices as one thread-block cluster, whose CTAs
+// swap partials through distributed shared memory; the cluster shrinks from
+// p.splits until every row's cluster is resident at once.
 template <typename T, int MODE, int KMAX>
 static cudaError_t launch_row_kernel(const RowParams &p, cudaStream_t stream)
 {
     static std::atomic<uint64_t> attr_done{0};
+    static std::atomic<int> max_clusters[64][kMaxClusterCtas + 1] = {};
     auto kernel = row_kernel<T, MODE, KMAX>;
     cudaError_t err = ensure_smem_attr(kernel, kDynSmemBytes, attr_done);
     if (err != cudaSuccess)
         return err;
-    const int64_t units = p.rows * p.splits;
-    kernel<<<static_cast<unsigned>(units), kRowThreads, kDynSmemBytes, stream>>>(p);
+    constexpr bool kStatsMode = !(MODE == kModeGrad || MODE == kModeGradCap ||
+                                  MODE == kModeLogpGrad || MODE == kModeLogpEntGrad);
+    RowParams q = p;
+    if (kStatsMode && q.splits > 1)
+        q.splits = one_wave_cluster_size(kernel, q.splits, q.rows, max_clusters);
+    const int64_t units = q.rows * q.splits;
+    if (!kStatsMode || q.splits == 1) {
+        kernel<<<static_cast<unsigned>(units), kRowThreads, kDynSmemBytes, stream>>>(q);
+        note_launches(1);
+        return cudaGetLastError();
+    }
+    ClusterLaunch l(units, q.splits, stream);
+    err = cudaLaunchKernelEx(&l.cfg, kernel, q);
     note_launches(1);
-    return cudaGetLastError();
+    return err;
 }
+
+template <typename T>
+cudaError_t launch_rows_dispatch(const RowParams &p, int mode, cudaStream_t stream);
 
 template <typename T>
 cudaError_t launch_rows(const RowParams &p, int mode, cudaStream_t stream)
@@ -1394,8 +1668,8 @@ cudaError_t launch_rows(const RowParams &p, int mode, cudaStream_t stream)
     return launch_rows_dispatch<T>(p, mode, stream);
 }
 
-// One CTA per work unit; the fallback for every shape the persistent kernels
-// do not take.
+// One CTA per work unit (clusters of them for split statistics): every call
+// that the persistent kernel does not take.
 template <typename T>
 cudaError_t launch_rows_per_unit(const RowParams &p, int mode, cudaStream_t stream)
 {
@@ -1418,6 +1692,8 @@ cudaError_t launch_rows_per_unit(const RowParams &p, int mode, cudaStream_t stre
         return launch_row_kernel<T, kModeCeSmooth, 1>(p, stream);
     case kModeCeCap:
         return launch_row_kernel<T, kModeCeCap, 1>(p, stream);
+    case kModeCeCapSmooth:
+        return launch_row_kernel<T, kModeCeCapSmooth, 1>(p, stream);
     case kModeGradCap:
         return launch_row_kernel<T, kModeGradCap, 1>(p, stream);
     case kModeGrad:
@@ -1439,27 +1715,6 @@ cudaError_t launch_rows_per_unit(const RowParams &p, int mode, cudaStream_t stre
     default:
         return cudaErrorInvalidValue;
     }
-}
-
-template <typename T>
-cudaError_t launch_combine(const RowParams &p, int mode, cudaStream_t stream)
-{
-    if (p.rows == 0)
-        return cudaSuccess;
-    const int threads = 128;
-    const unsigned blocks = static_cast<unsigned>((p.rows + threads - 1) / threads);
-    if (mode == kModeLogp)
-        combine_kernel<T, kModeLogp><<<blocks, threads, 0, stream>>>(p);
-    else if (mode == kModeLogpEnt)
-        combine_kernel<T, kModeLogpEnt><<<blocks, threads, 0, stream>>>(p);
-    else if (mode == kModeCeSmooth)
-        combine_kernel<T, kModeCeSmooth><<<blocks, threads, 0, stream>>>(p);
-    else if (mode == kModeCeCap)
-        combine_kernel<T, kModeCeCap><<<blocks, threads, 0, stream>>>(p);
-    else
-        combine_kernel<T, kModeCe><<<blocks, threads, 0, stream>>>(p);
-    note_launches(1);
-    return cudaGetLastError();
 }
 
 }  // namespace gbce

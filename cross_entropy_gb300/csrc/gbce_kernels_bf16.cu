@@ -3,5 +3,4 @@
 
 namespace gbce {
 template cudaError_t launch_rows<__nv_bfloat16>(const RowParams &, int, cudaStream_t);
-template cudaError_t launch_combine<__nv_bfloat16>(const RowParams &, int, cudaStream_t);
 }  // namespace gbce

@@ -3,5 +3,4 @@
 
 namespace gbce {
 template cudaError_t launch_rows<float>(const RowParams &, int, cudaStream_t);
-template cudaError_t launch_combine<float>(const RowParams &, int, cudaStream_t);
 }  // namespace gbce

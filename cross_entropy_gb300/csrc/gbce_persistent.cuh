@@ -1,11 +1,16 @@
 // Persistent fused cross-entropy forward + backward (sm_103a).
 //
-// One CTA per SM walks rows r = blockIdx.x, r += gridDim.x.  Its producer
-// lane streams, without gaps, row r's statistics pass (bulk copies with L2
-// evict_last), row r's gradient pass (the same bytes again, now L2 hits),
-// then row r+1's statistics pass, ... through a ring of 32 KB stages.  The
-// consumer warps fold pass-1 chunks into the row's online (max, sum),
-// finalize log p between the passes, and write dlogits from pass-2 chunks.
+// One CTA per SM walks rows: row blockIdx.x first, then whichever row the
+// next ticket names (gridDim.x + an atomic counter in the workspace, zeroed
+// by the item-count kernel that runs before), so that CTAs that meet
+// ignored rows or finish early take more rows and the last rows spread over
+// every SM.  Its producer lane streams, without gaps, row r's statistics
+// pass (bulk copies with L2 evict_last), row r's gradient pass (the same
+// bytes again, now L2 hits), then the next row's statistics pass, ...
+// through a ring of 48 KB stages, and hands each row's id to the consumer
+// warps through a small queue in shared memory.  The consumer warps fold
+// pass-1 chunks into the row's online (max, sum), finalize log p between
+// the passes, and write dlogits from pass-2 chunks.
 //
 // Why one CTA per SM: a row must stay in L2 from its first read to its
 // re-read, so the L2 footprint is (rows in flight) x (row bytes).  One row
@@ -49,7 +54,9 @@ constexpr int kPersistThreads = (kPersistWarps + 1) * 32;
 constexpr int kPersistDynSmem = kPersistStages * kPersistChunk + kRingAlign;
 
 // SMOOTH: label smoothing, which also needs each row's sum of logits.
-template <typename T, bool SMOOTH>
+// CAP: logit soft-capping, cap * tanh(x / cap) on every logit (and the
+// chain factor 1 - tanh^2 in the gradient).
+template <typename T, bool SMOOTH, bool CAP>
 __global__ void __launch_bounds__(kPersistThreads, 1) persistent_fused_kernel(const RowParams p)
 {
     using E = Elem<T>;
@@ -68,6 +75,9 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persistent_fused_kernel(co
         (reinterpret_cast<uintptr_t>(dyn_smem) + (kRingAlign - 1)) & ~uintptr_t(kRingAlign - 1));
     __shared__ uint64_t full_bar[S];
     __shared__ uint64_t empty_bar[S];
+    constexpr int Q = 4;  // row-id queue, producer -> consumers
+    __shared__ uint64_t rq_full[Q], rq_empty[Q];
+    __shared__ int32_t rq_row[Q];
     __shared__ float red_m[NCW], red_s[NCW], red_x[NCW];
     __shared__ float bc_logp;
 
@@ -75,12 +85,20 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persistent_fused_kernel(co
     const int warp = tid >> 5, lane = tid & 31;
     const int64_t V = p.vocab;
     const float c = p.c;
+    const CapConsts capk = cap_consts(p.softcap, p.inv_cap, p.c);
+    // a logit as the softmax sees it
+    const auto capped = [&](float x) { return CAP ? p.softcap * tanhf(x * p.inv_cap) : x; };
 
     if (tid == 0) {
 #pragma unroll
         for (int s = 0; s < S; ++s) {
             mbar_init(&full_bar[s], 1);
             mbar_init(&empty_bar[s], NCW);
+        }
+#pragma unroll
+        for (int q = 0; q < Q; ++q) {
+            mbar_init(&rq_full[q], 1);
+            mbar_init(&rq_empty[q], NCW);
         }
         fence_barrier_init();
     }
@@ -94,15 +112,40 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persistent_fused_kernel(co
             uint32_t seq = 0;          // chunks issued
             uint32_t slot = 0, lap = 0;  // ring position of chunk seq, and its lap
             bool ok = true;
-            for (int64_t r = blockIdx.x; r < p.rows && ok; r += gridDim.x) {
-                const int64_t lab = p.targets[r];
-                if (lab == p.ignore_index || lab < 0 || lab >= V)
+            int64_t r = blockIdx.x;
+            int64_t lab = r < p.rows ? p.targets[r] : 0;
+            for (uint32_t qi = 0; ok; ++qi) {
+                // hand row r (-1: no more rows) to the consumers
+                const uint32_t qs = qi % Q;
+                if (qi >= Q && !mbar_wait(&rq_empty[qs], ((qi / Q) - 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                rq_row[qs] = r < p.rows ? static_cast<int32_t>(r) : -1;
+                mbar_arrive(&rq_full[qs]);  // (release: the consumers see rq_row)
+                if (r >= p.rows)
+                    break;
+                // the ticket for the row after this one, fetched while this
+                // one streams (without a ticket counter: the static walk)
+                const int64_t next =
+                    p.row_ticket != nullptr
+                        ? gridDim.x + static_cast<int64_t>(atomicAdd(p.row_ticket, 1))
+                        : r + gridDim.x;
+                if (lab == p.ignore_index || lab < 0 || lab >= V) {
+                    r = next;
+                    lab = r < p.rows ? p.targets[r] : 0;
                     continue;
+                }
+                // the next row's label, read while this row's gradient pass
+                // streams (the ticket has long returned by then)
+                int64_t next_lab = 0;
                 const T *row = static_cast<const T *>(p.logits) + r * p.row_stride;
                 const RowGeom g = row_geom<T>(row, V);
                 const char *body = reinterpret_cast<const char *>(row + g.head);
                 const int64_t bytes_total = g.nvec * 16;
                 for (int pass = 0; pass < 2 && ok; ++pass) {
+                    if (pass == 1 && next < p.rows)
+                        next_lab = p.targets[next];
                     for (int64_t off = 0; off < bytes_total; off += CHUNK, ++seq) {
                         if (lap > 0 && !mbar_wait(&empty_bar[slot], (lap - 1) & 1)) {
                             ok = false;
@@ -119,6 +162,8 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persistent_fused_kernel(co
                         }
                     }
                 }
+                r = next;
+                lab = next_lab;
             }
             if (!ok)
                 report(p.dev_status, GBCE_DEV_TIMEOUT);
@@ -132,7 +177,19 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persistent_fused_kernel(co
     // ------------------------------------------------------------ consumers
     uint32_t slot = 0, lap = 0;  // ring position of the next chunk, and its lap
     bool alive = true;
-    for (int64_t r = blockIdx.x; r < p.rows; r += gridDim.x) {
+    for (uint32_t qi = 0;; ++qi) {
+        // the next row from the producer
+        const uint32_t qs = qi % Q;
+        if (!mbar_wait(&rq_full[qs], (qi / Q) & 1)) {
+            report(p.dev_status, GBCE_DEV_TIMEOUT);
+            break;
+        }
+        const int64_t r = rq_row[qs];
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(&rq_empty[qs]);
+        if (r < 0)
+            break;
         const T *row = static_cast<const T *>(p.logits) + r * p.row_stride;
         T *drow = static_cast<T *>(p.dlogits) + r * p.d_stride;
         const int64_t lab = p.targets[r];
@@ -172,20 +229,21 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persistent_fused_kernel(co
         const int32_t col0 = static_cast<int32_t>(g.head);
         // the label logit and the upstream gradient are read now (every thread,
         // one cached address each), so their latency hides under pass 1
-        const float xy = E::load(row + y);
+        const float xy = capped(E::load(row + y));
         const float gup = upstream_grad(p, r);
 
         // pass 1: statistics
         OnlineStats<false, SMOOTH> st;
         int32_t nt = next_target_vector<1>(tv, 0, g.nvec, tid, NC, -1);
         const bool wcheck = __any_sync(0xffffffffu, nt != INT32_MAX);
+        float mraw = kNegInf;  // soft-capped sweep: the raw max behind st.m
         for (int64_t e = tid; e < g.head; e += NC) {
-            const float x = E::load(row + e);
+            const float x = capped(E::load(row + e));
             st.add1(e == y ? kNegInf : x, c);
             st.sumx_add(x);
         }
         for (int64_t e = g.tail0 + tid; e < V; e += NC) {
-            const float x = E::load(row + e);
+            const float x = capped(E::load(row + e));
             st.add1(e == y ? kNegInf : x, c);
             st.sumx_add(x);
         }
@@ -198,7 +256,25 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persistent_fused_kernel(co
                 const uint4 *chunk = reinterpret_cast<const uint4 *>(ring + slot * CHUNK);
                 const int32_t vb0 = static_cast<int32_t>(i * CV);
                 const int32_t nv = static_cast<int32_t>((g.nvec - i * CV) < CV ? (g.nvec - i * CV) : CV);
-                if (nv == CV) {
+                if (CAP && nv == CV) {
+                    uint4 raw[PER_THREAD];
+#pragma unroll
+                    for (int u = 0; u < PER_THREAD; ++u)
+                        raw[u] = chunk[tid + u * NC];
+                    stats_capped_chunk<T, 1, PER_THREAD>(st, mraw, raw, vb0, col0, nt, tg, tv, 0,
+                                                        g.nvec, tid, NC, wcheck, c, capk);
+                } else if (CAP) {
+                    for (int v = tid; v < nv; v += NC) {
+                        const int32_t vb = vb0 + v;
+                        if (wcheck && nt == vb) {
+                            stats_capped_target<T, 1>(st, chunk[v], col0 + vb * VEC, tg, c, capk);
+                            nt = next_target_vector<1>(tv, 0, g.nvec, tid, NC, vb);
+                            continue;
+                        }
+                        const uint4 one[1] = {chunk[v]};
+                        stats_capped<T, 1>(st, mraw, one, c, capk);
+                    }
+                } else if (nv == CV) {
                     uint4 raw[PER_THREAD];
 #pragma unroll
                     for (int u = 0; u < PER_THREAD; ++u)
@@ -265,10 +341,19 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persistent_fused_kernel(co
         const GradConsts gk = grad_consts_ce(xy, c, bc_logp, gup, p.T, p.ls_eps, p.dft, V);
 
         // pass 2: gradient
+        // soft-capped element: its plain value on z = cap tanh(x / cap) times
+        // the chain factor 1 - tanh^2(x / cap)
+        const auto elem = [&](float x, bool is_y) {
+            if (!CAP)
+                return is_y ? gk.dy : grad_scalar(x, gk);
+            const float t = tanhf(x * p.inv_cap);
+            const float d = is_y ? gk.dy : fmaf(gk.gs, ex2(fmaf(t, capk.capc, gk.kbx)), gk.c0);
+            return d * ((1.0f - t) * (1.0f + t));
+        };
         for (int64_t e = tid; e < g.head; e += NC)
-            E::store(drow + e, e == y ? gk.dy : grad_scalar(E::load(row + e), gk));
+            E::store(drow + e, elem(E::load(row + e), e == y));
         for (int64_t e = g.tail0 + tid; e < V; e += NC)
-            E::store(drow + e, e == y ? gk.dy : grad_scalar(E::load(row + e), gk));
+            E::store(drow + e, elem(E::load(row + e), e == y));
         for (int64_t i = 0; i < nchunks; ++i) {
             if (alive && !mbar_wait(&full_bar[slot], lap & 1)) {
                 alive = false;
@@ -280,7 +365,27 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persistent_fused_kernel(co
                 const int32_t nv = static_cast<int32_t>((g.nvec - vbase) < CV ? (g.nvec - vbase) : CV);
                 const int32_t ybase = y - static_cast<int32_t>(g.head + vbase * VEC);
                 T *dbase = drow + g.head + vbase * VEC;
-                if (nv == CV && p.vec_store) {
+                if (CAP) {
+                    for (int v = tid; v < nv; v += NC) {
+                        const int32_t yoff = ybase - v * VEC;
+                        if (p.vec_store && static_cast<uint32_t>(yoff) >= static_cast<uint32_t>(VEC)) {
+                            st_cs_v4(dbase + v * VEC, grad_capped<T>(chunk[v], gk, capk));
+                            continue;
+                        }
+                        float f[VEC];
+                        E::unpack(chunk[v], f);
+#pragma unroll
+                        for (int e = 0; e < VEC; ++e)
+                            f[e] = elem(f[e], e == yoff);
+                        if (p.vec_store) {
+                            st_cs_v4(dbase + v * VEC, E::pack(f));
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < VEC; ++e)
+                                E::store(dbase + v * VEC + e, f[e]);
+                        }
+                    }
+                } else if (nv == CV && p.vec_store) {
                     uint4 raw[PER_THREAD];
 #pragma unroll
                     for (int u = 0; u < PER_THREAD; ++u)
@@ -314,31 +419,11 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persistent_fused_kernel(co
     }
 }
 
-// Streaming multiprocessors of the current device (cached per device).
-inline int device_sm_count()
-{
-    static std::atomic<int> cache[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess)
-        return 0;
-    if (dev >= 0 && dev < 64) {
-        const int v = cache[dev].load(std::memory_order_relaxed);
-        if (v > 0)
-            return v;
-    }
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        return 0;
-    if (dev >= 0 && dev < 64)
-        cache[dev].store(n, std::memory_order_relaxed);
-    return n;
-}
-
-template <typename T, bool SMOOTH>
+template <typename T, bool SMOOTH, bool CAP>
 cudaError_t launch_persistent_fused_as(const RowParams &p, int grid, cudaStream_t stream)
 {
     static std::atomic<uint64_t> attr_done{0};
-    auto kernel = persistent_fused_kernel<T, SMOOTH>;
+    auto kernel = persistent_fused_kernel<T, SMOOTH, CAP>;
     cudaError_t err = ensure_smem_attr(kernel, kPersistDynSmem, attr_done);
     if (err != cudaSuccess)
         return err;
@@ -350,8 +435,11 @@ cudaError_t launch_persistent_fused_as(const RowParams &p, int grid, cudaStream_
 template <typename T>
 cudaError_t launch_persistent_fused(const RowParams &p, int grid, cudaStream_t stream)
 {
-    return p.ls_eps != 0.0f ? launch_persistent_fused_as<T, true>(p, grid, stream)
-                            : launch_persistent_fused_as<T, false>(p, grid, stream);
+    if (p.softcap > 0.0f)
+        return p.ls_eps != 0.0f ? launch_persistent_fused_as<T, true, true>(p, grid, stream)
+                                : launch_persistent_fused_as<T, false, true>(p, grid, stream);
+    return p.ls_eps != 0.0f ? launch_persistent_fused_as<T, true, false>(p, grid, stream)
+                            : launch_persistent_fused_as<T, false, false>(p, grid, stream);
 }
 
 }  // namespace gbce

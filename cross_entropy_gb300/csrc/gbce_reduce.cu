@@ -77,9 +77,12 @@ __device__ int64_t count_items(const int64_t *labels, int64_t rows, int64_t igno
 }
 
 __global__ void __launch_bounds__(kReduceThreads)
-    count_items_kernel(const int64_t *labels, int64_t rows, int64_t ignore_index, int64_t *n_out)
+    count_items_kernel(const int64_t *labels, int64_t rows, int64_t ignore_index, int64_t *n_out,
+                       int32_t *zero_out)
 {
     __shared__ int64_t scratch[kReduceThreads / 32];
+    if (threadIdx.x == 0 && zero_out != nullptr)
+        *zero_out = 0;
     const int64_t n = count_items(labels, rows, ignore_index, scratch);
     if (threadIdx.x == 0)
         *n_out = n;
@@ -128,9 +131,10 @@ __global__ void __launch_bounds__(kReduceThreads)
 }
 
 cudaError_t launch_count_items(const int64_t *labels, int64_t rows, int64_t ignore_index,
-                               int64_t *n_out, cudaStream_t stream)
+                               int64_t *n_out, int32_t *zero_out, cudaStream_t stream)
 {
-    count_items_kernel<<<1, kReduceThreads, 0, stream>>>(labels, rows, ignore_index, n_out);
+    count_items_kernel<<<1, kReduceThreads, 0, stream>>>(labels, rows, ignore_index, n_out,
+                                                         zero_out);
     note_launches(1);
     return cudaGetLastError();
 }

@@ -92,9 +92,10 @@ uint64_t gbce_kernel_launches(void);
  * is NULL); masked-out rows are not read and get 0.  With entropy_out, the
  * same sweep also gives the entropy of each row's softmax,
  * entropy_out[r] = -sum_j p_j log p_j (0 log 0 = 0; 0 for masked rows),
- * with the first index as the reference column whose probability may be
- * near 1: its 1 - p comes from its accurate log p, so a confident row keeps
- * its small positive entropy.
+ * with the dominant column's 1 - p taken from its accurate log p, so a
+ * confident row keeps its small positive entropy whichever column it is
+ * confident in (when that is not the first index, the row's entropy is
+ * recomputed around it in a second pass over that row).
  *
  * Source: "perf(rlhf): chunk selective_log_softmax instead of looping per
  * token" (ms-swift PR #10337), "PR information": the naive
@@ -298,12 +299,16 @@ gbce_status ce_fwd_bwd_fused(const void *logits, gbce_dtype dtype, int64_t rows,
  * Arguments and results are those of ce_fwd_bwd_fused minus the workspace.
  * Returns GBCE_EWORKSPACE, before any GPU work, when
  * gbce_workspace_size(rows, vocab, 1) > GBCE_NOALLOC_SCRATCH_BYTES (about
- * 130 000 rows at large vocabularies).  The first call on each device looks
- * up the array's device address (cudaGetSymbolAddress) with that device
- * current; make that first call before any stream capture.  All calls share
- * the one array: calls whose GPU work overlaps (e.g. on two streams) race and
- * must be serialized by the caller.  Nothing in the array needs zeroing:
- * each call writes every scratch value before reading it.
+ * 130 000 rows).  The first call on each device looks up the array's device
+ * address (cudaGetSymbolAddress) with that device current and keeps it for
+ * the rest of the process; make that first call before any stream capture.
+ * The kept address belongs to the device's primary context as it was then:
+ * after cudaDeviceReset (or any other reset of that context) it is stale,
+ * so a program that resets a device must not call this entry point on it
+ * afterwards.  All calls share the one array: calls whose GPU work overlaps
+ * (e.g. on two streams) race and must be serialized by the caller.  Nothing
+ * in the array needs zeroing beforehand: each call writes every scratch
+ * value it reads (the item count, the row ticket, the per-row losses) first.
  */
 #define GBCE_NOALLOC_SCRATCH_BYTES (1u << 20)
 gbce_status ce_fwd_bwd_fused_noalloc(const void *logits, gbce_dtype dtype, int64_t rows,

@@ -99,3 +99,30 @@ def assert_entropy_close(got, ref, what="entropy"):
     worst = rel.max() if rel.size else 0.0
     assert worst <= ENTROPY_TOL, f"{what}: worst relative error {worst:.3e} > {ENTROPY_TOL:.0e}"
     return worst
+
+
+def assert_grad_block_close(got, ref, dtype, what="dlogits", tol=None):
+    """assert_grad_rows_close for a block of rows at once (vectorized)."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape
+    tol = GRAD_TOL[dtype] if tol is None else tol
+    nan_rows = np.all(np.isnan(ref), axis=1)
+    assert np.all(np.isnan(got[nan_rows])), f"{what}: NaN rows differ"
+    ok = ~nan_rows
+    nr = np.linalg.norm(ref[ok], axis=1)
+    zero = nr == 0.0
+    assert np.all(got[ok][zero] == 0.0), f"{what}: a zero row is not exactly zero"
+    err = np.linalg.norm(got[ok][~zero] - ref[ok][~zero], axis=1) / nr[~zero]
+    worst = err.max() if err.size else 0.0
+    assert worst <= tol, f"{what}: worst row relative error {worst:.3e} > {tol:.0e}"
+    return worst
+
+
+def assert_zero_sum_block(got, dtype):
+    """assert_zero_sum_rows for a block of rows at once; numpy's pairwise fp64
+    sums (error far below the tolerance) instead of exact ones."""
+    got = np.asarray(got, dtype=np.float64)
+    s = np.abs(np.sum(got, axis=1))
+    a = np.sum(np.abs(got), axis=1)
+    assert np.all(s <= ZERO_SUM_TOL[dtype] * a), "a gradient row does not sum to zero"

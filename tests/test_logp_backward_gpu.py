@@ -7,7 +7,8 @@ import torch
 
 import oracle
 import workloads
-from helpers import assert_grad_rows_close, assert_zero_sum_rows, to_f64
+from helpers import (assert_grad_block_close, assert_grad_rows_close, assert_zero_sum_block,
+                     assert_zero_sum_rows, to_f64)
 
 pytestmark = pytest.mark.gpu
 
@@ -179,6 +180,28 @@ def test_entropy_term_matches_oracle(dtype, K):
     assert np.all(got[mask.numpy()[sel] == 0] == 0.0)
 
 
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("K", [1, 4])
+def test_entropy_term_rows_confident_in_another_column(dtype, K):
+    # the dominant column (margins 17..50) outside the gathered set, or (K = 4,
+    # even rows) gathered at index 1..3; rows 1 and 2 mod 4 have only the
+    # entropy's upstream, where that column's entry is most of the gradient
+    rows, V = 560, 24001
+    w = workloads.dominated_elsewhere(dtype, rows=rows, V=V, K=K, seed=90 + K)
+    gen = torch.Generator().manual_seed(91 + K)
+    g = torch.randn((rows, K), generator=gen)
+    g[(torch.arange(rows) % 4 == 1) | (torch.arange(rows) % 4 == 2)] = 0.0
+    gh = torch.randn(rows, generator=gen)
+    got, ref, status, bad = run_ent_case(w.logits, w.index, g, gh, 0.9)
+    assert status == 0 and bad == 0
+    assert_grad_rows_close(got, ref, dtype, "selective_logsoftmax_bwd + entropy")
+    assert_zero_sum_rows(got, dtype)
+    d = w.labels.numpy()
+    at_d = got[np.arange(rows), d]
+    want = ref[np.arange(rows), d]
+    assert np.all(np.sign(at_d) == np.sign(want)) and np.all(at_d != 0.0)
+
+
 def test_entropy_only_gradient_of_confident_rows():
     # g = 0: the gradient of the entropy alone; a confident row's dominant
     # column has d H / d x_t = -(p_t / T)(log p_t + H) < 0, tiny but not 0
@@ -222,12 +245,14 @@ def test_full_size_grpo_k4_with_entropy():
     d = gbce.selective_logsoftmax_bwd(w.logits, w.index, g, lp, 0.9, grad_entropy=gh,
                                       saved_entropy=h)
     torch.cuda.synchronize()
-    rng = np.random.default_rng(5)
-    sel = np.sort(np.concatenate([rng.choice(w.rows, 16, replace=False),
-                                  w.peaked_rows.cpu().numpy()[:8]]))
-    st = torch.as_tensor(sel, device=DEV)
-    ref, _ = oracle.selective_logsoftmax_backward(workloads.to_numpy_f64(w.logits[st]),
-                                                  w.index[st].cpu().numpy(),
-                                                  g[st].double().cpu().numpy(), 0.9,
-                                                  grad_entropy=gh[st].double().cpu().numpy())
-    assert_grad_rows_close(to_f64(d[st]), ref, torch.bfloat16)
+    # every row against the oracle, in row blocks
+    for r0 in range(0, w.rows, 512):
+        r1 = min(w.rows, r0 + 512)
+        ref, _ = oracle.selective_logsoftmax_backward(
+            workloads.to_numpy_f64(w.logits[r0:r1]), w.index[r0:r1].cpu().numpy(),
+            g[r0:r1].double().cpu().numpy(), 0.9,
+            grad_entropy=gh[r0:r1].double().cpu().numpy())
+        got = to_f64(d[r0:r1])
+        assert_grad_block_close(got, ref, torch.bfloat16)
+        assert_zero_sum_block(got, torch.bfloat16)
+        del got, ref

@@ -5,6 +5,7 @@ same bf16/fp32 logits.  Tolerances are in tests/helpers.py.
 """
 
 import hashlib
+import math
 
 import numpy as np
 import pytest
@@ -12,8 +13,8 @@ import torch
 
 import oracle
 import workloads
-from helpers import (assert_grad_rows_close, assert_logp_close, assert_loss_close,
-                     assert_zero_sum_rows, to_f64)
+from helpers import (assert_grad_block_close, assert_grad_rows_close, assert_logp_close,
+                     assert_loss_close, assert_zero_sum_block, assert_zero_sum_rows, to_f64)
 
 pytestmark = pytest.mark.gpu
 
@@ -37,12 +38,8 @@ def new_status():
     return torch.zeros(1, dtype=torch.int32, device=DEV)
 
 
-def run_all(w: workloads.Workload, temperature=None, reduction=None, grad_out=None,
-            rows_sel=None):
-    """Every entry point on one workload; oracle on `rows_sel` (default all rows)."""
-    T = w.temperature if temperature is None else temperature
-    red = w.reduction if reduction is None else reduction
-    g = w.grad_out if grad_out is None else grad_out
+def run_gpu(w: workloads.Workload, T, red, g):
+    """Every entry point on one workload, on the GPU."""
     x = w.logits.to(DEV)
     lab = w.labels.to(DEV)
     status = new_status()
@@ -58,20 +55,34 @@ def run_all(w: workloads.Workload, temperature=None, reduction=None, grad_out=No
                                          want_lse=True, dev_status=status)
     torch.cuda.synchronize()
     res["status"] = int(status.item())
+    return res
+
+
+def upstream_rows(w, red, g, sel):
+    """Each selected row's upstream gradient (the mean's 1/n_items folded in)."""
+    n_full = int((w.labels.cpu().numpy() != workloads.IGNORE_INDEX).sum())
+    g_np = g.cpu().double().numpy()
+    if red == "none":
+        return g_np[sel], n_full
+    if red == "sum":
+        return np.full(len(sel), g_np[0]), n_full
+    return np.full(len(sel), g_np[0] / n_full if n_full else 0.0), n_full
+
+
+def run_all(w: workloads.Workload, temperature=None, reduction=None, grad_out=None,
+            rows_sel=None):
+    """Every entry point on one workload; oracle on `rows_sel` (default all rows)."""
+    T = w.temperature if temperature is None else temperature
+    red = w.reduction if reduction is None else reduction
+    g = w.grad_out if grad_out is None else grad_out
+    res = run_gpu(w, T, red, g)
 
     sel = np.arange(w.rows) if rows_sel is None else np.asarray(rows_sel)
     x64 = workloads.to_numpy_f64(w.logits[torch.as_tensor(sel)])
     lab_np = w.labels.cpu().numpy()
     mask_np = None if w.row_mask is None else w.row_mask.cpu().numpy()[sel]
     ref_lp, _ = oracle.selective_logsoftmax(x64, w.index.cpu().numpy()[sel], T, mask_np)
-    n_full = int((lab_np != workloads.IGNORE_INDEX).sum())
-    g_np = g.cpu().double().numpy()
-    if red == "none":
-        g_rows = g_np[sel]
-    elif red == "sum":
-        g_rows = np.full(len(sel), g_np[0])
-    else:
-        g_rows = np.full(len(sel), g_np[0] / n_full if n_full else 0.0)
+    g_rows, n_full = upstream_rows(w, red, g, sel)
     ref = oracle.cross_entropy(x64, lab_np[sel], temperature=T, reduction="none",
                                grad_out=g_rows)
     ref["n_full"] = n_full
@@ -178,12 +189,53 @@ def sample_rows(w, n_plain=24, seed=0):
     return np.array(sorted(rows))
 
 
+def check_every_row(w, res, T, red, g, block=512):
+    """Every row of a full-size run against the oracle, in row blocks (host
+    memory stays bounded): both log-probs, the lse, both gradients and
+    their zero sums; then the reduced loss against the oracle's own."""
+    dt = w.logits.dtype
+    assert res["status"] == 0
+    fwd, fused = res["fwd"], res["fused"]
+    lab_np = w.labels.cpu().numpy()
+    mask_np = None if w.row_mask is None else w.row_mask.cpu().numpy()
+    g_all, n_full = upstream_rows(w, red, g, np.arange(w.rows))
+    assert int(fwd.n_items.item()) == n_full == int(fused.n_items.item())
+    loss_rows = np.empty(w.rows)
+    Te = oracle.exact_temperature(T)
+    for r0 in range(0, w.rows, block):
+        r1 = min(w.rows, r0 + block)
+        x64 = workloads.to_numpy_f64(w.logits[r0:r1])
+        ref_sel, _ = oracle.selective_logsoftmax(
+            x64, w.index[r0:r1].cpu().numpy(), T, None if mask_np is None else mask_np[r0:r1])
+        assert_logp_close(to_f64(res["logp_sel"][r0:r1]), ref_sel, dt, "selective")
+        ref = oracle.cross_entropy(x64, lab_np[r0:r1], temperature=T, reduction="none",
+                                   grad_out=g_all[r0:r1])
+        for name, lp in (("ce_fwd logp", fwd.logp), ("fused logp", fused.logp)):
+            assert_logp_close(to_f64(lp[r0:r1]), ref["logp"], dt, name)
+        live = lab_np[r0:r1] != workloads.IGNORE_INDEX
+        lse = to_f64(fwd.lse[r0:r1])
+        assert np.all(lse[~live] == 0.0)
+        xy = x64[np.arange(r1 - r0), np.where(live, lab_np[r0:r1], 0)]
+        np.testing.assert_allclose(lse[live], (xy / Te - ref["logp"])[live], rtol=2e-6,
+                                   atol=2e-6)
+        loss_rows[r0:r1] = ref["loss_rows"]
+        for name, d in (("ce_bwd", res["bwd"]), ("fused", fused.dlogits)):
+            got = to_f64(d[r0:r1])
+            assert_grad_block_close(got, ref["dlogits"], dt, name)
+            assert_zero_sum_block(got, dt)
+            del got
+        del x64, ref
+    total = math.fsum(loss_rows)
+    want = total if red == "sum" else (total / n_full if n_full else 0.0)
+    assert_loss_close(float(fwd.loss.item()), want, "ce_fwd loss vs oracle")
+    assert_loss_close(float(fused.loss.item()), want, "fused loss vs oracle")
+
+
 def test_grpo_bf16_8192x152064_k4_full_size():
-    """Full size, launch configuration of the benchmark; oracle on sampled rows."""
+    """Full size, launch configuration of the benchmark; every row against the oracle."""
     w = workloads.grpo_bf16(device=DEV)
-    sel = sample_rows(w)
-    res, ref, sel = run_all(w, rows_sel=sel)
-    check_all(w, res, ref, sel)
+    res = run_gpu(w, w.temperature, w.reduction, w.grad_out)
+    check_every_row(w, res, w.temperature, w.reduction, w.grad_out)
     # invariants on every row
     lp = res["logp_sel"]
     assert bool(torch.all(lp <= 0)) and bool(torch.all(torch.isfinite(lp)))
@@ -201,9 +253,8 @@ def test_grpo_bf16_8192x152064_k4_full_size():
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 def test_collapse_stress_2048x151936_full_size(dtype):
     w = workloads.collapse_stress(dtype=dtype, device=DEV)
-    sel = sample_rows(w, n_plain=32, seed=1)
-    res, ref, sel = run_all(w, rows_sel=sel)
-    check_all(w, res, ref, sel)
+    res = run_gpu(w, w.temperature, w.reduction, w.grad_out)
+    check_every_row(w, res, w.temperature, w.reduction, w.grad_out)
     fused = res["fused"]
     live = (w.labels != workloads.IGNORE_INDEX)
     assert int(fused.n_items.item()) == int(live.sum().item()) == 2048 - 205
@@ -265,10 +316,12 @@ def test_strided_misaligned_rows_and_unaligned_dlogits(dtype):
     assert_loss_close(float(out.loss.item()), ref["loss"])
 
 
-@pytest.mark.parametrize("rows", [1, 3, 100])
+@pytest.mark.parametrize("rows", [1, 3, 64, 100, 200])
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 def test_few_rows_split_vocab(rows, dtype):
-    """Few rows with a large vocabulary take the split partial + combine path."""
+    """Few rows with a large vocabulary split it: each row's slices run as one
+    cluster of CTAs that swap their partials through distributed shared memory
+    (8 slices at 1 and 3 rows, 7 at 64, 4 at 100, 2 at 200 on 152 SMs)."""
     w = workloads.collapse_stress(dtype=dtype, rows=rows, V=152064, seed=rows)
     res, ref, sel = run_all(w, temperature=0.9)
     check_all(w, res, ref, sel, T=0.9)
@@ -377,15 +430,15 @@ def test_stream_argument_is_honoured():
     assert_loss_close(float(out.loss.item()), ref["loss"])
 
 
-# ------------------------------------------------ persistent / cluster paths
+# ------------------------------------------- persistent fused kernel shapes
 
 @pytest.mark.parametrize("dtype,V", [
-    (torch.bfloat16, 40001),     # row 80 KB: one CTA holds the row
-    (torch.float32, 100003),     # 400 KB: a 3-CTA cluster, misaligned rows
-    (torch.bfloat16, 262144),    # 512 KB: a 4-CTA cluster
-    (torch.float32, 500000),     # 2 MB: too long for 8 CTAs, L2 re-read kernel
+    (torch.bfloat16, 40001),     # row 80 KB
+    (torch.float32, 100003),     # 400 KB, misaligned rows
+    (torch.bfloat16, 262144),    # 512 KB
+    (torch.float32, 500000),     # 2 MB: the rows in flight no longer all fit L2
 ])
-def test_fused_cluster_shapes(dtype, V):
+def test_fused_persistent_row_sizes(dtype, V):
     w = workloads.collapse_stress(dtype=dtype, rows=520, V=V, seed=V % 97)
     sel = sample_rows(w, n_plain=16, seed=2)
     res, ref, sel = run_all(w, temperature=0.7, rows_sel=sel)
@@ -393,7 +446,7 @@ def test_fused_cluster_shapes(dtype, V):
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
-def test_fused_cluster_strided_rows_and_unaligned_dlogits(dtype):
+def test_fused_persistent_strided_rows_and_unaligned_dlogits(dtype):
     g = torch.Generator().manual_seed(17)
     rows, V = 520, 70001
     big = torch.randn((rows, V + 9), generator=g).mul(2).to(dtype)

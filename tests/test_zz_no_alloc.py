@@ -3,10 +3,10 @@ cannot give the library a workspace (a C program or plugin with no device
 allocator of its own, which must not call cudaMalloc on its hot path).
 
 Its scratch is a fixed array inside the library, shared by every call.  These
-tests call it through the C ABI twice in a row, with different problems so
-that the second call runs over what the first left in the array, and compare
-each result with the workspace-taking ce_fwd_bwd_fused on the same inputs.
-The file is named to be collected last.
+tests call it through the C ABI several times in a row, with different
+problems so that each call runs over what the previous one left in the array,
+and compare each result with the workspace-taking ce_fwd_bwd_fused on the
+same inputs and with the fp64 oracle.  The file is named to be collected last.
 """
 
 import ctypes
@@ -15,6 +15,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import workloads
 from helpers import assert_grad_rows_close, assert_logp_close, assert_loss_close, to_f64
 
@@ -76,21 +77,46 @@ def _compare(got, ref, dtype):
     assert_grad_rows_close(to_f64(d), to_f64(ref.dlogits), dtype, "noalloc dlogits")
 
 
-def test_two_calls_in_a_row_match_the_workspace_entry_point(lib):
-    # call 1: many rows, mean, bf16 -> per-row losses and the item count in scratch
+def _against_oracle(got, w, grad, T, red, dtype):
+    """The no-allocation call's outputs against the fp64 oracle."""
+    loss, logp, _, n, d = got
+    names = {0: "none", 1: "sum", 2: "mean"}
+    ref = oracle.cross_entropy(workloads.to_numpy_f64(w.logits), w.labels.numpy(), temperature=T,
+                               reduction=names[red], grad_out=grad.double().cpu().numpy())
+    assert int(n.item()) == ref["n_items"]
+    assert_logp_close(to_f64(logp), ref["logp"], dtype, "noalloc logp vs oracle")
+    if red == 0:
+        assert_logp_close(-to_f64(loss), -ref["loss_rows"], dtype, "noalloc rows vs oracle")
+    else:
+        assert_loss_close(float(loss.item()), ref["loss"], "noalloc loss vs oracle")
+    assert_grad_rows_close(to_f64(d), ref["dlogits"], dtype, "noalloc dlogits vs oracle")
+
+
+def test_calls_in_a_row_match_the_workspace_entry_point_and_the_oracle(lib):
+    # call 1: many rows, mean, bf16 -> the persistent kernel's row ticket, the
+    # per-row losses and the item count in scratch
     w1 = workloads.collapse_stress(dtype=torch.bfloat16, rows=700, V=32000, seed=11)
     x1, l1 = w1.logits.to(DEV), w1.labels.to(DEV)
     g1 = torch.ones(1, device=DEV)
     got1 = _noalloc(lib, x1, l1, g1, 0.9, 2)
     _compare(got1, _reference(x1, l1, g1, 0.9, 2), torch.bfloat16)
-    # call 2: few rows, large vocabulary, fp32, sum -> the split path's partials
-    # land in the same scratch the first call left behind
+    _against_oracle(got1, w1, g1, 0.9, 2, torch.bfloat16)
+    # call 2: few rows, large vocabulary, fp32, sum -> a vocabulary split,
+    # over what the first call left in the scratch
     w2 = workloads.collapse_stress(dtype=torch.float32, rows=3, V=152064, seed=12)
     x2, l2 = w2.logits.to(DEV), w2.labels.to(DEV)
     g2 = torch.tensor([0.5], device=DEV)
     got2 = _noalloc(lib, x2, l2, g2, 1.0, 1)
     _compare(got2, _reference(x2, l2, g2, 1.0, 1), torch.float32)
-    # and the first problem again, now over the second call's leftovers
+    _against_oracle(got2, w2, g2, 1.0, 1, torch.float32)
+    # call 3: reduction none with a per-row upstream gradient
+    w3 = workloads.collapse_stress(dtype=torch.bfloat16, rows=300, V=4099, seed=13)
+    x3, l3 = w3.logits.to(DEV), w3.labels.to(DEV)
+    g3 = torch.randn(300, generator=torch.Generator().manual_seed(3)).to(DEV)
+    got3 = _noalloc(lib, x3, l3, g3, 0.7, 0)
+    _compare(got3, _reference(x3, l3, g3, 0.7, 0), torch.bfloat16)
+    _against_oracle(got3, w3, g3, 0.7, 0, torch.bfloat16)
+    # and the first problem again, now over the other calls' leftovers
     again = _noalloc(lib, x1, l1, g1, 0.9, 2)
     _compare(again, _reference(x1, l1, g1, 0.9, 2), torch.bfloat16)
 

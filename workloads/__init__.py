@@ -228,6 +228,32 @@ def peaked_rows_tiny(V: int, margins, dtype=torch.float64, temperature: float = 
                     margins=m)
 
 
+def dominated_elsewhere(dtype, rows: int, V: int, K: int, seed: int = 0,
+                        device="cpu") -> Workload:
+    """Confident rows whose dominant column is not the first gathered index.
+
+    N(0,1) logits; every row gets one column d with x_d = max_{j != d} x_j +
+    margin, margins cycling 17/20/30/50 (the collapse margins).  The first
+    gathered index is never d.  With K > 1, every other row gathers d at an
+    index k > 0; the other rows leave d out of the gathered set (a sampled
+    token that is not the row's argmax).
+    """
+    g = _gen(seed, "cpu")
+    logits = torch.randn((rows, V), generator=g).to(dtype)
+    d = torch.randint(0, V, (rows,), generator=g)
+    margins = torch.tensor([17.0, 20.0, 30.0, 50.0]).repeat((rows + 3) // 4)[:rows]
+    set_target_margin(logits, torch.arange(rows), d, margins)
+    index = torch.randint(0, V, (rows, K), generator=g)
+    index = torch.where(index == d[:, None], (index + 1) % V, index)
+    if K > 1:
+        k = 1 + torch.arange(rows) % (K - 1)
+        even = torch.arange(rows) % 2 == 0
+        index[even, k[even]] = d[even]
+    return Workload(f"dominated_elsewhere_{rows}x{V}_k{K}", logits.to(device), d.to(device),
+                    index.to(device), None, 1.0, "sum", torch.ones(1, device=device),
+                    peaked_rows=torch.arange(rows), margins=margins)
+
+
 def to_numpy_f64(t: torch.Tensor):
     """Exact fp64 copy of bf16/fp32/fp64 logits for the oracle."""
     return t.detach().to("cpu").to(torch.float64).numpy()
