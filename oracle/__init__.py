@@ -31,8 +31,14 @@ Functions and the passages they follow:
   smoothing included there); the DFT variant weights each row by p_y, held
   constant in the backward (ms-swift PR #10353, "PR information").
 
+* :func:`vocab_slice_partials`, :func:`vocab_slice_combine` -- the same
+  log-probs computed from slices of the vocabulary: each slice's max and
+  sum over its non-target columns and the target logits it holds, merged
+  in slice order (the vocab-parallel bullet of the same page's "Summary").
+
 Pins: closed forms, 120-digit brute force, invariants and the pages' collapse
-thresholds, in ``tests/test_oracle_pins.py``.
+thresholds, in ``tests/test_oracle_pins.py``; the slice functions against
+the full-row log-probs for many slicings and against brute force.
 """
 
 from __future__ import annotations
@@ -244,3 +250,89 @@ def cross_entropy(x, labels, ignore_index: int = -100, temperature: float = 1.0,
         dx.ctypes.data if dx is not None else None, V)
     return {"logp": logp, "loss_rows": loss_rows, "loss": float(loss[0]),
             "n_items": int(n_items[0]), "dlogits": dx, "n_bad": int(bad)}
+
+
+def vocab_slice_partials(x_slice, index, vocab_offset: int, temperature: float = 1.0,
+                         row_mask=None):
+    """Statistics of one vocabulary slice, global columns [vocab_offset,
+    vocab_offset + n): over its columns that are not gathered targets,
+    m = max z_j and s = sum_j exp(z_j - m) (z = x / T), and the logit of
+    every target the slice holds (0 for the others).  The vocab-parallel
+    form of "Fix softmax collapse in CE, GRPO, KL/JSD and softmax"
+    ("Summary", first bullet): every shard keeps the sum without the target.
+
+    Returns ``(m[rows], s[rows], xt[rows, K])`` in fp64; rows with
+    row_mask == 0 give (-inf, 0, 0).
+    """
+    x = _as_rows(x_slice)
+    rows, n = x.shape
+    idx = np.asarray(index, dtype=np.int64).reshape(rows, -1)
+    T = exact_temperature(temperature)
+    local = idx - int(vocab_offset)
+    owned = (local >= 0) & (local < n)
+    z = x / T
+    zm = z.copy()
+    r_ix = np.repeat(np.arange(rows), idx.shape[1])
+    zm[r_ix[owned.ravel()], local[owned]] = -np.inf
+    m = zm.max(axis=1) if n else np.full(rows, -np.inf)
+    with np.errstate(invalid="ignore"):
+        s = np.where(np.isfinite(m), np.exp(zm - m[:, None]).sum(axis=1), 0.0)
+    xt = np.zeros(idx.shape, dtype=np.float64)
+    xt[owned] = x[r_ix[owned.ravel()], local[owned]]
+    if row_mask is not None:
+        dead = np.asarray(row_mask).reshape(rows) == 0
+        m[dead], s[dead], xt[dead] = -np.inf, 0.0, 0.0
+    return m, s, xt
+
+
+def vocab_slice_combine(parts, offsets, index, temperature: float = 1.0, row_mask=None):
+    """log p at the gathered indices from the slices' partials.
+
+    ``parts`` is a list (slice order) of ``(m, s, xt)`` from
+    :func:`vocab_slice_partials`; ``offsets`` the slices' first global
+    columns plus the vocabulary size at the end.  The (m, s) of all slices
+    are merged into the state of every non-target column, each target's
+    logit is taken from the slice that holds it, and log p_t follows the
+    single-device form: the other targets join t's "others", then
+    log p_t = -softplus(log s + (m - x_t) / T).  Masked rows give 0.
+    Returns ``(logp[rows, K], xt0[rows])``.
+    """
+    T = exact_temperature(temperature)
+    idx = np.asarray(index, dtype=np.int64)
+    rows = idx.shape[0]
+    idx = idx.reshape(rows, -1)
+    K = idx.shape[1]
+    ms = np.stack([p[0] for p in parts])        # [S, rows]
+    ss = np.stack([p[1] for p in parts])
+    M = ms.max(axis=0)
+    with np.errstate(invalid="ignore"):
+        S = np.where(np.isfinite(M), np.sum(np.where(np.isfinite(ms), ss * np.exp(ms - M), 0.0),
+                                            axis=0), 0.0)
+    off = np.asarray(offsets, dtype=np.int64)
+    owner = np.searchsorted(off, idx, side="right") - 1   # slice of each target
+    xt = np.zeros((rows, K))
+    for r in range(rows):
+        for k in range(K):
+            xt[r, k] = parts[owner[r, k]][2][r, k]
+    logp = np.zeros((rows, K))
+    for r in range(rows):
+        if row_mask is not None and np.asarray(row_mask).reshape(rows)[r] == 0:
+            continue
+        for k in range(K):
+            m, s = M[r], S[r]
+            seen = set()
+            for j in range(K):
+                tj = int(idx[r, j])
+                if tj == int(idx[r, k]) or tj in seen:
+                    continue
+                seen.add(tj)
+                zj = xt[r, j] / T
+                if zj > m:
+                    s = s * np.exp(m - zj) + 1.0
+                    m = zj
+                else:
+                    s = s + np.exp(zj - m)
+            a = (np.log(s) if s > 0 else -np.inf) + (m - xt[r, k] / T)
+            logp[r, k] = -(max(a, 0.0) + np.log1p(np.exp(-abs(a)))) if np.isfinite(a) else \
+                (0.0 if a < 0 else -np.inf)
+    return logp, xt[:, 0]

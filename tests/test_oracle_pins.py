@@ -788,3 +788,41 @@ def test_softcap_limits_closed_form_and_finite_differences():
             # abs: one ulp of a loss of order 10 over 2h is about 1e-9
             assert d[r, j] == pytest.approx((fp["loss"] - fm["loss"]) / (2 * h),
                                             rel=2e-6, abs=5e-9)
+
+
+# ----------------------------------------------- vocabulary-slice partials
+
+@pytest.mark.parametrize("cuts", [[0, 33], [0, 16, 33], [0, 1, 5, 20, 33], [0, 32, 33]])
+@pytest.mark.parametrize("T", [1.0, 0.7])
+def test_vocab_slices_reproduce_the_full_row(cuts, T):
+    # slicing the vocabulary anywhere (slices of one column, targets at the
+    # edges, duplicates, a masked row, collapse margins) and merging the
+    # slices' partials gives the full-row log-probs
+    rng = np.random.default_rng(len(cuts) + int(T * 10))
+    V = 33
+    w = workloads.peaked_rows_tiny(V, [0.0, 17.0, 30.0, 50.0], seed=41)
+    x = w.logits.numpy()
+    y = w.labels.numpy()
+    idx = np.stack([y, rng.integers(0, V, 4), np.full(4, V - 1), y], axis=1)
+    mask = np.array([1, 1, 0, 1], dtype=np.uint8)
+    full, _ = oracle.selective_logsoftmax(x, idx, T, mask)
+    parts = [oracle.vocab_slice_partials(x[:, a:b], idx, a, T, mask)
+             for a, b in zip(cuts[:-1], cuts[1:])]
+    got, xt0 = oracle.vocab_slice_combine(parts, cuts, idx, T, mask)
+    np.testing.assert_allclose(got, full, rtol=1e-13, atol=0.0)
+    np.testing.assert_array_equal(xt0[mask == 1], x[np.arange(4), idx[:, 0]][mask == 1])
+
+
+def test_vocab_slices_brute_force_on_confident_rows():
+    V, T = 9, 0.9
+    w = workloads.peaked_rows_tiny(V, [17.0, 50.0], seed=43)
+    x = w.logits.numpy()
+    y = w.labels.numpy()
+    idx = y[:, None]
+    parts = [oracle.vocab_slice_partials(x[:, a:b], idx, a, T) for a, b in ((0, 4), (4, 9))]
+    got, _ = oracle.vocab_slice_combine(parts, [0, 4, 9], idx, T)
+    Te = oracle.exact_temperature(T)
+    for r in range(2):
+        _, want = brute_row(x[r], y[r], Te)
+        assert got[r, 0] == pytest.approx(float(want), rel=1e-12), r
+        assert got[r, 0] < 0.0
