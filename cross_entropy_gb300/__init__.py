@@ -20,6 +20,12 @@ Functions (same names as the C ABI):
   g*softmax - g*onehot of ms-swift PR #10353 ("PR information"), optional
   label smoothing, DFT row weights and logit soft-capping.
 * :func:`ce_fwd_bwd_fused_noalloc` -- the fused call without a workspace.
+* :func:`vocab_slice_stats`, :func:`vocab_slice_combine`,
+  :func:`vocab_slice_grad` -- the selective log-softmax (and token CE) over
+  a vocabulary split into slices, e.g. one per device of a vocab-parallel
+  head ("Fix softmax collapse ...", "Summary", first bullet), with
+  :func:`gather_slice_partials` moving the per-slice statistics between
+  ranks through torch.distributed.
 
 Caller-supplied output, scratch and status tensors are checked for device,
 dtype and size before any GPU work: the kernels write through their data
@@ -63,7 +69,14 @@ _SIGNATURES = {
                                 _vp, _vp, _vp, _vp, _vp, _i64, _vp, _sz, _vp, _vp]),
     "ce_fwd_bwd_fused_noalloc": (_i32, [_vp, _i32, _i64, _i64, _i64, _vp, _i64, _f32, _i32,
                                         _vp, _vp, _vp, _vp, _vp, _vp, _i64, _vp, _vp]),
+    "vocab_slice_stats": (_i32, [_vp, _i32, _i64, _i64, _i64, _i64, _i64, _vp, _i64, _i64, _vp,
+                                 _f32, _vp, _vp, _vp]),
+    "vocab_slice_combine": (_i32, [_vp, _i64, _vp, _i64, _vp, _i64, _i64, _vp, _f32, _vp, _vp,
+                                   _vp, _vp]),
+    "vocab_slice_grad": (_i32, [_vp, _i32, _i64, _i64, _i64, _i64, _i64, _vp, _i64, _i64, _vp,
+                                _f32, _vp, _vp, _vp, _vp, _i64, _vp, _vp]),
 }
+MAX_SLICES = 64
 
 _lib = None
 
@@ -451,3 +464,128 @@ def ce_fwd_bwd_fused_noalloc(logits: torch.Tensor, labels, grad_out=None,
                                           _ptr(dev_status), _stream_ptr(stream, x.device))
     _check(st, "ce_fwd_bwd_fused_noalloc")
     return CeFused(loss if red == 0 else loss[0], dlogits, logp, None, n_items[0])
+
+
+# ------------------------------------------------ vocabulary-parallel path
+
+def _slice_index(index, lead_shape, rows, device):
+    idx = _dev_int64(index, device)
+    K = 1 if idx.dim() == len(lead_shape) else idx.shape[-1]
+    return idx.reshape(rows, K).contiguous(), K
+
+
+def vocab_slice_stats(logits_slice: torch.Tensor, index, vocab_offset: int, vocab: int,
+                      temperature: float = 1.0, row_mask: Optional[torch.Tensor] = None, *,
+                      ignore_index: int = -100, out: Optional[torch.Tensor] = None,
+                      dev_status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Partials [rows, 2 + K] fp32 of one vocabulary slice: the max and the
+    sum over its non-target columns and the logits of the targets it holds.
+
+    ``logits_slice`` [..., n] holds global columns [vocab_offset, vocab_offset
+    + n) of a ``vocab``-column vocabulary; ``index`` [..., K] (or [...]) holds
+    global columns.  Rows with ``row_mask == 0`` or whose first index equals
+    ``ignore_index`` are skipped.
+    """
+    lib = load_library()
+    lead_shape = logits_slice.shape[:-1]
+    x = _rows_view(logits_slice)
+    rows, n = x.shape
+    idx, K = _slice_index(index, lead_shape, rows, x.device)
+    mask = None
+    if row_mask is not None:
+        mask = row_mask.to(device=x.device, dtype=torch.uint8).reshape(rows).contiguous()
+    if out is None:
+        out = torch.empty((rows, 2 + K), dtype=torch.float32, device=x.device)
+    _check_buffer(out, "out", torch.float32, rows * (2 + K), x.device)
+    _check_status(dev_status, x.device)
+    with torch.cuda.device(x.device):
+        st = lib.vocab_slice_stats(x.data_ptr(), _dtype_code(x), rows, n, x.stride(0),
+                                   int(vocab_offset), int(vocab), idx.data_ptr(), K,
+                                   int(ignore_index), _ptr(mask), float(temperature),
+                                   out.data_ptr(), _ptr(dev_status),
+                                   _stream_ptr(stream, x.device))
+    _check(st, "vocab_slice_stats")
+    return out
+
+
+def gather_slice_partials(partials: torch.Tensor, group=None) -> torch.Tensor:
+    """All ranks' partials stacked in rank order, [world, rows, 2 + K]: the one
+    exchange of the vocab-parallel path (rank i holds slice i).  With no
+    initialised process group, the local partials as a single slice."""
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()):
+        return partials.unsqueeze(0)
+    world = dist.get_world_size(group)
+    parts = [torch.empty_like(partials) for _ in range(world)]
+    dist.all_gather(parts, partials.contiguous(), group=group)
+    return torch.stack(parts)
+
+
+def vocab_slice_combine(partials: torch.Tensor, slice_offsets, index, temperature: float = 1.0,
+                        row_mask: Optional[torch.Tensor] = None, *, ignore_index: int = -100,
+                        dev_status: Optional[torch.Tensor] = None, stream=None):
+    """log p [rows, K] (and the logit of index[:, 0], [rows]) from all slices'
+    partials stacked in slice order, [slices, rows, 2 + K]; ``slice_offsets``
+    are the slices' first global columns followed by the vocabulary size."""
+    lib = load_library()
+    if not partials.is_cuda or partials.dtype != torch.float32 or partials.dim() != 3:
+        raise ValueError("partials must be a float32 CUDA tensor [slices, rows, 2 + K]")
+    slices, rows, width = partials.shape
+    K = width - 2
+    offs = [int(o) for o in slice_offsets]
+    if len(offs) != slices + 1:
+        raise ValueError("slice_offsets needs one entry per slice plus the vocabulary size")
+    idx = _dev_int64(index, partials.device).reshape(rows, -1).contiguous()
+    if idx.shape[1] != K:
+        raise ValueError("index must have K columns, as the partials")
+    mask = None
+    if row_mask is not None:
+        mask = row_mask.to(device=partials.device, dtype=torch.uint8).reshape(rows).contiguous()
+    part = partials.contiguous()
+    logp = torch.empty((rows, K), dtype=torch.float32, device=partials.device)
+    xt0 = torch.empty(rows, dtype=torch.float32, device=partials.device)
+    host_offs = (ctypes.c_int64 * len(offs))(*offs)
+    _check_status(dev_status, partials.device)
+    with torch.cuda.device(partials.device):
+        st = lib.vocab_slice_combine(part.data_ptr(), slices, ctypes.cast(host_offs, _vp), rows,
+                                     idx.data_ptr(), K, int(ignore_index), _ptr(mask),
+                                     float(temperature), logp.data_ptr(), xt0.data_ptr(),
+                                     _ptr(dev_status), _stream_ptr(stream, partials.device))
+    _check(st, "vocab_slice_combine")
+    return logp, xt0
+
+
+def vocab_slice_grad(logits_slice: torch.Tensor, index, vocab_offset: int, vocab: int,
+                     grad_logp, logp: torch.Tensor, target_logit: torch.Tensor,
+                     temperature: float = 1.0, row_mask: Optional[torch.Tensor] = None, *,
+                     ignore_index: int = -100, dlogits: Optional[torch.Tensor] = None,
+                     dev_status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """dL/d logits_slice for upstream grad_logp = dL/d logp, from the combined
+    log-probs and target logit of :func:`vocab_slice_combine`."""
+    lib = load_library()
+    lead_shape = logits_slice.shape[:-1]
+    x = _rows_view(logits_slice)
+    rows, n = x.shape
+    idx, K = _slice_index(index, lead_shape, rows, x.device)
+    g = torch.as_tensor(grad_logp, dtype=torch.float32, device=x.device).reshape(rows, K)
+    g = g.contiguous()
+    lp = logp.to(device=x.device, dtype=torch.float32).reshape(rows, K).contiguous()
+    xt = target_logit.to(device=x.device, dtype=torch.float32).reshape(rows).contiguous()
+    mask = None
+    if row_mask is not None:
+        mask = row_mask.to(device=x.device, dtype=torch.uint8).reshape(rows).contiguous()
+    if dlogits is None:
+        dlogits = torch.empty_like(logits_slice)
+    d = _rows_view(dlogits)
+    _check_dlogits(d, x)
+    _check_status(dev_status, x.device)
+    with torch.cuda.device(x.device):
+        st = lib.vocab_slice_grad(x.data_ptr(), _dtype_code(x), rows, n, x.stride(0),
+                                  int(vocab_offset), int(vocab), idx.data_ptr(), K,
+                                  int(ignore_index), _ptr(mask), float(temperature),
+                                  g.data_ptr(), lp.data_ptr(), xt.data_ptr(), d.data_ptr(),
+                                  d.stride(0), _ptr(dev_status), _stream_ptr(stream, x.device))
+    _check(st, "vocab_slice_grad")
+    return dlogits
+

@@ -21,7 +21,7 @@ BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libgbce.so")
 
 SOURCES = ["gbce_api.cu", "gbce_reduce.cu", "gbce_kernels_f32.cu", "gbce_kernels_bf16.cu",
-           "gbce_noalloc.cu"]
+           "gbce_noalloc.cu", "gbce_slices.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE]
 

@@ -502,4 +502,99 @@ gbce_status ce_fwd_bwd_fused(const void *logits, gbce_dtype dtype, int64_t rows,
     return cuda_status(e);
 }
 
+gbce_status vocab_slice_stats(const void *logits, gbce_dtype dtype, int64_t rows,
+                              int64_t slice_vocab, int64_t row_stride, int64_t vocab_offset,
+                              int64_t vocab, const int64_t *index, int64_t k,
+                              int64_t ignore_index, const uint8_t *row_mask, float temperature,
+                              float *partials, int32_t *dev_status, void *stream)
+{
+    gbce_status st = check_logits(logits, dtype, rows, slice_vocab, row_stride, temperature);
+    if (st != GBCE_OK)
+        return st;
+    if (k < 1 || k > GBCE_MAX_K || vocab_offset < 0 || vocab > kMaxVocab ||
+        vocab_offset > vocab - slice_vocab)
+        return GBCE_EINVAL;
+    if (rows == 0)
+        return GBCE_OK;
+    if (index == nullptr || partials == nullptr)
+        return GBCE_EINVAL;
+    RowParams p = base_params(logits, dtype, rows, slice_vocab, row_stride, temperature,
+                              dev_status);
+    p.targets = index;
+    p.k = k;
+    p.ignore_index = ignore_index;
+    p.row_mask = row_mask;
+    p.vocab_offset = vocab_offset;
+    p.vocab_total = vocab;
+    p.slice_partials = partials;
+    return cuda_status(launch_rows(p, dtype, gbce::kModeSliceStats,
+                                   static_cast<cudaStream_t>(stream)));
+}
+
+gbce_status vocab_slice_combine(const float *partials, int64_t slices,
+                                const int64_t *slice_offsets, int64_t rows, const int64_t *index,
+                                int64_t k, int64_t ignore_index, const uint8_t *row_mask,
+                                float temperature, float *logp_out, float *target_logit_out,
+                                int32_t *dev_status, void *stream)
+{
+    if (slices < 1 || slices > GBCE_MAX_SLICES || slice_offsets == nullptr || rows < 0 ||
+        k < 1 || k > GBCE_MAX_K || !(std::isfinite(temperature) && temperature > 0.0f))
+        return GBCE_EINVAL;
+    gbce::SliceOffsets offs{};
+    if (slice_offsets[0] != 0 || slice_offsets[slices] > kMaxVocab)
+        return GBCE_EINVAL;
+    for (int64_t i = 0; i <= slices; ++i) {
+        if (i > 0 && slice_offsets[i] <= slice_offsets[i - 1])
+            return GBCE_EINVAL;
+        offs.off[i] = slice_offsets[i];
+    }
+    if (rows == 0)
+        return GBCE_OK;
+    if (partials == nullptr || index == nullptr || logp_out == nullptr)
+        return GBCE_EINVAL;
+    const float c = static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
+    return cuda_status(gbce::launch_slice_combine(
+        partials, static_cast<int>(slices), offs, rows, index, k, ignore_index, row_mask,
+        temperature, c, logp_out, target_logit_out, dev_status,
+        static_cast<cudaStream_t>(stream)));
+}
+
+gbce_status vocab_slice_grad(const void *logits, gbce_dtype dtype, int64_t rows,
+                             int64_t slice_vocab, int64_t row_stride, int64_t vocab_offset,
+                             int64_t vocab, const int64_t *index, int64_t k, int64_t ignore_index,
+                             const uint8_t *row_mask, float temperature, const float *grad_logp,
+                             const float *logp, const float *target_logit, void *dlogits,
+                             int64_t dlogits_row_stride, int32_t *dev_status, void *stream)
+{
+    gbce_status st = check_logits(logits, dtype, rows, slice_vocab, row_stride, temperature);
+    if (st != GBCE_OK)
+        return st;
+    if (k < 1 || k > GBCE_MAX_K || vocab_offset < 0 || vocab > kMaxVocab ||
+        vocab_offset > vocab - slice_vocab)
+        return GBCE_EINVAL;
+    if (rows == 0)
+        return GBCE_OK;
+    if (index == nullptr || grad_logp == nullptr || logp == nullptr || target_logit == nullptr)
+        return GBCE_EINVAL;
+    if ((st = check_dlogits(logits, dtype, rows, slice_vocab, row_stride, dlogits,
+                            dlogits_row_stride)) != GBCE_OK)
+        return st;
+    RowParams p = base_params(logits, dtype, rows, slice_vocab, row_stride, temperature,
+                              dev_status);
+    p.targets = index;
+    p.k = k;
+    p.ignore_index = ignore_index;
+    p.row_mask = row_mask;
+    p.vocab_offset = vocab_offset;
+    p.vocab_total = vocab;
+    p.dlogits = dlogits;
+    p.d_stride = dlogits_row_stride;
+    p.vec_store = same_vector_phase(logits, row_stride, dlogits, dlogits_row_stride, dtype);
+    p.grad_out = grad_logp;
+    p.saved_logp = logp;
+    p.target_logit = target_logit;
+    return cuda_status(launch_rows(p, dtype, gbce::kModeLogpGrad,
+                                   static_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

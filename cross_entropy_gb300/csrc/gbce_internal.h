@@ -27,6 +27,7 @@ enum Mode : int {
     kModeCeCap = 8,        // kModeCe on soft-capped logits cap * tanh(x / cap)
     kModeGradCap = 9,      // kModeGrad on soft-capped logits, with the chain factor
     kModeCeCapSmooth = 10,  // kModeCeCap plus the sum of each row's capped logits
+    kModeSliceStats = 11,   // a vocabulary slice's (max, sum) and target logits (partials)
 };
 
 struct RowParams {
@@ -62,7 +63,26 @@ struct RowParams {
 
     int32_t *dev_status;
     int32_t *row_ticket;  // persistent fused kernel: rows handed out beyond the first wave
+
+    // Vocabulary-slice calls (vocab_total > 0): the logits hold global
+    // columns [vocab_offset, vocab_offset + vocab); targets are global
+    // indices in [0, vocab_total); rows whose first index equals
+    // ignore_index are skipped like masked rows.
+    int64_t vocab_offset, vocab_total;
+    float *slice_partials;      // kModeSliceStats: [rows, 2 + k] (m, s, target logits)
+    const float *target_logit;  // slice gradient: [rows] logit of the first index
 };
+
+// Merge vocabulary-slice partials into log-probs (one thread per row).
+struct SliceOffsets {
+    static constexpr int kMax = 64;
+    int64_t off[kMax + 1];
+};
+cudaError_t launch_slice_combine(const float *partials, int slices, const SliceOffsets &offs,
+                                 int64_t rows, const int64_t *index, int64_t k,
+                                 int64_t ignore_index, const uint8_t *row_mask, float T, float c,
+                                 float *logp_out, float *target_logit_out, int32_t *dev_status,
+                                 cudaStream_t stream);
 
 // Row kernel (one CTA per work unit) for logit type T (float / bf16).
 template <typename T>

@@ -956,7 +956,8 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
     constexpr bool kGrad = (kCeGrad || MODE == kModeFused || kSelGrad);
     constexpr bool kEnt = (MODE == kModeLogpEnt);                  // + row entropy
     constexpr bool kLogpFwd = (MODE == kModeLogp || kEnt);         // log p of K indices
-    constexpr bool kGather = (kLogpFwd || kSelGrad);  // K indices
+    constexpr bool kSlice = (MODE == kModeSliceStats);  // a vocabulary slice's partials
+    constexpr bool kGather = (kLogpFwd || kSelGrad || kSlice);  // K indices
     // + sum of logits (label smoothing; the fused mode runs only for few rows,
     // where the extra add costs nothing)
     constexpr bool kSumx =
@@ -997,15 +998,26 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
     int32_t y = -1;
     int state = 0;  // 0 live, 1 skipped (ignored label / masked row), 2 bad label / index
     if (kGather) {
-        // (the mask and the indices are read together: one memory latency)
+        // (the mask and the indices are read together: one memory latency).
+        // A vocabulary slice holds the global columns [vocab_offset,
+        // vocab_offset + V): a target elsewhere is simply not here.
+        const bool slice = p.vocab_total > 0;
+        const int64_t range = slice ? p.vocab_total : V;
         bool any_bad = false;
+        int64_t first = -1;
 #pragma unroll
         for (int k = 0; k < KMAX; ++k) {
             const int64_t t = k < p.k ? p.targets[r * p.k + k] : -1;
-            any_bad |= k < p.k && (t < 0 || t >= V);
-            tg[k] = (t >= 0 && t < V) ? static_cast<int32_t>(t) : -1;
+            if (k == 0)
+                first = t;
+            any_bad |= k < p.k && (t < 0 || t >= range);
+            const int64_t loc = slice ? t - p.vocab_offset : t;
+            tg[k] = (k < p.k && t >= 0 && t < range && loc >= 0 && loc < V)
+                        ? static_cast<int32_t>(loc)
+                        : -1;
         }
-        if (p.row_mask != nullptr && p.row_mask[r] == 0) {
+        if ((p.row_mask != nullptr && p.row_mask[r] == 0) ||
+            (slice && first == p.ignore_index)) {
             state = 1;
             any_bad = false;
 #pragma unroll
@@ -1038,6 +1050,11 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
                 p.logp_out[r * p.k + tid] = 0.0f;
             if (kEnt && direct && tid == 0)
                 p.entropy_out[r] = 0.0f;
+        } else if (kSlice) {
+            // a skipped row's partials: an empty state and no target logits
+            float *part = p.slice_partials + r * (2 + p.k);
+            if (direct && tid < 2 + p.k)
+                part[tid] = tid == 0 ? kNegInf : 0.0f;
         } else if (kSelGrad) {
             if (tid == 0 && split == 0 && state == 2)
                 report(p.dev_status, GBCE_DEV_BAD_INDEX);
@@ -1159,7 +1176,7 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
                 s_lp0 = lp;
                 s_gH = gH;
                 s_H = H;
-                s_xt[0] = E::load(row + mine);
+                s_xt[0] = p.target_logit != nullptr ? p.target_logit[r] : E::load(row + mine);
             }
         }
     }
@@ -1309,6 +1326,9 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
                 bc_m = m;
                 bc_s = s;
                 bc_h = h;
+            } else if (kSlice) {
+                p.slice_partials[r * (2 + p.k)] = m;
+                p.slice_partials[r * (2 + p.k) + 1] = s;
             } else {
                 xy = s_xt[0];
                 logp = finalize_logp(m, s, xy, p.T);
@@ -1322,6 +1342,8 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
                 bc_logp = logp;
             }
         }
+        if (kSlice && tid < p.k)  // the logits of the targets this slice holds
+            p.slice_partials[r * (2 + p.k) + 2 + tid] = s_tg[tid] >= 0 ? s_xt[tid] : 0.0f;
         if (kLogpFwd) {
             named_sync(1, NC);
             // the last warp finalizes the entropy while warp 0 writes the
@@ -1694,6 +1716,12 @@ cudaError_t launch_rows_per_unit(const RowParams &p, int mode, cudaStream_t stre
         return launch_row_kernel<T, kModeCeCap, 1>(p, stream);
     case kModeCeCapSmooth:
         return launch_row_kernel<T, kModeCeCapSmooth, 1>(p, stream);
+    case kModeSliceStats:
+        if (p.k <= 1)
+            return launch_row_kernel<T, kModeSliceStats, 1>(p, stream);
+        if (p.k <= 4)
+            return launch_row_kernel<T, kModeSliceStats, 4>(p, stream);
+        return launch_row_kernel<T, kModeSliceStats, GBCE_MAX_K>(p, stream);
     case kModeGradCap:
         return launch_row_kernel<T, kModeGradCap, 1>(p, stream);
     case kModeGrad:

@@ -286,6 +286,90 @@ gbce_status ce_fwd_bwd_fused(const void *logits, gbce_dtype dtype, int64_t rows,
                              size_t workspace_bytes, int32_t *dev_status, void *stream);
 
 /*
+ * Vocabulary-parallel selective log-softmax: the vocabulary is split into
+ * slices (e.g. one per device, as a vocab-parallel LM head leaves it), each
+ * slice's statistics are computed where its logits are, the caller gathers
+ * them (any transport: an all-gather over devices, or nothing when every
+ * slice is on one device), and one combine gives the log-probs.  The
+ * gradient is then computed slice by slice from the combined log-probs.
+ * Token cross-entropy is the case k = 1, index = labels, ignore_index = the
+ * ignored label: loss_r = -logp[r], and its gradient is vocab_slice_grad
+ * with grad_logp[r] = -(upstream of row r).
+ *
+ * Source: "Fix softmax collapse in CE, GRPO, KL/JSD and softmax"
+ * (Liger-Kernel PR #1555), "Summary", first bullet: the vocab-parallel form
+ * keeps, per slice, the sum over the columns other than the target, and
+ * reduces both sums across slices.
+ *
+ * Slices are described by their global column ranges: slice i holds columns
+ * [slice_offsets[i], slice_offsets[i + 1]) of a vocabulary of `vocab`
+ * columns, slice_offsets[0] = 0 and slice_offsets[slices] = vocab.
+ * Indices are global columns.  A row is skipped (log p 0, zero gradient)
+ * when row_mask[r] == 0 or index[r, 0] == ignore_index.  Label smoothing,
+ * DFT, soft-capping and the entropy are not available on this path.
+ */
+#define GBCE_MAX_SLICES 64
+
+/*
+ * Statistics of one slice.  logits: [rows, row_stride] holding the slice's
+ * slice_vocab columns, global columns [vocab_offset, vocab_offset +
+ * slice_vocab).  partials: [rows, 2 + k] fp32, device, written as
+ *   partials[r, 0] = m_r = max over the slice's non-target columns of x / T
+ *                    (in units of x, i.e. the raw max),
+ *   partials[r, 1] = sum of exp((x_j - m_r) / T) over those columns,
+ *   partials[r, 2 + k'] = logit of index[r, k'] if this slice holds it, else 0;
+ * a skipped row gets (-inf, 0, 0, ...).
+ * Errors: as selective_logsoftmax; GBCE_EINVAL also for vocab_offset < 0 or
+ * vocab_offset + slice_vocab > vocab.  Indices outside [0, vocab) are
+ * reported by the combine.
+ */
+gbce_status vocab_slice_stats(const void *logits, gbce_dtype dtype, int64_t rows,
+                              int64_t slice_vocab, int64_t row_stride, int64_t vocab_offset,
+                              int64_t vocab, const int64_t *index, int64_t k,
+                              int64_t ignore_index, const uint8_t *row_mask, float temperature,
+                              float *partials, int32_t *dev_status, void *stream);
+
+/*
+ * Combine of all slices' partials, stacked in slice order as
+ * partials[slices, rows, 2 + k] (device).  slice_offsets: HOST array of
+ * slices + 1 int64 (read during the call).  logp_out: [rows, k] fp32 as
+ * selective_logsoftmax would give on the whole vocabulary (a bad index: NaN
+ * and GBCE_DEV_BAD_INDEX); target_logit_out: [rows] fp32 or NULL, the logit
+ * of index[r, 0], which vocab_slice_grad needs.  The merge runs in slice
+ * order, so the result does not depend on the order the slices were
+ * computed in.
+ * Errors: GBCE_EINVAL for slices outside [1, GBCE_MAX_SLICES], offsets not
+ * starting at 0 or not increasing, k outside [1, GBCE_MAX_K], a bad
+ * temperature or NULL required pointers.
+ */
+gbce_status vocab_slice_combine(const float *partials, int64_t slices,
+                                const int64_t *slice_offsets, int64_t rows, const int64_t *index,
+                                int64_t k, int64_t ignore_index, const uint8_t *row_mask,
+                                float temperature, float *logp_out, float *target_logit_out,
+                                int32_t *dev_status, void *stream);
+
+/*
+ * Gradient of sum_k grad_logp[r, k] * logp[r, k] with respect to one
+ * slice's logits (the columns of selective_logsoftmax_bwd that the slice
+ * holds), from the combined log-probs and target logit:
+ *   dlogits[r, j] = (1/T) (sum_{k : index[r, k] = j} g[r, k] - G_r p_j),
+ *   p_j = exp((x_j - x_{t0}) / T + logp[r, 0]),
+ * gathered columns in the -expm1 form.
+ *   logp         [rows, k] fp32 from vocab_slice_combine
+ *   target_logit [rows] fp32 from vocab_slice_combine
+ *   dlogits      [rows, dlogits_row_stride] of the logits' type, the slice's
+ *                columns; must not overlap the logits
+ * Errors: as selective_logsoftmax_bwd; a row with an index outside
+ * [0, vocab) gets a NaN row and GBCE_DEV_BAD_INDEX.
+ */
+gbce_status vocab_slice_grad(const void *logits, gbce_dtype dtype, int64_t rows,
+                             int64_t slice_vocab, int64_t row_stride, int64_t vocab_offset,
+                             int64_t vocab, const int64_t *index, int64_t k, int64_t ignore_index,
+                             const uint8_t *row_mask, float temperature, const float *grad_logp,
+                             const float *logp, const float *target_logit, void *dlogits,
+                             int64_t dlogits_row_stride, int32_t *dev_status, void *stream);
+
+/*
  * ce_fwd_bwd_fused without a caller workspace and without any allocation.
  *
  * The pages have no counterpart: this exists for callers that cannot provide

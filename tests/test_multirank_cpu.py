@@ -63,3 +63,53 @@ def test_single_rank_needs_no_process_group():
 
     assert bench.max_over_ranks(3.5, 1, "cpu") == 3.5
     assert bench.aggregate_gbs(1, 2_000_000_000, 10, 1000.0) == pytest.approx(20.0)
+
+
+def _slice_worker(rank, world, port, out):
+    # each rank holds one slice of the vocabulary; the partials of its slice
+    # (the oracle's, on CPU) go through the library's gather helper, and the
+    # merged result must be the full-row log-probs
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world))
+    import sys
+
+    sys.path.insert(0, ROOT)
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import cross_entropy_gb300 as gbce
+    import oracle
+    import workloads
+
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    V, T = 101, 0.8
+    w = workloads.peaked_rows_tiny(V, [0.0, 17.0, 30.0, 50.0, 5.0], seed=9)
+    x = w.logits.numpy()
+    idx = np.stack([w.labels.numpy(), (w.labels.numpy() * 7 + 3) % V], axis=1)
+    offsets = [0, 37, V] if world == 2 else [0, V]
+    a, b = offsets[rank], offsets[rank + 1]
+    m, s, xt = oracle.vocab_slice_partials(x[:, a:b], idx, a, T)
+    mine = torch.from_numpy(np.concatenate([m[:, None], s[:, None], xt], axis=1))
+    everyone = gbce.gather_slice_partials(mine)
+    parts = [(p[:, 0].numpy(), p[:, 1].numpy(), p[:, 2:].numpy()) for p in everyone]
+    got, _ = oracle.vocab_slice_combine(parts, offsets, idx, T)
+    want, _ = oracle.selective_logsoftmax(x, idx, T)
+    out.put((rank, tuple(everyone.shape), float(np.max(np.abs(got - want) / np.abs(want)))))
+    dist.destroy_process_group()
+
+
+def test_vocab_slices_gathered_across_two_gloo_ranks():
+    world, port = 2, _free_port()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_slice_worker, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    results = sorted(q.get(timeout=120) for _ in range(world))
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, shape, err in results:
+        assert shape == (2, 5, 4)      # [slices, rows, 2 + K], in rank order
+        assert err <= 1e-13
