@@ -48,7 +48,7 @@ METRIC = "HBM GB/s (% of GB300 peak) for CE fwd+bwd & selective logp, 8192x15206
 UNIT = "GB/s"
 ROWS, VOCAB, K, TEMPERATURE = 8192, 152064, 4, 0.9
 FALLBACK_HBM_GBS = 6800.0
-PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "fused_ce_bf16_8192x152064.txt")
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "persistent_fused_kernel_bf16_1024x152064.md")
 
 
 def algorithmic_bytes(rows=None, vocab=VOCAB, k=K, esize=2, entropy=False):
@@ -86,7 +86,9 @@ def kernel_source_hash():
 
 
 def profiled_traffic():
-    """DRAM bytes per fused launch from the committed ncu summary, if still current."""
+    """DRAM bytes per fused launch at 8192 rows from the committed ncu summary
+    (one-pass counters at 1024 and 2048 rows, scaled by the marginal row),
+    if the kernel sources are still the ones captured; else None."""
     try:
         fields = {}
         with open(PROFILE_TRAFFIC) as f:
@@ -96,7 +98,7 @@ def profiled_traffic():
                     fields[k.strip()] = v.strip()
         if fields.get("kernel_source_sha256") != kernel_source_hash():
             return None
-        return int(fields["dram_bytes_per_launch"])
+        return int(fields["dram_bytes_per_launch_8192_rows"])
     except (OSError, KeyError, ValueError):
         return None
 
@@ -371,7 +373,9 @@ def run_gbce(args):
                      "frac": achieved / peak, "traffic": traffic,
                      "kernel": "ce_fwd_bwd_fused call: persistent_fused_kernel + item count "
                                "+ loss reduction (events around the whole call)",
-                     "algorithmic_bytes": nbytes["ce_fwd_bwd_fused"], "peak_kind": peak_kind},
+                     "algorithmic_bytes": nbytes["ce_fwd_bwd_fused"], "peak_kind": peak_kind,
+                     "traffic_note": "ncu DRAM read+write of the persistent kernel at 1024 and "
+                                     "2048 rows, scaled to 8192 rows by the marginal row"},
         "e2e": e2e,
         "gpu_launches": launches,
         "clocks": clocks,
@@ -628,6 +632,69 @@ def cpu_baseline(w):
                       f"{secs:.1f} s, fp64 oracle, OpenMP over rows"}
 
 
+PROFILE_CASES = ("ce", "logp", "fused", "split", "slice")
+
+
+def run_profile_case(case: str, rows: int = 1024):
+    """One launch of every op of a kernel family, nothing else, for ncu.
+
+    On `rows` of the packed workload (64 for "split", the few-row cluster
+    path): "ce" = ce_fwd plain / label-smoothed / soft-capped
+    (30) / capped + smoothed, ce_bwd plain / capped; "logp" = selective
+    log-softmax K = 4 with and without the entropy and both backwards;
+    "fused" = ce_fwd_bwd_fused plain / smoothed + DFT / capped; "split" =
+    selective log-softmax, ce_fwd and the fused call on 64 rows; "slice" =
+    vocab_slice_stats on two halves, the combine and one slice's gradient.
+    """
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import cross_entropy_gb300 as gbce
+
+    dev = torch.device("cuda:0")
+    rows = 64 if case == "split" else rows
+    w = workloads.grpo_bf16(device=dev, rows=rows, seed=3)
+    x, idx, lab, V = w.logits, w.index, w.labels, w.vocab
+    d = torch.empty_like(x)
+    g1 = torch.ones(1, device=dev)
+    g4 = torch.ones((rows, K), device=dev)
+    ws = gbce.new_workspace(rows, V, K, device=dev)
+    o = torch.empty((rows, K), dtype=torch.float32, device=dev)
+    h = torch.empty(rows, dtype=torch.float32, device=dev)
+    torch.cuda.synchronize()
+    T = TEMPERATURE
+    if case == "ce":
+        fwd = gbce.ce_fwd(x, lab, temperature=T, workspace=ws)
+        gbce.ce_fwd(x, lab, temperature=T, workspace=ws, label_smoothing=0.1)
+        gbce.ce_bwd(x, lab, g1, fwd.logp, fwd.n_items, temperature=T, dlogits=d)
+        fc = gbce.ce_fwd(x, lab, temperature=T, workspace=ws, softcap=30.0)
+        gbce.ce_bwd(x, lab, g1, fc.logp, fc.n_items, temperature=T, dlogits=d, softcap=30.0)
+        gbce.ce_fwd(x, lab, temperature=T, workspace=ws, softcap=30.0, label_smoothing=0.1)
+    elif case == "logp":
+        gbce.selective_logsoftmax(x, idx, T, out=o, workspace=ws)
+        gbce.selective_logsoftmax(x, idx, T, out=o, entropy_out=h, workspace=ws)
+        gbce.selective_logsoftmax_bwd(x, idx, g4, o, T, dlogits=d)
+        gbce.selective_logsoftmax_bwd(x, idx, g4, o, T, dlogits=d, saved_entropy=h,
+                                      grad_entropy=torch.full((rows,), 0.01, device=dev))
+    elif case == "fused":
+        gbce.ce_fwd_bwd_fused(x, lab, g1, temperature=T, dlogits=d, workspace=ws)
+        gbce.ce_fwd_bwd_fused(x, lab, g1, temperature=T, dlogits=d, workspace=ws,
+                              label_smoothing=0.1, dft=True)
+        gbce.ce_fwd_bwd_fused(x, lab, g1, temperature=T, dlogits=d, workspace=ws, softcap=30.0)
+    elif case == "split":
+        gbce.selective_logsoftmax(x, idx, T, out=o, workspace=ws)
+        gbce.ce_fwd(x, lab, temperature=T, workspace=ws)
+        gbce.ce_fwd_bwd_fused(x, lab, g1, temperature=T, dlogits=d, workspace=ws)
+    elif case == "slice":
+        cuts = [0, V // 2, V]
+        parts = torch.stack([gbce.vocab_slice_stats(x[:, a:b], idx, a, V, T)
+                             for a, b in zip(cuts[:-1], cuts[1:])])
+        lp, xt0 = gbce.vocab_slice_combine(parts, cuts, idx, T)
+        gbce.vocab_slice_grad(x[:, :cuts[1]], idx, 0, V, g4, lp, xt0, T)
+    torch.cuda.synchronize()
+    print(f"profile case {case}: done", flush=True)
+
+
 def main():
     global ROWS
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
@@ -641,10 +708,16 @@ def main():
                     help="skip the per-workload, per-op timings")
     ap.add_argument("--entropy", action="store_true",
                     help="the step's selective log-softmax also writes each row's entropy")
-    ap.add_argument("--rows", type=int, default=ROWS,
-                    help="rows of the workload (a smaller case for profiling captures)")
+    ap.add_argument("--rows", type=int, default=None,
+                    help="rows of the workload (a smaller case for profiling captures; "
+                         f"default {ROWS}, or 1024 with --profile-case)")
+    ap.add_argument("--profile-case", choices=PROFILE_CASES,
+                    help="launch every op of one kernel family once (for ncu) and exit")
     args = ap.parse_args()
-    ROWS = args.rows
+    if args.profile_case:
+        run_profile_case(args.profile_case, args.rows or 1024)
+        return
+    ROWS = args.rows or ROWS
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
