@@ -553,6 +553,8 @@ def run_e2e(gbce, w, dev, stream, args, world, blocks=8):
     mean over all rows is taken as per-block sums with upstream gradient
     1 / n_items (n_items from the host's own labels) and the partial losses
     added on the host, the same loss and gradient as one mean-reduced call.
+    The gradient (dlogits, 2.49 GB) stays on the device, where a training
+    step consumes it; only the log-probs and the block losses come back.
     """
     steps = max(3, min(args.steps, 20))
     rows = w.rows
