@@ -1076,8 +1076,6 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
     }
 
     const RowGeom g = row_geom<T>(row, V);
-    int32_t tv[KMAX];
-    target_vectors<T, KMAX>(tg, g, tv);
     const int64_t v0 = g.nvec * split / p.splits;
     const int64_t v1 = g.nvec * (split + 1) / p.splits;
     const int64_t nchunks = (v1 - v0 + CV - 1) / CV;
@@ -1138,7 +1136,12 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
     }
 
     // ------------------------------------------------------------ consumers
-    // Per-row constants, computed while the producer already streams.
+    // Per-row constants, computed while the producer already streams (no
+    // use of a target index comes before this point, so the producer starts
+    // as soon as the row selection is known -- at once for an unmasked
+    // log-prob row).
+    int32_t tv[KMAX];
+    target_vectors<T, KMAX>(tg, g, tv);
     if (kSelGrad) {
         // gathered column t: (1/T)(-g_t expm1(log p_t) - (G - g_t) exp(log p_t)),
         // g_t the upstream of every k that gathers t; every other column j:

@@ -15,75 +15,87 @@
 
 namespace gbce {
 
-constexpr int kReduceThreads = 1024;
+// One CTA of 256 threads: the inputs are a few rows' worth of bytes, so the
+// time is latency -- both arrays are read in one loop (their loads in flight
+// together) and both sums go through one block reduction.
+constexpr int kReduceThreads = 256;
+constexpr int kReduceWarps = kReduceThreads / 32;
 
-__device__ int64_t block_sum_i64(int64_t v, int64_t *scratch)
+// Block-wide sums of an int64 and an fp64 in a fixed tree; valid in thread 0.
+__device__ void block_sum2(int64_t &n, double &s, int64_t *iscratch, double *dscratch)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1)
-        v += __shfl_xor_sync(0xffffffffu, v, off);
-    if (lane == 0)
-        scratch[warp] = v;
-    __syncthreads();
-    if (warp == 0) {
-        v = lane < (kReduceThreads / 32) ? scratch[lane] : 0;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1)
-            v += __shfl_xor_sync(0xffffffffu, v, off);
+    for (int off = 16; off > 0; off >>= 1) {
+        n += __shfl_xor_sync(0xffffffffu, n, off);
+        s += __shfl_xor_sync(0xffffffffu, s, off);
+    }
+    if (lane == 0) {
+        iscratch[warp] = n;
+        dscratch[warp] = s;
     }
     __syncthreads();
-    return v;  // valid in thread 0
-}
-
-__device__ double block_sum_f64(double v, double *scratch)
-{
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1)
-        v += __shfl_xor_sync(0xffffffffu, v, off);
-    if (lane == 0)
-        scratch[warp] = v;
-    __syncthreads();
     if (warp == 0) {
-        v = lane < (kReduceThreads / 32) ? scratch[lane] : 0.0;
+        n = lane < kReduceWarps ? iscratch[lane] : 0;
+        s = lane < kReduceWarps ? dscratch[lane] : 0.0;
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1)
-            v += __shfl_xor_sync(0xffffffffu, v, off);
-    }
-    __syncthreads();
-    return v;  // valid in thread 0
-}
-
-__device__ int64_t count_items(const int64_t *labels, int64_t rows, int64_t ignore_index,
-                               int64_t *scratch)
-{
-    int64_t n = 0;
-    int64_t r0 = 0;
-    if ((reinterpret_cast<uintptr_t>(labels) & 15u) == 0) {
-        // two labels per 16-byte load, several loads in flight per thread
-        const longlong2 *v = reinterpret_cast<const longlong2 *>(labels);
-        const int64_t nv = rows / 2;
-#pragma unroll 4
-        for (int64_t i = threadIdx.x; i < nv; i += kReduceThreads) {
-            const longlong2 w = v[i];
-            n += (w.x != ignore_index) + (w.y != ignore_index);
+        for (int off = 16; off > 0; off >>= 1) {
+            n += __shfl_xor_sync(0xffffffffu, n, off);
+            s += __shfl_xor_sync(0xffffffffu, s, off);
         }
-        r0 = nv * 2;
     }
-    for (int64_t r = r0 + threadIdx.x; r < rows; r += kReduceThreads)
-        n += (labels[r] != ignore_index);
-    return block_sum_i64(n, scratch);
+}
+
+// This thread's count of rows with label != ignore_index and (when loss_rows
+// is non-null) its fp64 sum of their losses, over a fixed strided subset of
+// rows in a fixed order; four rows per step when both arrays are 16-byte
+// aligned.
+__device__ void thread_partials(const float *loss_rows, const int64_t *labels, int64_t rows,
+                                int64_t ignore_index, bool count, int64_t &n, double &s)
+{
+    n = 0;
+    s = 0.0;
+    int64_t r0 = 0;
+    const bool lab_vec = !count || (reinterpret_cast<uintptr_t>(labels) & 15u) == 0;
+    const bool loss_vec = loss_rows == nullptr || (reinterpret_cast<uintptr_t>(loss_rows) & 15u) == 0;
+    if (lab_vec && loss_vec) {
+        const int64_t nv = rows / 4;
+#pragma unroll 2
+        for (int64_t i = threadIdx.x; i < nv; i += kReduceThreads) {
+            if (count) {
+                const longlong2 a = reinterpret_cast<const longlong2 *>(labels)[2 * i];
+                const longlong2 b = reinterpret_cast<const longlong2 *>(labels)[2 * i + 1];
+                n += (a.x != ignore_index) + (a.y != ignore_index) + (b.x != ignore_index) +
+                     (b.y != ignore_index);
+            }
+            if (loss_rows != nullptr) {
+                const float4 w = reinterpret_cast<const float4 *>(loss_rows)[i];
+                s += (static_cast<double>(w.x) + static_cast<double>(w.y)) +
+                     (static_cast<double>(w.z) + static_cast<double>(w.w));
+            }
+        }
+        r0 = nv * 4;
+    }
+    for (int64_t r = r0 + threadIdx.x; r < rows; r += kReduceThreads) {
+        if (count)
+            n += (labels[r] != ignore_index);
+        if (loss_rows != nullptr)
+            s += static_cast<double>(loss_rows[r]);
+    }
 }
 
 __global__ void __launch_bounds__(kReduceThreads)
     count_items_kernel(const int64_t *labels, int64_t rows, int64_t ignore_index, int64_t *n_out,
                        int32_t *zero_out)
 {
-    __shared__ int64_t scratch[kReduceThreads / 32];
+    __shared__ int64_t iscratch[kReduceWarps];
+    __shared__ double dscratch[kReduceWarps];
     if (threadIdx.x == 0 && zero_out != nullptr)
         *zero_out = 0;
-    const int64_t n = count_items(labels, rows, ignore_index, scratch);
+    int64_t n;
+    double s;
+    thread_partials(nullptr, labels, rows, ignore_index, true, n, s);
+    block_sum2(n, s, iscratch, dscratch);
     if (threadIdx.x == 0)
         *n_out = n;
 }
@@ -93,39 +105,22 @@ __global__ void __launch_bounds__(kReduceThreads)
                        int64_t ignore_index, int reduction, const int64_t *n_in,
                        int64_t *count_into, float *loss_out)
 {
-    __shared__ int64_t iscratch[kReduceThreads / 32];
-    __shared__ double dscratch[kReduceThreads / 32];
-    __shared__ int64_t s_n;
-    if (count_into != nullptr) {
-        const int64_t n = count_items(labels, rows, ignore_index, iscratch);
-        if (threadIdx.x == 0) {
-            *count_into = n;
-            s_n = n;
-        }
-    } else if (threadIdx.x == 0) {
-        s_n = n_in != nullptr ? *n_in : 0;
-    }
-    // per-thread partial over a fixed set of rows, in a fixed order
-    double acc = 0.0;
-    int64_t r0 = 0;
-    if ((reinterpret_cast<uintptr_t>(loss_rows) & 15u) == 0) {
-        const float4 *v = reinterpret_cast<const float4 *>(loss_rows);
-        const int64_t nv = rows / 4;
-#pragma unroll 4
-        for (int64_t i = threadIdx.x; i < nv; i += kReduceThreads) {
-            const float4 w = v[i];
-            acc += (static_cast<double>(w.x) + static_cast<double>(w.y)) +
-                   (static_cast<double>(w.z) + static_cast<double>(w.w));
-        }
-        r0 = nv * 4;
-    }
-    for (int64_t r = r0 + threadIdx.x; r < rows; r += kReduceThreads)
-        acc += static_cast<double>(loss_rows[r]);
-    const double total = block_sum_f64(acc, dscratch);  // ends with __syncthreads
+    __shared__ int64_t iscratch[kReduceWarps];
+    __shared__ double dscratch[kReduceWarps];
+    // the item count when this call counts (count_into), else a given one
+    const bool count = count_into != nullptr;
+    int64_t n;
+    double total;
+    thread_partials(loss_rows, labels, rows, ignore_index, count, n, total);
+    block_sum2(n, total, iscratch, dscratch);
     if (threadIdx.x == 0) {
+        if (count)
+            *count_into = n;
+        else
+            n = n_in != nullptr ? *n_in : 0;
         double out = total;
         if (reduction == 2)
-            out = s_n > 0 ? total / static_cast<double>(s_n) : 0.0;
+            out = n > 0 ? total / static_cast<double>(n) : 0.0;
         *loss_out = static_cast<float>(out);
     }
 }
