@@ -233,13 +233,20 @@ template <> struct CapVec<float> {
     }
 };
 
-// Soft-capping constants of a row pass: cap, 1 / cap, the exponent scale
-// capc = cap * c (c = log2(e) / T; a capped logit cap * t enters the
-// exponent as t * capc), and capc * kTanhQ, the coefficients that give the
-// capped logit's exponent as u * (capc P(s)) in one polynomial.
+// Soft-capping constants of a row pass.  A capped logit is cap * t with
+// t = tanh(u), u = x / cap, and in the series range t = u P(u^2) with
+// P(s) = 1 + s Q(s) (tanh_poly_pair).  Evaluating P directly in X = x^2
+// saves the division by the cap:
+//   exponent   capc t = x * A(X),  A = c P(X / cap^2),   coefficients ax
+//   value      t      = x * B(X),  B = P(X / cap^2) / cap, coefficients bx
+// (capc = cap * c, c = log2(e) / T).  ax[k] and bx[k] scale Q_k by
+// cap^-2(k+1), which stays a normal, finite float for caps in
+// [2^-13, 2^13]; outside that (no cap in use comes close) every vector takes
+// the lane-by-lane path: series_lim = 0.
 struct CapConsts {
-    float cap, inv_cap, capc;
-    float aq[4];
+    float cap, inv_cap, capc, inv_c;
+    float series_lim;  // kCapSeriesBound * cap, or 0
+    float ax[4], bx[4];
 };
 
 __device__ __forceinline__ CapConsts cap_consts(float cap, float inv_cap, float c)
@@ -248,72 +255,129 @@ __device__ __forceinline__ CapConsts cap_consts(float cap, float inv_cap, float 
     k.cap = cap;
     k.inv_cap = inv_cap;
     k.capc = cap * c;
-    k.aq[0] = k.capc * kTanhQ0;
-    k.aq[1] = k.capc * kTanhQ1;
-    k.aq[2] = k.capc * kTanhQ2;
-    k.aq[3] = k.capc * kTanhQ3;
+    k.inv_c = 1.0f / c;
+    k.series_lim = (cap >= 0x1p-13f && cap <= 0x1p13f) ? kCapSeriesBound * cap : 0.0f;
+    const float i2 = inv_cap * inv_cap;
+    const float q[4] = {kTanhQ0, kTanhQ1, kTanhQ2, kTanhQ3};
+    float w = i2;
+#pragma unroll
+    for (int j = 0; j < 4; ++j, w *= i2) {
+        k.ax[j] = c * w * q[j];
+        k.bx[j] = inv_cap * w * q[j];
+    }
     return k;
 }
 
-// Whether every logit of a 16-byte vector is inside the series range of
-// tanh_poly_pair (|x| < kCapSeriesBound * cap), from its raw max and min.
+// Whether every logit of a 16-byte vector is inside the series range
+// (|x| < series_lim), from its raw max and min.
 template <typename T>
-__device__ __forceinline__ bool vector_in_series_range(const uint4 &a, float vmax, float cap)
+__device__ __forceinline__ bool vector_in_series_range(const uint4 &a, float vmax,
+                                                       const CapConsts &k)
 {
-    return fmaxf(vmax, -FastVec<T>::vmin(a)) < kCapSeriesBound * cap;
+    return fmaxf(vmax, -FastVec<T>::vmin(a)) < k.series_lim;
 }
 
+// cap * tanh(x / cap) with CUDA's tanhf, out of line: it is long and the
+// sweeps take it only for a running max outside the series range.
+static __device__ __noinline__ float capped_tanhf(float x, float cap, float inv_cap)
+{
+    return cap * tanhf(x * inv_cap);
+}
+
+// The capped value of a new running max: the series in its range (the same
+// polynomial as the columns it shifts), else tanhf.  Any value close to the
+// capped max serves as the shift: the sum is taken relative to it.
+__device__ __forceinline__ float capped_max(float x, const CapConsts &k)
+{
+    const float u = x * k.inv_cap;
+    if (fabsf(u) < kCapSeriesBound) {
+        const float s = u * u;
+        float h = fmaf(kTanhQ3, s, kTanhQ2);
+        h = fmaf(h, s, kTanhQ1);
+        h = fmaf(h, s, kTanhQ0);
+        return k.cap * fmaf(u * s, h, u);
+    }
+    return capped_tanhf(x, k.cap, k.inv_cap);  // also -inf -> -cap, NaN -> NaN
+}
+
+// One vector with a logit outside the series range, lane by lane and out of
+// line (so the packed loop stays short): returns the sum of 2^{t capc + nmc}
+// and the sum of the capped logits cap * t, t = tanh(x / cap).
+template <typename T>
+__device__ __noinline__ float2 capped_vector_sums(uint4 a, float inv_cap, float cap, float capc,
+                                                  float nmc)
+{
+    constexpr int VEC = Elem<T>::kVec;
+    float f[VEC];
+    Elem<T>::unpack(a, f);
+    float s = 0.0f, sx = 0.0f;
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) {
+        float chain;
+        const float t = tanh_lane(f[e] * inv_cap, chain);
+        s += ex2(fmaf(t, capc, nmc));
+        sx = fmaf(t, cap, sx);
+    }
+    return make_float2(s, sx);
+}
+
+// Raw-max start value of a soft-capped sweep: NaN, so that the first vector
+// always raises (a row may open with vectors that are all -inf, whose capped
+// value -cap is still a finite max).
+__device__ __forceinline__ float capped_sweep_start() { return __uint_as_float(0x7fc00000u); }
+
 // Fold NV soft-capped vectors that hold no target (one, or a thread's two
-// consecutive vectors): the running max comes from the raw vectors' exact
-// max (tanh is increasing, so the capped max is the cap of the raw max,
-// taken only when the raw running max mraw rises); in the series range each
-// pair's exponent is u * (capc P(s)) - m c, one polynomial (u = x / cap,
-// s = u^2); outside it, tanh one lane at a time.
+// or four consecutive vectors).  The running max follows the raw vectors' exact max
+// (tanh is increasing, so the capped max is the cap of the raw max, taken
+// only when the raw running max mraw rises).  In the series range each
+// pair's exponent is x * A(x^2) - m c (CapConsts), in packed pairs; outside
+// it the vectors go lane by lane, and in_range turns false.
 template <typename T, int NV, typename S>
-__device__ __forceinline__ void stats_capped(S &st, float &mraw, const uint4 (&a)[NV], float c,
-                                             const CapConsts &k)
+__device__ __forceinline__ void stats_capped(S &st, float &mraw, bool &in_range,
+                                             const uint4 (&a)[NV], float c, const CapConsts &k)
 {
     constexpr int NP = CapVec<T>::kPairs;
-    const float vmax = NV == 2 ? FastVec<T>::vmax(a[0], a[NV - 1]) : FastVec<T>::vmax(a[0]);
-    if (vmax > mraw || mraw != mraw) {  // (a NaN max keeps re-raising: NaN results)
+    static_assert(NV == 1 || NV == 2 || NV == 4, "one, two or four vectors");
+    float vmax = NV == 1 ? FastVec<T>::vmax(a[0]) : FastVec<T>::vmax(a[0], a[NV > 1 ? 1 : 0]);
+    if (NV == 4)
+        vmax = fmaxf(vmax, FastVec<T>::vmax(a[NV - 2], a[NV - 1]));
+    if (!(vmax <= mraw)) {  // a new raw max, the first vector, or NaN (which keeps raising)
         mraw = vmax;
-        st.raise_to(k.cap * tanhf(vmax * k.inv_cap), c);  // >= -cap, never -inf
+        st.raise_to(capped_max(vmax, k), c);
     }
     float vmin = FastVec<T>::vmin(a[0]);
-    if (NV == 2)
-        vmin = fminf(vmin, FastVec<T>::vmin(a[NV - 1]));
-    const float2 ic = make_float2(k.inv_cap, k.inv_cap);
-    const float2 kk = make_float2(st.nmc, st.nmc);
-    const bool series = fmaxf(vmax, -vmin) < kCapSeriesBound * k.cap;
 #pragma unroll
-    for (int v = 0; v < NV; ++v) {
-        float2 x[NP];
-        CapVec<T>::pairs(a[v], x);
+    for (int v = 1; v < NV; ++v)
+        vmin = fminf(vmin, FastVec<T>::vmin(a[v]));
+    const bool series = fmaxf(vmax, -vmin) < k.series_lim;
+    in_range = in_range && series;
+    if (series) {
+        const float2 kk = make_float2(st.nmc, st.nmc);
 #pragma unroll
-        for (int i = 0; i < NP; i += 2) {
-            float2 z[2];
+        for (int v = 0; v < NV; ++v) {
+            float2 x[NP];
+            CapVec<T>::pairs(a[v], x);
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const float2 u = fmul2(x[i + j], ic);
-                if (series) {
-                    const float2 A = tanh_poly_pair(fmul2(u, u), k.aq, k.capc);
-                    if (S::kSumx) {
-                        const float2 zc = fmul2(u, A);  // capc * t
-                        z[j] = fadd2(zc, kk);
-                        st.sumx_pairs(fmul2(zc, make_float2(1.0f / c, 1.0f / c)),
-                                      make_float2(0.0f, 0.0f));
-                    } else {
-                        z[j] = ffma2(u, A, kk);
-                    }
+            for (int i = 0; i < NP; i += 2) {
+                const float2 up = x[i], uq = x[i + 1];
+                const float2 ap = tanh_poly_pair(fmul2(up, up), k.ax, c);
+                const float2 aq = tanh_poly_pair(fmul2(uq, uq), k.ax, c);
+                if (S::kSumx) {
+                    const float2 zp = fmul2(up, ap), zq = fmul2(uq, aq);  // capc * t
+                    st.add_exponent_pairs(fadd2(zp, kk), fadd2(zq, kk));
+                    const float2 ics = make_float2(k.inv_c, k.inv_c);
+                    st.sumx_pairs(fmul2(zp, ics), fmul2(zq, ics));
                 } else {
-                    float cx, cy;
-                    const float2 t = make_float2(tanh_lane(u.x, cx), tanh_lane(u.y, cy));
-                    z[j] = ffma2(t, make_float2(k.capc, k.capc), kk);
-                    if (S::kSumx)
-                        st.sumx_pairs(fmul2(t, make_float2(k.cap, k.cap)), make_float2(0.0f, 0.0f));
+                    st.add_exponent_pairs(ffma2(up, ap, kk), ffma2(uq, aq, kk));
                 }
             }
-            st.add_exponent_pairs(z[0], z[1]);
+        }
+    } else {
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {
+            const float2 r = capped_vector_sums<T>(a[v], k.inv_cap, k.cap, k.capc, st.nmc);
+            st.sa.x += r.x;
+            st.sumx_add(r.y);
         }
     }
 }
@@ -340,11 +404,14 @@ __device__ __forceinline__ void stats_capped_target(S &st, const uint4 &raw, int
 }
 
 // One thread's NPT vectors of a full chunk (thread tid's vectors vb0 + tid +
-// u * nc), soft-capped: two at a time, the pair that holds a target (nt) one
-// at a time with the target masked.
+// u * nc), soft-capped: all four at once when none holds a target (the
+// usual case: more independent work between the running-max tests), else
+// two at a time, the pair that holds a target (nt) one at a time with the
+// target masked.
 template <typename T, int KMAX, int NPT, typename S>
-__device__ __forceinline__ void stats_capped_chunk(S &st, float &mraw, const uint4 (&raw)[NPT],
-                                                   int32_t vb0, int32_t col0, int32_t &nt,
+__device__ __forceinline__ void stats_capped_chunk(S &st, float &mraw, bool &in_range,
+                                                   const uint4 (&raw)[NPT], int32_t vb0,
+                                                   int32_t col0, int32_t &nt,
                                                    const int32_t (&tg)[KMAX],
                                                    const int32_t (&tv)[KMAX], int64_t v0,
                                                    int64_t v1, int tid, int nc, bool check,
@@ -352,6 +419,13 @@ __device__ __forceinline__ void stats_capped_chunk(S &st, float &mraw, const uin
 {
     constexpr int VEC = Elem<T>::kVec;
     static_assert(NPT % 2 == 0, "vectors go in pairs");
+    if (NPT == 4 && !(check && static_cast<uint32_t>(nt - (vb0 + tid)) <=
+                                   static_cast<uint32_t>(3 * nc))) {
+        stats_capped<T, NPT == 4 ? 4 : 2>(st, mraw, in_range,
+                                          reinterpret_cast<const uint4(&)[NPT == 4 ? 4 : 2]>(raw),
+                                          c, k);
+        return;
+    }
 #pragma unroll
     for (int u = 0; u < NPT; u += 2) {
         const int32_t va = vb0 + tid + u * nc, vb = va + nc;
@@ -362,7 +436,7 @@ __device__ __forceinline__ void stats_capped_chunk(S &st, float &mraw, const uin
             continue;
         }
         const uint4 two[2] = {raw[u], raw[u + 1]};
-        stats_capped<T, 2>(st, mraw, two, c, k);
+        stats_capped<T, 2>(st, mraw, in_range, two, c, k);
     }
 }
 
@@ -796,46 +870,123 @@ template <> struct GradVec<float> {
     }
 };
 
-// Gradient of one soft-capped vector that does not hold the label, packed:
-// element j is fma(gs, 2^z, c0) * (1 - t^2), t = tanh(x_j / cap), with the
-// exponent z = t * capc + kbx of the uncapped formula on the capped logit
-// (kbx from the capped label logit).  In the series range it is evaluated
-// as (-gs 2^z - c0)(t^2 - 1): the sign goes into the constants, so the chain
-// factor is one fused multiply-add.
+// grad_capped for a vector with a logit outside the series range, lane by
+// lane and out of line: fma(gs, 2^z, c0) * (1 - t^2), z = t * capc + kbx.
 template <typename T>
-__device__ __forceinline__ uint4 grad_capped(const uint4 &a, const GradConsts &k,
-                                             const CapConsts &cp)
+__device__ __noinline__ uint4 grad_capped_lanes(uint4 a, float inv_cap, float capc, float kbx,
+                                                float gs, float c0)
+{
+    constexpr int VEC = Elem<T>::kVec;
+    float f[VEC];
+    Elem<T>::unpack(a, f);
+    float d[VEC];
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) {
+        float chain;
+        const float t = tanh_lane(f[e] * inv_cap, chain);
+        d[e] = fmaf(gs, ex2(fmaf(t, capc, kbx)), c0) * chain;
+    }
+    return Elem<T>::pack(d);
+}
+
+// The soft-capped gradient of the vector that holds the label (element
+// yoff), lane by lane with tanhf and out of line (once per row): the label
+// element is dy * (1 - t^2), the others as in grad_capped_lanes.
+template <typename T>
+__device__ __noinline__ uint4 grad_capped_label_vector(uint4 a, int32_t yoff, float dy,
+                                                       float inv_cap, float capc, float kbx,
+                                                       float gs, float c0)
+{
+    constexpr int VEC = Elem<T>::kVec;
+    float f[VEC];
+    Elem<T>::unpack(a, f);
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) {
+        const float t = tanhf(f[e] * inv_cap);
+        const float d = e == yoff ? dy : fmaf(gs, ex2(fmaf(t, capc, kbx)), c0);
+        f[e] = d * ((1.0f - t) * (1.0f + t));
+    }
+    return Elem<T>::pack(f);
+}
+
+// Gradient of one soft-capped vector without the label whose logits are
+// all inside the series range, packed: element j is fma(gs, 2^z, c0) *
+// (1 - t^2), t = tanh(x_j / cap) = x_j B(x_j^2) (CapConsts), with the
+// exponent z = t * capc + kbx of the uncapped formula on the capped logit
+// (kbx from the capped label logit), evaluated as (-gs 2^z - c0)(t^2 - 1):
+// the sign goes into the constants, so the chain factor is one fused
+// multiply-add.
+template <typename T>
+__device__ __forceinline__ uint4 grad_capped_series(const uint4 &a, const GradConsts &k,
+                                                    const CapConsts &cp)
 {
     constexpr int NP = CapVec<T>::kPairs;
     float2 x[NP];
     CapVec<T>::pairs(a, x);
-    const float2 ic = make_float2(cp.inv_cap, cp.inv_cap);
     const float2 cc = make_float2(cp.capc, cp.capc), kk = make_float2(k.kbx, k.kbx);
+    const float2 ngs = make_float2(-k.gs, -k.gs), nc0 = make_float2(-k.c0, -k.c0);
+    const float2 m1 = make_float2(-1.0f, -1.0f);
     float2 d[NP];
-    if (vector_in_series_range<T>(a, FastVec<T>::vmax(a), cp.cap)) {
-        const float q[4] = {kTanhQ0, kTanhQ1, kTanhQ2, kTanhQ3};
-        const float2 ngs = make_float2(-k.gs, -k.gs), nc0 = make_float2(-k.c0, -k.c0);
-        const float2 m1 = make_float2(-1.0f, -1.0f);
 #pragma unroll
-        for (int i = 0; i < NP; ++i) {
-            const float2 u = fmul2(x[i], ic);
-            const float2 t = fmul2(u, tanh_poly_pair(fmul2(u, u), q, 1.0f));
-            const float2 z = ffma2(t, cc, kk);
-            const float2 e = make_float2(ex2(z.x), ex2(z.y));
-            d[i] = fmul2(ffma2(e, ngs, nc0), ffma2(t, t, m1));
-        }
-    } else {
-        const float2 gs = make_float2(k.gs, k.gs), c0 = make_float2(k.c0, k.c0);
-#pragma unroll
-        for (int i = 0; i < NP; ++i) {
-            const float2 u = fmul2(x[i], ic);
-            float cx, cy;
-            const float2 t = make_float2(tanh_lane(u.x, cx), tanh_lane(u.y, cy));
-            const float2 z = ffma2(t, cc, kk);
-            d[i] = fmul2(ffma2(make_float2(ex2(z.x), ex2(z.y)), gs, c0), make_float2(cx, cy));
-        }
+    for (int i = 0; i < NP; ++i) {
+        const float2 t = fmul2(x[i], tanh_poly_pair(fmul2(x[i], x[i]), cp.bx, cp.inv_cap));
+        const float2 z = ffma2(t, cc, kk);
+        const float2 e = make_float2(ex2(z.x), ex2(z.y));
+        d[i] = fmul2(ffma2(e, ngs, nc0), ffma2(t, t, m1));
     }
     return CapVec<T>::pack(d);
+}
+
+// Gradient of one soft-capped vector without the label: packed in the
+// series range, else lane by lane.
+template <typename T>
+__device__ __forceinline__ uint4 grad_capped(const uint4 &a, const GradConsts &k,
+                                             const CapConsts &cp)
+{
+    if (vector_in_series_range<T>(a, FastVec<T>::vmax(a), cp))
+        return grad_capped_series<T>(a, k, cp);
+    return grad_capped_lanes<T>(a, cp.inv_cap, cp.capc, k.kbx, k.gs, k.c0);
+}
+
+// The soft-capped gradient of one thread's NPT vectors of a full chunk
+// (vectors tid + u * nc, the label at column offset ybase of the chunk),
+// stored with 16-byte streaming stores.  One range test covers all NPT
+// vectors, and none is needed when the statistics pass already found every
+// logit of the row inside the series range (row_in_range).
+template <typename T, int NPT>
+__device__ __forceinline__ void grad_capped_chunk(const uint4 *chunk, T *dbase, int32_t ybase,
+                                                  int tid, int nc, bool row_in_range,
+                                                  const GradConsts &k, const CapConsts &cp)
+{
+    constexpr int VEC = Elem<T>::kVec;
+    uint4 raw[NPT];
+#pragma unroll
+    for (int u = 0; u < NPT; ++u)
+        raw[u] = chunk[tid + u * nc];
+    bool series = row_in_range;
+    if (!series) {
+        float vmax = FastVec<T>::vmax(raw[0]), vmin = FastVec<T>::vmin(raw[0]);
+#pragma unroll
+        for (int u = 1; u < NPT; ++u) {
+            vmax = fmaxf(vmax, FastVec<T>::vmax(raw[u]));
+            vmin = fminf(vmin, FastVec<T>::vmin(raw[u]));
+        }
+        series = fmaxf(vmax, -vmin) < cp.series_lim;
+    }
+#pragma unroll
+    for (int u = 0; u < NPT; ++u) {
+        const int v = tid + u * nc;
+        const int32_t yoff = ybase - v * VEC;
+        uint4 d;
+        if (static_cast<uint32_t>(yoff) < static_cast<uint32_t>(VEC))
+            d = grad_capped_label_vector<T>(raw[u], yoff, k.dy, cp.inv_cap, cp.capc, k.kbx,
+                                            k.gs, k.c0);
+        else if (series)
+            d = grad_capped_series<T>(raw[u], k, cp);
+        else
+            d = grad_capped_lanes<T>(raw[u], cp.inv_cap, cp.capc, k.kbx, k.gs, k.c0);
+        st_cs_v4(dbase + v * VEC, d);
+    }
 }
 
 // log p of target k, whose "others" are every column outside the target set
@@ -1207,7 +1358,8 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
         // holds one skips even the cursor test (warp-uniform branch)
         int32_t nt = next_target_vector<KMAX>(tv, v0, v1, tid, NC, -1);
         const bool wcheck = __any_sync(0xffffffffu, nt != INT32_MAX);
-        float mraw = kNegInf;  // soft-capped sweep: the raw max behind st.m
+        float mraw = capped_sweep_start();  // soft-capped sweep: the raw max behind st.m
+        bool in_range = true;               // (unused here: no gradient pass follows)
         if (split == 0)
             for (int64_t e = tid; e < g.head; e += NC) {
                 const float x = capped(E::load(row + e));
@@ -1236,8 +1388,9 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
 #pragma unroll
                     for (int u = 0; u < PER_THREAD; ++u)
                         raw[u] = chunk[tid + u * NC];
-                    stats_capped_chunk<T, KMAX, PER_THREAD>(st, mraw, raw, vb0, col0, nt, tg, tv,
-                                                           v0, v1, tid, NC, wcheck, c, capk);
+                    stats_capped_chunk<T, KMAX, PER_THREAD>(st, mraw, in_range, raw, vb0, col0,
+                                                           nt, tg, tv, v0, v1, tid, NC, wcheck,
+                                                           c, capk);
                 } else if (kCap) {
                     for (int v = tid; v < nv; v += NC) {
                         const int32_t vb = vb0 + v;
@@ -1248,7 +1401,7 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
                             continue;
                         }
                         const uint4 one[1] = {chunk[v]};
-                        stats_capped<T, 1>(st, mraw, one, c, capk);
+                        stats_capped<T, 1>(st, mraw, in_range, one, c, capk);
                     }
                 } else if (nv == CV) {
                     uint4 raw[PER_THREAD];
@@ -1513,24 +1666,29 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
                     const int64_t vbase = v0 + i * CV;
                     const int64_t col_base = g.head + vbase * VEC;
                     T *dbase = drow + col_base;
-                    for (int v = tid; v < nv; v += NC) {
-                        const int64_t yoff = y - (col_base + v * VEC);
-                        if (p.vec_store && (yoff < 0 || yoff >= VEC)) {
-                            st_cs_v4(dbase + v * VEC,
-                                     grad_capped<T>(chunk[v], gk, capk));
-                            continue;
-                        }
-                        float f[VEC];
-                        E::unpack(chunk[v], f);
-#pragma unroll
-                        for (int e = 0; e < VEC; ++e)
-                            f[e] = elem(f[e], col_base + v * VEC + e == y);
-                        if (p.vec_store) {
-                            st_cs_v4(dbase + v * VEC, E::pack(f));
-                        } else {
+                    if (nv == CV && p.vec_store) {
+                        grad_capped_chunk<T, PER_THREAD>(
+                            chunk, dbase, static_cast<int32_t>(y - col_base), tid, NC, false, gk,
+                            capk);
+                    } else {
+                        for (int v = tid; v < nv; v += NC) {
+                            const int64_t yoff = y - (col_base + v * VEC);
+                            if (p.vec_store && (yoff < 0 || yoff >= VEC)) {
+                                st_cs_v4(dbase + v * VEC, grad_capped<T>(chunk[v], gk, capk));
+                                continue;
+                            }
+                            float f[VEC];
+                            E::unpack(chunk[v], f);
 #pragma unroll
                             for (int e = 0; e < VEC; ++e)
-                                E::store(dbase + v * VEC + e, f[e]);
+                                f[e] = elem(f[e], col_base + v * VEC + e == y);
+                            if (p.vec_store) {
+                                st_cs_v4(dbase + v * VEC, E::pack(f));
+                            } else {
+#pragma unroll
+                                for (int e = 0; e < VEC; ++e)
+                                    E::store(dbase + v * VEC + e, f[e]);
+                            }
                         }
                     }
                 }

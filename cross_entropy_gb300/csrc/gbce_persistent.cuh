@@ -79,7 +79,9 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persistent_fused_kernel(co
     __shared__ uint64_t rq_full[Q], rq_empty[Q];
     __shared__ int32_t rq_row[Q];
     __shared__ float red_m[NCW], red_s[NCW], red_x[NCW];
+    __shared__ int red_in[NCW];
     __shared__ float bc_logp;
+    __shared__ int bc_in_range;  // CAP: every logit of the row in the series range
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -236,7 +238,8 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persistent_fused_kernel(co
         OnlineStats<false, SMOOTH> st;
         int32_t nt = next_target_vector<1>(tv, 0, g.nvec, tid, NC, -1);
         const bool wcheck = __any_sync(0xffffffffu, nt != INT32_MAX);
-        float mraw = kNegInf;  // soft-capped sweep: the raw max behind st.m
+        float mraw = capped_sweep_start();  // soft-capped sweep: the raw max behind st.m
+        bool in_range = true;  // CAP: this thread's vectors all in the series range
         for (int64_t e = tid; e < g.head; e += NC) {
             const float x = capped(E::load(row + e));
             st.add1(e == y ? kNegInf : x, c);
@@ -261,8 +264,9 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persistent_fused_kernel(co
 #pragma unroll
                     for (int u = 0; u < PER_THREAD; ++u)
                         raw[u] = chunk[tid + u * NC];
-                    stats_capped_chunk<T, 1, PER_THREAD>(st, mraw, raw, vb0, col0, nt, tg, tv, 0,
-                                                        g.nvec, tid, NC, wcheck, c, capk);
+                    stats_capped_chunk<T, 1, PER_THREAD>(st, mraw, in_range, raw, vb0, col0, nt,
+                                                        tg, tv, 0, g.nvec, tid, NC, wcheck, c,
+                                                        capk);
                 } else if (CAP) {
                     for (int v = tid; v < nv; v += NC) {
                         const int32_t vb = vb0 + v;
@@ -272,7 +276,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persistent_fused_kernel(co
                             continue;
                         }
                         const uint4 one[1] = {chunk[v]};
-                        stats_capped<T, 1>(st, mraw, one, c, capk);
+                        stats_capped<T, 1>(st, mraw, in_range, one, c, capk);
                     }
                 } else if (nv == CV) {
                     uint4 raw[PER_THREAD];
@@ -309,16 +313,22 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persistent_fused_kernel(co
             if (SMOOTH)
                 sx = __fadd_rn(sx, __shfl_xor_sync(0xffffffffu, sx, off));
         }
+        if (CAP)
+            in_range = __all_sync(0xffffffffu, in_range);
         if (lane == 0) {
             red_m[warp] = m;
             red_s[warp] = s;
             red_x[warp] = sx;
+            if (CAP)
+                red_in[warp] = in_range;
         }
         named_sync(1, NC);
         if (warp == 0) {
             m = lane < NCW ? red_m[lane] : kNegInf;
             s = lane < NCW ? red_s[lane] : 0.0f;
             sx = lane < NCW ? red_x[lane] : 0.0f;
+            if (CAP)
+                in_range = __all_sync(0xffffffffu, lane < NCW ? red_in[lane] != 0 : true);
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) {
                 const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
@@ -330,6 +340,8 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persistent_fused_kernel(co
             if (lane == 0) {
                 const float lp = finalize_logp(m, s, xy, p.T);
                 bc_logp = lp;
+                if (CAP)
+                    bc_in_range = in_range;
                 p.loss_rows[r] = ce_row_loss(lp, xy, sx, p.T, p.ls_eps, p.dft, V);
                 if (p.logp_out)
                     p.logp_out[r] = lp;
@@ -365,7 +377,10 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persistent_fused_kernel(co
                 const int32_t nv = static_cast<int32_t>((g.nvec - vbase) < CV ? (g.nvec - vbase) : CV);
                 const int32_t ybase = y - static_cast<int32_t>(g.head + vbase * VEC);
                 T *dbase = drow + g.head + vbase * VEC;
-                if (CAP) {
+                if (CAP && nv == CV && p.vec_store) {
+                    grad_capped_chunk<T, PER_THREAD>(chunk, dbase, ybase, tid, NC,
+                                                     bc_in_range != 0, gk, capk);
+                } else if (CAP) {
                     for (int v = tid; v < nv; v += NC) {
                         const int32_t yoff = ybase - v * VEC;
                         if (p.vec_store && static_cast<uint32_t>(yoff) >= static_cast<uint32_t>(VEC)) {

@@ -183,6 +183,40 @@ def test_softcap_split_path_and_saturated_logits():
     assert_grad_rows_close(to_f64(out.dlogits), ref["dlogits"], torch.float32, tol=g_tol)
 
 
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("rows", [3, 400])
+def test_softcap_rows_opening_with_minus_infinity(dtype, rows):
+    # a vocabulary mask over each row's first 8192 columns: every thread's
+    # first vectors are all -inf, which the cap maps to -cap (finite), so the
+    # capped sweep must take them into its max and sum like any other value
+    # (3 rows: the split path; 400 rows: one CTA per row and the persistent
+    # fused kernel)
+    V, cap, T = 32000, 30.0, 0.9
+    gen = torch.Generator().manual_seed(rows)
+    x_cpu = torch.randn((rows, V), generator=gen) * 3.0
+    x_cpu[:, :8192] = float("-inf")
+    lab = torch.randint(8192, V, (rows,), generator=gen)
+    x_cpu = x_cpu.to(dtype)
+    x, lab_d = x_cpu.to(DEV), lab.to(DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    fwd = gbce.ce_fwd(x, lab_d, temperature=T, reduction="none", softcap=cap, dev_status=status)
+    smooth = gbce.ce_fwd(x, lab_d, temperature=T, reduction="none", softcap=cap,
+                         label_smoothing=0.1, dev_status=status)
+    fused = gbce.ce_fwd_bwd_fused(x, lab_d, torch.ones(1, device=DEV), temperature=T,
+                                  reduction="sum", softcap=cap, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    x64 = workloads.to_numpy_f64(x_cpu)
+    ref = oracle.cross_entropy(x64, lab.numpy(), temperature=T, reduction="sum", softcap=cap,
+                               grad_out=[1.0])
+    ref_s = oracle.cross_entropy(x64, lab.numpy(), temperature=T, reduction="none",
+                                 softcap=cap, label_smoothing=0.1)
+    check_rows_loss(fwd.loss, ref["loss_rows"], dtype, "capped rows")
+    check_rows_loss(smooth.loss, ref_s["loss_rows"], dtype, "capped smoothed rows")
+    assert_loss_close(float(fused.loss.item()), ref["loss"], "capped fused sum")
+    assert_grad_rows_close(to_f64(fused.dlogits), ref["dlogits"], dtype, "capped fused")
+
+
 def test_full_size_grpo_softcap_fused_every_row():
     # the benchmark's rows with a soft-cap of 30: the persistent fused kernel
     # with the cap, every row's log p and gradient against the oracle
