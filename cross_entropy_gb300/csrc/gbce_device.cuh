@@ -378,6 +378,15 @@ __device__ __forceinline__ float fmax3(float a, float b, float c)
     return d;
 }
 
+// Max of v over the warp's active lanes, in one warp-wide reduction; a NaN
+// lane is ignored unless every lane is NaN.
+__device__ __forceinline__ float warp_max_active(float v)
+{
+    float r;
+    asm volatile("redux.sync.max.f32 %0, %1, %2;" : "=f"(r) : "f"(v), "r"(__activemask()));
+    return r;
+}
+
 __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w)
 {
     return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));

@@ -326,24 +326,33 @@ __device__ __noinline__ float2 capped_vector_sums(uint4 a, float inv_cap, float 
 // value -cap is still a finite max).
 __device__ __forceinline__ float capped_sweep_start() { return __uint_as_float(0x7fc00000u); }
 
-// Fold NV soft-capped vectors that hold no target (one, or a thread's two
-// or four consecutive vectors).  The running max follows the raw vectors' exact max
-// (tanh is increasing, so the capped max is the cap of the raw max, taken
-// only when the raw running max mraw rises).  In the series range each
-// pair's exponent is x * A(x^2) - m c (CapConsts), in packed pairs; outside
-// it the vectors go lane by lane, and in_range turns false.
-template <typename T, int NV, typename S>
-__device__ __forceinline__ void stats_capped(S &st, float &mraw, bool &in_range,
-                                             const uint4 (&a)[NV], float c, const CapConsts &k)
+// The raw max of one, two or four vectors.
+template <typename T, int NV>
+__device__ __forceinline__ float raw_vmax(const uint4 (&a)[NV])
 {
-    constexpr int NP = CapVec<T>::kPairs;
     static_assert(NV == 1 || NV == 2 || NV == 4, "one, two or four vectors");
     float vmax = NV == 1 ? FastVec<T>::vmax(a[0]) : FastVec<T>::vmax(a[0], a[NV > 1 ? 1 : 0]);
     if (NV == 4)
         vmax = fmaxf(vmax, FastVec<T>::vmax(a[NV - 2], a[NV - 1]));
-    if (!(vmax <= mraw)) {  // a new raw max, the first vector, or NaN (which keeps raising)
-        mraw = vmax;
-        st.raise_to(capped_max(vmax, k), c);
+    return vmax;
+}
+
+// Fold NV soft-capped vectors that hold no target (one, or a thread's two
+// or four consecutive vectors), whose raw max is vmax.  The running max
+// follows the raw max `rise` (vmax, or the max over the warp's lanes: tanh
+// is increasing, so the capped max is the cap of the raw max, taken only
+// when the raw running max mraw rises).  In the series range each pair's
+// exponent is x * A(x^2) - m c (CapConsts), in packed pairs; outside it the
+// vectors go lane by lane, and in_range turns false.
+template <typename T, int NV, typename S>
+__device__ __forceinline__ void stats_capped(S &st, float &mraw, bool &in_range,
+                                             const uint4 (&a)[NV], float vmax, float rise,
+                                             float c, const CapConsts &k)
+{
+    constexpr int NP = CapVec<T>::kPairs;
+    if (!(rise <= mraw)) {  // a new raw max, the first vector, or NaN (which keeps raising)
+        mraw = rise;
+        st.raise_to(capped_max(rise, k), c);
     }
     float vmin = FastVec<T>::vmin(a[0]);
 #pragma unroll
@@ -418,13 +427,21 @@ __device__ __forceinline__ void stats_capped_chunk(S &st, float &mraw, bool &in_
                                                    float c, const CapConsts &k)
 {
     constexpr int VEC = Elem<T>::kVec;
+    constexpr int NG = NPT == 4 ? 4 : 2;
     static_assert(NPT % 2 == 0, "vectors go in pairs");
-    if (NPT == 4 && !(check && static_cast<uint32_t>(nt - (vb0 + tid)) <=
-                                   static_cast<uint32_t>(3 * nc))) {
-        stats_capped<T, NPT == 4 ? 4 : 2>(st, mraw, in_range,
-                                          reinterpret_cast<const uint4(&)[NPT == 4 ? 4 : 2]>(raw),
-                                          c, k);
-        return;
+    if (NPT == 4) {
+        // the warp's lanes raise the running max together, from a warp-wide
+        // max of the lanes whose four vectors hold no target; those lanes
+        // fold all four at once
+        const bool hit =
+            check && static_cast<uint32_t>(nt - (vb0 + tid)) <= static_cast<uint32_t>(3 * nc);
+        const uint4(&four)[NG] = reinterpret_cast<const uint4(&)[NG]>(raw);
+        const float own = raw_vmax<T, NG>(four);
+        const float wmax = warp_max_active(hit ? kNegInf : own);
+        if (!hit) {
+            stats_capped<T, NG>(st, mraw, in_range, four, own, wmax, c, k);
+            return;
+        }
     }
 #pragma unroll
     for (int u = 0; u < NPT; u += 2) {
@@ -436,7 +453,8 @@ __device__ __forceinline__ void stats_capped_chunk(S &st, float &mraw, bool &in_
             continue;
         }
         const uint4 two[2] = {raw[u], raw[u + 1]};
-        stats_capped<T, 2>(st, mraw, in_range, two, c, k);
+        const float own = raw_vmax<T, 2>(two);
+        stats_capped<T, 2>(st, mraw, in_range, two, own, own, c, k);
     }
 }
 
@@ -461,7 +479,14 @@ __device__ __forceinline__ void stats_one(S &st, const uint4 &a, int32_t va, int
         st.sumx_add(kNegInf);  // the whole vector is -inf
 }
 
-template <typename T, int KMAX, typename S>
+// Two vectors of a full chunk.  With WARP_MAX every lane of the warp folds
+// them together: the running max rises for the whole warp at once (one
+// warp-wide max, then a uniform raise, where a per-lane max branches apart
+// in most groups early in a row -- a gain where many warps share an SM's
+// issue slots, a loss of latency where the sweep already runs at the
+// bandwidth bound).  A lane whose pair holds a target keeps it out of the
+// shared max and folds the pair alone, the target masked.
+template <typename T, int KMAX, bool WARP_MAX, typename S>
 __device__ __forceinline__ void stats_two(S &st, const uint4 &a, const uint4 &b, int32_t va,
                                           int32_t vb, int32_t col0, int32_t &nt,
                                           const int32_t (&tg)[KMAX], float c,
@@ -469,13 +494,17 @@ __device__ __forceinline__ void stats_two(S &st, const uint4 &a, const uint4 &b,
                                           int tid, int nc, bool check = true)
 {
     constexpr int VEC = Elem<T>::kVec;
-    if (check && static_cast<uint32_t>(nt - va) <= static_cast<uint32_t>(vb - va)) {
+    const bool hit = check && static_cast<uint32_t>(nt - va) <= static_cast<uint32_t>(vb - va);
+    const float own = hit ? kNegInf : FastVec<T>::vmax(a, b);
+    const float wmax = WARP_MAX ? warp_max_active(own) : own;
+    if (hit) {
         stats_vector<T, KMAX>(st, a, col0 + va * VEC, tg, c);
         stats_vector<T, KMAX>(st, b, col0 + vb * VEC, tg, c);
         nt = next_target_vector<KMAX>(tv, v0, v1, tid, nc, vb);
         return;
     }
-    if (st.raise_to(FastVec<T>::vmax(a, b), c)) {
+    st.raise_to(wmax, c);
+    if (own != kNegInf) {
         FastVec<T>::add(st, a, c);
         FastVec<T>::add(st, b, c);
     } else {
@@ -1133,6 +1162,7 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
     __shared__ int32_t s_tg[KMAX];
     __shared__ float bc_m, bc_s, bc_h, bc_logp;
     __shared__ uint64_t xbar;                   // cluster of CTAs per row: partials landed
+    __shared__ uint64_t xt_bar;                 // statistics: s_xt written
     __shared__ __align__(16) float4 xchg[kMaxClusterCtas];  // every CTA's (m, s, h) partial
 
     const int tid = threadIdx.x;
@@ -1143,6 +1173,27 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
     const int64_t V = p.vocab;
     const T *row = static_cast<const T *>(p.logits) + r * p.row_stride;
     T *drow = kGrad ? static_cast<T *>(p.dlogits) + r * p.d_stride : nullptr;
+
+    // statistics over a vocabulary split: the row's CTAs form a cluster and
+    // send their (m, s, h) partials through distributed shared memory to the
+    // first CTA (to every CTA in the fused mode, which needs log p for its
+    // gradient slice)
+    const bool exchange = (kStats && p.splits > 1);
+    // the mbarriers first: their setup overlaps the row selection's loads
+    // (a skipped row leaves them unused)
+    if (tid == 0) {
+#pragma unroll
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], NCW);
+        }
+        if (exchange)
+            mbar_init(&xbar, 1);
+        if (kStats)
+            mbar_init(&xt_bar, 1);
+        fence_barrier_init();
+    }
+    __syncthreads();  // the mbarriers exist before anyone uses them
 
     // ---- row selection, before any read of this row's logits
     int32_t tg[KMAX];
@@ -1227,29 +1278,13 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
     }
 
     const RowGeom g = row_geom<T>(row, V);
-    const int64_t v0 = g.nvec * split / p.splits;
-    const int64_t v1 = g.nvec * (split + 1) / p.splits;
+    const int64_t v0 = p.splits == 1 ? 0 : g.nvec * split / p.splits;
+    const int64_t v1 = p.splits == 1 ? g.nvec : g.nvec * (split + 1) / p.splits;
     const int64_t nchunks = (v1 - v0 + CV - 1) / CV;
     const int64_t total = nchunks * kPasses;
     const char *body = reinterpret_cast<const char *>(row + g.head) + v0 * 16;
     const int64_t body_bytes = (v1 - v0) * 16;
 
-    // statistics over a vocabulary split: the row's CTAs form a cluster and
-    // send their (m, s, h) partials through distributed shared memory to the
-    // first CTA (to every CTA in the fused mode, which needs log p for its
-    // gradient slice)
-    const bool exchange = (kStats && p.splits > 1);
-    if (tid == 0) {
-#pragma unroll
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&full_bar[s], 1);
-            mbar_init(&empty_bar[s], NCW);
-        }
-        if (exchange)
-            mbar_init(&xbar, 1);
-        fence_barrier_init();
-    }
-    __syncthreads();  // the mbarriers exist before anyone uses them
     if (exchange)
         cluster_arrive_relaxed();
 
@@ -1282,6 +1317,20 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
             // no copy may still be in flight when the CTA exits
             for (int64_t j = (i > kStages ? i - kStages : 0); j < i; ++j)
                 mbar_wait(&full_bar[j % kStages], static_cast<uint32_t>((j / kStages) & 1));
+        }
+        if (kStats && lane == 1) {
+            // the target logits, for the finalize step: read by an idle
+            // producer lane, so that no consumer waits on these dependent
+            // loads before its sweep (all issued, then all stored)
+            float xt[KMAX];
+#pragma unroll
+            for (int k = 0; k < KMAX; ++k)
+                xt[k] = (k < p.k && tg[k] >= 0) ? E::load(row + tg[k]) : 0.0f;
+#pragma unroll
+            for (int k = 0; k < KMAX; ++k)
+                if (k < p.k)
+                    s_xt[k] = tg[k] >= 0 ? capped(xt[k]) : 0.0f;
+            mbar_arrive(&xt_bar);
         }
         return;
     }
@@ -1335,14 +1384,12 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
         }
     }
     if (kStats) {
-        // target logits, for the finalize step (read after the merge's
-        // barrier; their load latency hides under the sweep)
+        // target columns, for the finalize step (read after the merge's
+        // barrier; the producer warp reads their logits)
 #pragma unroll
         for (int k = 0; k < KMAX; ++k)
-            if (tid == k) {
+            if (tid == k)
                 s_tg[k] = tg[k];
-                s_xt[k] = tg[k] >= 0 ? capped(E::load(row + tg[k])) : 0.0f;
-            }
     }
     if (kSelGrad)
         named_sync(1, NC);  // the gradient constants before the sweep uses them
@@ -1401,7 +1448,8 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
                             continue;
                         }
                         const uint4 one[1] = {chunk[v]};
-                        stats_capped<T, 1>(st, mraw, in_range, one, c, capk);
+                        const float own = raw_vmax<T, 1>(one);
+                        stats_capped<T, 1>(st, mraw, in_range, one, own, own, c, capk);
                     }
                 } else if (nv == CV) {
                     uint4 raw[PER_THREAD];
@@ -1410,9 +1458,9 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
                         raw[u] = chunk[tid + u * NC];
 #pragma unroll
                     for (int u = 0; u + 1 < PER_THREAD; u += 2)
-                        stats_two<T, KMAX>(st, raw[u], raw[u + 1], vb0 + tid + u * NC,
-                                           vb0 + tid + (u + 1) * NC, col0, nt, tg, c, tv, v0, v1,
-                                           tid, NC, wcheck);
+                        stats_two<T, KMAX, false>(st, raw[u], raw[u + 1], vb0 + tid + u * NC,
+                                                  vb0 + tid + (u + 1) * NC, col0, nt, tg, c, tv,
+                                                  v0, v1, tid, NC, wcheck);
                     if (PER_THREAD & 1)
                         stats_one<T, KMAX>(st, raw[PER_THREAD - 1],
                                            vb0 + tid + (PER_THREAD - 1) * NC, col0, nt, tg, c, tv,
@@ -1426,6 +1474,13 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&empty_bar[slot]);
+        }
+
+        // the target logits have landed (long since: the loads were issued
+        // when the sweep began); every reader of s_xt comes after this
+        if (alive && !mbar_wait(&xt_bar, 0)) {
+            alive = false;
+            report(p.dev_status, GBCE_DEV_TIMEOUT);
         }
 
         // CTA-wide merge of the per-thread (max, sum[, h]) in a fixed order;

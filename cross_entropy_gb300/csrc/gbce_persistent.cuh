@@ -276,7 +276,8 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persistent_fused_kernel(co
                             continue;
                         }
                         const uint4 one[1] = {chunk[v]};
-                        stats_capped<T, 1>(st, mraw, in_range, one, c, capk);
+                        const float own = raw_vmax<T, 1>(one);
+                        stats_capped<T, 1>(st, mraw, in_range, one, own, own, c, capk);
                     }
                 } else if (nv == CV) {
                     uint4 raw[PER_THREAD];
@@ -285,9 +286,9 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persistent_fused_kernel(co
                         raw[u] = chunk[tid + u * NC];
 #pragma unroll
                     for (int u = 0; u < PER_THREAD; u += 2)
-                        stats_two<T, 1>(st, raw[u], raw[u + 1], vb0 + tid + u * NC,
-                                        vb0 + tid + (u + 1) * NC, col0, nt, tg, c, tv, 0, g.nvec,
-                                        tid, NC, wcheck);
+                        stats_two<T, 1, true>(st, raw[u], raw[u + 1], vb0 + tid + u * NC,
+                                              vb0 + tid + (u + 1) * NC, col0, nt, tg, c, tv, 0,
+                                              g.nvec, tid, NC, wcheck);
                 } else {
                     for (int v = tid; v < nv; v += NC)
                         stats_one<T, 1>(st, chunk[v], vb0 + v, col0, nt, tg, c, tv, 0, g.nvec,
