@@ -141,6 +141,13 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
         : "memory");
 }
 
+// Bring `bytes` of global memory at `src` into L2 (no destination, no
+// completion to wait for); src 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // Named barrier over the first `threads` threads of the CTA (warp multiple).
 __device__ __forceinline__ void named_sync(uint32_t id, uint32_t threads)
 {

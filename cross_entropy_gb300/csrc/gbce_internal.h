@@ -63,6 +63,10 @@ struct RowParams {
 
     int32_t *dev_status;
     int32_t *row_ticket;  // persistent fused kernel: rows handed out beyond the first wave
+    // one-CTA-per-row launches of more than one wave: each CTA warms in L2
+    // the start of the row this many rows ahead (about the CTA that takes
+    // its place on the SM); 0 for none
+    int64_t prefetch_ahead;
 
     // Vocabulary-slice calls (vocab_total > 0): the logits hold global
     // columns [vocab_offset, vocab_offset + vocab); targets are global

@@ -1314,6 +1314,31 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
             }
             if (!ok)
                 report(p.dev_status, GBCE_DEV_TIMEOUT);
+            if (kStats && ok && total > kStages && p.prefetch_ahead > 0 &&
+                r + p.prefetch_ahead < p.rows) {
+                // the start of the row about to follow this CTA on its SM
+                // (one CTA per row here), unless that row is skipped: its
+                // first ring's worth of logits, so that its first copies
+                // come from L2.  Taken once this CTA's last copy is issued
+                // (a few chunks before its sweep ends), and only by the
+                // statistics sweeps: the read+write gradient streams have no
+                // bandwidth to spare for it.
+                const int64_t r2 = r + p.prefetch_ahead;
+                bool live = true;
+                if (kGather)
+                    live = p.row_mask == nullptr || p.row_mask[r2] != 0;
+                else
+                    live = p.targets[r2] != p.ignore_index;
+                if (live) {
+                    const T *row2 = static_cast<const T *>(p.logits) + r2 * p.row_stride;
+                    const RowGeom g2 = row_geom<T>(row2, V);
+                    const int64_t b2 = g2.nvec * 16;
+                    const int64_t ring_bytes = static_cast<int64_t>(kStages) * kChunkBytes;
+                    if (b2 > 0)
+                        bulk_prefetch_l2(row2 + g2.head,
+                                         static_cast<uint32_t>(b2 < ring_bytes ? b2 : ring_bytes));
+                }
+            }
             // no copy may still be in flight when the CTA exits
             for (int64_t j = (i > kStages ? i - kStages : 0); j < i; ++j)
                 mbar_wait(&full_bar[j % kStages], static_cast<uint32_t>((j / kStages) & 1));
@@ -1884,6 +1909,23 @@ static cudaError_t launch_row_kernel(const RowParams &p, cudaStream_t stream)
     if (kStatsMode && q.splits > 1)
         q.splits = one_wave_cluster_size(kernel, q.splits, q.rows, max_clusters);
     const int64_t units = q.rows * q.splits;
+    q.prefetch_ahead = 0;
+    if (kStatsMode && q.splits == 1) {
+        // CTAs resident at once: a launch of more than that many rows warms
+        // each next row in L2 from the CTA it follows
+        static std::atomic<int> per_sm{0};
+        int n = per_sm.load(std::memory_order_relaxed);
+        if (n == 0) {
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kRowThreads,
+                                                              kDynSmemBytes) == cudaSuccess)
+                per_sm.store(n, std::memory_order_relaxed);
+            else
+                (void)cudaGetLastError();  // no prefetch; the launch itself decides
+        }
+        const int64_t resident = static_cast<int64_t>(n) * device_sm_count();
+        if (resident > 0 && units > resident)
+            q.prefetch_ahead = resident;
+    }
     if (!kStatsMode || q.splits == 1) {
         kernel<<<static_cast<unsigned>(units), kRowThreads, kDynSmemBytes, stream>>>(q);
         note_launches(1);
