@@ -670,18 +670,38 @@ __device__ __forceinline__ void merge_state(float &m, float &s, float &h, float 
     }
 }
 
-// Butterfly merge over the 32 lanes of a warp.  Because merge_state is
-// exactly commutative, every lane ends with the same bits.
+// Sum over the 32 lanes of a warp by a butterfly of rounded adds: each add
+// is commutative, so every lane ends with the same bits, in a fixed order.
+__device__ __forceinline__ float warp_sum(float v)
+{
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, off));
+    return v;
+}
+
+// Merge the (m, s[, h]) states of the 32 lanes of a warp (all active) into
+// one, on every lane: the warp's max in one reduction, each lane's sum (and
+// moment: h -> 2^d (h + d s), d = (m - M) c) moved to it, then butterfly
+// sums.  A lane with m = -inf adds nothing; a NaN max is ignored by the max
+// and turns the sums NaN.
 template <int HK>
 __device__ __forceinline__ void warp_merge_state(float &m, float &s, float &h, float c)
 {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
-        const float s2 = __shfl_xor_sync(0xffffffffu, s, off);
-        const float h2 = HK != kHNone ? __shfl_xor_sync(0xffffffffu, h, off) : 0.0f;
-        merge_state<HK>(m, s, h, m2, s2, h2, c);
+    float M;
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(M) : "f"(m));
+    float sv = 0.0f, hv = HK == kHSum ? h : 0.0f;
+    if (M != kNegInf && m != kNegInf) {
+        const float d = __fmul_rn(__fsub_rn(m, M), c);
+        const float f = ex2(d);
+        sv = __fmul_rn(s, f);
+        if (HK == kHMoment)
+            hv = __fmul_rn(__fadd_rn(h, __fmul_rn(d, s)), f);
     }
+    m = M;
+    s = warp_sum(sv);
+    if (HK != kHNone)
+        h = warp_sum(hv);
 }
 
 // log p_t from the others' (m, s) and the target logit, all in raw logit

@@ -78,10 +78,12 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persistent_fused_kernel(co
     constexpr int Q = 4;  // row-id queue, producer -> consumers
     __shared__ uint64_t rq_full[Q], rq_empty[Q];
     __shared__ int32_t rq_row[Q];
-    __shared__ float red_m[NCW], red_s[NCW], red_x[NCW];
-    __shared__ int red_in[NCW];
-    __shared__ float bc_logp;
-    __shared__ int bc_in_range;  // CAP: every logit of the row in the series range
+    __shared__ int64_t rq_lab[Q];  // each handed-out row's label, read by the producer
+    // per-warp partials of a row, double-buffered by the parity of the
+    // consumers' live-row count: a warp that has merged one row can write
+    // the next row's partials while a slower warp still reads this row's
+    __shared__ float red_m[2][NCW], red_s[2][NCW], red_x[2][NCW];
+    __shared__ int red_in[2][NCW];  // CAP: the warp's vectors all in the series range
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -124,7 +126,8 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persistent_fused_kernel(co
                     break;
                 }
                 rq_row[qs] = r < p.rows ? static_cast<int32_t>(r) : -1;
-                mbar_arrive(&rq_full[qs]);  // (release: the consumers see rq_row)
+                rq_lab[qs] = lab;
+                mbar_arrive(&rq_full[qs]);  // (release: the consumers see rq_row, rq_lab)
                 if (r >= p.rows)
                     break;
                 // the ticket for the row after this one, fetched while this
@@ -179,6 +182,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persistent_fused_kernel(co
     // ------------------------------------------------------------ consumers
     uint32_t slot = 0, lap = 0;  // ring position of the next chunk, and its lap
     bool alive = true;
+    uint32_t live_rows = 0;  // rows merged so far (the partials' buffer parity)
     for (uint32_t qi = 0;; ++qi) {
         // the next row from the producer
         const uint32_t qs = qi % Q;
@@ -187,6 +191,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persistent_fused_kernel(co
             break;
         }
         const int64_t r = rq_row[qs];
+        const int64_t lab = rq_lab[qs];
         __syncwarp();
         if (lane == 0)
             mbar_arrive(&rq_empty[qs]);
@@ -194,7 +199,6 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persistent_fused_kernel(co
             break;
         const T *row = static_cast<const T *>(p.logits) + r * p.row_stride;
         T *drow = static_cast<T *>(p.dlogits) + r * p.d_stride;
-        const int64_t lab = p.targets[r];
         if (lab == p.ignore_index || lab < 0 || lab >= V) {
             const bool bad = lab != p.ignore_index;
             const float fill = bad ? __int_as_float(0x7fc00000) : 0.0f;
@@ -304,54 +308,36 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persistent_fused_kernel(co
             }
         }
 
-        // merge: warp shuffles, then warp 0 over the warps, then finalize
+        // merge: each warp's state, one barrier, then every warp merges the
+        // warps' states itself (no second barrier to broadcast log p)
+        const int rb = static_cast<int>(live_rows++ & 1u);
         float m = st.m, s = st.sum(), sx = SMOOTH ? st.xsum() : 0.0f;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
-            const float s2 = __shfl_xor_sync(0xffffffffu, s, off);
-            merge_max_sum(m, s, m2, s2, c);
-            if (SMOOTH)
-                sx = __fadd_rn(sx, __shfl_xor_sync(0xffffffffu, sx, off));
-        }
+        warp_merge_state<SMOOTH ? kHSum : kHNone>(m, s, sx, c);
         if (CAP)
             in_range = __all_sync(0xffffffffu, in_range);
         if (lane == 0) {
-            red_m[warp] = m;
-            red_s[warp] = s;
-            red_x[warp] = sx;
+            red_m[rb][warp] = m;
+            red_s[rb][warp] = s;
+            red_x[rb][warp] = sx;
             if (CAP)
-                red_in[warp] = in_range;
+                red_in[rb][warp] = in_range;
         }
         named_sync(1, NC);
-        if (warp == 0) {
-            m = lane < NCW ? red_m[lane] : kNegInf;
-            s = lane < NCW ? red_s[lane] : 0.0f;
-            sx = lane < NCW ? red_x[lane] : 0.0f;
-            if (CAP)
-                in_range = __all_sync(0xffffffffu, lane < NCW ? red_in[lane] != 0 : true);
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
-                const float s2 = __shfl_xor_sync(0xffffffffu, s, off);
-                merge_max_sum(m, s, m2, s2, c);
-                if (SMOOTH)
-                    sx = __fadd_rn(sx, __shfl_xor_sync(0xffffffffu, sx, off));
-            }
-            if (lane == 0) {
-                const float lp = finalize_logp(m, s, xy, p.T);
-                bc_logp = lp;
-                if (CAP)
-                    bc_in_range = in_range;
-                p.loss_rows[r] = ce_row_loss(lp, xy, sx, p.T, p.ls_eps, p.dft, V);
-                if (p.logp_out)
-                    p.logp_out[r] = lp;
-                if (p.lse_out)
-                    p.lse_out[r] = xy / p.T - lp;
-            }
+        m = lane < NCW ? red_m[rb][lane] : kNegInf;
+        s = lane < NCW ? red_s[rb][lane] : 0.0f;
+        sx = lane < NCW ? red_x[rb][lane] : 0.0f;
+        if (CAP)
+            in_range = __all_sync(0xffffffffu, lane < NCW ? red_in[rb][lane] != 0 : true);
+        warp_merge_state<SMOOTH ? kHSum : kHNone>(m, s, sx, c);
+        const float lp = finalize_logp(m, s, xy, p.T);
+        if (tid == 0) {
+            p.loss_rows[r] = ce_row_loss(lp, xy, sx, p.T, p.ls_eps, p.dft, V);
+            if (p.logp_out)
+                p.logp_out[r] = lp;
+            if (p.lse_out)
+                p.lse_out[r] = xy / p.T - lp;
         }
-        named_sync(1, NC);
-        const GradConsts gk = grad_consts_ce(xy, c, bc_logp, gup, p.T, p.ls_eps, p.dft, V);
+        const GradConsts gk = grad_consts_ce(xy, c, lp, gup, p.T, p.ls_eps, p.dft, V);
 
         // pass 2: gradient
         // soft-capped element: its plain value on z = cap tanh(x / cap) times
@@ -379,8 +365,8 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persistent_fused_kernel(co
                 const int32_t ybase = y - static_cast<int32_t>(g.head + vbase * VEC);
                 T *dbase = drow + g.head + vbase * VEC;
                 if (CAP && nv == CV && p.vec_store) {
-                    grad_capped_chunk<T, PER_THREAD>(chunk, dbase, ybase, tid, NC,
-                                                     bc_in_range != 0, gk, capk);
+                    grad_capped_chunk<T, PER_THREAD>(chunk, dbase, ybase, tid, NC, in_range, gk,
+                                                     capk);
                 } else if (CAP) {
                     for (int v = tid; v < nv; v += NC) {
                         const int32_t yoff = ybase - v * VEC;
