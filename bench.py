@@ -16,6 +16,12 @@ memory and the results (loss, log-probs) read back every step; the copy goes
 in row blocks on a second stream so that each block's compute overlaps the
 next block's copy.
 
+``per_config`` times every op of every seeded workload alone (``ms``: a
+lone CUDA-graph launch after an L2 flush).  For workloads smaller than L2
+it adds ``ms_steady``: the same call back to back over rotating copies of
+its inputs (more than twice the L2 in all), without the fixed floor of a
+lone launch that ``_launch_floor`` records.
+
 ``--impl reference`` times the fp64 CPU oracle on a bounded sample of the
 same rows instead (the only other place this file runs the oracle is the
 ``cpu_baseline`` leg of the default arm).
@@ -441,16 +447,71 @@ def time_op(fn, stream, reps, flush=None):
     return statistics.median(times[2:])
 
 
+L2_BYTES = 129 * 1024 * 1024  # GB300 L2
+
+
+def time_op_steady(make, copies, reps=5):
+    """Median per-call time (ms) of `copies` calls back to back, call i on
+    copy i of the inputs, captured in one CUDA graph.
+
+    For workloads smaller than L2: the copies together hold more than twice
+    the L2, so each call's inputs were last touched `copies - 1` calls ago
+    and come from HBM, as in time_op after a flush.  Unlike time_op's lone
+    call, the call runs among others, so the fixed cost of getting one
+    graph onto the GPU (the floor of a lone launch) is not in it.
+    """
+    fns = [make(i) for i in range(copies)]
+    for f in fns:
+        f()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for f in fns:
+            f()
+    times = []
+    for _ in range(reps + 1):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        graph.replay()
+        b.record()
+        b.synchronize()
+        times.append(a.elapsed_time(b) / copies)
+    del graph
+    return statistics.median(times[1:])
+
+
+def launch_floor_ms(dev, stream):
+    """time_op of a one-element fill after the same L2 flush: the floor that
+    a lone launch's event time carries whatever its kernel does."""
+    flush = torch.empty(128 * 1024 * 1024, dtype=torch.float32, device=dev)
+    e = torch.zeros(1, device=dev)
+    ms = time_op(lambda: e.fill_(0.0), stream, 20, flush)
+    del flush
+    return ms
+
+
 def measure_configs(gbce, dev, stream, peak):
     """Every seeded workload, each op timed alone: ms, rows/s, GB/s, fraction."""
     flush = torch.empty(128 * 1024 * 1024, dtype=torch.float32, device=dev)  # 512 MB > L2
     out = {}
 
-    def record(name, w, op, ms, k=1):
+    def record(name, w, op, ms, k=1, steady=None):
         nb = op_bytes(w, op, k)
         gbs = nb / (ms * 1e-3) / 1e9
         out[name] = {"ms": round(ms, 5), "rows_per_s": round(w.rows / (ms * 1e-3)),
                      "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4), "bytes": nb}
+        if steady is not None:
+            # back to back over rotating copies of the inputs (time_op_steady)
+            out[name]["ms_steady"] = round(steady, 5)
+            out[name]["frac_steady"] = round(nb / (steady * 1e-3) / 1e9 / peak, 4)
+
+    def copies_for(w):
+        """Input copies for time_op_steady (None: the workload exceeds L2)."""
+        nb = w.logits.numel() * w.logits.element_size()
+        if nb >= (256 << 20):
+            return None
+        return max(2, min(512, -(-(5 * L2_BYTES // 2) // nb)))
 
     def ce_ops(tag, w, T, red, g, options=False):
         x, lab = w.logits, w.labels
@@ -458,15 +519,25 @@ def measure_configs(gbce, dev, stream, peak):
         ws = gbce.new_workspace(w.rows, w.vocab, 1, device=dev)
         fwd = gbce.ce_fwd(x, lab, temperature=T, reduction=red, workspace=ws)
         fl = flush if w.logits.numel() * w.logits.element_size() < (256 << 20) else None
+        n = copies_for(w)
+        xs = [x] + [x.clone() for _ in range(n - 1)] if n else None
+        ds = [d] + [torch.empty_like(x) for _ in range(n - 1)] if n else None
+
+        def st(make):
+            return time_op_steady(make, n) if n else None
+
+        fused = lambda xi, di: gbce.ce_fwd_bwd_fused(xi, lab, g, temperature=T, reduction=red,  # noqa: E731
+                                                     dlogits=di, workspace=ws)
+        cfwd = lambda xi: gbce.ce_fwd(xi, lab, temperature=T, reduction=red, workspace=ws)  # noqa: E731
+        cbwd = lambda xi, di: gbce.ce_bwd(xi, lab, g, fwd.logp, fwd.n_items, temperature=T,  # noqa: E731
+                                          reduction=red, dlogits=di)
         record(f"{tag}/ce_fwd_bwd_fused", w, "fused", time_op(
-            lambda: gbce.ce_fwd_bwd_fused(x, lab, g, temperature=T, reduction=red, dlogits=d,
-                                          workspace=ws), stream, 10, fl))
-        record(f"{tag}/ce_fwd", w, "ce_fwd", time_op(
-            lambda: gbce.ce_fwd(x, lab, temperature=T, reduction=red, workspace=ws),
-            stream, 10, fl))
-        record(f"{tag}/ce_bwd", w, "ce_bwd", time_op(
-            lambda: gbce.ce_bwd(x, lab, g, fwd.logp, fwd.n_items, temperature=T, reduction=red,
-                                dlogits=d), stream, 10, fl))
+            lambda: fused(x, d), stream, 10, fl),
+            steady=st(lambda i: lambda: fused(xs[i], ds[i])))
+        record(f"{tag}/ce_fwd", w, "ce_fwd", time_op(lambda: cfwd(x), stream, 10, fl),
+               steady=st(lambda i: lambda: cfwd(xs[i])))
+        record(f"{tag}/ce_bwd", w, "ce_bwd", time_op(lambda: cbwd(x, d), stream, 10, fl),
+               steady=st(lambda i: lambda: cbwd(xs[i], ds[i])))
         if options:  # label smoothing 0.1 with DFT weights: the smoothing sum in the sweep
             kw = dict(temperature=T, reduction=red, label_smoothing=0.1, dft=True)
             record(f"{tag}/ce_fwd_bwd_fused+smooth+dft", w, "fused", time_op(
@@ -490,14 +561,19 @@ def measure_configs(gbce, dev, stream, peak):
         o = torch.empty((w.rows, K_), dtype=torch.float32, device=dev)
         ws = gbce.new_workspace(w.rows, w.vocab, K_, device=dev)
         fl = flush if w.logits.numel() * w.logits.element_size() < (256 << 20) else None
+        n = copies_for(w)
+        xs = [x] + [x.clone() for _ in range(n - 1)] if n else None
+        lp = lambda xi: gbce.selective_logsoftmax(xi, idx, T, mask, out=o, workspace=ws)  # noqa: E731
         record(f"{tag}/selective_logsoftmax", w, "logp", time_op(
-            lambda: gbce.selective_logsoftmax(x, idx, T, mask, out=o, workspace=ws),
-            stream, 10, fl), k=K_)
+            lambda: lp(x), stream, 10, fl), k=K_,
+            steady=time_op_steady(lambda i: lambda: lp(xs[i]), n) if n else None)
         if entropy:
             h = torch.empty(w.rows, dtype=torch.float32, device=dev)
+            le = lambda xi: gbce.selective_logsoftmax(xi, idx, T, mask, out=o, entropy_out=h,  # noqa: E731
+                                                      workspace=ws)
             record(f"{tag}/selective_logsoftmax+entropy", w, "logp_ent", time_op(
-                lambda: gbce.selective_logsoftmax(x, idx, T, mask, out=o, entropy_out=h,
-                                                  workspace=ws), stream, 10, fl), k=K_)
+                lambda: le(x), stream, 10, fl), k=K_,
+                steady=time_op_steady(lambda i: lambda: le(xs[i]), n) if n else None)
         if backward:
             g = torch.ones((w.rows, K_), device=dev)
             d = torch.empty_like(x)
@@ -539,6 +615,9 @@ def measure_configs(gbce, dev, stream, peak):
     logp_op(f"grpo_bf16_{ROWS}x{VOCAB}_k1", w, TEMPERATURE, backward=True, k=1, entropy=True)
     del w, flush
     torch.cuda.empty_cache()
+    out["_launch_floor"] = {"ms": round(launch_floor_ms(dev, stream), 5),
+                            "what": "time_op of a one-element fill: the event time of any "
+                                    "lone launch after the flush starts here"}
     return out
 
 
