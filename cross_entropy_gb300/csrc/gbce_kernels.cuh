@@ -1195,6 +1195,38 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
     }
     __syncthreads();  // the mbarriers exist before anyone uses them
 
+    // this unit's body: 16-byte vectors [v0, v1) of the row, in chunks
+    // (chunk i of a two-pass unit is chunk i mod nchunks of the body)
+    const RowGeom g = row_geom<T>(row, V);
+    const int64_t v0 = p.splits == 1 ? 0 : g.nvec * split / p.splits;
+    const int64_t v1 = p.splits == 1 ? g.nvec : g.nvec * (split + 1) / p.splits;
+    const int64_t nchunks = (v1 - v0 + CV - 1) / CV;
+    const int64_t total = nchunks * kPasses;
+    const char *body = reinterpret_cast<const char *>(row + g.head) + v0 * 16;
+    const int64_t body_bytes = (v1 - v0) * 16;
+    // copy chunk i into its ring slot (the statistics pass of a two-pass
+    // unit keeps its bytes in L2 for the gradient pass)
+    const auto issue_chunk = [&](int64_t i, uint64_t keep, uint64_t stream) {
+        const int slot = static_cast<int>(i % kStages);
+        const int64_t off = (i % nchunks) * kChunkBytes;
+        const int64_t left = body_bytes - off;
+        const uint32_t bytes = static_cast<uint32_t>(left < kChunkBytes ? left : kChunkBytes);
+        const bool first_of_two = (kPasses == 2 && i < nchunks);
+        mbar_arrive_expect_tx(&full_bar[slot], bytes);
+        bulk_load(ring + slot * kChunkBytes, body + off, bytes, &full_bar[slot],
+                  first_of_two ? keep : stream);
+    };
+    // A row split over several CTAs (few rows: latency, not bandwidth, sets
+    // the pace) starts streaming before its row selection is known: the
+    // producer issues the ring's first copies at once, and if the row turns
+    // out to be skipped it waits for them to land before the CTA exits.
+    int64_t issued = 0;
+    if (p.splits > 1 && warp == NCW && lane == 0) {
+        const uint64_t keep = policy_evict_last(), stream = policy_evict_first();
+        for (; issued < total && issued < kStages; ++issued)
+            issue_chunk(issued, keep, stream);
+    }
+
     // ---- row selection, before any read of this row's logits
     int32_t tg[KMAX];
     int32_t y = -1;
@@ -1274,16 +1306,11 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
             if (kGrad)
                 fill_row_slice<T>(drow, V, split, p.splits, fill);
         }
+        // no copy may still be in flight when the CTA exits
+        for (int64_t j = 0; j < issued; ++j)
+            mbar_wait(&full_bar[j], 0);
         return;
     }
-
-    const RowGeom g = row_geom<T>(row, V);
-    const int64_t v0 = p.splits == 1 ? 0 : g.nvec * split / p.splits;
-    const int64_t v1 = p.splits == 1 ? g.nvec : g.nvec * (split + 1) / p.splits;
-    const int64_t nchunks = (v1 - v0 + CV - 1) / CV;
-    const int64_t total = nchunks * kPasses;
-    const char *body = reinterpret_cast<const char *>(row + g.head) + v0 * 16;
-    const int64_t body_bytes = (v1 - v0) * 16;
 
     if (exchange)
         cluster_arrive_relaxed();
@@ -1293,7 +1320,7 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
         if (lane == 0 && total > 0) {
             const uint64_t keep = policy_evict_last();
             const uint64_t stream = policy_evict_first();
-            int64_t i = 0;
+            int64_t i = issued;  // (a split row's first copies are already on their way)
             bool ok = true;
             for (; i < total; ++i) {
                 const int slot = static_cast<int>(i % kStages);
@@ -1302,15 +1329,7 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
                     ok = false;
                     break;
                 }
-                const int64_t ci = i % nchunks;
-                const int64_t off = ci * kChunkBytes;
-                const int64_t left = body_bytes - off;
-                const uint32_t bytes =
-                    static_cast<uint32_t>(left < kChunkBytes ? left : kChunkBytes);
-                const bool first_of_two = (kPasses == 2 && i < nchunks);
-                mbar_arrive_expect_tx(&full_bar[slot], bytes);
-                bulk_load(ring + slot * kChunkBytes, body + off, bytes, &full_bar[slot],
-                          first_of_two ? keep : stream);
+                issue_chunk(i, keep, stream);
             }
             if (!ok)
                 report(p.dev_status, GBCE_DEV_TIMEOUT);
