@@ -47,28 +47,41 @@ namespace gbce {
 #ifndef GBCE_PERSIST_STAGES
 #define GBCE_PERSIST_STAGES 4
 #endif
-constexpr int kPersistWarps = GBCE_PERSIST_WARPS;    // consumer warps
-constexpr int kPersistChunk = GBCE_PERSIST_CHUNK;    // bytes per ring stage
-constexpr int kPersistStages = GBCE_PERSIST_STAGES;  // 192 KB ring: one CTA per SM
-constexpr int kPersistThreads = (kPersistWarps + 1) * 32;
-constexpr int kPersistDynSmem = kPersistStages * kPersistChunk + kRingAlign;
+//
+// The soft-capped kernel is bound by its FMA pipe rather than by HBM, and it
+// runs two half-size CTAs per SM (12 consumer warps, a 4 x 24 KB ring each):
+// one CTA's per-row merge then overlaps the other's sweep (1.18 -> 1.12 ms
+// at 8192 rows).  The uncapped kernel loses with two rows per SM in flight
+// (0.78 -> 0.90 ms): its gradient pass re-reads each row from L2, and twice
+// the rows in flight crowd them out.
+template <bool CAP>
+struct PersistShape {
+    static constexpr int kWarps = CAP ? 12 : GBCE_PERSIST_WARPS;     // consumer warps
+    static constexpr int kChunk = CAP ? 24576 : GBCE_PERSIST_CHUNK;  // bytes per ring stage
+    static constexpr int kStages = CAP ? 4 : GBCE_PERSIST_STAGES;
+    static constexpr int kCtasPerSm = CAP ? 2 : 1;
+    static constexpr int kThreads = (kWarps + 1) * 32;
+    static constexpr int kDynSmem = kStages * kChunk + kRingAlign;
+};
 
 // SMOOTH: label smoothing, which also needs each row's sum of logits.
 // CAP: logit soft-capping, cap * tanh(x / cap) on every logit (and the
 // chain factor 1 - tanh^2 in the gradient).
 template <typename T, bool SMOOTH, bool CAP>
-__global__ void __launch_bounds__(kPersistThreads, 1) persistent_fused_kernel(const RowParams p)
+__global__ void __launch_bounds__(PersistShape<CAP>::kThreads, PersistShape<CAP>::kCtasPerSm)
+    persistent_fused_kernel(const RowParams p)
 {
     using E = Elem<T>;
     constexpr int VEC = E::kVec;
-    constexpr int NCW = kPersistWarps;
+    using Shape = PersistShape<CAP>;
+    constexpr int NCW = Shape::kWarps;
     constexpr int NC = NCW * 32;
-    constexpr int S = kPersistStages;
-    constexpr int CHUNK = kPersistChunk;
+    constexpr int S = Shape::kStages;
+    constexpr int CHUNK = Shape::kChunk;
     constexpr int CV = CHUNK / 16;
     constexpr int PER_THREAD = CV / NC;
     static_assert(CV % NC == 0 && PER_THREAD % 2 == 0, "chunk must split evenly into pairs");
-    static_assert(kPersistThreads <= 1024, "at most 1024 threads per CTA");
+    static_assert(Shape::kThreads <= 1024, "at most 1024 threads per CTA");
 
     extern __shared__ __align__(128) uint8_t dyn_smem[];
     uint8_t *ring = reinterpret_cast<uint8_t *>(
@@ -422,26 +435,29 @@ __global__ void __launch_bounds__(kPersistThreads, 1) persistent_fused_kernel(co
 }
 
 template <typename T, bool SMOOTH, bool CAP>
-cudaError_t launch_persistent_fused_as(const RowParams &p, int grid, cudaStream_t stream)
+cudaError_t launch_persistent_fused_as(const RowParams &p, int sms, cudaStream_t stream)
 {
+    using Shape = PersistShape<CAP>;
     static std::atomic<uint64_t> attr_done{0};
     auto kernel = persistent_fused_kernel<T, SMOOTH, CAP>;
-    cudaError_t err = ensure_smem_attr(kernel, kPersistDynSmem, attr_done);
+    cudaError_t err = ensure_smem_attr(kernel, Shape::kDynSmem, attr_done);
     if (err != cudaSuccess)
         return err;
-    kernel<<<grid, kPersistThreads, kPersistDynSmem, stream>>>(p);
+    const int64_t slots = static_cast<int64_t>(Shape::kCtasPerSm) * sms;
+    const int grid = static_cast<int>(p.rows < slots ? p.rows : slots);
+    kernel<<<grid, Shape::kThreads, Shape::kDynSmem, stream>>>(p);
     note_launches(1);
     return cudaGetLastError();
 }
 
 template <typename T>
-cudaError_t launch_persistent_fused(const RowParams &p, int grid, cudaStream_t stream)
+cudaError_t launch_persistent_fused(const RowParams &p, int sms, cudaStream_t stream)
 {
     if (p.softcap > 0.0f)
-        return p.ls_eps != 0.0f ? launch_persistent_fused_as<T, true, true>(p, grid, stream)
-                                : launch_persistent_fused_as<T, false, true>(p, grid, stream);
-    return p.ls_eps != 0.0f ? launch_persistent_fused_as<T, true, false>(p, grid, stream)
-                            : launch_persistent_fused_as<T, false, false>(p, grid, stream);
+        return p.ls_eps != 0.0f ? launch_persistent_fused_as<T, true, true>(p, sms, stream)
+                                : launch_persistent_fused_as<T, false, true>(p, sms, stream);
+    return p.ls_eps != 0.0f ? launch_persistent_fused_as<T, true, false>(p, sms, stream)
+                            : launch_persistent_fused_as<T, false, false>(p, sms, stream);
 }
 
 }  // namespace gbce
