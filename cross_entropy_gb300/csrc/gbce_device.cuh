@@ -490,7 +490,12 @@ struct OnlineStats {
     __device__ __forceinline__ bool raise_to(float vmax, float c)
     {
         if (vmax > m) {
-            const float d = (m - vmax) * c;
+            // every z so far was x c + nmc: moving the sums to the new shift
+            // multiplies them by 2^(nmc' - nmc), a difference of the two
+            // rounded shifts (exact when they are within a factor of two), so
+            // all terms keep sharing one rounding of the shift (finish)
+            const float nmc_new = -vmax * c;
+            const float d = nmc_new - nmc;
             const float f = ex2(d);
             const float2 ff = make_float2(f, f);
             if (ENT && m != kNegInf) {
@@ -502,7 +507,7 @@ struct OnlineStats {
             sa = fmul2(sa, ff);
             sb = fmul2(sb, ff);
             m = vmax;
-            nmc = -vmax * c;
+            nmc = nmc_new;
         }
         return vmax != kNegInf;
     }
@@ -589,6 +594,16 @@ struct OnlineStats {
     __device__ __forceinline__ float sum() const
     {
         return __fadd_rn(__fadd_rn(sa.x, sa.y), __fadd_rn(sb.x, sb.y));
+    }
+    // Every exponent was evaluated as x c + nmc, nmc the rounded -m c, so
+    // each carries the same r = m c + nmc (exact as one fma; |r| is at most
+    // half an ulp of m c): the sums are 2^r times their values relative to
+    // m.  warp_merge_state takes r out as it moves each lane to the warp's
+    // max.  Left in, a row whose logits are large (|m| / T in the hundreds)
+    // would carry ~2^-24 |m c| of error in every probability.
+    __device__ __forceinline__ float residual(float c) const
+    {
+        return (m == kNegInf || !(m == m)) ? 0.0f : fmaf(m, c, nmc);
     }
     // ENT: the thread's sum of 2^z z.
     __device__ __forceinline__ float hsum() const
@@ -682,17 +697,19 @@ __device__ __forceinline__ float warp_sum(float v)
 
 // Merge the (m, s[, h]) states of the 32 lanes of a warp (all active) into
 // one, on every lane: the warp's max in one reduction, each lane's sum (and
-// moment: h -> 2^d (h + d s), d = (m - M) c) moved to it, then butterfly
-// sums.  A lane with m = -inf adds nothing; a NaN max is ignored by the max
-// and turns the sums NaN.
+// moment: h -> 2^d (h + d s), d = (m - M) c - r) moved to it, then butterfly
+// sums.  r is the lane's exponent residual (OnlineStats::residual; 0 for
+// states that carry none).  A lane with m = -inf adds nothing; a NaN max is
+// ignored by the max and turns the sums NaN.
 template <int HK>
-__device__ __forceinline__ void warp_merge_state(float &m, float &s, float &h, float c)
+__device__ __forceinline__ void warp_merge_state(float &m, float &s, float &h, float c,
+                                                 float r = 0.0f)
 {
     float M;
     asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(M) : "f"(m));
     float sv = 0.0f, hv = HK == kHSum ? h : 0.0f;
     if (M != kNegInf && m != kNegInf) {
-        const float d = __fmul_rn(__fsub_rn(m, M), c);
+        const float d = __fsub_rn(__fmul_rn(__fsub_rn(m, M), c), r);
         const float f = ex2(d);
         sv = __fmul_rn(s, f);
         if (HK == kHMoment)

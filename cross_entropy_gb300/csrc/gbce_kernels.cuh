@@ -651,7 +651,7 @@ __device__ float entropy_around(const T *row, const RowGeom &g, int64_t V, int32
     for_each_own_column<T>(row, g, V, tid, NC,
                            [&](float x, int64_t col) { st.add1(col == d ? kNegInf : x, c); });
     float m = st.m, s = st.sum(), h = st.hsum();
-    warp_merge_state<kHMoment>(m, s, h, c);
+    warp_merge_state<kHMoment>(m, s, h, c, st.residual(c));
     if (NCW == 1)
         return finalize_entropy(m, s, h, xd, temperature);
     if (lane == 0) {
@@ -672,6 +672,37 @@ __device__ float entropy_around(const T *row, const RowGeom &g, int64_t V, int32
     return H;
 }
 
+// The whole row's max M and its sum S = sum_j 2^{(x_j - M) c} (x_j capped
+// under CAP), from NCW consumer warps reading the row from global memory
+// (all of them take part; every one gets both).  For a backward whose
+// gathered column lies far below the row's max (rebase_grad_consts): a
+// second read of that rare row.
+template <typename T, int NCW, bool CAP>
+__device__ void row_max_sum(const T *row, const RowGeom &g, int64_t V, int tid, float c,
+                            float cap, float inv_cap, float *red_m, float *red_s, float &M,
+                            float &S)
+{
+    constexpr int NC = NCW * 32;
+    const int warp = tid >> 5, lane = tid & 31;
+    OnlineStats<false> st;
+    for_each_own_column<T>(row, g, V, tid, NC, [&](float x, int64_t) {
+        st.add1(CAP ? cap * tanhf(x * inv_cap) : x, c);
+    });
+    float m = st.m, s = st.sum(), h = 0.0f;
+    warp_merge_state<kHNone>(m, s, h, c, st.residual(c));
+    if (lane == 0) {
+        red_m[warp] = m;
+        red_s[warp] = s;
+    }
+    named_sync(1, NC);
+    m = lane < NCW ? red_m[lane] : kNegInf;
+    s = lane < NCW ? red_s[lane] : 0.0f;
+    warp_merge_state<kHNone>(m, s, h, c);
+    named_sync(1, NC);  // the scratch arrays are free again
+    M = m;
+    S = s;
+}
+
 // Q = sum_{j != d} p_j (x_d - x_j) / T over a row, with p_j = exp((x_j - x_t)/T
 // + log p_t) taken from a column t whose log p is known accurately.  For the
 // dominant column d, Q equals H + log p_d (H the row entropy), but as a sum
@@ -679,16 +710,17 @@ __device__ float entropy_around(const T *row, const RowGeom &g, int64_t V, int32
 // and H + log p_d cancels when p_d is near 1.  Every consumer thread gets Q.
 template <typename T, int NCW>
 __device__ float entropy_gap(const T *row, const RowGeom &g, int64_t V, int32_t d, float xd,
-                             float xt, float lpt, float c, float inv_t, int tid, float *red)
+                             float xref, float lref2, float c, float inv_t, int tid, float *red)
 {
     constexpr int NC = NCW * 32;
     const int warp = tid >> 5, lane = tid & 31;
-    // 2^(z + 32), z = log2 p_j: p_j down to 2^-158 although ex2 flushes below 2^-126
-    const float kb = fmaf(lpt, kLog2e, 32.0f);
+    // 2^(z + 32), z = log2 p_j from a reference column (x_ref, log2 p_ref):
+    // p_j down to 2^-158 although ex2 flushes below 2^-126
+    const float kb = lref2 + 32.0f;
     float acc = 0.0f;
     for_each_own_column<T>(row, g, V, tid, NC, [&](float x, int64_t col) {
         if (col != d) {
-            const float pj = ex2(fmaf(x - xt, c, kb));
+            const float pj = ex2(fmaf(x - xref, c, kb));
             if (pj > 0.0f || pj != pj)  // a -inf logit adds 0 (not 0 * inf); NaN stays
                 acc = fmaf(pj, (xd - x) * inv_t, acc);
         }
@@ -711,10 +743,11 @@ __device__ float entropy_gap(const T *row, const RowGeom &g, int64_t V, int32_t 
 // (confident rows) come out as exact fp32 subnormals although ex2 itself
 // flushes subnormal results; |g/T| < 2^-90 skips the offset.
 struct GradConsts {
-    float nxy;  // -x_y
+    float nxy;  // -x_ref (x_y, or the row max after rebase_grad_consts)
     float c;    // log2(e) / T
-    float kb;   // log p * log2(e) + offset
-    float kbx;  // kb - x_y * c: the bf16 path's exponent is x * c + kbx
+    float kb;   // log2 p_ref + offset
+    float kbx;  // kb - x_ref * c: the bf16 path's exponent is x * c + kbx
+    float off;  // the offset: 32 or 0
     float gs;   // g / T * 2^-offset
     float dy;   // g / T * expm1(log p), the label column
     float c0;   // constant added to every non-label element (label smoothing)
@@ -728,13 +761,47 @@ __device__ __forceinline__ GradConsts grad_consts(float xy, float c, float logp,
     GradConsts k;
     k.nxy = -xy;
     k.c = c;
-    k.kb = fmaf(logp, kLog2e, offset ? 32.0f : 0.0f);
+    k.off = offset ? 32.0f : 0.0f;
+    k.kb = fmaf(logp, kLog2e, k.off);
     k.kbx = fmaf(-xy, c, k.kb);
     k.gs = offset ? gscale * 0x1p-32f : gscale;
     k.dy = gscale * expm1f(logp);
     k.c0 = 0.0f;
     k.ea = k.eb = 0.0f;
     return k;
+}
+
+// Every gradient element evaluates z_j = log2 p_j + off as (x_j - x_ref) c +
+// log2 p_ref + off.  With the gathered column as the reference (x_y and the
+// forward's log p_y), a column far above it gets z_j as the sum of two large
+// numbers of opposite sign, which leaves it an error of about 2^-24 times
+// their size: past ~40 nats, more than the gradient's fp32 bound.  Moved to
+// the row's max M with log2 p_M = -log2 S (S, the row's sum relative to M,
+// lies in [1, V]), the dominant column's z is exact to rounding and every
+// other column's error is that of its own distance below M.
+__device__ __forceinline__ void rebase_grad_consts(GradConsts &k, float M, float S)
+{
+    if (!(S > 0.0f) || !isfinite(M))  // (an empty or NaN row: nothing to gain)
+        return;
+    k.nxy = -M;
+    k.kb = k.off - log2f(S);
+    k.kbx = fmaf(-M, k.c, k.kb);
+}
+
+// Gathered log p below which the standalone backwards first read the row's
+// max and sum (row_max_sum) to rebase their constants: with the gathered
+// reference, the error of a dominant column's gradient grows as 2^-24 times
+// (|log p| + its margin); below this it could pass the fp32 bound.
+constexpr float kRebaseLogp = -40.0f;
+
+// The (max, sum) state of a row that a fused call's statistics left over
+// its non-target columns (m, s), with the target logit xt folded in: the
+// row's max M and S = sum_j 2^{(x_j - M) c}.
+__device__ __forceinline__ void row_state_with_target(float m, float s, float xt, float c,
+                                                      float &M, float &S)
+{
+    M = fmaxf(m, xt);
+    S = (m == kNegInf ? 0.0f : s * ex2((m - M) * c)) + (xt == kNegInf ? 0.0f : ex2((xt - M) * c));
 }
 
 // Loss of one kept row of the token CE from log p_y, x_y and (label
@@ -1442,6 +1509,7 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
     int64_t seq = 0;  // chunk sequence number across passes (slot, parity)
     bool alive = true;
     float logp = 0.0f, xy = 0.0f;
+    float fm = kNegInf, fs = 0.0f;  // fused: the non-target columns' (max, sum)
 
     if (kStats) {
         OnlineStats<kEnt, kSumx> st;
@@ -1533,7 +1601,7 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
         if (kEnt && alive && isnan(h) && !isnan(s))
             h = rescan_entropy_moment<T, KMAX>(row, g, V, v0, v1, split == 0,
                                                split == p.splits - 1, tg, c, st.nmc, tid, NC);
-        warp_merge_state<kH>(m, s, h, c);
+        warp_merge_state<kH>(m, s, h, c, st.residual(c));
         if (lane == 0) {
             red_m[warp] = m;
             red_s[warp] = s;
@@ -1595,6 +1663,8 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
                         p.lse_out[r] = xy / p.T - logp;
                 }
                 bc_logp = logp;
+                bc_m = m;
+                bc_s = s;
             }
         }
         if (kSlice && tid < p.k)  // the logits of the targets this slice holds
@@ -1639,13 +1709,27 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
             named_sync(1, NC);
             logp = bc_logp;
             xy = s_xt[0];
+            fm = bc_m;
+            fs = bc_s;
         }
     }
 
     if (kSelGrad) {
-        const GradConsts gk =
+        GradConsts gk =
             kEntGrad ? grad_consts_ent(s_xt[0], c, s_lp0, -fmaf(s_gH, s_H, s_G) / p.T, -s_gH / p.T)
                      : grad_consts(s_xt[0], c, s_lp0, -s_G / p.T);
+        // the exponents' reference: the first gathered column, or for a row
+        // far below its max, the max itself (rebase_grad_consts)
+        float xref = s_xt[0], lref2 = s_lp0 * kLog2e;
+        if (s_lp0 < kRebaseLogp) {
+            float M, S;
+            row_max_sum<T, NCW, false>(row, g, V, tid, c, 0.0f, 0.0f, red_m, red_s, M, S);
+            rebase_grad_consts(gk, M, S);
+            if (S > 0.0f && isfinite(M)) {
+                xref = M;
+                lref2 = -log2f(S);
+            }
+        }
         const auto elem = [&](float x) {
             return kEntGrad ? grad_scalar_ent(x, gk) : grad_scalar(x, gk);
         };
@@ -1669,9 +1753,9 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
             for (int k = 0; k < KMAX; ++k)
                 gathered |= (tg[k] == d);
             if (!gathered && d < V) {
-                const float Q = entropy_gap<T, NCW>(row, g, V, d, M, s_xt[0], s_lp0, c,
+                const float Q = entropy_gap<T, NCW>(row, g, V, d, M, xref, lref2, c,
                                                     1.0f / p.T, tid, red_m);
-                const float pd = ex2(fmaf(M - s_xt[0], c, s_lp0 * kLog2e));
+                const float pd = ex2(fmaf(M - xref, c, lref2));
                 dval = pd * (-(s_G / p.T) - (s_gH / p.T) * Q);
                 dcol = d;
                 dvec = (d >= g.head && d < g.tail0) ? static_cast<int32_t>((d - g.head) / VEC) : -1;
@@ -1734,8 +1818,21 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
             logp = p.saved_logp[r];
             xy = capped(E::load(row + y));
         }
-        const GradConsts gk =
+        GradConsts gk =
             grad_consts_ce(xy, c, logp, upstream_grad(p, r), p.T, p.ls_eps, p.dft, V);
+        // the exponents' reference moved to the row's max (rebase_grad_consts):
+        // the fused call has the row's state at hand; ce_bwd reads it again for
+        // a row far below its max
+        if (MODE == kModeFused) {
+            float M, S;
+            row_state_with_target(fm, fs, xy, c, M, S);
+            rebase_grad_consts(gk, M, S);
+        } else if (kCeGrad && logp < kRebaseLogp) {
+            float M, S;
+            row_max_sum<T, NCW, kCap>(row, g, V, tid, c, p.softcap, p.inv_cap, red_m, red_s, M,
+                                      S);
+            rebase_grad_consts(gk, M, S);
+        }
         if (kCap) {
             // soft-capped: element j is (its plain value on z = cap tanh(x / cap))
             // times the chain factor 1 - tanh^2(x / cap)

@@ -325,7 +325,7 @@ __global__ void __launch_bounds__(PersistShape<CAP>::kThreads, PersistShape<CAP>
         // warps' states itself (no second barrier to broadcast log p)
         const int rb = static_cast<int>(live_rows++ & 1u);
         float m = st.m, s = st.sum(), sx = SMOOTH ? st.xsum() : 0.0f;
-        warp_merge_state<SMOOTH ? kHSum : kHNone>(m, s, sx, c);
+        warp_merge_state<SMOOTH ? kHSum : kHNone>(m, s, sx, c, st.residual(c));
         if (CAP)
             in_range = __all_sync(0xffffffffu, in_range);
         if (lane == 0) {
@@ -350,7 +350,14 @@ __global__ void __launch_bounds__(PersistShape<CAP>::kThreads, PersistShape<CAP>
             if (p.lse_out)
                 p.lse_out[r] = xy / p.T - lp;
         }
-        const GradConsts gk = grad_consts_ce(xy, c, lp, gup, p.T, p.ls_eps, p.dft, V);
+        GradConsts gk = grad_consts_ce(xy, c, lp, gup, p.T, p.ls_eps, p.dft, V);
+        if (lp < kRebaseLogp) {
+            // a row far below its max: the exponents' reference moves to the
+            // max (rebase_grad_consts), whose state the merge just gave
+            float M, S;
+            row_state_with_target(m, s, xy, c, M, S);
+            rebase_grad_consts(gk, M, S);
+        }
 
         // pass 2: gradient
         // soft-capped element: its plain value on z = cap tanh(x / cap) times

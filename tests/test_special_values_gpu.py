@@ -6,7 +6,8 @@ values, and so does a row whose every column but the label is -inf (log p
 0, entropy 0, gradient exactly 0).  The sizes take the persistent fused
 kernel (more rows than SMs), the row kernels' next-wave L2 prefetch (more
 rows than resident CTAs, rows longer than one ring) and, for 3 rows, the
-split path.
+split path.  Rows led by one column far above their target (hundreds of
+nats) check that every gradient keeps its bound there too.
 """
 
 import numpy as np
@@ -105,3 +106,57 @@ def test_special_values_match_the_oracle(dtype, rows):
     live = np.setdiff1d(np.arange(rows), nan_rows)
     d = to_f64(mean.dlogits[torch.as_tensor(live, device=DEV)])
     assert np.all(np.isfinite(d))
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("rows", [3, 600])
+def test_rows_dominated_far_above_their_target(dtype, rows):
+    # One column leads each row by 60..400 logit units at T = 0.5 (120..800
+    # nats); the label and the gathered indices lie elsewhere.  The gathered
+    # log p is then far below 0, and the dominant column's gradient must
+    # still meet the gradient bound (in ce_bwd and the selective backward,
+    # which only get the saved log p, and in the fused calls).
+    Vd, T = 4099, 0.5
+    gen = torch.Generator().manual_seed(rows + 11)
+    x_cpu = torch.randn((rows, Vd), generator=gen) * 2.0
+    dom = torch.randint(0, Vd, (rows,), generator=gen)
+    lab = (dom + torch.randint(1, Vd, (rows,), generator=gen)) % Vd
+    margin = 60.0 + 340.0 * torch.rand(rows, generator=gen)
+    x_cpu[torch.arange(rows), dom] += margin
+    x_cpu = x_cpu.to(dtype)
+    idx = torch.stack([lab, (lab + 7) % Vd], dim=1)
+    idx[:, 1] = torch.where(idx[:, 1] == dom, (lab + 8) % Vd, idx[:, 1])
+    g = torch.randn(rows, generator=gen)
+    gK = torch.randn((rows, 2), generator=gen)
+    gH = torch.full((rows,), 0.05)
+    x, lab_d, idx_d = x_cpu.to(DEV), lab.to(DEV), idx.to(DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    fwd = gbce.ce_fwd(x, lab_d, temperature=T, reduction="none", dev_status=status)
+    fused = gbce.ce_fwd_bwd_fused(x, lab_d, g.to(DEV), temperature=T, reduction="none",
+                                  dev_status=status)
+    bwd = gbce.ce_bwd(x, lab_d, g.to(DEV), fwd.logp, fwd.n_items, temperature=T,
+                      reduction="none", dev_status=status)
+    capped = gbce.ce_fwd_bwd_fused(x, lab_d, g.to(DEV), temperature=T, reduction="none",
+                                   softcap=150.0, dev_status=status)
+    lp, ent = gbce.selective_logsoftmax(x, idx_d, T, with_entropy=True, dev_status=status)
+    dsel = gbce.selective_logsoftmax_bwd(x, idx_d, gK.to(DEV), lp, T, dev_status=status)
+    dent = gbce.selective_logsoftmax_bwd(x, idx_d, gK.to(DEV), lp, T, grad_entropy=gH.to(DEV),
+                                         saved_entropy=ent, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+
+    x64 = workloads.to_numpy_f64(x_cpu)
+    ref = oracle.cross_entropy(x64, lab.numpy(), temperature=T, reduction="none",
+                               grad_out=g.double().numpy())
+    ref_cap = oracle.cross_entropy(x64, lab.numpy(), temperature=T, reduction="none",
+                                   grad_out=g.double().numpy(), softcap=150.0)
+    assert np.all(ref["logp"] < -100.0)
+    assert_logp_close(to_f64(fwd.logp), ref["logp"], dtype, "ce_fwd log p")
+    assert_grad_rows_close(to_f64(fused.dlogits), ref["dlogits"], dtype, "fused dlogits")
+    assert_grad_rows_close(to_f64(bwd), ref["dlogits"], dtype, "ce_bwd dlogits")
+    assert_grad_rows_close(to_f64(capped.dlogits), ref_cap["dlogits"], dtype, "capped dlogits")
+    ref_d, _ = oracle.selective_logsoftmax_backward(x64, idx.numpy(), gK.double().numpy(), T)
+    ref_de, _ = oracle.selective_logsoftmax_backward(x64, idx.numpy(), gK.double().numpy(), T,
+                                                     grad_entropy=gH.double().numpy())
+    assert_grad_rows_close(to_f64(dsel), ref_d, dtype, "selective backward")
+    assert_grad_rows_close(to_f64(dent), ref_de, dtype, "selective backward + entropy")
