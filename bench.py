@@ -770,8 +770,8 @@ def run_profile_case(case: str, rows: int = 1024):
         cuts = [0, V // 2, V]
         parts = torch.stack([gbce.vocab_slice_stats(x[:, a:b], idx, a, V, T)
                              for a, b in zip(cuts[:-1], cuts[1:])])
-        lp, xt0 = gbce.vocab_slice_combine(parts, cuts, idx, T)
-        gbce.vocab_slice_grad(x[:, :cuts[1]], idx, 0, V, g4, lp, xt0, T)
+        lp, xt0, state = gbce.vocab_slice_combine(parts, cuts, idx, T)
+        gbce.vocab_slice_grad(x[:, :cuts[1]], idx, 0, V, g4, lp, xt0, T, row_state=state)
     torch.cuda.synchronize()
     print(f"profile case {case}: done", flush=True)
 

@@ -72,9 +72,9 @@ _SIGNATURES = {
     "vocab_slice_stats": (_i32, [_vp, _i32, _i64, _i64, _i64, _i64, _i64, _vp, _i64, _i64, _vp,
                                  _f32, _vp, _vp, _vp]),
     "vocab_slice_combine": (_i32, [_vp, _i64, _vp, _i64, _vp, _i64, _i64, _vp, _f32, _vp, _vp,
-                                   _vp, _vp]),
+                                   _vp, _vp, _vp]),
     "vocab_slice_grad": (_i32, [_vp, _i32, _i64, _i64, _i64, _i64, _i64, _vp, _i64, _i64, _vp,
-                                _f32, _vp, _vp, _vp, _vp, _i64, _vp, _vp]),
+                                _f32, _vp, _vp, _vp, _vp, _vp, _i64, _vp, _vp]),
 }
 MAX_SLICES = 64
 
@@ -525,9 +525,11 @@ def gather_slice_partials(partials: torch.Tensor, group=None) -> torch.Tensor:
 def vocab_slice_combine(partials: torch.Tensor, slice_offsets, index, temperature: float = 1.0,
                         row_mask: Optional[torch.Tensor] = None, *, ignore_index: int = -100,
                         dev_status: Optional[torch.Tensor] = None, stream=None):
-    """log p [rows, K] (and the logit of index[:, 0], [rows]) from all slices'
-    partials stacked in slice order, [slices, rows, 2 + K]; ``slice_offsets``
-    are the slices' first global columns followed by the vocabulary size."""
+    """From all slices' partials stacked in slice order, [slices, rows, 2 + K]:
+    ``(logp [rows, K], target_logit [rows], row_state [rows, 2])`` -- the
+    log-probs, the logit of index[:, 0] and each row's whole (max, sum),
+    the last two for :func:`vocab_slice_grad`.  ``slice_offsets`` are the
+    slices' first global columns followed by the vocabulary size."""
     lib = load_library()
     if not partials.is_cuda or partials.dtype != torch.float32 or partials.dim() != 3:
         raise ValueError("partials must be a float32 CUDA tensor [slices, rows, 2 + K]")
@@ -545,24 +547,28 @@ def vocab_slice_combine(partials: torch.Tensor, slice_offsets, index, temperatur
     part = partials.contiguous()
     logp = torch.empty((rows, K), dtype=torch.float32, device=partials.device)
     xt0 = torch.empty(rows, dtype=torch.float32, device=partials.device)
+    state = torch.empty((rows, 2), dtype=torch.float32, device=partials.device)
     host_offs = (ctypes.c_int64 * len(offs))(*offs)
     _check_status(dev_status, partials.device)
     with torch.cuda.device(partials.device):
         st = lib.vocab_slice_combine(part.data_ptr(), slices, ctypes.cast(host_offs, _vp), rows,
                                      idx.data_ptr(), K, int(ignore_index), _ptr(mask),
                                      float(temperature), logp.data_ptr(), xt0.data_ptr(),
-                                     _ptr(dev_status), _stream_ptr(stream, partials.device))
+                                     state.data_ptr(), _ptr(dev_status),
+                                     _stream_ptr(stream, partials.device))
     _check(st, "vocab_slice_combine")
-    return logp, xt0
+    return logp, xt0, state
 
 
 def vocab_slice_grad(logits_slice: torch.Tensor, index, vocab_offset: int, vocab: int,
                      grad_logp, logp: torch.Tensor, target_logit: torch.Tensor,
                      temperature: float = 1.0, row_mask: Optional[torch.Tensor] = None, *,
-                     ignore_index: int = -100, dlogits: Optional[torch.Tensor] = None,
+                     row_state: Optional[torch.Tensor] = None, ignore_index: int = -100,
+                     dlogits: Optional[torch.Tensor] = None,
                      dev_status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
     """dL/d logits_slice for upstream grad_logp = dL/d logp, from the combined
-    log-probs and target logit of :func:`vocab_slice_combine`."""
+    log-probs, target logit and (optional, for rows whose first index lies far
+    below the row's max) row state of :func:`vocab_slice_combine`."""
     lib = load_library()
     lead_shape = logits_slice.shape[:-1]
     x = _rows_view(logits_slice)
@@ -572,6 +578,9 @@ def vocab_slice_grad(logits_slice: torch.Tensor, index, vocab_offset: int, vocab
     g = g.contiguous()
     lp = logp.to(device=x.device, dtype=torch.float32).reshape(rows, K).contiguous()
     xt = target_logit.to(device=x.device, dtype=torch.float32).reshape(rows).contiguous()
+    rs = None
+    if row_state is not None:
+        rs = row_state.to(device=x.device, dtype=torch.float32).reshape(rows, 2).contiguous()
     mask = None
     if row_mask is not None:
         mask = row_mask.to(device=x.device, dtype=torch.uint8).reshape(rows).contiguous()
@@ -584,8 +593,9 @@ def vocab_slice_grad(logits_slice: torch.Tensor, index, vocab_offset: int, vocab
         st = lib.vocab_slice_grad(x.data_ptr(), _dtype_code(x), rows, n, x.stride(0),
                                   int(vocab_offset), int(vocab), idx.data_ptr(), K,
                                   int(ignore_index), _ptr(mask), float(temperature),
-                                  g.data_ptr(), lp.data_ptr(), xt.data_ptr(), d.data_ptr(),
-                                  d.stride(0), _ptr(dev_status), _stream_ptr(stream, x.device))
+                                  g.data_ptr(), lp.data_ptr(), xt.data_ptr(), _ptr(rs),
+                                  d.data_ptr(), d.stride(0), _ptr(dev_status),
+                                  _stream_ptr(stream, x.device))
     _check(st, "vocab_slice_grad")
     return dlogits
 

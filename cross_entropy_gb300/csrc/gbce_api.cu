@@ -535,7 +535,7 @@ gbce_status vocab_slice_combine(const float *partials, int64_t slices,
                                 const int64_t *slice_offsets, int64_t rows, const int64_t *index,
                                 int64_t k, int64_t ignore_index, const uint8_t *row_mask,
                                 float temperature, float *logp_out, float *target_logit_out,
-                                int32_t *dev_status, void *stream)
+                                float *row_state_out, int32_t *dev_status, void *stream)
 {
     if (slices < 1 || slices > GBCE_MAX_SLICES || slice_offsets == nullptr || rows < 0 ||
         k < 1 || k > GBCE_MAX_K || !(std::isfinite(temperature) && temperature > 0.0f))
@@ -555,7 +555,7 @@ gbce_status vocab_slice_combine(const float *partials, int64_t slices,
     const float c = static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
     return cuda_status(gbce::launch_slice_combine(
         partials, static_cast<int>(slices), offs, rows, index, k, ignore_index, row_mask,
-        temperature, c, logp_out, target_logit_out, dev_status,
+        temperature, c, logp_out, target_logit_out, row_state_out, dev_status,
         static_cast<cudaStream_t>(stream)));
 }
 
@@ -563,8 +563,9 @@ gbce_status vocab_slice_grad(const void *logits, gbce_dtype dtype, int64_t rows,
                              int64_t slice_vocab, int64_t row_stride, int64_t vocab_offset,
                              int64_t vocab, const int64_t *index, int64_t k, int64_t ignore_index,
                              const uint8_t *row_mask, float temperature, const float *grad_logp,
-                             const float *logp, const float *target_logit, void *dlogits,
-                             int64_t dlogits_row_stride, int32_t *dev_status, void *stream)
+                             const float *logp, const float *target_logit,
+                             const float *row_state, void *dlogits, int64_t dlogits_row_stride,
+                             int32_t *dev_status, void *stream)
 {
     gbce_status st = check_logits(logits, dtype, rows, slice_vocab, row_stride, temperature);
     if (st != GBCE_OK)
@@ -593,6 +594,7 @@ gbce_status vocab_slice_grad(const void *logits, gbce_dtype dtype, int64_t rows,
     p.grad_out = grad_logp;
     p.saved_logp = logp;
     p.target_logit = target_logit;
+    p.row_state = row_state;
     return cuda_status(launch_rows(p, dtype, gbce::kModeLogpGrad,
                                    static_cast<cudaStream_t>(stream)));
 }

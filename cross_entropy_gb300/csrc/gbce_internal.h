@@ -75,6 +75,9 @@ struct RowParams {
     int64_t vocab_offset, vocab_total;
     float *slice_partials;      // kModeSliceStats: [rows, 2 + k] (m, s, target logits)
     const float *target_logit;  // slice gradient: [rows] logit of the first index
+    // slice gradient: [rows, 2] the whole row's max M (raw logit) and sum S of
+    // 2^{(x_j - M) c} over all its columns, from the combine; nullable
+    const float *row_state;
 };
 
 // Merge vocabulary-slice partials into log-probs (one thread per row).
@@ -85,7 +88,8 @@ struct SliceOffsets {
 cudaError_t launch_slice_combine(const float *partials, int slices, const SliceOffsets &offs,
                                  int64_t rows, const int64_t *index, int64_t k,
                                  int64_t ignore_index, const uint8_t *row_mask, float T, float c,
-                                 float *logp_out, float *target_logit_out, int32_t *dev_status,
+                                 float *logp_out, float *target_logit_out, float *row_state_out,
+                                 int32_t *dev_status,
                                  cudaStream_t stream);
 
 // Row kernel (one CTA per work unit) for logit type T (float / bf16).

@@ -788,6 +788,10 @@ __device__ __forceinline__ void rebase_grad_consts(GradConsts &k, float M, float
     k.kbx = fmaf(-M, k.c, k.kb);
 }
 
+// A vocabulary slice's gradient: the row is not all here, so its whole
+// state comes from the combine (RowParams::row_state) instead of a re-read.
+__device__ __forceinline__ bool kSliceGradRow(const RowParams &p) { return p.vocab_total > 0; }
+
 // Gathered log p below which the standalone backwards first read the row's
 // max and sum (row_max_sum) to rebase their constants: with the gathered
 // reference, the error of a dominant column's gradient grows as 2^-24 times
@@ -1721,9 +1725,14 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
         // the exponents' reference: the first gathered column, or for a row
         // far below its max, the max itself (rebase_grad_consts)
         float xref = s_xt[0], lref2 = s_lp0 * kLog2e;
-        if (s_lp0 < kRebaseLogp) {
+        if (s_lp0 < kRebaseLogp && (!kSliceGradRow(p) || p.row_state != nullptr)) {
             float M, S;
-            row_max_sum<T, NCW, false>(row, g, V, tid, c, 0.0f, 0.0f, red_m, red_s, M, S);
+            if (kSliceGradRow(p)) {  // a vocabulary slice: the combine's whole-row state
+                M = p.row_state[2 * r];
+                S = p.row_state[2 * r + 1];
+            } else {
+                row_max_sum<T, NCW, false>(row, g, V, tid, c, 0.0f, 0.0f, red_m, red_s, M, S);
+            }
             rebase_grad_consts(gk, M, S);
             if (S > 0.0f && isfinite(M)) {
                 xref = M;

@@ -8,7 +8,10 @@
 // device ran first -- takes each target's logit from the slice that holds
 // it, and finishes exactly as the single-device sweep does: the other
 // targets join a target's "others", then log p = -softplus(log s + (m -
-// x_t) / T).
+// x_t) / T).  It also gives each row's whole state -- the max M over all
+// its columns and the sum S of exp((x_j - M) / T) -- which the slice
+// gradient takes as its exponents' reference for a row whose first index
+// lies far below the row's max.
 //
 // Source: "Fix softmax collapse in CE, GRPO, KL/JSD and softmax"
 // (Liger-Kernel PR #1555), "Summary", first bullet (the vocab-parallel form
@@ -22,7 +25,7 @@ __global__ void slice_combine_kernel(const float *partials, int slices, SliceOff
                                      int64_t rows, const int64_t *index, int K,
                                      int64_t ignore_index, const uint8_t *row_mask, float T,
                                      float c, float *logp_out, float *target_logit_out,
-                                     int32_t *dev_status)
+                                     float *row_state_out, int32_t *dev_status)
 {
     const int64_t r = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (r >= rows)
@@ -35,6 +38,10 @@ __global__ void slice_combine_kernel(const float *partials, int slices, SliceOff
             logp_out[r * K + k] = 0.0f;
         if (target_logit_out)
             target_logit_out[r] = 0.0f;
+        if (row_state_out) {
+            row_state_out[2 * r] = kNegInf;
+            row_state_out[2 * r + 1] = 0.0f;
+        }
         return;
     }
     float m = kNegInf, s = 0.0f;
@@ -67,13 +74,26 @@ __global__ void slice_combine_kernel(const float *partials, int slices, SliceOff
     }
     if (target_logit_out)
         target_logit_out[r] = tg[0] >= 0 ? xt[0] : __int_as_float(0x7fc00000);
+    if (row_state_out) {
+        // the other columns' state with each distinct target folded in
+        float M = m, S = s;
+        for (int k = 0; k < K; ++k) {
+            bool dup = tg[k] < 0;
+            for (int i = 0; i < k; ++i)
+                dup |= (tg[i] == tg[k]);
+            if (!dup)
+                merge_max_sum(M, S, xt[k], 1.0f, c);
+        }
+        row_state_out[2 * r] = M;
+        row_state_out[2 * r + 1] = S;
+    }
 }
 
 cudaError_t launch_slice_combine(const float *partials, int slices, const SliceOffsets &offs,
                                  int64_t rows, const int64_t *index, int64_t k,
                                  int64_t ignore_index, const uint8_t *row_mask, float T, float c,
-                                 float *logp_out, float *target_logit_out, int32_t *dev_status,
-                                 cudaStream_t stream)
+                                 float *logp_out, float *target_logit_out, float *row_state_out,
+                                 int32_t *dev_status, cudaStream_t stream)
 {
     if (rows == 0)
         return cudaSuccess;
@@ -82,7 +102,8 @@ cudaError_t launch_slice_combine(const float *partials, int slices, const SliceO
     slice_combine_kernel<<<blocks, threads, 0, stream>>>(partials, slices, offs, rows, index,
                                                          static_cast<int>(k), ignore_index,
                                                          row_mask, T, c, logp_out,
-                                                         target_logit_out, dev_status);
+                                                         target_logit_out, row_state_out,
+                                                         dev_status);
     note_launches(1);
     return cudaGetLastError();
 }

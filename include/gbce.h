@@ -335,7 +335,10 @@ gbce_status vocab_slice_stats(const void *logits, gbce_dtype dtype, int64_t rows
  * slices + 1 int64 (read during the call).  logp_out: [rows, k] fp32 as
  * selective_logsoftmax would give on the whole vocabulary (a bad index: NaN
  * and GBCE_DEV_BAD_INDEX); target_logit_out: [rows] fp32 or NULL, the logit
- * of index[r, 0], which vocab_slice_grad needs.  The merge runs in slice
+ * of index[r, 0], which vocab_slice_grad needs; row_state_out: [rows, 2]
+ * fp32 or NULL, each row's max M over all its columns (raw logit) and S =
+ * sum_j exp((x_j - M) / T) (a skipped row: -inf, 0), which vocab_slice_grad
+ * takes for rows far below their max.  The merge runs in slice
  * order, so the result does not depend on the order the slices were
  * computed in.
  * Errors: GBCE_EINVAL for slices outside [1, GBCE_MAX_SLICES], offsets not
@@ -346,7 +349,7 @@ gbce_status vocab_slice_combine(const float *partials, int64_t slices,
                                 const int64_t *slice_offsets, int64_t rows, const int64_t *index,
                                 int64_t k, int64_t ignore_index, const uint8_t *row_mask,
                                 float temperature, float *logp_out, float *target_logit_out,
-                                int32_t *dev_status, void *stream);
+                                float *row_state_out, int32_t *dev_status, void *stream);
 
 /*
  * Gradient of sum_k grad_logp[r, k] * logp[r, k] with respect to one
@@ -354,9 +357,13 @@ gbce_status vocab_slice_combine(const float *partials, int64_t slices,
  * holds), from the combined log-probs and target logit:
  *   dlogits[r, j] = (1/T) (sum_{k : index[r, k] = j} g[r, k] - G_r p_j),
  *   p_j = exp((x_j - x_{t0}) / T + logp[r, 0]),
- * gathered columns in the -expm1 form.
+ * gathered columns in the -expm1 form.  A row with logp[r, 0] < -40 and a
+ * row_state takes p_j = exp((x_j - M) / T) / S from the row state instead:
+ * taken relative to index 0, a column hundreds of nats above it would lose
+ * fp32 accuracy.
  *   logp         [rows, k] fp32 from vocab_slice_combine
  *   target_logit [rows] fp32 from vocab_slice_combine
+ *   row_state    [rows, 2] fp32 from vocab_slice_combine, or NULL
  *   dlogits      [rows, dlogits_row_stride] of the logits' type, the slice's
  *                columns; must not overlap the logits
  * Errors: as selective_logsoftmax_bwd; a row with an index outside
@@ -366,8 +373,9 @@ gbce_status vocab_slice_grad(const void *logits, gbce_dtype dtype, int64_t rows,
                              int64_t slice_vocab, int64_t row_stride, int64_t vocab_offset,
                              int64_t vocab, const int64_t *index, int64_t k, int64_t ignore_index,
                              const uint8_t *row_mask, float temperature, const float *grad_logp,
-                             const float *logp, const float *target_logit, void *dlogits,
-                             int64_t dlogits_row_stride, int32_t *dev_status, void *stream);
+                             const float *logp, const float *target_logit,
+                             const float *row_state, void *dlogits, int64_t dlogits_row_stride,
+                             int32_t *dev_status, void *stream);
 
 /*
  * ce_fwd_bwd_fused without a caller workspace and without any allocation.

@@ -36,12 +36,13 @@ def run_slices(x, idx, cuts, T, mask=None, g=None, ignore_index=-100):
     parts = [gbce.vocab_slice_stats(x[:, a:b], idx, a, V, T, mask, ignore_index=ignore_index,
                                     dev_status=status)
              for a, b in zip(cuts[:-1], cuts[1:])]
-    logp, xt0 = gbce.vocab_slice_combine(torch.stack(parts), cuts, idx, T, mask,
-                                         ignore_index=ignore_index, dev_status=status)
+    logp, xt0, state = gbce.vocab_slice_combine(torch.stack(parts), cuts, idx, T, mask,
+                                                ignore_index=ignore_index, dev_status=status)
     d = None
     if g is not None:
         d = torch.cat([gbce.vocab_slice_grad(x[:, a:b], idx, a, V, g, logp, xt0, T, mask,
-                                             ignore_index=ignore_index, dev_status=status)
+                                             row_state=state, ignore_index=ignore_index,
+                                             dev_status=status)
                        for a, b in zip(cuts[:-1], cuts[1:])], dim=1)
     torch.cuda.synchronize()
     return logp, xt0, d, int(status.item())
@@ -125,3 +126,25 @@ def test_slice_arguments_are_checked_on_the_host():
         gbce.vocab_slice_combine(parts, [0, 10, 10], idx)  # offsets not increasing
     with pytest.raises(gbce.GbceError):
         gbce.vocab_slice_combine(parts, [5, 10, 20], idx)  # not starting at 0
+
+
+def test_slices_of_rows_dominated_far_above_their_first_index():
+    # a column outside the gathered set leads each row by 60..400 units at
+    # T = 0.5 (hundreds of nats): the combine's row state keeps the slice
+    # gradient within the fp32 bound
+    rows, V, T = 300, 9001, 0.5
+    gen = torch.Generator().manual_seed(77)
+    x_cpu = torch.randn((rows, V), generator=gen) * 2.0
+    dom = torch.randint(0, V, (rows,), generator=gen)
+    idx = ((dom + torch.randint(1, V, (rows,), generator=gen)) % V)[:, None]
+    x_cpu[torch.arange(rows), dom] += 60.0 + 340.0 * torch.rand(rows, generator=gen)
+    g = torch.randn((rows, 1), generator=gen)
+    cuts = [0, 3000, 6001, V]
+    logp, _, d, status = run_slices(x_cpu.to(DEV), idx.to(DEV), cuts, T, g=g.to(DEV))
+    assert status == 0
+    x64 = x_cpu.double().numpy()
+    ref, _ = oracle.selective_logsoftmax(x64, idx.numpy(), T)
+    assert np.all(ref < -100.0)
+    assert_logp_close(to_f64(logp), ref, torch.float32, "sliced log p")
+    ref_d, _ = oracle.selective_logsoftmax_backward(x64, idx.numpy(), g.double().numpy(), T)
+    assert_grad_block_close(to_f64(d), ref_d, torch.float32, "sliced gradient")
