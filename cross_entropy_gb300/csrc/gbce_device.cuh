@@ -156,34 +156,6 @@ __device__ __forceinline__ void named_sync(uint32_t id, uint32_t threads)
 
 // ------------------------------------------------------ PTX: thread-block clusters
 
-__device__ __forceinline__ uint32_t cluster_rank()
-{
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-__device__ __forceinline__ uint32_t cluster_size()
-{
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
-    return r;
-}
-
-__device__ __forceinline__ uint32_t cluster_index()
-{
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
-    return r;
-}
-
-__device__ __forceinline__ uint32_t cluster_count()
-{
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
-    return r;
-}
-
 // The cluster barrier in two halves.  Every thread of every CTA arrives
 // once, right after its CTA's mbarriers are initialised (whose
 // fence.mbarrier_init makes them visible to the cluster); the relaxed arrive

@@ -37,7 +37,9 @@ namespace gbce {
 // 8 x 32K x 4: 75%, 16 x 16K x 8: 80%, 16 x 64K x 2: 78%, 16 x 32K x 4: 86%,
 // 20 x 40K x 4: 91.5%, 24 x 48K x 4: 94.8%, 28 x 28K x 4: 81% of measured
 // HBM bandwidth -- more warps hide the exp chains' latency as long as each
-// thread still gets four 16-byte vectors per chunk.
+// thread still gets four 16-byte vectors per chunk.  Later, with the
+// one-barrier merge: 24 x 48K x 4 at 0.95-0.96 against 24 x 72K x 3 at 0.89
+// and 24 x 24K x 8 at 0.90.
 #ifndef GBCE_PERSIST_WARPS
 #define GBCE_PERSIST_WARPS 24
 #endif
