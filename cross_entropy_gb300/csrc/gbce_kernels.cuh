@@ -790,7 +790,7 @@ __device__ __forceinline__ void rebase_grad_consts(GradConsts &k, float M, float
 
 // A vocabulary slice's gradient: the row is not all here, so its whole
 // state comes from the combine (RowParams::row_state) instead of a re-read.
-__device__ __forceinline__ bool kSliceGradRow(const RowParams &p) { return p.vocab_total > 0; }
+__device__ __forceinline__ bool slice_row(const RowParams &p) { return p.vocab_total > 0; }
 
 // Gathered log p below which the standalone backwards first read the row's
 // max and sum (row_max_sum) to rebase their constants: with the gathered
@@ -1725,9 +1725,9 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
         // the exponents' reference: the first gathered column, or for a row
         // far below its max, the max itself (rebase_grad_consts)
         float xref = s_xt[0], lref2 = s_lp0 * kLog2e;
-        if (s_lp0 < kRebaseLogp && (!kSliceGradRow(p) || p.row_state != nullptr)) {
+        if (s_lp0 < kRebaseLogp && (!slice_row(p) || p.row_state != nullptr)) {
             float M, S;
-            if (kSliceGradRow(p)) {  // a vocabulary slice: the combine's whole-row state
+            if (slice_row(p)) {  // a vocabulary slice: the combine's whole-row state
                 M = p.row_state[2 * r];
                 S = p.row_state[2 * r + 1];
             } else {
