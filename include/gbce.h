@@ -135,7 +135,11 @@ gbce_status selective_logsoftmax(const void *logits, gbce_dtype dtype, int64_t r
  * grad_entropy, the gradient of gH_r * H_r (H_r the row entropy of the
  * forward's entropy_out) is added:
  *   - (gH_r / T) * p_j * (log p_j + H_r)   for every column j,
- * 0 where p_j = 0, with log p of the gathered columns from saved_logp.
+ * 0 where p_j = 0, with log p of the gathered columns from saved_logp.  The
+ * other columns' p_j are taken relative to index[r, 0]; a row with
+ * saved_logp[r, 0] < -40 reads its max and sum in a second pass over that
+ * row and takes them relative to the max (hundreds of nats between the
+ * two would cost fp32 accuracy).
  *
  * Source: the gradient a GRPO-style loss sends back through the accurate
  * log-probs of "Fix softmax collapse in CE, GRPO, KL/JSD and softmax"
@@ -237,8 +241,11 @@ gbce_status ce_fwd(const void *logits, gbce_dtype dtype, int64_t rows, int64_t v
  *   dlogits[r, y] = (g_r / T) * expm1(log p_y),
  * i.e. g_r * (softmax - onehot) / T with the target term in the form that
  * does not round to zero (with options: the smoothed and DFT-weighted
- * gradient described at gbce_ce_options); ignored rows get a zero row.
- * g_r = grad_out[r]
+ * gradient described at gbce_ce_options); ignored rows get a zero row.  A
+ * row with log p_y < -40 evaluates its exponents from the row's max instead
+ * (z_j - z_max - log S), read in a second pass over that row: taken
+ * relative to the label, a column hundreds of nats above it would lose fp32
+ * accuracy.  g_r = grad_out[r]
  * (NONE), grad_out[0] (SUM) or grad_out[0] / n_items (MEAN, 0 when
  * n_items == 0).
  *
