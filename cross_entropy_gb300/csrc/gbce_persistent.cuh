@@ -56,6 +56,10 @@ namespace gbce {
 // at 8192 rows).  The uncapped kernel loses with two rows per SM in flight
 // (0.78 -> 0.90 ms): its gradient pass re-reads each row from L2, and twice
 // the rows in flight crowd them out.
+// L2 bytes the rows awaiting their gradient pass may take (see
+// launch_persistent_fused_as).
+constexpr int64_t kPersistL2Budget = int64_t(76) << 20;
+
 template <bool CAP>
 struct PersistShape {
     static constexpr int kWarps = CAP ? 12 : GBCE_PERSIST_WARPS;     // consumer warps
@@ -452,7 +456,19 @@ cudaError_t launch_persistent_fused_as(const RowParams &p, int sms, cudaStream_t
     cudaError_t err = ensure_smem_attr(kernel, Shape::kDynSmem, attr_done);
     if (err != cudaSuccess)
         return err;
-    const int64_t slots = static_cast<int64_t>(Shape::kCtasPerSm) * sms;
+    int64_t slots = static_cast<int64_t>(Shape::kCtasPerSm) * sms;
+    if (!CAP) {
+        // every CTA keeps one row in L2 from its first read to its re-read:
+        // with long rows, fewer CTAs, so that those rows stay within about
+        // 80 MB (fp32 rows of 152K columns: 131 CTAs, 0.43 -> 0.42 ms at
+        // 2048 rows; 152 rows in flight, 92 MB, lose their re-read), but
+        // never fewer than half the SMs (rows too long for L2 miss anyway)
+        const int64_t row_bytes = p.vocab * static_cast<int64_t>(sizeof(T));
+        const int64_t fit = kPersistL2Budget / (row_bytes > 0 ? row_bytes : 1);
+        const int64_t floor = sms / 2 > 0 ? sms / 2 : 1;
+        if (fit < slots)
+            slots = fit > floor ? fit : floor;
+    }
     const int grid = static_cast<int>(p.rows < slots ? p.rows : slots);
     kernel<<<grid, Shape::kThreads, Shape::kDynSmem, stream>>>(p);
     note_launches(1);
