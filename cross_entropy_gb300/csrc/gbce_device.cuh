@@ -592,8 +592,8 @@ struct OnlineStats {
 using OnlineMaxSum = OnlineStats<false>;
 
 // Merge two (max, sum) partial states with the same scale c.  Exactly
-// commutative (no fused multiply-add), so every lane of a butterfly
-// reduction ends with the same bits.
+// commutative (no fused multiply-add): merging the slices of a row in slice
+// order, or two partials in either order, gives the same bits.
 __device__ __forceinline__ void merge_max_sum(float &m, float &s, float m2, float s2, float c)
 {
     const float M = fmaxf(m, m2);
