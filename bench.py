@@ -80,14 +80,23 @@ def measured_peak():
 
 
 def kernel_source_hash():
+    """Hash of the CUDA sources' code: comments and blank space left out,
+    so that a comment edit does not void counters taken on the same code
+    (a string literal holding a comment marker would be cut too: there is
+    none that matters in these sources)."""
     import hashlib
+    import re
 
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "cross_entropy_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
         if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(f.read())
+            with open(os.path.join(csrc, name), encoding="utf-8") as f:
+                text = f.read()
+            text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+            text = re.sub(r"//[^\n]*", " ", text)
+            h.update(name.encode())
+            h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 
