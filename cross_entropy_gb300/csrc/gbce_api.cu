@@ -71,9 +71,11 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct WsLayout {
     size_t count = 0;     // int64 n_items scratch
-    size_t ticket = 0;    // int32 row ticket of the persistent fused kernel
+    size_t ticket = 0;    // int32 row ticket of the persistent fused kernel, then the int32
+                          // flag of its row order
     size_t loss = 0;      // float [rows] per-row losses
-    size_t logp = 0;      // float [rows] per-row log p (two-pass fused calls)
+    size_t logp = 0;      // float [rows] per-row log p (two-pass fused calls), or int32
+                          // [rows] the persistent kernel's row order
     size_t total = 0;
 };
 
@@ -376,7 +378,8 @@ gbce_status ce_fwd(const void *logits, gbce_dtype dtype, int64_t rows, int64_t v
         e = gbce::launch_reduce_loss(loss_rows, labels, rows, ignore_index,
                                      static_cast<int>(reduction), nullptr, n_ptr, loss_out, s);
     else if (e == cudaSuccess && n_items_out != nullptr)
-        e = gbce::launch_count_items(labels, rows, ignore_index, n_items_out, nullptr, s);
+        e = gbce::launch_count_items(labels, rows, ignore_index, n_items_out, nullptr, nullptr,
+                                     nullptr, s);
     return cuda_status(e);
 }
 
@@ -445,7 +448,8 @@ gbce_status ce_fwd_bwd_fused(const void *logits, gbce_dtype dtype, int64_t rows,
                                          static_cast<int>(reduction), nullptr, n_items_out,
                                          loss_out, s);
         else if (n_items_out != nullptr)
-            e = gbce::launch_count_items(labels, 0, ignore_index, n_items_out, nullptr, s);
+            e = gbce::launch_count_items(labels, 0, ignore_index, n_items_out, nullptr, nullptr,
+                                         nullptr, s);
         return cuda_status(e);
     }
     if (labels == nullptr || loss_out == nullptr || grad_out == nullptr)
@@ -465,9 +469,16 @@ gbce_status ce_fwd_bwd_fused(const void *logits, gbce_dtype dtype, int64_t rows,
     // a ticket that the item count zeroes first
     const bool persistent = p.splits == 1;
     p.row_ticket = persistent ? ws_at<int32_t>(workspace, w.ticket) : nullptr;
+    // the persistent kernel's row order (live rows first) shares the space
+    // of the per-row log p, which only the few-row two-pass path uses
+    int32_t *order = persistent ? ws_at<int32_t>(workspace, w.logp) : nullptr;
+    int32_t *order_flag = persistent ? ws_at<int32_t>(workspace, w.ticket + 4) : nullptr;
+    p.row_order = order;
+    p.row_order_flag = order_flag;
     cudaError_t e = cudaSuccess;
     if (reduction == GBCE_MEAN || n_items_out != nullptr || persistent)
-        e = gbce::launch_count_items(labels, rows, ignore_index, n_ptr, p.row_ticket, s);
+        e = gbce::launch_count_items(labels, rows, ignore_index, n_ptr, p.row_ticket, order,
+                                     order_flag, s);
 
     p.targets = labels;
     p.ignore_index = ignore_index;

@@ -63,6 +63,10 @@ struct RowParams {
 
     int32_t *dev_status;
     int32_t *row_ticket;  // persistent fused kernel: rows handed out beyond the first wave
+    // persistent fused kernel: the order rows are handed out in (live rows
+    // first, then ignored ones), valid when *row_order_flag != 0; nullable
+    const int32_t *row_order;
+    const int32_t *row_order_flag;
     // one-CTA-per-row launches of more than one wave: each CTA warms in L2
     // the start of the row this many rows ahead (about the CTA that takes
     // its place on the SM); 0 for none
@@ -98,8 +102,13 @@ cudaError_t launch_rows(const RowParams &p, int mode, cudaStream_t stream);
 
 // n_items = #(labels != ignore_index) into *n_out (one CTA); also zeroes
 // *zero_out when it is non-null (the persistent kernel's row ticket).
+// n_items of the labels; zero_out (nullable) is zeroed; with order_out
+// (nullable, [rows]) the rows are also listed live first, then ignored, each
+// group in row order, when most rows are ignored, and *order_flag says
+// whether that order was written (0: the identity order).
 cudaError_t launch_count_items(const int64_t *labels, int64_t rows, int64_t ignore_index,
-                               int64_t *n_out, int32_t *zero_out, cudaStream_t stream);
+                               int64_t *n_out, int32_t *zero_out, int32_t *order_out,
+                               int32_t *order_flag, cudaStream_t stream);
 
 // loss_out[0] = sum (SUM) or sum / n (MEAN, 0 when n == 0) of loss_rows in a
 // fixed order with fp64 accumulation; when count_into is non-null the item

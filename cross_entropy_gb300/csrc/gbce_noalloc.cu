@@ -17,8 +17,8 @@
 //
 // The array is shared by all calls and keeps whatever the last call left in
 // it.  Nothing in it has to start at zero: the fused call writes every part
-// of its workspace it reads (item count, the persistent kernel's row ticket,
-// per-row losses, per-row log p) before reading it.  Two calls whose GPU
+// of its workspace it reads (item count, the persistent kernel's row ticket
+// and row order, per-row losses, per-row log p) before reading it.  Two calls whose GPU
 // work overlaps in time (for example on two streams) use the same array and
 // race; serialize them.  The looked-up address is kept for the process: it
 // goes stale if the device's primary context is reset (cudaDeviceReset).

@@ -135,7 +135,16 @@ __global__ void __launch_bounds__(PersistShape<CAP>::kThreads, PersistShape<CAP>
             uint32_t seq = 0;          // chunks issued
             uint32_t slot = 0, lap = 0;  // ring position of chunk seq, and its lap
             bool ok = true;
-            int64_t r = blockIdx.x;
+            // ticket t -> row: in the order the item count wrote when most
+            // rows are ignored (live rows first, then the ignored ones, which
+            // only write zeros and so even out the last rows' finishing
+            // times), else row t
+            const bool ordered = p.row_order != nullptr && *p.row_order_flag != 0;
+            const auto row_of = [&](int64_t t) -> int64_t {
+                return t >= p.rows ? p.rows : (ordered ? p.row_order[t] : t);
+            };
+            int64_t t = blockIdx.x;
+            int64_t r = row_of(t);
             int64_t lab = r < p.rows ? p.targets[r] : 0;
             for (uint32_t qi = 0; ok; ++qi) {
                 // hand row r (-1: no more rows) to the consumers
@@ -151,11 +160,13 @@ __global__ void __launch_bounds__(PersistShape<CAP>::kThreads, PersistShape<CAP>
                     break;
                 // the ticket for the row after this one, fetched while this
                 // one streams (without a ticket counter: the static walk)
-                const int64_t next =
+                const int64_t next_t =
                     p.row_ticket != nullptr
                         ? gridDim.x + static_cast<int64_t>(atomicAdd(p.row_ticket, 1))
-                        : r + gridDim.x;
+                        : t + gridDim.x;
+                const int64_t next = row_of(next_t);
                 if (lab == p.ignore_index || lab < 0 || lab >= V) {
+                    t = next_t;
                     r = next;
                     lab = r < p.rows ? p.targets[r] : 0;
                     continue;
@@ -186,6 +197,7 @@ __global__ void __launch_bounds__(PersistShape<CAP>::kThreads, PersistShape<CAP>
                         }
                     }
                 }
+                t = next_t;
                 r = next;
                 lab = next_lab;
             }

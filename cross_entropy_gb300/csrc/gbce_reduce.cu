@@ -84,20 +84,70 @@ __device__ void thread_partials(const float *loss_rows, const int64_t *labels, i
     }
 }
 
+// The count, and for the persistent fused kernel the order it hands rows
+// out in: live rows first, then the ignored ones (each group in row order),
+// so that the cheap ignored rows, which only write zeros, come last and
+// even out the CTAs' finishing times.  Written only when most rows are
+// ignored (sparse supervision: 0.494 -> 0.478 ms at 8192 rows, 25%
+// labelled); with a few ignored rows spread among the others it costs time
+// instead (2048 rows, 10% ignored: 0.207 -> 0.209 ms), as their zero writes
+// then bunch up at the end rather than mixing with the other rows' reads.
+// A stable partition, 256 rows at a time, by warp ballots and a scan over
+// the eight warps.
 __global__ void __launch_bounds__(kReduceThreads)
     count_items_kernel(const int64_t *labels, int64_t rows, int64_t ignore_index, int64_t *n_out,
-                       int32_t *zero_out)
+                       int32_t *zero_out, int32_t *order_out, int32_t *order_flag)
 {
     __shared__ int64_t iscratch[kReduceWarps];
     __shared__ double dscratch[kReduceWarps];
+    __shared__ int64_t s_live;
+    __shared__ int32_t s_wl[kReduceWarps], s_wi[kReduceWarps];
     if (threadIdx.x == 0 && zero_out != nullptr)
         *zero_out = 0;
     int64_t n;
     double s;
     thread_partials(nullptr, labels, rows, ignore_index, true, n, s);
     block_sum2(n, s, iscratch, dscratch);
-    if (threadIdx.x == 0)
+    if (threadIdx.x == 0) {
         *n_out = n;
+        s_live = n;
+        if (order_flag != nullptr)
+            *order_flag = (order_out != nullptr && 2 * n < rows) ? 1 : 0;
+    }
+    __syncthreads();
+    const int64_t live = s_live;
+    if (order_out == nullptr || order_flag == nullptr || 2 * live >= rows)
+        return;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const unsigned below = (1u << lane) - 1u;
+    int64_t base_live = 0, base_ign = live;
+    for (int64_t t0 = 0; t0 < rows; t0 += kReduceThreads) {
+        const int64_t r = t0 + threadIdx.x;
+        const bool in = r < rows;
+        const bool is_live = in && labels[r] != ignore_index;
+        const unsigned bl = __ballot_sync(0xffffffffu, is_live);
+        const unsigned bi = __ballot_sync(0xffffffffu, in && !is_live);
+        if (lane == 0) {
+            s_wl[warp] = __popc(bl);
+            s_wi[warp] = __popc(bi);
+        }
+        __syncthreads();
+        int32_t off_l = 0, off_i = 0, tot_l = 0, tot_i = 0;
+#pragma unroll
+        for (int w = 0; w < kReduceWarps; ++w) {
+            off_l += w < warp ? s_wl[w] : 0;
+            off_i += w < warp ? s_wi[w] : 0;
+            tot_l += s_wl[w];
+            tot_i += s_wi[w];
+        }
+        if (is_live)
+            order_out[base_live + off_l + __popc(bl & below)] = static_cast<int32_t>(r);
+        else if (in)
+            order_out[base_ign + off_i + __popc(bi & below)] = static_cast<int32_t>(r);
+        base_live += tot_l;
+        base_ign += tot_i;
+        __syncthreads();  // before the next tile overwrites s_wl, s_wi
+    }
 }
 
 __global__ void __launch_bounds__(kReduceThreads)
@@ -126,10 +176,11 @@ __global__ void __launch_bounds__(kReduceThreads)
 }
 
 cudaError_t launch_count_items(const int64_t *labels, int64_t rows, int64_t ignore_index,
-                               int64_t *n_out, int32_t *zero_out, cudaStream_t stream)
+                               int64_t *n_out, int32_t *zero_out, int32_t *order_out,
+                               int32_t *order_flag, cudaStream_t stream)
 {
     count_items_kernel<<<1, kReduceThreads, 0, stream>>>(labels, rows, ignore_index, n_out,
-                                                         zero_out);
+                                                         zero_out, order_out, order_flag);
     note_launches(1);
     return cudaGetLastError();
 }
