@@ -311,21 +311,34 @@ __device__ __forceinline__ float2 tanh_series_pair(float2 u)
 
 // tanh(u) for any u, one lane at a time: the series below kCapSeriesBound,
 // else t = 1 - 2 r with r = 1 / (e + 1), e = e^{2|u|} (t >= 0.5 there, so
-// nothing cancels; e = +inf gives t = 1).  *chain receives 1 - t^2, as
-// 4 e r^2 beyond the series range: it keeps its relative accuracy when t
-// nears 1.
-__device__ __forceinline__ float tanh_lane(float u, float &chain)
+// nothing cancels; e = +inf gives t = 1).
+__device__ __forceinline__ float tanh_lane(float u)
 {
     const float a = fabsf(u);
-    if (a < kCapSeriesBound) {
-        const float2 t = tanh_series_pair(make_float2(u, u));
-        chain = fmaf(-t.x, t.x, 1.0f);
-        return t.x;
-    }
+    if (a < kCapSeriesBound)
+        return tanh_series_pair(make_float2(u, u)).x;
     const float e = ex2(2.0f * 1.4426950408889634f * a);
     const float r = rcp_approx(e + 1.0f);
-    chain = e < 1e30f ? 4.0f * e * r * r : 0.0f;
     return copysignf(fmaf(-2.0f, r, 1.0f), u);
+}
+
+// The soft-cap's chain factor 1 - tanh^2(u) = sech^2(u), to a few ulp
+// relative for every u: (2 h / (1 + h^2))^2 with h = e^{-|u|}, a sum and a
+// quotient of positive numbers (1 - t^2 from a rounded t loses every digit
+// once t rounds to 1, from |u| of about 9).  Past |u| = 20 the factor
+// (below 2^-55) would soon leave fp32's normal range: it comes back times
+// 2^64, with *unscale = 2^-64 for the caller to apply to its final product,
+// so that a gradient element down in the subnormals is rounded once.  The
+// factor is 0 for |u| = inf, NaN for a NaN u.
+__device__ __forceinline__ float tanh_chain(float u, float &unscale)
+{
+    const float a = fabsf(u);
+    const bool far = a > 20.0f;
+    const float h = expf(-a) * (far ? 0x1p32f : 1.0f);
+    const float w = far ? 0.0f : h * h;  // far out, 1 + e^{-2|u|} rounds to 1
+    const float q = __fdiv_rn(2.0f * h, 1.0f + w);
+    unscale = far ? 0x1p-64f : 1.0f;
+    return q * q;
 }
 
 __device__ __forceinline__ uint32_t bf16x2_min(uint32_t a, uint32_t b)

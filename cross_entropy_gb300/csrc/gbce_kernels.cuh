@@ -313,8 +313,7 @@ __device__ __noinline__ float2 capped_vector_sums(uint4 a, float inv_cap, float 
     float s = 0.0f, sx = 0.0f;
 #pragma unroll
     for (int e = 0; e < VEC; ++e) {
-        float chain;
-        const float t = tanh_lane(f[e] * inv_cap, chain);
+        const float t = tanh_lane(f[e] * inv_cap);
         s += ex2(fmaf(t, capc, nmc));
         sx = fmaf(t, cap, sx);
     }
@@ -971,7 +970,8 @@ template <> struct GradVec<float> {
 };
 
 // grad_capped for a vector with a logit outside the series range, lane by
-// lane and out of line: fma(gs, 2^z, c0) * (1 - t^2), z = t * capc + kbx.
+// lane and out of line: fma(gs, 2^z, c0) * (1 - t^2), z = t * capc + kbx,
+// the chain factor from tanh_chain.
 template <typename T>
 __device__ __noinline__ uint4 grad_capped_lanes(uint4 a, float inv_cap, float capc, float kbx,
                                                 float gs, float c0)
@@ -982,16 +982,18 @@ __device__ __noinline__ uint4 grad_capped_lanes(uint4 a, float inv_cap, float ca
     float d[VEC];
 #pragma unroll
     for (int e = 0; e < VEC; ++e) {
-        float chain;
-        const float t = tanh_lane(f[e] * inv_cap, chain);
-        d[e] = fmaf(gs, ex2(fmaf(t, capc, kbx)), c0) * chain;
+        const float u = f[e] * inv_cap;
+        float unscale;
+        const float chain = tanh_chain(u, unscale);
+        d[e] = (fmaf(gs, ex2(fmaf(tanh_lane(u), capc, kbx)), c0) * chain) * unscale;
     }
     return Elem<T>::pack(d);
 }
 
 // The soft-capped gradient of the vector that holds the label (element
 // yoff), lane by lane with tanhf and out of line (once per row): the label
-// element is dy * (1 - t^2), the others as in grad_capped_lanes.
+// element is dy * (1 - t^2), the others as in grad_capped_lanes, the chain
+// factor from tanh_chain.
 template <typename T>
 __device__ __noinline__ uint4 grad_capped_label_vector(uint4 a, int32_t yoff, float dy,
                                                        float inv_cap, float capc, float kbx,
@@ -1002,9 +1004,11 @@ __device__ __noinline__ uint4 grad_capped_label_vector(uint4 a, int32_t yoff, fl
     Elem<T>::unpack(a, f);
 #pragma unroll
     for (int e = 0; e < VEC; ++e) {
-        const float t = tanhf(f[e] * inv_cap);
-        const float d = e == yoff ? dy : fmaf(gs, ex2(fmaf(t, capc, kbx)), c0);
-        f[e] = d * ((1.0f - t) * (1.0f + t));
+        const float u = f[e] * inv_cap;
+        float unscale;
+        const float chain = tanh_chain(u, unscale);
+        const float d = e == yoff ? dy : fmaf(gs, ex2(fmaf(tanhf(u), capc, kbx)), c0);
+        f[e] = (d * chain) * unscale;
     }
     return Elem<T>::pack(f);
 }
@@ -1844,13 +1848,14 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
         }
         if (kCap) {
             // soft-capped: element j is (its plain value on z = cap tanh(x / cap))
-            // times the chain factor 1 - tanh^2(x / cap)
+            // times the chain factor 1 - tanh^2(x / cap) (tanh_chain)
             const auto elem = [&](float x, bool is_y) {
-                const float t = tanhf(x * p.inv_cap);
-                const float chain = (1.0f - t) * (1.0f + t);
-                const float z = p.softcap * t;
+                const float u = x * p.inv_cap;
+                float unscale;
+                const float chain = tanh_chain(u, unscale);
+                const float z = p.softcap * tanhf(u);
                 const float d = is_y ? gk.dy : fmaf(gk.gs, ex2(fmaf(z + gk.nxy, gk.c, gk.kb)), gk.c0);
-                return d * chain;
+                return (d * chain) * unscale;
             };
             if (split == 0)
                 for (int64_t e = tid; e < g.head; e += NC)

@@ -379,13 +379,16 @@ __global__ void __launch_bounds__(PersistShape<CAP>::kThreads, PersistShape<CAP>
 
         // pass 2: gradient
         // soft-capped element: its plain value on z = cap tanh(x / cap) times
-        // the chain factor 1 - tanh^2(x / cap)
+        // the chain factor 1 - tanh^2(x / cap) (tanh_chain)
         const auto elem = [&](float x, bool is_y) {
             if (!CAP)
                 return is_y ? gk.dy : grad_scalar(x, gk);
-            const float t = tanhf(x * p.inv_cap);
-            const float d = is_y ? gk.dy : fmaf(gk.gs, ex2(fmaf(t, capk.capc, gk.kbx)), gk.c0);
-            return d * ((1.0f - t) * (1.0f + t));
+            const float u = x * p.inv_cap;
+            float unscale;
+            const float chain = tanh_chain(u, unscale);
+            const float d =
+                is_y ? gk.dy : fmaf(gk.gs, ex2(fmaf(tanhf(u), capk.capc, gk.kbx)), gk.c0);
+            return (d * chain) * unscale;
         };
         for (int64_t e = tid; e < g.head; e += NC)
             E::store(drow + e, elem(E::load(row + e), e == y));

@@ -364,7 +364,10 @@ static int64_t ce_core(const double *x, int64_t rows, int64_t V, int64_t ld,
  * The exported cross-entropy: ce_core above, with optional logit soft-capping.
  * softcap > 0 replaces every logit x by cap * tanh(x / cap) before the
  * temperature and the softmax (a per-element transform of the logits), and
- * the gradient with respect to x takes the chain factor 1 - tanh^2(x / cap).
+ * the gradient with respect to x takes the chain factor
+ * d/dx [cap tanh(x / cap)] = sech^2(x / cap), written as 1 / cosh^2: the
+ * equal form 1 - tanh^2 loses its digits once tanh rounds to +-1 (|x / cap|
+ * of about 19 in fp64), where the factor is still far above fp64's range.
  */
 int64_t oracle_cross_entropy(const double *x, int64_t rows, int64_t V, int64_t ld,
                              const int64_t *labels, int64_t ignore_index, double T,
@@ -388,8 +391,8 @@ int64_t oracle_cross_entropy(const double *x, int64_t rows, int64_t V, int64_t l
 #pragma omp parallel for schedule(static)
         for (int64_t r = 0; r < rows; ++r)
             for (int64_t j = 0; j < V; ++j) {
-                const double t = tanh(x[r * ld + j] / softcap);
-                dx[r * ldx + j] *= 1.0 - t * t;
+                const double sech = 1.0 / cosh(x[r * ld + j] / softcap);
+                dx[r * ldx + j] *= sech * sech;
             }
     }
     free(z);

@@ -3,6 +3,9 @@
 Tolerances (floating point, against the fp64 oracle):
   log p, element-wise relative: 2e-5 for fp32 logits, 1e-5 for bf16 logits;
     exactly 0 where the oracle gives exactly 0 (masked rows, V = 1); never > 0.
+    A log p may also differ by 2^-148 absolutely: that of a near-certain
+    column is about -(1 - p), which fp32 holds below 2^-126 only as a
+    subnormal (2 ulp = 2^-148 of error) and below 2^-149 not at all.
   dlogits, per row ||got - ref||_2 / ||ref||_2: 2e-5 fp32, 4e-3 bf16;
     ignored rows exactly zero.  The dlogits come in the logits' dtype, which
     cannot hold values below half its smallest subnormal (2^-150 fp32,
@@ -12,8 +15,14 @@ Tolerances (floating point, against the fp64 oracle):
   row entropy, element-wise relative: 2e-5 for either logit type (the sums
     behind it are fp32 whatever the input type); exactly 0 where the oracle
     gives exactly 0; never negative.
-  zero-sum rows: |sum_j dx_j| <= tol * sum_j |dx_j| (fp64 host sums), tol
-    1e-5 fp32 / 4e-3 bf16.
+  entropy may also differ by 2^-141 absolutely: it is an fp32 mass (1 - p
+    of the reference column) times that mass's mean surprisal, and where the
+    mass is below 2^-126 it is a subnormal with an absolute error of up to
+    2 ulp = 2^-148, while the surprisal stays under 2^7 nats (-log of a mass
+    fp32 can hold, 103.3, plus log V).  A mass below fp32's range reads as 0.
+  a DFT-weighted row loss p_y * CE_row may likewise differ by 2^-148 CE_row
+    + 2^-149 (p_y subnormal, then the product's rounding); a reduced DFT
+    loss by the sum of its rows' floors.
 Integer results (item counts, skipped rows) are compared exactly.
 """
 
@@ -29,26 +38,37 @@ ENTROPY_TOL = 2e-5
 ZERO_SUM_TOL = {torch.float32: 1e-5, torch.bfloat16: 4e-3}
 # half the smallest subnormal of the gradient's dtype: its rounding floor
 GRAD_FLOOR = {torch.float32: 2.0 ** -150, torch.bfloat16: 2.0 ** -134}
+# a subnormal fp32 mass (2 ulp = 2^-148 of error), alone (a log p near 0) or
+# times a surprisal < 2^7 nats (an entropy)
+LOGP_FLOOR = 2.0 ** -148
+SUBNORMAL_PRODUCT_FLOOR = 2.0 ** -141
 
 
 def to_f64(t: torch.Tensor) -> np.ndarray:
     return t.detach().float().cpu().double().numpy()
 
 
-def assert_logp_close(got, ref, dtype, what="logp", tol=None):
+def assert_logp_close(got, ref, dtype, what="logp", tol=None, floor=0.0):
+    """Element-wise relative error <= tol, plus LOGP_FLOOR and an extra
+    absolute `floor` (scalar or per element) for values that are products of
+    a subnormal mass, such as DFT-weighted losses."""
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     assert got.shape == ref.shape, (got.shape, ref.shape)
     assert np.all(np.isnan(got) == np.isnan(ref)), f"{what}: NaN pattern differs"
     ok = ~np.isnan(ref)
     g, r = got[ok], ref[ok]
+    floor = np.broadcast_to(np.asarray(floor, dtype=np.float64), ref.shape)[ok]
     assert np.all(g <= 0.0), f"{what}: positive log p {g.max()}"
     zero = r == 0.0
     assert np.all(g[zero] == 0.0), f"{what}: nonzero where the oracle is exactly 0"
-    rel = np.abs(g[~zero] - r[~zero]) / np.abs(r[~zero])
+    floor = floor[~zero] + LOGP_FLOOR
+    diff = np.abs(g[~zero] - r[~zero])
+    rel = diff / np.abs(r[~zero])
     tol = LOGP_TOL[dtype] if tol is None else tol
     worst = rel.max() if rel.size else 0.0
-    assert worst <= tol, f"{what}: worst relative error {worst:.3e} > {tol:.0e}"
+    bad = diff > tol * np.abs(r[~zero]) + floor
+    assert not np.any(bad), f"{what}: worst relative error {rel[bad].max():.3e} > {tol:.0e}"
     return worst
 
 
@@ -85,11 +105,13 @@ def assert_zero_sum_rows(got, dtype, rows=None):
         assert abs(math.fsum(row)) <= tol * s_abs, f"row {r}: gradient does not sum to zero"
 
 
-def assert_loss_close(got: float, ref: float, what="loss"):
+def assert_loss_close(got: float, ref: float, what="loss", floor=0.0):
+    """Relative error <= LOSS_TOL (+ an absolute `floor`, for a sum of
+    DFT-weighted row losses: the sum of their floors)."""
     if ref == 0.0:
         assert got == 0.0, f"{what}: {got} != 0"
         return
-    assert abs(got - ref) <= LOSS_TOL * abs(ref), f"{what}: {got} vs {ref}"
+    assert abs(got - ref) <= LOSS_TOL * abs(ref) + floor, f"{what}: {got} vs {ref}"
 
 
 def assert_entropy_close(got, ref, what="entropy"):
@@ -102,9 +124,12 @@ def assert_entropy_close(got, ref, what="entropy"):
     assert np.all(g >= 0.0), f"{what}: negative entropy {g.min()}"
     zero = r == 0.0
     assert np.all(g[zero] == 0.0), f"{what}: nonzero where the oracle is exactly 0"
-    rel = np.abs(g[~zero] - r[~zero]) / r[~zero]
+    diff = np.abs(g[~zero] - r[~zero])
+    rel = diff / r[~zero]
     worst = rel.max() if rel.size else 0.0
-    assert worst <= ENTROPY_TOL, f"{what}: worst relative error {worst:.3e} > {ENTROPY_TOL:.0e}"
+    bad = diff > ENTROPY_TOL * r[~zero] + SUBNORMAL_PRODUCT_FLOOR
+    assert not np.any(bad), (
+        f"{what}: worst relative error {rel[bad].max():.3e} > {ENTROPY_TOL:.0e}")
     return worst
 
 

@@ -184,6 +184,45 @@ def test_softcap_split_path_and_saturated_logits():
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("rows,V", [(300, 2), (300, 7), (300, 4099), (3, 70001)])
+@pytest.mark.parametrize("cap", [1.0, 3.0])
+def test_softcap_chain_factor_far_past_the_knee(dtype, rows, V, cap):
+    # logits of 25 cap standard deviations: most lie far past the cap's knee,
+    # where the chain factor 1 - tanh^2(x / cap) is tiny and a rounded tanh
+    # would leave none of its digits.  Every gradient element against the
+    # oracle: the head and tail elements, the label's vector, the
+    # lane-by-lane vectors (3 rows: the split path).  Per element: the
+    # gradient tolerance relative to the element, plus the dtype's rounding
+    # floor (one ulp of its smallest normal magnitude range).
+    T = 0.5
+    gen = torch.Generator().manual_seed(V + int(cap))
+    x_cpu = (torch.randn((rows, V), generator=gen) * (25.0 * cap)).to(dtype)
+    lab = torch.randint(0, V, (rows,), generator=gen)
+    g = torch.randn(rows, generator=gen)
+    x, lab_d, g_d = x_cpu.to(DEV), lab.to(DEV), g.to(DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    kw = dict(temperature=T, reduction="none", softcap=cap, dev_status=status)
+    fused = gbce.ce_fwd_bwd_fused(x, lab_d, g_d, **kw)
+    fwd = gbce.ce_fwd(x, lab_d, **kw)
+    bwd = gbce.ce_bwd(x, lab_d, g_d, fwd.logp, fwd.n_items, **kw)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref = oracle.cross_entropy(workloads.to_numpy_f64(x_cpu), lab.numpy(), temperature=T,
+                               reduction="none", grad_out=g.double().numpy(), softcap=cap)
+    from helpers import GRAD_TOL
+    tol = GRAD_TOL[dtype]
+    floor = 2.0 ** -148 if dtype == torch.float32 else 2.0 ** -133
+    r = ref["dlogits"]
+    far = np.abs(workloads.to_numpy_f64(x_cpu)) > 9.0 * cap
+    assert far.mean() > 0.5 and np.all(r[far] != 0.0)
+    for d, name in ((fused.dlogits, "fused"), (bwd, "ce_bwd")):
+        err = np.abs(to_f64(d) - r)
+        bad = err > tol * np.abs(r) + floor
+        assert not np.any(bad), (f"{name}: {int(bad.sum())} elements off, worst relative "
+                                 f"{(err[bad] / np.abs(r[bad])).max():.3e}")
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("rows", [3, 400])
 def test_softcap_rows_opening_with_minus_infinity(dtype, rows):
     # a vocabulary mask over each row's first 8192 columns: every thread's

@@ -56,7 +56,10 @@ MUTANTS = {
     "smoothing_mean_not_over_V": ("eps * (sum_value(&nl) / (double)V)", "eps * sum_value(&nl)"),
     "dft_weight_missing_in_gradient": ("double scale = (dft ? exp(lp) * g : g) / T;",
                                        "double scale = g / T;"),
-    "softcap_chain_factor_dropped": ("dx[r * ldx + j] *= 1.0 - t * t;", "dx[r * ldx + j] *= 1.0;"),
+    "softcap_chain_factor_dropped": ("dx[r * ldx + j] *= sech * sech;", "dx[r * ldx + j] *= 1.0;"),
+    "softcap_chain_factor_cancels": ("dx[r * ldx + j] *= sech * sech;",
+                                     "dx[r * ldx + j] *= 1.0 - tanh(x[r * ld + j] / softcap)"
+                                     " * tanh(x[r * ld + j] / softcap);"),
     "softcap_not_rescaled": ("z[r * V + j] = softcap * tanh(x[r * ld + j] / softcap);",
                              "z[r * V + j] = tanh(x[r * ld + j] / softcap);"),
     "sel_bwd_missing_inverse_T": ("dr[j] = -(Gv / T) * pj;",

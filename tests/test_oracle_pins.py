@@ -790,6 +790,24 @@ def test_softcap_limits_closed_form_and_finite_differences():
                                             rel=2e-6, abs=5e-9)
 
 
+def test_softcap_chain_factor_far_past_the_knee():
+    # d/dx [cap tanh(x / cap)] = 4 w / (1 + w)^2, w = e^{-2|u|}, u = x / cap:
+    # about 1.7e-17 at u = 20 and 3.5e-26 at u = -30, where 1 - tanh^2(u)
+    # is 0 in fp64; the plain softmax gradient (p - onehot) / T carries it
+    cap, T = 2.0, 0.5
+    x = np.array([[40.0, -60.0, 0.3, -1.7]])   # u = 20, -30, 0.15, -0.85
+    out = oracle.cross_entropy(x, [2], temperature=T, reduction="sum", softcap=cap)
+    Te = oracle.exact_temperature(T)
+    z = np.array([cap * math.tanh(v / cap) for v in x[0]]) / Te
+    e = np.exp(z - z.max())
+    dz = (e / e.sum() - np.array([0.0, 0.0, 1.0, 0.0])) / Te
+    for j, v in enumerate(x[0]):
+        w = math.exp(-2.0 * abs(v / cap))
+        want = dz[j] * 4.0 * w / (1.0 + w) ** 2
+        assert want != 0.0
+        assert abs(out["dlogits"][0, j] - want) <= 1e-12 * abs(want)
+
+
 # ----------------------------------------------- vocabulary-slice partials
 
 @pytest.mark.parametrize("cuts", [[0, 33], [0, 16, 33], [0, 1, 5, 20, 33], [0, 32, 33]])
