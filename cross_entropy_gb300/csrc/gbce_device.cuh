@@ -31,6 +31,22 @@ __device__ __forceinline__ void fence_barrier_init()
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic
+// stream serialization may start while the kernel before it in the stream
+// still runs.  grid_dependency_wait blocks the calling thread until that
+// kernel has completed and its memory writes are visible (at once when the
+// kernel was launched without the attribute).  launch_dependents lets the
+// kernel after this one start before this one ends.
+__device__ __forceinline__ void grid_dependency_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
 {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),

@@ -126,6 +126,9 @@ __global__ void __launch_bounds__(PersistShape<CAP>::kThreads, PersistShape<CAP>
         fence_barrier_init();
     }
     __syncthreads();
+    // launched as a programmatic dependent of the item count: the row
+    // ticket, the row order and n_items are read only after it completes
+    grid_dependency_wait();
 
     // ------------------------------------------------------------ producer
     if (warp == NCW) {
@@ -485,9 +488,21 @@ cudaError_t launch_persistent_fused_as(const RowParams &p, int sms, cudaStream_t
             slots = fit > floor ? fit : floor;
     }
     const int grid = static_cast<int>(p.rows < slots ? p.rows : slots);
-    kernel<<<grid, Shape::kThreads, Shape::kDynSmem, stream>>>(p);
+    // a programmatic dependent of the item count, which lets it start: the
+    // CTAs' launch and prologue overlap the count
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(Shape::kThreads);
+    cfg.dynamicSmemBytes = Shape::kDynSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    err = cudaLaunchKernelEx(&cfg, kernel, p);
     note_launches(1);
-    return cudaGetLastError();
+    return err != cudaSuccess ? err : cudaGetLastError();
 }
 
 template <typename T>

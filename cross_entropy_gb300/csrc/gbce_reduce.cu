@@ -102,6 +102,9 @@ __global__ void __launch_bounds__(kReduceThreads)
     __shared__ double dscratch[kReduceWarps];
     __shared__ int64_t s_live;
     __shared__ int32_t s_wl[kReduceWarps], s_wi[kReduceWarps];
+    // the row kernel after this one may start its prologue now: it waits
+    // for this kernel's outputs before it reads them
+    launch_dependents();
     if (threadIdx.x == 0 && zero_out != nullptr)
         *zero_out = 0;
     int64_t n;
@@ -157,6 +160,8 @@ __global__ void __launch_bounds__(kReduceThreads)
 {
     __shared__ int64_t iscratch[kReduceWarps];
     __shared__ double dscratch[kReduceWarps];
+    // launched as a dependent of the kernel that wrote the row losses
+    grid_dependency_wait();
     // the item count when this call counts (count_into), else a given one
     const bool count = count_into != nullptr;
     int64_t n;
@@ -189,10 +194,22 @@ cudaError_t launch_reduce_loss(const float *loss_rows, const int64_t *labels, in
                                int64_t ignore_index, int reduction, const int64_t *n_in,
                                int64_t *count_into, float *loss_out, cudaStream_t stream)
 {
-    reduce_loss_kernel<<<1, kReduceThreads, 0, stream>>>(loss_rows, labels, rows, ignore_index,
-                                                         reduction, n_in, count_into, loss_out);
+    // a programmatic dependent of the row kernel before it: its launch is
+    // under way while that kernel finishes
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1);
+    cfg.blockDim = dim3(kReduceThreads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t err = cudaLaunchKernelEx(&cfg, reduce_loss_kernel, loss_rows, labels, rows,
+                                               ignore_index, reduction, n_in, count_into,
+                                               loss_out);
     note_launches(1);
-    return cudaGetLastError();
+    return err != cudaSuccess ? err : cudaGetLastError();
 }
 
 }  // namespace gbce
