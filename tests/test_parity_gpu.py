@@ -421,6 +421,49 @@ def test_repeatable_bytes_and_inputs_untouched():
     assert h0 == h1, "logits were modified"
 
 
+@pytest.mark.parametrize("reduction", ["mean", "sum", "none"])
+def test_back_to_back_calls_see_the_kernel_written_inputs(reduction):
+    # Each call's logits and labels are written by a kernel just before it on
+    # the same stream, and its outputs are read by kernels right after it,
+    # alternating two input sets with different ignored rows and one shared
+    # workspace.  The fused call's persistent kernel and loss reduction start
+    # early, as programmatic dependents of the kernel before them: each must
+    # still see the writes before it and finish before the reads after it.
+    rows, V, T = 600, 24001, 0.9
+    sets = []
+    for seed in (11, 12):
+        w = workloads.collapse_stress(dtype=torch.bfloat16, rows=rows, V=V, seed=seed)
+        lab = w.labels.clone()
+        lab[torch.arange(seed, rows, 7)] = -100
+        g = torch.randn(rows) if reduction == "none" else torch.tensor([0.75])
+        ref = oracle.cross_entropy(workloads.to_numpy_f64(w.logits), lab.numpy(), temperature=T,
+                                   reduction=reduction, grad_out=g.double().numpy())
+        sets.append((w.logits.to(DEV), lab.to(DEV), g.to(DEV), ref))
+    x = torch.empty((rows, V), dtype=torch.bfloat16, device=DEV)
+    lab_d = torch.empty(rows, dtype=torch.int64, device=DEV)
+    ws = gbce.new_workspace(rows, V, 1, device=torch.device(DEV))
+    got = []
+    for i in range(6):
+        src, lab_src, g, _ = sets[i % 2]
+        torch.mul(src, 1.0, out=x)
+        torch.add(lab_src, 0, out=lab_d)
+        out = gbce.ce_fwd_bwd_fused(x, lab_d, g, temperature=T, reduction=reduction,
+                                    workspace=ws)
+        got.append((out.loss * 1.0, out.n_items * 1, out.dlogits * 1.0, out.logp * 1.0))
+    torch.cuda.synchronize()
+    for i, (loss, n, d, lp) in enumerate(got):
+        ref = sets[i % 2][3]
+        assert int(n.item()) == ref["n_items"], f"call {i}: n_items"
+        if reduction == "none":
+            assert_logp_close(-to_f64(loss), -ref["loss_rows"], torch.bfloat16, f"call {i} rows")
+        else:
+            assert_loss_close(float(loss.item()), ref["loss"], f"call {i} loss")
+        assert_logp_close(to_f64(lp), ref["logp"], torch.bfloat16, f"call {i} log p")
+        sel = np.arange(0, rows, 25)
+        assert_grad_rows_close(to_f64(d[torch.as_tensor(sel, device=DEV)]), ref["dlogits"][sel],
+                               torch.bfloat16, f"call {i} dlogits")
+
+
 def test_three_d_logits_flatten():
     x = torch.randn((2, 5, 700), device=DEV, dtype=torch.bfloat16)
     idx = torch.randint(0, 700, (2, 5), device=DEV)
@@ -493,6 +536,37 @@ def test_persistent_stats_many_rows_k16_and_masks():
     ref, _ = oracle.selective_logsoftmax(workloads.to_numpy_f64(x_cpu[sel]), idx.numpy()[sel],
                                          0.8, mask.numpy()[sel])
     assert_logp_close(to_f64(got)[sel], ref, torch.bfloat16)
+    assert np.all(to_f64(got)[mask.numpy() == 0] == 0.0)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("V,K,pad", [(4099, 1, 0), (32768, 4, 0), (1000, 16, 13), (32000, 4, 5)])
+def test_many_short_rows_every_row(dtype, V, K, pad):
+    # several waves of short rows, every row against the oracle: row strides
+    # that leave rows off 16-byte boundaries (scalar head and tail), ragged
+    # vocabularies, duplicated indices, masked rows, and a few out-of-range
+    # indices (NaN for just those, reported).
+    rows, T = 1300, 0.7
+    g = torch.Generator().manual_seed(V + K)
+    big = (torch.randn((rows, V + pad), generator=g) * 3.0).to(dtype)
+    x_cpu = big[:, :V]
+    idx = torch.randint(0, V, (rows, K), generator=g)
+    if K > 1:
+        idx[:, K - 1] = idx[:, 0]
+    idx[5, 0] = V
+    idx[rows - 2, K - 1] = -3
+    mask = (torch.rand(rows, generator=g) >= 0.2).to(torch.uint8)
+    mask[5] = 1
+    mask[rows - 2] = 1
+    status = new_status()
+    got = gbce.selective_logsoftmax(big.to(DEV)[:, :V], idx.to(DEV), T, mask.to(DEV),
+                                    dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == gbce.DEV_BAD_INDEX
+    ref, n_bad = oracle.selective_logsoftmax(workloads.to_numpy_f64(x_cpu), idx.numpy(), T,
+                                             mask.numpy())
+    assert n_bad == 2
+    assert_logp_close(to_f64(got), ref, dtype)
     assert np.all(to_f64(got)[mask.numpy() == 0] == 0.0)
 
 
