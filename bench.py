@@ -17,7 +17,8 @@ in row blocks on a second stream so that each block's compute overlaps the
 next block's copy.
 
 ``per_config`` times every op of every seeded workload alone (``ms``: a
-lone CUDA-graph launch after an L2 flush).  For workloads smaller than L2
+lone CUDA-graph launch, after an L2 flush for workloads smaller than 256 MB:
+a 512 MB write, then a 256 MB read that leaves L2 clean).  For workloads smaller than L2
 it adds ``ms_steady``: the same call back to back over rotating copies of
 its inputs (more than twice the L2 in all), without the fixed floor of a
 lone launch that ``_launch_floor`` records.
@@ -425,8 +426,27 @@ def op_bytes(w, op, k=1):
     return read + rows * V * es  # fused
 
 
+class L2Flush:
+    """Run before each lone timed call: a 512 MB write, larger than L2, so
+    none of the call's inputs stay cached; then a 256 MB read of another
+    buffer, so that L2 is left holding clean lines.  After the write alone,
+    L2 is full of dirty lines, and a call smaller than L2 then writes about
+    as many bytes back to HBM as it reads: the flush's traffic, timed as the
+    call's."""
+
+    def __init__(self, dev):
+        self.w = torch.empty(128 * 1024 * 1024, dtype=torch.float32, device=dev)
+        self.r = torch.ones(64 * 1024 * 1024, dtype=torch.float32, device=dev)
+        self.acc = torch.empty((), dtype=torch.float32, device=dev)
+
+    def __call__(self):
+        self.w.fill_(1.0)
+        torch.sum(self.r, dim=0, out=self.acc)
+
+
 def time_op(fn, stream, reps, flush=None):
-    """Median CUDA-event time (ms) of one call, L2 flushed before each rep.
+    """Median CUDA-event time (ms) of one call, L2 flushed (L2Flush) before
+    each rep.
 
     The call is captured once in a CUDA graph and replayed, so the time is
     the GPU's and not the Python launch path's (the library's calls never
@@ -445,7 +465,7 @@ def time_op(fn, stream, reps, flush=None):
     times = []
     for _ in range(reps + 2):
         if flush is not None:
-            flush.fill_(1.0)
+            flush()
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(stream)
@@ -493,7 +513,7 @@ def time_op_steady(make, copies, reps=5):
 def launch_floor_ms(dev, stream):
     """time_op of a one-element fill after the same L2 flush: the floor that
     a lone launch's event time carries whatever its kernel does."""
-    flush = torch.empty(128 * 1024 * 1024, dtype=torch.float32, device=dev)
+    flush = L2Flush(dev)
     e = torch.zeros(1, device=dev)
     ms = time_op(lambda: e.fill_(0.0), stream, 20, flush)
     del flush
@@ -502,7 +522,7 @@ def launch_floor_ms(dev, stream):
 
 def measure_configs(gbce, dev, stream, peak):
     """Every seeded workload, each op timed alone: ms, rows/s, GB/s, fraction."""
-    flush = torch.empty(128 * 1024 * 1024, dtype=torch.float32, device=dev)  # 512 MB > L2
+    flush = L2Flush(dev)
     out = {}
 
     def record(name, w, op, ms, k=1, steady=None):
