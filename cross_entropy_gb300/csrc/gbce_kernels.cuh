@@ -1019,7 +1019,7 @@ __device__ __noinline__ uint4 grad_capped_label_vector(uint4 a, int32_t yoff, fl
 // exponent z = t * capc + kbx of the uncapped formula on the capped logit
 // (kbx from the capped label logit), evaluated as (-gs 2^z - c0)(t^2 - 1):
 // the sign goes into the constants, so the chain factor is one fused
-// multiply-add.
+// multiply-add (|t| < 0.5 in this range: t^2 - 1 cancels nothing).
 template <typename T>
 __device__ __forceinline__ uint4 grad_capped_series(const uint4 &a, const GradConsts &k,
                                                     const CapConsts &cp)
