@@ -88,7 +88,7 @@ def test_two_level_rows(V, gap, T):
     lp, _ = oracle.selective_logsoftmax(x, [[y]], T)
     Te = oracle.exact_temperature(T)
     want = -math.log1p((V - 1) * math.exp((b - a) / Te))
-    assert lp[0, 0] == pytest.approx(want, rel=1e-13)
+    assert lp[0, 0] == pytest.approx(want, rel=1e-13, abs=0)
     assert lp[0, 0] < 0.0
 
 
@@ -127,7 +127,7 @@ def test_brute_force_logp(V, T):
     Te = oracle.exact_temperature(T)
     for r in range(len(margins)):
         _, want = brute_row(x[r], y[r], Te)
-        assert lp[r, 0] == pytest.approx(float(want), rel=1e-12), (r, margins[r])
+        assert lp[r, 0] == pytest.approx(float(want), rel=1e-12, abs=0), (r, margins[r])
 
 
 @pytest.mark.parametrize("V", [2, 9, 64])
@@ -156,7 +156,7 @@ def test_brute_force_k_indices_with_duplicates():
     for r in range(4):
         for k in range(4):
             _, want = brute_row(x[r], idx[r, k], Te)
-            assert lp[r, k] == pytest.approx(float(want), rel=1e-12)
+            assert lp[r, k] == pytest.approx(float(want), rel=1e-12, abs=0)
     assert lp[0, 1] == lp[0, 2] and lp[2, 0] == lp[2, 3]
 
 
@@ -258,7 +258,7 @@ def test_agrees_with_torch_fp64_on_ordinary_rows():
         live = y != -100
         want = ref_lp[torch.arange(rows)[live], y[live]].numpy()
         np.testing.assert_allclose(out["logp"][live.numpy()], want, rtol=1e-11)
-        assert out["loss"] == pytest.approx(loss.item(), rel=1e-13)
+        assert out["loss"] == pytest.approx(loss.item(), rel=1e-13, abs=0)
         np.testing.assert_allclose(out["dlogits"], xt.grad.numpy(), rtol=1e-10, atol=1e-18)
 
 
@@ -282,7 +282,8 @@ def test_collapse_thresholds_from_the_pages():
             assert (p_y == 1.0) == collapses, (key, margin, p_y)
             lp, _ = oracle.selective_logsoftmax(row.double().numpy(), [[1]], 1.0)
             assert lp[0, 0] < 0.0
-            assert lp[0, 0] == pytest.approx(-math.log1p(math.exp(-margin)), rel=1e-14)
+            m = float(row.double()[0, 1])  # the margin as the row holds it (fp32: rounded)
+            assert lp[0, 0] == pytest.approx(-math.log1p(math.exp(-m)), rel=1e-14, abs=0)
 
 
 def test_sparse_supervision_workload_matches_page():
@@ -314,8 +315,8 @@ def test_reductions_and_item_count():
     s = oracle.cross_entropy(x, y, reduction="sum")
     m = oracle.cross_entropy(x, y, reduction="mean")
     assert s["n_items"] == m["n_items"] == 7
-    assert s["loss"] == pytest.approx(math.fsum(none["loss_rows"]), rel=1e-15)
-    assert m["loss"] == pytest.approx(s["loss"] / 7, rel=1e-15)
+    assert s["loss"] == pytest.approx(math.fsum(none["loss_rows"]), rel=1e-15, abs=0)
+    assert m["loss"] == pytest.approx(s["loss"] / 7, rel=1e-15, abs=0)
     np.testing.assert_allclose(m["dlogits"], s["dlogits"] / 7, rtol=1e-15)
     np.testing.assert_allclose(none["dlogits"], s["dlogits"], rtol=1e-15)
 
@@ -502,7 +503,7 @@ def test_entropy_closed_forms_and_bounds():
     p_t = 1.0 / (1.0 + (V - 1) * math.exp(b - a))
     p_o = (1.0 - p_t) / (V - 1)
     want = -p_t * math.log(p_t) - (V - 1) * p_o * math.log(p_o)
-    assert oracle.entropy(x, [10], T)[0][0] == pytest.approx(want, rel=1e-13)
+    assert oracle.entropy(x, [10], T)[0][0] == pytest.approx(want, rel=1e-13, abs=0)
     # V = 1: certain, the reference column does not change the value
     assert oracle.entropy(np.array([[2.0]]), [0], 1.0)[0][0] == 0.0
     rng = np.random.default_rng(8)
@@ -528,7 +529,7 @@ def test_entropy_ignores_zero_probability_columns():
     want = oracle.entropy(base, [5], 0.9)[0][0]
     for ref in (5, 40, 42):
         got, bad = oracle.entropy(x, [ref], 0.9)
-        assert bad == 0 and got[0] == pytest.approx(want, rel=1e-13), ref
+        assert bad == 0 and got[0] == pytest.approx(want, rel=1e-13, abs=0), ref
 
 
 # ----------------------------------------------- entropy term of the backward
@@ -686,7 +687,7 @@ def test_smoothed_ce_matches_torch_fp64():
             if red == "none":
                 np.testing.assert_allclose(out["loss_rows"], ref.detach().numpy(), rtol=1e-13)
             else:
-                assert out["loss"] == pytest.approx(float(ref.detach()), rel=1e-13)
+                assert out["loss"] == pytest.approx(float(ref.detach()), rel=1e-13, abs=0)
             np.testing.assert_allclose(out["dlogits"], xt.grad.numpy(), rtol=1e-11, atol=1e-17)
 
 
@@ -752,7 +753,7 @@ def test_softcapped_ce_matches_torch_fp64(eps):
     ref = torch.nn.functional.cross_entropy(z / Te, torch.tensor(y), ignore_index=-100,
                                             reduction="sum", label_smoothing=eps)
     (0.5 * ref).backward()
-    assert out["loss"] == pytest.approx(float(ref.detach()), rel=1e-13)
+    assert out["loss"] == pytest.approx(float(ref.detach()), rel=1e-13, abs=0)
     np.testing.assert_allclose(out["dlogits"], xt.grad.numpy(), rtol=1e-10, atol=1e-16)
 
 
@@ -772,7 +773,7 @@ def test_softcap_limits_closed_form_and_finite_differences():
     a = (zo - zy) / Te
     want = max(a, 0.0) + math.log1p(math.exp(-abs(a)))
     got = oracle.cross_entropy(x2, [0], temperature=T, reduction="none", softcap=cap)
-    assert got["loss_rows"][0] == pytest.approx(want, rel=1e-13)
+    assert got["loss_rows"][0] == pytest.approx(want, rel=1e-13, abs=0)
     # finite differences through the cap
     x3 = rng.normal(scale=15.0, size=(2, 9))
     y3 = np.array([4, 0])
@@ -842,5 +843,5 @@ def test_vocab_slices_brute_force_on_confident_rows():
     Te = oracle.exact_temperature(T)
     for r in range(2):
         _, want = brute_row(x[r], y[r], Te)
-        assert got[r, 0] == pytest.approx(float(want), rel=1e-12), r
+        assert got[r, 0] == pytest.approx(float(want), rel=1e-12, abs=0), r
         assert got[r, 0] < 0.0
