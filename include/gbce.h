@@ -30,7 +30,12 @@
  *    type (bf16 rounded to nearest even).
  *  - Asynchrony.  Every call only enqueues work on `stream` and returns; it
  *    never synchronizes the host.  The returned status reports HOST-side
- *    argument checks (and launch errors) only.
+ *    argument checks (and launch errors) only.  Some kernels of a call are
+ *    programmatic dependents of the kernel before them on the stream (their
+ *    launch overlaps it), and each waits for that kernel to complete before
+ *    its first global memory access; to the caller a call still runs in
+ *    stream order, after all earlier work on `stream` and before all later
+ *    work.
  *  - Device-side errors.  A label or index outside [0, vocab) (labels equal
  *    to ignore_index excepted) sets a bit in `*dev_status` (atomic OR; pass
  *    NULL to skip reporting) and makes that row's outputs NaN.  A pipeline
