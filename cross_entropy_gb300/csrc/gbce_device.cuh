@@ -743,16 +743,25 @@ __device__ __forceinline__ float finalize_logp(float m, float s, float xt, float
 //   H = p_t softplus(a) + (1 - p_t) (L - ln2 h / s),
 // a sum of non-negative terms: nothing cancels when t holds almost all of
 // the mass (the confident rows), and 1 - p_t never rounds to 0 there.
+// Past a = -80, 1 - p_t and softplus(a) both equal e^a to a relative e^a
+// and fall below fp32's normal range, while H = e^a (1 + L - mean) may not:
+// there e^a is carried times 2^64 (the square of e^{a/2} 2^32, both normal
+// down to a = -174) and the product is scaled back in one rounding, so an
+// entropy down to fp32's smallest subnormal keeps its value.
 __device__ __forceinline__ float finalize_entropy(float m, float s, float h, float xt, float T)
 {
     if (!(s > 0.0f))
         return (s == 0.0f) ? 0.0f : __int_as_float(0x7fc00000);
     const float ls = logf(s);
     const float a = ls + (m - xt) / T;
+    const float mean_u = (h / s) * 0.69314718055994531f;  // <= 0
+    if (a < -80.0f) {
+        const float e2 = expf(0.5f * a) * 0x1p32f;
+        return ((e2 * e2) * ((1.0f + ls - a) - mean_u)) * 0x1p-64f;
+    }
     const float sp = softplus(a), spn = softplus(-a);
     const float pt = expf(-sp);  // e^{log p_t}
     const float q = -expm1f(-sp);
-    const float mean_u = (h / s) * 0.69314718055994531f;  // <= 0
     const float ht = pt > 0.0f ? pt * sp : 0.0f;
     return fmaf(q, (ls + spn) - mean_u, ht);
 }

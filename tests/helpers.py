@@ -23,6 +23,10 @@ Tolerances (floating point, against the fp64 oracle):
   a DFT-weighted row loss p_y * CE_row may likewise differ by 2^-148 CE_row
     + 2^-149 (p_y subnormal, then the product's rounding); a reduced DFT
     loss by the sum of its rows' floors.
+  soft-capped CE (cap_eps): every exponent carries the fp32 error of its
+    capped logit, eps = 2.5 ulp(cap) / T; log p and a CE row loss (the
+    label's exponent and the log-sum-exp's) may differ by 2 eps more, a DFT
+    row loss by 2 eps (|loss| + p_y), a gradient row by 3 eps relative.
 Integer results (item counts, skipped rows) are compared exactly.
 """
 
@@ -38,6 +42,18 @@ ENTROPY_TOL = 2e-5
 ZERO_SUM_TOL = {torch.float32: 1e-5, torch.bfloat16: 4e-3}
 # half the smallest subnormal of the gradient's dtype: its rounding floor
 GRAD_FLOOR = {torch.float32: 2.0 ** -150, torch.bfloat16: 2.0 ** -134}
+
+
+def cap_eps(cap: float, T: float) -> float:
+    """Absolute error, in a soft-capped exponent z / T, of forming z = cap *
+    tanh(x / cap) in fp32 at all: tanh within 2 ulp of t (CUDA's bound for
+    tanhf) and one rounding of the product, so 2.5 ulp(cap) for |t| < 1,
+    divided by T.  0 without a cap."""
+    if not cap > 0.0:
+        return 0.0
+    return 2.5 * 2.0 ** (math.floor(math.log2(cap)) - 23) / T
+
+
 # a subnormal fp32 mass (2 ulp = 2^-148 of error), alone (a log p near 0) or
 # times a surprisal < 2^7 nats (an entropy)
 LOGP_FLOOR = 2.0 ** -148
