@@ -828,7 +828,9 @@ __device__ __forceinline__ float ce_row_loss(float lp, float xy, float sumx, flo
 __device__ __forceinline__ GradConsts grad_consts_ce(float xy, float c, float logp, float g,
                                                      float T, float eps, int dft, int64_t V)
 {
-    const float gscale = (dft ? g * expf(logp) : g) / T;
+    // (g / T) first: with a DFT weight below fp32's normal range, g p_y
+    // could round to 0 where (g / T) p_y is still a subnormal
+    const float gscale = dft ? (g / T) * expf(logp) : g / T;
     GradConsts k = grad_consts(xy, c, logp, gscale);
     if (eps != 0.0f) {
         const float u = eps / static_cast<float>(V);
@@ -1463,12 +1465,14 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
     target_vectors<T, KMAX>(tg, g, tv);
     if (kSelGrad) {
         // gathered column t: (1/T)(-g_t expm1(log p_t) - (G - g_t) exp(log p_t)),
+        // G - g_t summed from the other indices' upstream (a difference of G
+        // and g_t would lose a small upstream beside a large one),
         // g_t the upstream of every k that gathers t; every other column j:
         // -(G/T) exp((x_j - x_{t0})/T + log p_{t0}).  The entropy term adds
         // -(gH/T) p_j (log p_j + H) to every column (0 where p_j = 0).
         if (tid < p.k) {
             const float *gr = p.grad_out + r * p.k;
-            float G = 0.0f, gt = 0.0f;
+            float G = 0.0f, gt = 0.0f, go = 0.0f;
             int32_t mine = -1;
 #pragma unroll
             for (int k = 0; k < KMAX; ++k)
@@ -1481,9 +1485,11 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
                     G += gk;
                     if (tg[k] == mine)
                         gt += gk;
+                    else
+                        go += gk;
                 }
             const float lp = p.saved_logp[r * p.k + tid];
-            float dt = (-gt * expm1f(lp) - (G - gt) * expf(lp)) / p.T;
+            float dt = (-gt * expm1f(lp) - go * expf(lp)) / p.T;
             float gH = 0.0f, H = 0.0f;
             if (kEntGrad) {
                 gH = p.grad_entropy[r];

@@ -81,6 +81,34 @@ def test_confident_rows_keep_their_target_gradient():
     assert_zero_sum_rows(got, torch.float32)
 
 
+def test_small_upstream_beside_a_large_one():
+    # K = 2 with upstream gradients a thousand times apart, on rows confident
+    # in their first index: each gathered column's gradient holds the other
+    # index's small upstream (times its p), which a difference G - g_t of the
+    # fp32 sums would carry only to the large upstream's rounding.  Every
+    # gathered element against the oracle, element by element.
+    rows, V, T = 512, 4099, 1.0
+    gen = torch.Generator().manual_seed(91)
+    x_cpu = torch.randn((rows, V), generator=gen) * 2.0
+    idx = torch.randint(0, V, (rows, 2), generator=gen)
+    x_cpu[torch.arange(rows), idx[:, 0]] += 30.0  # confident in index 0
+    g = torch.stack([torch.full((rows,), -1.5), 1e-3 + torch.rand(rows, generator=gen) * 2e-3], dim=1)
+    x = x_cpu.to(DEV)
+    lp = gbce.selective_logsoftmax(x, idx.to(DEV), T)
+    d = gbce.selective_logsoftmax_bwd(x, idx.to(DEV), g.to(DEV), lp, T)
+    torch.cuda.synchronize()
+    ref, _ = oracle.selective_logsoftmax_backward(workloads.to_numpy_f64(x_cpu), idx.numpy(),
+                                                  g.double().numpy(), T)
+    got = to_f64(d)
+    r = np.arange(rows)
+    for k in range(2):
+        want = ref[r, idx[:, k].numpy()]
+        have = got[r, idx[:, k].numpy()]
+        rel = np.abs(have - want) / np.abs(want)
+        assert rel.max() <= 2e-5, f"index {k}: worst relative error {rel.max():.3e}"
+    assert_grad_rows_close(got, ref, torch.float32, "small upstream")
+
+
 @pytest.mark.parametrize("rows", [1, 3])
 def test_few_rows_split_path(rows):
     w = workloads.collapse_stress(dtype=torch.bfloat16, rows=rows, V=152064, seed=rows)
