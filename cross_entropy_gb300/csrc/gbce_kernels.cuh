@@ -1466,13 +1466,15 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
     if (kSelGrad) {
         // gathered column t: (1/T)(-g_t expm1(log p_t) - (G - g_t) exp(log p_t)),
         // G - g_t summed from the other indices' upstream (a difference of G
-        // and g_t would lose a small upstream beside a large one),
+        // and g_t would lose a small upstream beside a large one), and every
+        // such sum of at most K upstream values taken in fp64 (in fp32 a sum
+        // that cancels keeps only the terms' rounding),
         // g_t the upstream of every k that gathers t; every other column j:
         // -(G/T) exp((x_j - x_{t0})/T + log p_{t0}).  The entropy term adds
         // -(gH/T) p_j (log p_j + H) to every column (0 where p_j = 0).
         if (tid < p.k) {
             const float *gr = p.grad_out + r * p.k;
-            float G = 0.0f, gt = 0.0f, go = 0.0f;
+            double G2 = 0.0, gt2 = 0.0, go2 = 0.0;
             int32_t mine = -1;
 #pragma unroll
             for (int k = 0; k < KMAX; ++k)
@@ -1481,13 +1483,15 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
 #pragma unroll
             for (int k = 0; k < KMAX; ++k)
                 if (k < p.k) {
-                    const float gk = gr[k];
-                    G += gk;
+                    const double gk = gr[k];
+                    G2 += gk;
                     if (tg[k] == mine)
-                        gt += gk;
+                        gt2 += gk;
                     else
-                        go += gk;
+                        go2 += gk;
                 }
+            const float G = static_cast<float>(G2), gt = static_cast<float>(gt2),
+                        go = static_cast<float>(go2);
             const float lp = p.saved_logp[r * p.k + tid];
             float dt = (-gt * expm1f(lp) - go * expf(lp)) / p.T;
             float gH = 0.0f, H = 0.0f;

@@ -81,6 +81,29 @@ def test_confident_rows_keep_their_target_gradient():
     assert_zero_sum_rows(got, torch.float32)
 
 
+def test_upstream_sums_that_cancel():
+    # K = 16 on three columns: indices 8..15 repeat 0..7 with each upstream
+    # negated to within 1e-4, so every column's summed upstream (and every
+    # gradient element) is a sum of O(1) terms that cancels to ~1e-4.  In
+    # fp32 such a sum keeps only the terms' rounding (~1e-7, about 1e-3 of
+    # these rows); the kernel's sums of at most K upstream values are exact
+    # enough to meet the row bound.
+    rows, V, K, T = 256, 3, 16, 0.8
+    gen = torch.Generator().manual_seed(92)
+    x_cpu = torch.randn((rows, V), generator=gen) * 2.0
+    idx = torch.randint(0, V, (rows, K), generator=gen)
+    idx[:, 8:] = idx[:, :8]
+    g = torch.randn((rows, K), generator=gen)
+    g[:, 8:] = -g[:, :8] + 1e-4 * torch.randn((rows, 8), generator=gen)
+    x = x_cpu.to(DEV)
+    lp = gbce.selective_logsoftmax(x, idx.to(DEV), T)
+    d = gbce.selective_logsoftmax_bwd(x, idx.to(DEV), g.to(DEV), lp, T)
+    torch.cuda.synchronize()
+    ref, _ = oracle.selective_logsoftmax_backward(workloads.to_numpy_f64(x_cpu), idx.numpy(),
+                                                  g.double().numpy(), T)
+    assert_grad_rows_close(to_f64(d), ref, torch.float32, "cancelling upstream")
+
+
 def test_small_upstream_beside_a_large_one():
     # K = 2 with upstream gradients a thousand times apart, on rows confident
     # in their first index: each gathered column's gradient holds the other
