@@ -32,7 +32,10 @@ Tolerances (floating point, against the fp64 oracle):
     so a row may move by |g/T| 2^-148; a DFT weight p_y is an fp32 value
     (a subnormal within 2^-150), moving the row by |g/T| 2^-150 sqrt(2); a
     soft-capped element is the plain one times its chain factor, two
-    roundings, so one more rounding floor per element.
+    roundings, so one more rounding floor per element.  With label
+    smoothing an element is p_j minus its smoothed target, both fp32 values
+    of order 1; where p sits on the target the element cancels, and the row
+    may move by |g/T| 2^-21 (a few ulps of parts of norm at most 1).
 Integer results (item counts, skipped rows) are compared exactly.
 """
 
