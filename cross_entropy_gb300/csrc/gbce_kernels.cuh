@@ -1490,10 +1490,13 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
                     else
                         go2 += gk;
                 }
-            const float G = static_cast<float>(G2), gt = static_cast<float>(gt2),
-                        go = static_cast<float>(go2);
+            // divided by T before they meet the probabilities: a product that
+            // lands in the subnormals keeps its one rounding instead of having
+            // it scaled by 1/T
+            const float G = static_cast<float>(G2);
+            const float gtT = static_cast<float>(gt2 / p.T), goT = static_cast<float>(go2 / p.T);
             const float lp = p.saved_logp[r * p.k + tid];
-            float dt = (-gt * expm1f(lp) - go * expf(lp)) / p.T;
+            float dt = fmaf(-gtT, expm1f(lp), -goT * expf(lp));
             float gH = 0.0f, H = 0.0f;
             if (kEntGrad) {
                 gH = p.grad_entropy[r];
