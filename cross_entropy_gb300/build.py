@@ -2,7 +2,7 @@
 
 Each CUDA translation unit is compiled in parallel, then linked into a shared
 library with the CUDA runtime linked statically, so the library depends only
-on the driver.  Output: ``cross_entropy_gb300/_build/libgbce.so``.
+on the NVIDIA driver (libcuda).  Output: ``cross_entropy_gb300/_build/libgbce.so``.
 """
 
 from __future__ import annotations
