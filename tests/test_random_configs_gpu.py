@@ -29,11 +29,13 @@ if torch.cuda.is_available():
 DEV = "cuda:0"
 
 
-def make_configs(seed, n, extreme=False):
+def make_configs(seed, n, extreme=False, temps=None):
     """n seeded configurations; `extreme` widens the temperature (0.1 .. 4),
-    the logit scale (up to 50) and the soft-cap (1 .. 200)."""
+    the logit scale (up to 50) and the soft-cap (1 .. 200); `temps`
+    replaces the temperatures drawn from."""
     rng = np.random.default_rng(seed)
-    temps = [0.1, 0.25, 0.5, 1.0, 4.0] if extreme else [0.5, 0.9, 1.0, 1.7]
+    if temps is None:
+        temps = [0.1, 0.25, 0.5, 1.0, 4.0] if extreme else [0.5, 0.9, 1.0, 1.7]
     scales = [1.0, 20.0, 50.0] if extreme else [1.0, 4.0, 20.0]
     caps = [0.0, 0.0, 1.0, 30.0, 200.0] if extreme else [0.0, 0.0, 30.0, 5.0]
     out = []
@@ -60,7 +62,8 @@ def make_configs(seed, n, extreme=False):
 
 
 CONFIGS = make_configs(2024, 36) + make_configs(106, 60) + make_configs(7, 24, extreme=True) + [
-    c for s in (14, 17, 19, 20, 22, 26, 30, 39) for c in make_configs(s, 60, extreme=True)]
+    c for s in (14, 17, 19, 20, 22, 26, 30, 39) for c in make_configs(s, 60, extreme=True)] + (
+    make_configs(60, 40, extreme=True, temps=[0.02, 0.05]))
 
 
 def _id(c):

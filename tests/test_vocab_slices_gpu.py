@@ -9,7 +9,8 @@ import torch
 
 import oracle
 import workloads
-from helpers import assert_grad_block_close, assert_logp_close, assert_zero_sum_block, to_f64
+from helpers import (assert_grad_block_close, assert_grad_rows_close, assert_logp_close,
+                     assert_zero_sum_block, to_f64)
 
 pytestmark = pytest.mark.gpu
 
@@ -148,3 +149,44 @@ def test_slices_of_rows_dominated_far_above_their_first_index():
     assert_logp_close(to_f64(logp), ref, torch.float32, "sliced log p")
     ref_d, _ = oracle.selective_logsoftmax_backward(x64, idx.numpy(), g.double().numpy(), T)
     assert_grad_block_close(to_f64(d), ref_d, torch.float32, "sliced gradient")
+
+
+def slice_config(seed):
+    """A seeded vocabulary-slice case: rows, vocabulary, K, dtype,
+    temperature, logit scale and 1..5 slices with random boundaries."""
+    rng = np.random.default_rng(seed)
+    rows = int(rng.choice([1, 3, 64, 300, 700]))
+    V = int(rng.choice([2, 9, 1000, 4099, 24001, 50001]))
+    K = int(rng.choice([1, 2, 4, 16]))
+    dtype = torch.float32 if rng.random() < 0.5 else torch.bfloat16
+    T = float(rng.choice([0.1, 0.25, 0.5, 1.0, 4.0]))
+    scale = float(rng.choice([1.0, 20.0, 50.0]))
+    nsl = int(rng.integers(1, min(V, 5) + 1))
+    cuts = sorted(set([0, V] + [int(c) for c in rng.integers(1, V, size=nsl - 1)]))
+    return rows, V, K, dtype, T, scale, cuts
+
+
+@pytest.mark.parametrize("seed", range(48))
+def test_seeded_slicings_match_the_oracle(seed):
+    # random slicings of random rows (extreme temperatures and scales): the
+    # combined log p and the per-slice gradients against the oracle.  The
+    # gradient takes the combine's fp32 log p, so a row may also move by
+    # 2^-147 sum|g| / T (the log p floor) and, where a gathered column's two
+    # terms cancel, by a few fp32 ulps of them, 2^-22 sum|g| / T.
+    rows, V, K, dtype, T, scale, cuts = slice_config(seed)
+    gen = torch.Generator().manual_seed(seed)
+    x_cpu = (torch.randn((rows, V), generator=gen) * scale).to(dtype)
+    idx = torch.randint(0, V, (rows, K), generator=gen)
+    mask = (torch.rand(rows, generator=gen) > 0.15).to(torch.uint8)
+    g = torch.randn((rows, K), generator=gen)
+    logp, xt0, d, status = run_slices(x_cpu.to(DEV), idx.to(DEV), cuts, T, mask.to(DEV),
+                                      g.to(DEV))
+    assert status == 0
+    x64 = workloads.to_numpy_f64(x_cpu)
+    ref, _ = oracle.selective_logsoftmax(x64, idx.numpy(), T, mask.numpy())
+    assert_logp_close(to_f64(logp), ref, dtype, "sliced log p")
+    ref_d, _ = oracle.selective_logsoftmax_backward(x64, idx.numpy(), g.double().numpy(), T,
+                                                    mask.numpy())
+    ga = np.abs(g.double().numpy()).sum(axis=1) / T
+    assert_grad_rows_close(to_f64(d), ref_d, dtype, "sliced dlogits",
+                           extra_floor=ga * (2.0 ** -147 + 2.0 ** -22))
