@@ -1465,13 +1465,13 @@ __global__ void __launch_bounds__(kRowThreads, (MODE != kModeFused && KMAX <= 4)
     target_vectors<T, KMAX>(tg, g, tv);
     if (kSelGrad) {
         // gathered column t: (1/T)(-g_t expm1(log p_t) - (G - g_t) exp(log p_t)),
-        // G - g_t summed from the other indices' upstream (a difference of G
-        // and g_t would lose a small upstream beside a large one), and every
-        // such sum of at most K upstream values taken in fp64 (in fp32 a sum
-        // that cancels keeps only the terms' rounding),
         // g_t the upstream of every k that gathers t; every other column j:
         // -(G/T) exp((x_j - x_{t0})/T + log p_{t0}).  The entropy term adds
         // -(gH/T) p_j (log p_j + H) to every column (0 where p_j = 0).
+        // G - g_t is summed from the other indices' upstream (a difference of
+        // G and g_t would keep a small upstream only to a large one's
+        // rounding), and each sum of at most K upstream values is taken in
+        // fp64 (in fp32 a sum that cancels keeps only its terms' rounding).
         if (tid < p.k) {
             const float *gr = p.grad_out + r * p.k;
             double G2 = 0.0, gt2 = 0.0, go2 = 0.0;
