@@ -29,7 +29,7 @@
  *    losses and log-sum-exps are written as fp32; dlogits have the logits'
  *    type (bf16 rounded to nearest even).
  *  - Accuracy.  Against an fp64 evaluation of the same definitions: log-probs,
- *    losses and entropies within about 1e-5 relative; dlogits within 2e-5
+ *    losses and entropies within 1e-5 to 2e-5 relative; dlogits within 2e-5
  *    (fp32) or 4e-3 (bf16) relative per row.  Confident rows keep these
  *    bounds (the sums run over the non-target columns, the target gradient
  *    is expm1(log p)), down to fp32's subnormals.  A value fp32 cannot hold
